@@ -1,0 +1,312 @@
+"""fp64 CPU oracle of the MoE expert layer (ctypes wrapper of moe_oracle.c).
+
+TEST INFRASTRUCTURE: only ``tests/``, ``__graft_entry__.smoke()`` and the
+benchmark's CPU-baseline leg use this package.  It shares no code with the
+CUDA path and imports nothing from it.
+
+Every function takes numpy arrays.  Inputs come either as the synthetic
+workloads' raw encodings (bf16 bits as uint16 for x / gate_up / down / dY /
+shared weights, fp32 for W_r and bias), which are widened exactly, or all as
+float64 (used by the finite-difference pins).  All arithmetic is fp64.
+
+Every function is pinned by tests/test_oracle_pins.py; none is "parity
+unpinned".
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRCS = [os.path.join(_HERE, "moe_oracle.c"), os.path.join(_HERE, "moe_oracle_body.h")]
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle into liboracle.so (in place) when missing or stale."""
+    newest = max(os.path.getmtime(s) for s in _SRCS)
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < newest:
+        tmp = _LIB + ".%d.tmp" % os.getpid()
+        subprocess.check_call(["gcc", "-O2", "-std=c99", "-fPIC", "-shared", "-fopenmp",
+                               "-ffp-contract=off", _SRCS[0], "-o", tmp, "-lm"])
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+_P = ctypes.c_void_p
+_I = ctypes.c_int64
+
+_SIGS = {
+    "oracle_route": [_I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P],
+    "oracle_dense_ffn": [_I, _I, _I, _P, _P, _P, _P],
+    "oracle_forward_permuted": [_I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _I, _P, _P,
+                                _P, _P, _P, _P, _P],
+    "oracle_forward_dense": [_I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _I, _P, _P, _P],
+    "oracle_forward_tokens": [_I, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _I, _P, _P, _P, _P],
+    "oracle_backward_tokens": [_I, _P, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P],
+    "oracle_backward_expert": [_I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P],
+    "oracle_backward": [_I, _I, _I, _I, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P],
+}
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        build()
+        lib = ctypes.CDLL(_LIB)
+        for base, sig in _SIGS.items():
+            for suf in ("_bits", "_f64"):
+                f = getattr(lib, base + suf)
+                f.argtypes = sig
+                f.restype = None
+        lib.oracle_permute.argtypes = [_I, _I, _I, _P, _P, _P, _P, _P]
+        lib.oracle_permute.restype = ctypes.c_int
+        lib.oracle_permute_rows.argtypes = [_I, _I, _P, _P, _P]
+        lib.oracle_permute_rows.restype = None
+        lib.oracle_unpermute_combine.argtypes = [_I, _I, _I, _P, _P, _P, _P, _P]
+        lib.oracle_unpermute_combine.restype = None
+        _lib = lib
+    return _lib
+
+
+def _ptr(a):
+    if a is None:
+        return None
+    assert a.flags["C_CONTIGUOUS"], "oracle inputs must be C-contiguous"
+    return a.ctypes.data
+
+
+def _variant(*acts):
+    """'_bits' when the activation/weight arrays are bf16 bits, '_f64' for doubles."""
+    kinds = {a.dtype for a in acts if a is not None}
+    if kinds == {np.dtype(np.uint16)}:
+        return "_bits"
+    if kinds == {np.dtype(np.float64)}:
+        return "_f64"
+    raise TypeError("oracle inputs must be all bf16 bits (uint16) or all float64, got %s" % kinds)
+
+
+def _router_arr(a, suffix):
+    if a is None:
+        return None
+    want = np.float32 if suffix == "_bits" else np.float64
+    assert a.dtype == want, "router arrays must be %s for this variant" % np.dtype(want)
+    return np.ascontiguousarray(a)
+
+
+def _f(name, suffix):
+    return getattr(_load(), name + suffix)
+
+
+# --------------------------------------------------------------------- router
+
+def route(x, w_r, bias, k):
+    """Router: fp64 logits, softmax, top-k (ties to the lower index), renormalised weights.
+
+    Returns dict(ids [T,k] int32, w [T,k] f64, logits [T,E], probs [T,E], kgap [T], ordgap [T]).
+    """
+    T, H = x.shape
+    E = w_r.shape[1]
+    sfx = _variant(x)
+    w_r = _router_arr(w_r, sfx)
+    bias = _router_arr(bias, sfx)
+    out = dict(ids=np.empty((T, k), np.int32), w=np.empty((T, k)), logits=np.empty((T, E)),
+               probs=np.empty((T, E)), kgap=np.empty(T), ordgap=np.empty(T))
+    _f("oracle_route", sfx)(T, H, E, k, _ptr(x), _ptr(w_r), _ptr(bias), _ptr(out["logits"]),
+                            _ptr(out["probs"]), _ptr(out["ids"]), _ptr(out["w"]), _ptr(out["kgap"]),
+                            _ptr(out["ordgap"]))
+    return out
+
+
+# -------------------------------------------------------------------- permute
+
+def permute(ids, E):
+    """Per-expert counts, exclusive-scan offsets, stable row_map and src_row."""
+    ids = np.ascontiguousarray(ids, dtype=np.int32)
+    T, k = ids.shape
+    R = T * k
+    counts = np.empty(E, np.int32)
+    offsets = np.empty(E + 1, np.int32)
+    row_map = np.empty(R, np.int32)
+    src_row = np.empty(R, np.int32)
+    rc = _load().oracle_permute(T, k, E, _ptr(ids), _ptr(counts), _ptr(offsets), _ptr(row_map),
+                                _ptr(src_row))
+    if rc != 0:
+        raise ValueError("expert id out of range")
+    return dict(counts=counts, offsets=offsets, row_map=row_map, src_row=src_row)
+
+
+def permute_rows(x, src_row):
+    """x_perm[row] = x[src_row[row]] (float64)."""
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    src_row = np.ascontiguousarray(src_row, dtype=np.int32)
+    R, H = src_row.shape[0], x.shape[1]
+    out = np.empty((R, H))
+    _load().oracle_permute_rows(R, H, _ptr(x), _ptr(src_row), _ptr(out))
+    return out
+
+
+def unpermute_combine(y_perm, row_map, w, y_shared=None):
+    """y[t] = sum_j w[t,j] * y_perm[row_map[t*k+j]] (+ y_shared[t]) (float64)."""
+    y_perm = np.ascontiguousarray(y_perm, dtype=np.float64)
+    w = np.ascontiguousarray(w, dtype=np.float64)
+    row_map = np.ascontiguousarray(row_map, dtype=np.int32)
+    T, k = w.shape
+    H = y_perm.shape[1]
+    if y_shared is not None:
+        y_shared = np.ascontiguousarray(y_shared, dtype=np.float64)
+    y = np.empty((T, H))
+    _load().oracle_unpermute_combine(T, k, H, _ptr(y_perm), _ptr(row_map), _ptr(w), _ptr(y_shared),
+                                     _ptr(y))
+    return y
+
+
+# -------------------------------------------------------------------- forward
+
+def dense_ffn(x, gu, dn):
+    """A dense SwiGLU FFN on every row of x: gu [H, 2I], dn [I, H]."""
+    T, H = x.shape
+    I = dn.shape[0]
+    sfx = _variant(x, gu, dn)
+    y = np.empty((T, H))
+    _f("oracle_dense_ffn", sfx)(T, H, I, _ptr(x), _ptr(gu), _ptr(dn), _ptr(y))
+    return y
+
+
+def forward_permuted(x, gate_up, down, w, perm, k, sh_gu=None, sh_dn=None, want_intermediates=False):
+    """The permuted-form forward.  perm is the dict from ``permute``."""
+    T, H = x.shape
+    E = perm["counts"].shape[0]
+    I = down.shape[0] // E
+    R = T * k
+    I_s = sh_dn.shape[0] if sh_dn is not None else 0
+    sfx = _variant(x, gate_up, down, sh_gu, sh_dn)
+    w = np.ascontiguousarray(w, dtype=np.float64)
+    y = np.empty((T, H))
+    extra = {}
+    if want_intermediates:
+        extra = dict(gu_perm=np.empty((R, 2 * I)), h_perm=np.empty((R, I)), y_perm=np.empty((R, H)))
+        if I_s:
+            extra["y_shared"] = np.empty((T, H))
+    _f("oracle_forward_permuted", sfx)(
+        T, H, E, k, I, _ptr(x), _ptr(gate_up), _ptr(down), _ptr(w), _ptr(perm["offsets"]),
+        _ptr(perm["row_map"]), _ptr(perm["src_row"]), I_s, _ptr(sh_gu), _ptr(sh_dn),
+        _ptr(extra.get("gu_perm")), _ptr(extra.get("h_perm")), _ptr(extra.get("y_perm")),
+        _ptr(extra.get("y_shared")), _ptr(y))
+    if want_intermediates:
+        return y, extra
+    return y
+
+
+def forward_dense(x, gate_up, down, ids, w, sh_gu=None, sh_dn=None):
+    """Brute force: every expert on every token, masked by the routing."""
+    T, H = x.shape
+    k = ids.shape[1]
+    E = gate_up.shape[0] // H
+    I = down.shape[0] // E
+    I_s = sh_dn.shape[0] if sh_dn is not None else 0
+    sfx = _variant(x, gate_up, down, sh_gu, sh_dn)
+    y = np.empty((T, H))
+    _f("oracle_forward_dense", sfx)(T, H, E, k, I, _ptr(x), _ptr(gate_up), _ptr(down),
+                                    _ptr(np.ascontiguousarray(ids, np.int32)),
+                                    _ptr(np.ascontiguousarray(w, np.float64)), I_s, _ptr(sh_gu),
+                                    _ptr(sh_dn), _ptr(y))
+    return y
+
+
+def forward_tokens(tokens, x, gate_up, down, ids, w, sh_gu=None, sh_dn=None, want_f=False):
+    """The per-token definition on a token list; returns y [n, H] (and f [n, k, H])."""
+    tokens = np.ascontiguousarray(tokens, dtype=np.int64)
+    n = tokens.shape[0]
+    T, H = x.shape
+    k = ids.shape[1]
+    E = gate_up.shape[0] // H
+    I = down.shape[0] // E
+    I_s = sh_dn.shape[0] if sh_dn is not None else 0
+    sfx = _variant(x, gate_up, down, sh_gu, sh_dn)
+    y = np.empty((n, H))
+    f = np.empty((n, k, H)) if want_f else None
+    _f("oracle_forward_tokens", sfx)(n, _ptr(tokens), H, E, k, I, _ptr(x), _ptr(gate_up), _ptr(down),
+                                     _ptr(np.ascontiguousarray(ids, np.int32)),
+                                     _ptr(np.ascontiguousarray(w, np.float64)), I_s, _ptr(sh_gu),
+                                     _ptr(sh_dn), _ptr(y), _ptr(f))
+    return (y, f) if want_f else y
+
+
+# ------------------------------------------------------------------- backward
+
+def backward(x, w_r, gate_up, down, ids, w, dy, want_dw=True, want_dwr=False):
+    """Full analytic backward of L = sum <dY, y>: dict(dX, dlogits, dw, d_gate_up, d_down, d_w_r)."""
+    T, H = x.shape
+    k = ids.shape[1]
+    E = w_r.shape[1]
+    I = down.shape[0] // E
+    sfx = _variant(x, gate_up, down, dy)
+    w_r = _router_arr(w_r, sfx)
+    out = dict(dX=np.empty((T, H)), dlogits=np.empty((T, E)), dw=np.empty((T, k)))
+    if want_dw:
+        out["d_gate_up"] = np.empty((E * H, 2 * I))
+        out["d_down"] = np.empty((E * I, H))
+    if want_dwr:
+        out["d_w_r"] = np.empty((H, E))
+    _f("oracle_backward", sfx)(T, H, E, k, I, _ptr(x), _ptr(w_r), _ptr(gate_up), _ptr(down),
+                               _ptr(np.ascontiguousarray(ids, np.int32)),
+                               _ptr(np.ascontiguousarray(w, np.float64)), _ptr(dy), _ptr(out["dX"]),
+                               _ptr(out["dlogits"]), _ptr(out["dw"]), _ptr(out.get("d_gate_up")),
+                               _ptr(out.get("d_down")), _ptr(out.get("d_w_r")))
+    return out
+
+
+def backward_tokens(tokens, x, w_r, gate_up, down, ids, w, dy):
+    """dX [n, H], dlogits [n, E], dw [n, k] for a token list."""
+    tokens = np.ascontiguousarray(tokens, dtype=np.int64)
+    n = tokens.shape[0]
+    T, H = x.shape
+    k = ids.shape[1]
+    E = w_r.shape[1]
+    I = down.shape[0] // E
+    sfx = _variant(x, gate_up, down, dy)
+    w_r = _router_arr(w_r, sfx)
+    dX, dl, dw = np.empty((n, H)), np.empty((n, E)), np.empty((n, k))
+    _f("oracle_backward_tokens", sfx)(n, _ptr(tokens), H, E, k, I, _ptr(x), _ptr(w_r),
+                                      _ptr(gate_up), _ptr(down),
+                                      _ptr(np.ascontiguousarray(ids, np.int32)),
+                                      _ptr(np.ascontiguousarray(w, np.float64)), _ptr(dy), _ptr(dX),
+                                      _ptr(dl), _ptr(dw))
+    return dict(dX=dX, dlogits=dl, dw=dw)
+
+
+def backward_expert(e, x, gate_up, down, ids, w, dy):
+    """d_gate_up_e [H, 2I] and d_down_e [I, H] of one expert."""
+    T, H = x.shape
+    k = ids.shape[1]
+    E = gate_up.shape[0] // H
+    I = down.shape[0] // E
+    sfx = _variant(x, gate_up, down, dy)
+    dgu = np.empty((H, 2 * I))
+    ddn = np.empty((I, H))
+    _f("oracle_backward_expert", sfx)(int(e), T, H, k, I, _ptr(x), _ptr(gate_up), _ptr(down),
+                                      _ptr(np.ascontiguousarray(ids, np.int32)),
+                                      _ptr(np.ascontiguousarray(w, np.float64)), _ptr(dy), _ptr(dgu),
+                                      _ptr(ddn))
+    return dgu, ddn
+
+
+# --------------------------------------------------------------- whole layer
+
+def layer_forward(inp, want_intermediates=False):
+    """Route -> permute -> experts -> combine on a synth.MoEInputs (full size)."""
+    cfg = inp.cfg
+    r = route(inp.x, inp.w_router, inp.bias, cfg.k)
+    perm = permute(r["ids"], cfg.E)
+    res = forward_permuted(inp.x, inp.gate_up, inp.down, r["w"], perm, cfg.k, inp.sh_gate_up,
+                           inp.sh_down, want_intermediates=want_intermediates)
+    if want_intermediates:
+        y, extra = res
+    else:
+        y, extra = res, {}
+    return dict(route=r, perm=perm, y=y, **extra)
