@@ -1,0 +1,178 @@
+"""GPU parity of the grouped GEMMs and the whole layer, forward and backward,
+against the fp64 oracle (through the C ABI).
+
+Small cases are compared element by element; they span several 128-row and
+256-column tiles, ragged expert tails, empty experts, and partial column
+tiles.  The named workloads (Qwen3-MoE shape, skewed routing, the training
+step, DeepSeek-V3 shape) run at full size in the launch configuration the
+benchmark times and are compared on seeded token / expert samples the oracle
+computes one by one; their integer outputs are compared in full.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from gpu_helpers import bf, f32, f64, i32, lib, npi
+from parity import assert_close, compare_ids, sample_tokens
+
+pytestmark = pytest.mark.gpu
+
+SMALL = [
+    # T, H, E, k, I
+    (64, 128, 8, 2, 64),        # the tiny workload's shapes
+    (200, 128, 8, 2, 128),      # ragged expert tails
+    (512, 256, 16, 4, 192),     # I = 192: a partial gate/up column tile
+    (300, 384, 6, 3, 320),      # H = 384: a partial 256-column output tile
+    (50, 128, 64, 1, 64),       # mostly empty experts
+    (1100, 256, 4, 2, 128),     # experts with several 128-row tiles
+]
+
+
+def _inputs(T, H, E, k, I, seed, **kw):
+    cfg = synth.MoEConfig("c", T=T, H=H, E=E, k=k, I=I, seed=seed, **kw)
+    return cfg, synth.make_inputs(cfg, with_dy=True)
+
+
+def _forward(moe, inp, save=False):
+    x, wr = bf(inp.x), f32(inp.w_router)
+    gu, dn = bf(inp.gate_up), bf(inp.down)
+    bias = f32(inp.bias) if inp.bias is not None else None
+    sgu = bf(inp.sh_gate_up) if inp.sh_gate_up is not None else None
+    sdn = bf(inp.sh_down) if inp.sh_down is not None else None
+    y, st = moe.moe_forward(x, wr, gu, dn, inp.cfg.k, bias, sgu, sdn, save_for_backward=save)
+    moe.sync_status()
+    return (x, wr, gu, dn), y, st
+
+
+@pytest.mark.parametrize("T,H,E,k,I", SMALL)
+def test_forward_elementwise(T, H, E, k, I):
+    moe = lib()
+    cfg, inp = _inputs(T, H, E, k, I, seed=T + H + I)
+    _, y, st = _forward(moe, inp, save=True)
+    ref = oracle.layer_forward(inp, want_intermediates=True)
+    same, tol = compare_ids(npi(st.ids), ref["route"])
+    assert tol == 0 and same.all()
+    for key in ("counts", "offsets", "row_map", "src_row"):
+        np.testing.assert_array_equal(npi(getattr(st, key)), ref["perm"][key], err_msg=key)
+    assert_close("gu_pre", f64(st.gu_pre), ref["gu_perm"])
+    assert_close("h", f64(st.h), ref["h_perm"])
+    assert_close("y_perm", f64(st.y_perm), ref["y_perm"])
+    assert_close("y", f64(y), ref["y"])
+
+
+@pytest.mark.parametrize("T,H,I", [(256, 128, 64), (300, 256, 192), (129, 512, 1024)])
+def test_dense_mode_is_one_swiglu_ffn(T, H, I):
+    """src_row = offsets = NULL, E = 1: the shared-expert (dense) mode."""
+    moe = lib()
+    x = synth.normal_bf16(T, synth.TID_X, (T, H), 1.0)
+    gu = synth.normal_bf16(T, synth.TID_SH_GATE_UP, (H, 2 * I), H ** -0.5)
+    dn = synth.normal_bf16(T, synth.TID_SH_DOWN, (I, H), I ** -0.5)
+    h, _ = moe.grouped_gemm_gate_up_swiglu(bf(x), None, None, bf(gu), I)
+    y = moe.grouped_gemm_down(h, None, bf(dn), H)
+    moe.sync_status()
+    assert_close("dense ffn", f64(y), oracle.dense_ffn(x, gu, dn))
+
+
+def test_shared_expert_layer():
+    moe = lib()
+    cfg, inp = _inputs(300, 256, 8, 2, 128, seed=21, I_shared=256)
+    _, y, st = _forward(moe, inp)
+    ref = oracle.layer_forward(inp)
+    same, tol = compare_ids(npi(st.ids), ref["route"])
+    assert tol == 0
+    assert_close("y", f64(y), ref["y"])
+
+
+@pytest.mark.parametrize("T,H,E,k,I", SMALL)
+def test_backward_elementwise(T, H, E, k, I):
+    moe = lib()
+    cfg, inp = _inputs(T, H, E, k, I, seed=3 * T + I)
+    (x, wr, gu, dn), y, st = _forward(moe, inp, save=True)
+    g = moe.moe_backward(bf(inp.dy), st, wr, gu, dn, want_dw_router=True)
+    moe.sync_status()
+    r = oracle.route(inp.x, inp.w_router, None, k)
+    same, tol = compare_ids(npi(st.ids), r)
+    assert tol == 0 and same.all()
+    b = oracle.backward(inp.x, inp.w_router, inp.gate_up, inp.down, r["ids"], r["w"], inp.dy,
+                        want_dw=True, want_dwr=True)
+    assert_close("dw", f64(g["dw"]), b["dw"])
+    assert_close("d_logits", f64(g["d_logits"]), b["dlogits"])
+    assert_close("dX", f64(g["dx"]), b["dX"])
+    assert_close("d_gate_up", f64(g["d_gate_up"]), b["d_gate_up"])
+    assert_close("d_down", f64(g["d_down"]), b["d_down"])
+    assert_close("d_w_router", f64(g["d_w_router"]), b["d_w_r"])
+
+
+def test_backward_empty_experts_get_zero_weight_grads():
+    moe = lib()
+    cfg, inp = _inputs(40, 128, 32, 1, 64, seed=5)
+    (x, wr, gu, dn), y, st = _forward(moe, inp, save=True)
+    g = moe.moe_backward(bf(inp.dy), st, wr, gu, dn)
+    moe.sync_status()
+    counts = npi(st.counts)
+    empty = np.nonzero(counts == 0)[0]
+    assert empty.size > 0
+    dgu = f64(g["d_gate_up"]).reshape(32, 128, 128)
+    ddn = f64(g["d_down"]).reshape(32, 64, 128)
+    assert not dgu[empty].any() and not ddn[empty].any()
+
+
+def _sampled_forward_check(cfg_name, n_tokens=192):
+    moe = lib()
+    cfg = synth.CONFIGS[cfg_name]
+    inp = synth.make_inputs(cfg)
+    _, y, st = _forward(moe, inp)
+    r = oracle.route(inp.x, inp.w_router, inp.bias, cfg.k)
+    same, tol = compare_ids(npi(st.ids), r)
+    assert tol <= 2
+    if same.all():
+        perm = oracle.permute(r["ids"], cfg.E)
+        for key in ("counts", "offsets", "row_map", "src_row"):
+            np.testing.assert_array_equal(npi(getattr(st, key)), perm[key], err_msg=key)
+    tok = sample_tokens(cfg.T, n_tokens, cfg.seed)
+    tok = tok[same[tok]]
+    yref = oracle.forward_tokens(tok, inp.x, inp.gate_up, inp.down, r["ids"], r["w"], inp.sh_gate_up,
+                                 inp.sh_down)
+    assert_close("y[sample]", f64(y)[tok], yref)
+    return st
+
+
+def test_qwen3_moe_forward_sampled():
+    _sampled_forward_check("qwen3_moe")
+
+
+def test_skewed_routing_forward_sampled():
+    st = _sampled_forward_check("qwen3_moe_skewed")
+    counts = npi(st.counts)
+    assert (counts == 0).sum() >= 8
+
+
+def test_deepseek_v3_forward_sampled():
+    _sampled_forward_check("deepseek_v3", n_tokens=96)
+
+
+def test_training_step_backward_sampled():
+    moe = lib()
+    cfg = synth.CONFIGS["qwen3_moe_train"]
+    inp = synth.make_inputs(cfg)
+    (x, wr, gu, dn), y, st = _forward(moe, inp, save=True)
+    g = moe.moe_backward(bf(inp.dy), st, wr, gu, dn)
+    moe.sync_status()
+    r = oracle.route(inp.x, inp.w_router, None, cfg.k)
+    same, tol = compare_ids(npi(st.ids), r)
+    assert tol <= 2
+    tok = sample_tokens(cfg.T, 96, 33)
+    tok = tok[same[tok]]
+    b = oracle.backward_tokens(tok, inp.x, inp.w_router, inp.gate_up, inp.down, r["ids"], r["w"], inp.dy)
+    assert_close("dX[sample]", f64(g["dx"])[tok], b["dX"])
+    assert_close("d_logits[sample]", f64(g["d_logits"])[tok], b["dlogits"])
+    assert_close("dw[sample]", f64(g["dw"])[tok], b["dw"])
+    if same.all():
+        H, I = cfg.H, cfg.I
+        dgu = g["d_gate_up"]
+        ddn = g["d_down"]
+        for e in (0, 77, 127):
+            rgu, rdn = oracle.backward_expert(e, inp.x, inp.gate_up, inp.down, r["ids"], r["w"], inp.dy)
+            assert_close("d_gate_up[%d]" % e, f64(dgu[e * H:(e + 1) * H]), rgu)
+            assert_close("d_down[%d]" % e, f64(ddn[e * I:(e + 1) * I]), rdn)

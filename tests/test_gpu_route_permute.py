@@ -1,0 +1,122 @@
+"""GPU parity of the router, the permutation and the combine (through the C ABI)."""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from gpu_helpers import bf, f32, f64, i32, lib, npi
+from parity import assert_close, compare_ids
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("T,H,E,k", [(64, 128, 8, 2), (1, 64, 4, 1), (333, 256, 16, 4), (1000, 512, 128, 8),
+                                     (97, 128, 200, 8), (50, 64, 32, 32), (40, 96, 1024, 6)])
+def test_route_matches_oracle(T, H, E, k):
+    moe = lib()
+    cfg = synth.MoEConfig("r", T=T, H=H, E=E, k=k, I=64, seed=T + E)
+    inp = synth.make_inputs(cfg, weights=False)
+    ids, w, logits = moe.route(bf(inp.x), f32(inp.w_router), k, return_logits=True)
+    moe.sync_status()
+    ref = oracle.route(inp.x, inp.w_router, None, k)
+    same, tolerated = compare_ids(npi(ids), ref)
+    assert tolerated <= max(1, T // 1000)
+    assert_close("logits", f64(logits), ref["logits"])
+    assert_close("w", f64(w)[same], ref["w"][same])
+    np.testing.assert_allclose(f64(w).sum(1), 1.0, atol=1e-5)
+
+
+def test_route_bias_and_skewed_workload():
+    moe = lib()
+    cfg = synth.CONFIGS["qwen3_moe_skewed"]
+    inp = synth.make_inputs(cfg, weights=False)
+    ids, w = moe.route(bf(inp.x), f32(inp.w_router), cfg.k, f32(inp.bias))
+    moe.sync_status()
+    ref = oracle.route(inp.x, inp.w_router, inp.bias, cfg.k)
+    same, tolerated = compare_ids(npi(ids), ref)
+    assert tolerated <= 2
+    assert_close("w", f64(w)[same], ref["w"][same])
+    counts = np.bincount(npi(ids).reshape(-1), minlength=cfg.E)
+    assert (counts == 0).sum() >= 8 and counts.max() > 0.10 * cfg.R   # hotspot + empty experts
+
+
+def test_route_exact_ties_lower_index_first():
+    """Duplicate router columns give bit-identical fp32 logits on the GPU: the
+    lower expert index must come first, and at the k boundary only it is kept."""
+    moe = lib()
+    T, H, E = 64, 128, 16
+    rng = np.random.default_rng(0)
+    xa = np.abs(synth.bf16_to_f32(synth.normal_bf16(3, synth.TID_X, (T, H), 1.0)))
+    x = np.ascontiguousarray((xa.view(np.uint32) >> 16).astype(np.uint16))   # |x|, exact in bf16
+    wr = (rng.standard_normal((H, E)) * 0.01).astype(np.float32)
+    wr[:, 3] = 0.2     # experts 3 and 9 tie exactly and lead every token
+    wr[:, 9] = 0.2
+    wr[:, 12] = 0.1    # third
+    for k, want in ((1, [3]), (2, [3, 9]), (3, [3, 9, 12])):
+        ids, w = moe.route(bf(x), f32(wr), k)
+        got = npi(ids)
+        for t in range(T):
+            assert got[t].tolist() == want
+        if k >= 2:
+            np.testing.assert_array_equal(npi(w)[:, 0], npi(w)[:, 1])
+
+
+@pytest.mark.parametrize("T,k,E,kind", [(64, 2, 8, "distinct"), (1, 1, 1, "distinct"), (4096, 8, 128, "distinct"),
+                                        (5000, 3, 7, "uniform"), (777, 8, 1024, "distinct"),
+                                        (16384, 8, 256, "distinct"), (3000, 4, 64, "sparse")])
+def test_permute_bit_exact(T, k, E, kind):
+    moe = lib()
+    if kind == "distinct":
+        ids = synth.distinct_ids(T + k, synth.TID_IDS, T, k, E)
+    elif kind == "uniform":
+        ids = synth.uniform_ints(T, synth.TID_IDS, T * k, E).reshape(T, k)
+    else:  # only a few experts used: many empty experts
+        ids = (synth.uniform_ints(T, synth.TID_IDS, T * k, 5) * 7).astype(np.int32).reshape(T, k)
+    counts, offsets, row_map, src_row = moe.permute(i32(ids), E)
+    moe.sync_status()
+    ref = oracle.permute(ids, E)
+    np.testing.assert_array_equal(npi(counts), ref["counts"])
+    np.testing.assert_array_equal(npi(offsets), ref["offsets"])
+    np.testing.assert_array_equal(npi(row_map), ref["row_map"])
+    np.testing.assert_array_equal(npi(src_row), ref["src_row"])
+
+
+def test_permute_rejects_out_of_range_id_on_device():
+    moe = lib()
+    ids = np.array([[0, 1], [2, 9]], dtype=np.int32)
+    moe.permute(i32(ids), 4)
+    with pytest.raises(moe.MoEError) as ei:
+        moe.sync_status()
+    assert ei.value.status == 6   # MOE_ERR_DEVICE
+    moe.sync_status()             # the status word was cleared
+
+
+@pytest.mark.parametrize("T,H,k,shared", [(64, 128, 2, False), (300, 256, 8, True), (1, 64, 1, False),
+                                          (1000, 2048, 8, False)])
+def test_combine_matches_oracle(T, H, k, shared):
+    moe = lib()
+    R = T * k
+    yp_bits = synth.normal_bf16(5, 50, (R, H), 1.0)
+    ys_bits = synth.normal_bf16(5, 51, (T, H), 1.0) if shared else None
+    E = max(k, 16)
+    ids = synth.distinct_ids(5, synth.TID_IDS, T, k, E)
+    perm = oracle.permute(ids, E)
+    _, _, row_map, _ = moe.permute(i32(ids), E)      # the GPU path's own permutation
+    w = np.random.default_rng(T).uniform(0.05, 1.0, (T, k)).astype(np.float32)
+    y = moe.unpermute_combine(bf(yp_bits), row_map, f32(w), bf(ys_bits) if shared else None)
+    moe.sync_status()
+    ref = oracle.unpermute_combine(synth.bf16_to_f32(yp_bits).astype(np.float64), perm["row_map"],
+                                   w.astype(np.float64),
+                                   synth.bf16_to_f32(ys_bits).astype(np.float64) if shared else None)
+    assert_close("y", f64(y), ref)
+
+
+def test_permute_rows_gathers():
+    moe = lib()
+    T, k, E, H = 100, 4, 8, 256
+    ids = synth.distinct_ids(9, synth.TID_IDS, T, k, E)
+    perm = oracle.permute(ids, E)
+    _, _, _, src_row = moe.permute(i32(ids), E)
+    x = synth.normal_bf16(9, synth.TID_X, (T, H), 1.0)
+    xp = moe.permute_rows(bf(x), src_row)
+    np.testing.assert_array_equal(npi(xp.view(__import__("torch").int16)).view(np.uint16), x[perm["src_row"]])

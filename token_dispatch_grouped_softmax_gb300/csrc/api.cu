@@ -1,0 +1,322 @@
+// C ABI of libmoe_gb300.so (declared in include/moe_gb300.h): argument
+// validation on the host, then the launches.  Nothing here allocates device
+// memory; every buffer is the caller's.
+#include <mutex>
+
+#include "../../include/moe_gb300.h"
+#include "kernels.h"
+
+namespace moe {
+
+__device__ uint32_t g_status_word;   // first device-side error (see common.cuh)
+
+namespace {
+
+std::mutex g_mu;
+DeviceInfo g_dev[kMaxDevices];
+bool g_dev_ready[kMaxDevices] = {false};
+uint64_t g_wait_limit_ns = 2000000000ull;
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+// Device information of the current device, set up on first use.
+int current_device(DeviceInfo* out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return MOE_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (!g_dev_ready[dev]) {
+    DeviceInfo d;
+    d.ordinal = dev;
+    if (cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    void* addr = nullptr;
+    if (cudaGetSymbolAddress(&addr, g_status_word) != cudaSuccess) return MOE_ERR_CUDA;
+    d.status = static_cast<uint32_t*>(addr);
+    g_dev[dev] = d;
+    g_dev_ready[dev] = true;
+  }
+  *out = g_dev[dev];
+  out->wait_limit_ns = g_wait_limit_ns;
+  return MOE_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int cuda_status(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+int gemm_status(int rc) { return rc == 0 ? MOE_OK : (rc < 0 ? MOE_ERR_UNSUPPORTED : MOE_ERR_CUDA); }
+
+constexpr int64_t kMaxI32 = 2147483647;
+
+}  // namespace
+
+bool encode_tensor_map_2d_bf16(CUtensorMap* map, const void* base, const cuuint64_t* dims,
+                               const cuuint64_t* strides, const cuuint32_t* box,
+                               const cuuint32_t* estr) {
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (!g_encode) {
+      void* fn = nullptr;
+      cudaDriverEntryPointQueryResult q;
+      if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                           &q) != cudaSuccess ||
+          q != cudaDriverEntryPointSuccess || !fn)
+        return false;
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+  }
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
+                        strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+}  // namespace moe
+
+using moe::aligned16;
+using moe::cuda_status;
+using moe::kMaxI32;
+
+extern "C" {
+
+int moe_version(void) { return 10000; }
+
+const char* moe_error_string(int status) {
+  switch (status) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "unsupported shape or alignment";
+    case MOE_ERR_CUDA: return "CUDA error";
+    case MOE_ERR_TIMEOUT: return "device-side wait timed out";
+    case MOE_ERR_WORKSPACE: return "workspace missing or too small";
+    case MOE_ERR_DEVICE: return "device-side check failed";
+    default: return "unknown status";
+  }
+}
+
+int moe_set_wait_limit_ns(uint64_t ns) {
+  moe::g_wait_limit_ns = ns ? ns : 2000000000ull;
+  return MOE_OK;
+}
+
+int moe_sync_status(void* stream, uint32_t* detail) {
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return MOE_ERR_CUDA;
+  uint32_t v = 0;
+  if (cudaMemcpyFromSymbol(&v, moe::g_status_word, sizeof(v)) != cudaSuccess) return MOE_ERR_CUDA;
+  if (v != 0) {
+    const uint32_t zero = 0;
+    if (cudaMemcpyToSymbol(moe::g_status_word, &zero, sizeof(zero)) != cudaSuccess) return MOE_ERR_CUDA;
+  }
+  if (detail) *detail = v;
+  if (v == 0) return MOE_OK;
+  return (v & 0xFFu) == moe::kStatusTimeout ? MOE_ERR_TIMEOUT : MOE_ERR_DEVICE;
+}
+
+/* ------------------------------------------------------------------ route */
+
+int moe_route_workspace_size(int64_t T, int64_t E, int has_logits_out, size_t* bytes) {
+  if (!bytes || T < 0 || E < 1) return MOE_ERR_INVALID_ARG;
+  *bytes = has_logits_out ? 0 : (size_t)(T * E * (int64_t)sizeof(float));
+  return MOE_OK;
+}
+
+int moe_route(const uint16_t* x, const float* w_router, const float* bias, int64_t T, int64_t H,
+              int64_t E, int64_t k, int32_t* ids, float* w, float* logits, void* workspace,
+              size_t workspace_bytes, void* stream) {
+  if (T < 0 || H < 1 || E < 1 || k < 1 || k > E || T > kMaxI32 || T * k > kMaxI32)
+    return MOE_ERR_INVALID_ARG;
+  if (T > 0 && (!x || !w_router || !ids || !w)) return MOE_ERR_INVALID_ARG;
+  if (E > moe::kMaxExperts || k > 32 || H % 8 != 0) return MOE_ERR_UNSUPPORTED;
+  if ((x && !aligned16(x)) || (w_router && !aligned16(w_router))) return MOE_ERR_INVALID_ARG;
+  float* lg = logits;
+  if (!lg) {
+    if (T > 0 && (!workspace || workspace_bytes < (size_t)(T * E * 4))) return MOE_ERR_WORKSPACE;
+    lg = static_cast<float*>(workspace);
+  }
+  if (T == 0) return MOE_OK;
+  return cuda_status(moe::launch_route(x, w_router, bias, T, H, E, k, ids, w, lg,
+                                       static_cast<cudaStream_t>(stream)));
+}
+
+/* ---------------------------------------------------------------- permute */
+
+int moe_permute_workspace_size(int64_t T, int64_t k, int64_t E, size_t* bytes) {
+  if (!bytes || T < 0 || k < 1 || E < 1) return MOE_ERR_INVALID_ARG;
+  *bytes = moe::permute_workspace_bytes(T * k, E);
+  return MOE_OK;
+}
+
+int moe_permute(const int32_t* ids, int64_t T, int64_t k, int64_t E, int32_t* counts,
+                int32_t* offsets, int32_t* row_map, int32_t* src_row, void* workspace,
+                size_t workspace_bytes, void* stream) {
+  if (T < 0 || k < 1 || E < 1 || T * k > kMaxI32) return MOE_ERR_INVALID_ARG;
+  if (!counts || !offsets || (T > 0 && (!ids || !row_map || !src_row))) return MOE_ERR_INVALID_ARG;
+  if (E > moe::kMaxExperts) return MOE_ERR_UNSUPPORTED;
+  if (!workspace || workspace_bytes < moe::permute_workspace_bytes(T * k, E)) return MOE_ERR_WORKSPACE;
+  moe::DeviceInfo dev;
+  int rc = moe::current_device(&dev);
+  if (rc != MOE_OK) return rc;
+  return cuda_status(moe::launch_permute(ids, T, k, E, counts, offsets, row_map, src_row, workspace,
+                                         dev.status, static_cast<cudaStream_t>(stream)));
+}
+
+int moe_permute_rows(const uint16_t* x, const int32_t* src_row, int64_t R, int64_t H,
+                     uint16_t* x_perm, void* stream) {
+  if (R < 0 || H < 1 || R > kMaxI32) return MOE_ERR_INVALID_ARG;
+  if (R > 0 && (!x || !src_row || !x_perm)) return MOE_ERR_INVALID_ARG;
+  if (H % 8 != 0) return MOE_ERR_UNSUPPORTED;
+  if (R > 0 && (!aligned16(x) || !aligned16(x_perm))) return MOE_ERR_INVALID_ARG;
+  return cuda_status(moe::launch_permute_rows(x, src_row, R, H, x_perm, static_cast<cudaStream_t>(stream)));
+}
+
+/* ----------------------------------------------------------- grouped GEMMs */
+
+static int gemm_shape_check(int64_t R, int64_t H, int64_t E, int64_t I) {
+  if (R < 0 || H < 1 || E < 1 || I < 1 || R > kMaxI32) return MOE_ERR_INVALID_ARG;
+  if (H % 64 != 0 || I % 64 != 0 || E > moe::kMaxExperts) return MOE_ERR_UNSUPPORTED;
+  if (E * H > kMaxI32 || E * I > kMaxI32) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
+int moe_grouped_gemm_gate_up_swiglu(const uint16_t* x, const int32_t* src_row,
+                                    const int32_t* offsets, const uint16_t* gate_up, int64_t T,
+                                    int64_t R, int64_t H, int64_t E, int64_t I, uint16_t* h,
+                                    uint16_t* gu_pre, void* stream) {
+  int rc = gemm_shape_check(R, H, E, I);
+  if (rc != MOE_OK) return rc;
+  if (T < 0 || T > kMaxI32) return MOE_ERR_INVALID_ARG;
+  if (!offsets && E != 1) return MOE_ERR_INVALID_ARG;
+  if (!src_row && T < R) return MOE_ERR_INVALID_ARG;
+  if (R == 0) return MOE_OK;
+  if (!x || !gate_up || !h || T < 1) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(gate_up) || !aligned16(h) || (gu_pre && !aligned16(gu_pre)))
+    return MOE_ERR_INVALID_ARG;
+  moe::DeviceInfo dev;
+  if ((rc = moe::current_device(&dev)) != MOE_OK) return rc;
+  return moe::gemm_status(moe::launch_gemm_gate_up(x, src_row, offsets, gate_up, T, R, H, E, I, h,
+                                                   gu_pre, dev, static_cast<cudaStream_t>(stream)));
+}
+
+int moe_grouped_gemm_down(const uint16_t* h, const int32_t* offsets, const uint16_t* down, int64_t R,
+                          int64_t H, int64_t E, int64_t I, uint16_t* y_perm, void* stream) {
+  int rc = gemm_shape_check(R, H, E, I);
+  if (rc != MOE_OK) return rc;
+  if (!offsets && E != 1) return MOE_ERR_INVALID_ARG;
+  if (R == 0) return MOE_OK;
+  if (!h || !down || !y_perm) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(h) || !aligned16(down) || !aligned16(y_perm)) return MOE_ERR_INVALID_ARG;
+  moe::DeviceInfo dev;
+  if ((rc = moe::current_device(&dev)) != MOE_OK) return rc;
+  return moe::gemm_status(moe::launch_gemm_down(h, offsets, down, R, H, E, I, y_perm, dev,
+                                                static_cast<cudaStream_t>(stream)));
+}
+
+/* ---------------------------------------------------------------- combine */
+
+int moe_unpermute_combine(const uint16_t* y_perm, const int32_t* row_map, const float* w,
+                          const uint16_t* y_shared, int64_t T, int64_t H, int64_t k, uint16_t* y,
+                          void* stream) {
+  if (T < 0 || H < 1 || k < 1 || T > kMaxI32 || T * k > kMaxI32) return MOE_ERR_INVALID_ARG;
+  if (k > 32 || H % 8 != 0) return MOE_ERR_UNSUPPORTED;
+  if (T == 0) return MOE_OK;
+  if (!y_perm || !row_map || !w || !y) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(y_perm) || !aligned16(y) || (y_shared && !aligned16(y_shared))) return MOE_ERR_INVALID_ARG;
+  return cuda_status(moe::launch_combine(y_perm, row_map, w, y_shared, T, H, k, y,
+                                         static_cast<cudaStream_t>(stream)));
+}
+
+/* --------------------------------------------------------------- backward */
+
+int moe_unpermute_combine_bwd(const uint16_t* dy, const uint16_t* y_perm, const int32_t* row_map,
+                              const float* w, int64_t T, int64_t H, int64_t k, uint16_t* dy_perm,
+                              float* dw, void* stream) {
+  if (T < 0 || H < 1 || k < 1 || T > kMaxI32 || T * k > kMaxI32) return MOE_ERR_INVALID_ARG;
+  if (k > 32 || H % 8 != 0) return MOE_ERR_UNSUPPORTED;
+  if (T == 0) return MOE_OK;
+  if (!dy || !y_perm || !row_map || !w || !dy_perm || !dw) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(dy) || !aligned16(y_perm) || !aligned16(dy_perm)) return MOE_ERR_INVALID_ARG;
+  return cuda_status(moe::launch_combine_bwd(dy, y_perm, row_map, w, T, H, k, dy_perm, dw,
+                                             static_cast<cudaStream_t>(stream)));
+}
+
+int moe_route_bwd(const float* dw, const float* w, const int32_t* ids, int64_t T, int64_t E,
+                  int64_t k, float* d_logits, void* stream) {
+  if (T < 0 || E < 1 || k < 1 || k > E || T > kMaxI32 || T * k > kMaxI32) return MOE_ERR_INVALID_ARG;
+  if (k > 32) return MOE_ERR_UNSUPPORTED;
+  if (T == 0) return MOE_OK;
+  if (!dw || !w || !ids || !d_logits) return MOE_ERR_INVALID_ARG;
+  return cuda_status(moe::launch_route_bwd(dw, w, ids, T, E, k, d_logits, static_cast<cudaStream_t>(stream)));
+}
+
+int moe_grouped_gemm_down_bwd(const uint16_t* dy_perm, const uint16_t* h, const uint16_t* gu_pre,
+                              const int32_t* offsets, const uint16_t* down, int64_t R, int64_t H,
+                              int64_t E, int64_t I, uint16_t* dgu, uint16_t* d_down, void* stream) {
+  int rc = gemm_shape_check(R, H, E, I);
+  if (rc != MOE_OK) return rc;
+  if (!offsets && E != 1) return MOE_ERR_INVALID_ARG;
+  if (!down || !d_down || (R > 0 && (!dy_perm || !h || !gu_pre || !dgu))) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(down) || !aligned16(d_down) ||
+      (R > 0 && (!aligned16(dy_perm) || !aligned16(h) || !aligned16(gu_pre) || !aligned16(dgu))))
+    return MOE_ERR_INVALID_ARG;
+  if (R == 0) return cuda_status(cudaMemsetAsync(d_down, 0, (size_t)(E * I * H * 2), static_cast<cudaStream_t>(stream)));
+  moe::DeviceInfo dev;
+  if ((rc = moe::current_device(&dev)) != MOE_OK) return rc;
+  return moe::gemm_status(moe::launch_gemm_down_bwd(dy_perm, h, gu_pre, offsets, down, R, H, E, I,
+                                                    dgu, d_down, dev, static_cast<cudaStream_t>(stream)));
+}
+
+int moe_grouped_gemm_gate_up_bwd(const uint16_t* dgu, const uint16_t* x, const int32_t* src_row,
+                                 const int32_t* offsets, const uint16_t* gate_up, int64_t T,
+                                 int64_t R, int64_t H, int64_t E, int64_t I, uint16_t* dx_perm,
+                                 uint16_t* d_gate_up, void* stream) {
+  int rc = gemm_shape_check(R, H, E, I);
+  if (rc != MOE_OK) return rc;
+  if (T < 0 || T > kMaxI32) return MOE_ERR_INVALID_ARG;
+  if (!offsets && E != 1) return MOE_ERR_INVALID_ARG;
+  if (!src_row && T < R) return MOE_ERR_INVALID_ARG;
+  if (!gate_up || !d_gate_up || (R > 0 && (!dgu || !x || !dx_perm))) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(gate_up) || !aligned16(d_gate_up) ||
+      (R > 0 && (!aligned16(dgu) || !aligned16(x) || !aligned16(dx_perm))))
+    return MOE_ERR_INVALID_ARG;
+  if (R == 0)
+    return cuda_status(cudaMemsetAsync(d_gate_up, 0, (size_t)(E * H * 2 * I * 2), static_cast<cudaStream_t>(stream)));
+  moe::DeviceInfo dev;
+  if ((rc = moe::current_device(&dev)) != MOE_OK) return rc;
+  return moe::gemm_status(moe::launch_gemm_gate_up_bwd(dgu, x, src_row, offsets, gate_up, T, R, H, E,
+                                                       I, dx_perm, d_gate_up, dev,
+                                                       static_cast<cudaStream_t>(stream)));
+}
+
+int moe_gather_dx_workspace_size(int64_t H, int64_t E, size_t* bytes) {
+  if (!bytes || H < 1 || E < 1) return MOE_ERR_INVALID_ARG;
+  *bytes = moe::gather_dx_workspace_bytes(H, E);
+  return MOE_OK;
+}
+
+int moe_gather_dx(const uint16_t* dx_perm, const int32_t* row_map, const float* d_logits,
+                  const int32_t* ids, const float* w_router, int64_t T, int64_t H, int64_t E,
+                  int64_t k, uint16_t* dx, void* workspace, size_t workspace_bytes, void* stream) {
+  if (T < 0 || H < 1 || E < 1 || k < 1 || k > E || T > kMaxI32 || T * k > kMaxI32)
+    return MOE_ERR_INVALID_ARG;
+  if (k > 32 || H % 8 != 0) return MOE_ERR_UNSUPPORTED;
+  if ((d_logits == nullptr) != (w_router == nullptr)) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  if (!dx_perm || !row_map || !dx || (d_logits && !ids)) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(dx_perm) || !aligned16(dx)) return MOE_ERR_INVALID_ARG;
+  if (d_logits && (!workspace || !aligned16(workspace) ||
+                   workspace_bytes < moe::gather_dx_workspace_bytes(H, E)))
+    return MOE_ERR_WORKSPACE;
+  return cuda_status(moe::launch_gather_dx(dx_perm, row_map, d_logits, ids, w_router, T, H, E, k, dx,
+                                           workspace, static_cast<cudaStream_t>(stream)));
+}
+
+int moe_route_bwd_weight(const uint16_t* x, const float* d_logits, int64_t T, int64_t H, int64_t E,
+                         float* d_w_router, void* stream) {
+  if (T < 0 || H < 1 || E < 1 || T > kMaxI32) return MOE_ERR_INVALID_ARG;
+  if (!d_w_router || (T > 0 && (!x || !d_logits))) return MOE_ERR_INVALID_ARG;
+  return cuda_status(moe::launch_route_bwd_weight(x, d_logits, T, H, E, d_w_router,
+                                                  static_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

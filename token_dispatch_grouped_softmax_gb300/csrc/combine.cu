@@ -1,0 +1,289 @@
+// Unpermute with the gate-weighted combine and the token-side backward steps.
+//
+// Forward ("Awesome-ML-SYS-Tutorial" MoE/EP guide, gsyq.cn, "Expert
+// Parallelism": the experts' outputs summed with the gate weights;
+// "InternVL3.5 接入 pure FSDP2 后端开发实践" §8.3: unpermute):
+//   y[t] = sum_{j<k} w[t,j] * y_perm[row_map[t*k+j]]  (+ y_shared[t])
+// One warp per token; each lane owns 16-byte (8 x bf16) column chunks and
+// accumulates in fp32 in increasing j, so the result does not depend on the
+// launch shape (a gather, not a scatter-add: deterministic).
+//
+// Backward (the gradient of the same expression, experts held fixed):
+//   combine_bwd   dy_perm[row_map[t*k+j]] = w[t,j] * dY[t];
+//                 dw[t,j] = <dY[t], y_perm[row]>   (warp-shuffle reduction)
+//   route_bwd     d_logits[t, ids_j] = w_j (dw_j - sum_i w_i dw_i), 0 elsewhere
+//   gather_dx     dX[t] = sum_j dx_perm[row_map[t*k+j]]
+//                         + sum_j d_logits[t, ids_j] * W_r[:, ids_j]
+//                 (W_r read through a transposed copy [E, H] so the router
+//                 term streams contiguous rows)
+//   route_bwd_weight  d_W_r = x^T . d_logits (fp32 register-tiled GEMM)
+#include "kernels.h"
+
+namespace moe {
+
+namespace {
+
+constexpr int kWarpsPerBlock = 8;
+
+__global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict__ y_perm,
+                                                      const int32_t* __restrict__ row_map,
+                                                      const float* __restrict__ w,
+                                                      const uint16_t* __restrict__ y_shared,
+                                                      int T, int H, int k,
+                                                      uint16_t* __restrict__ y) {
+  const int lane = threadIdx.x & 31;
+  const int t = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
+  if (t >= T) return;
+  int my_row = 0;
+  float my_w = 0.f;
+  if (lane < k) {
+    my_row = row_map[(int64_t)t * k + lane];
+    my_w = w[(int64_t)t * k + lane];
+  }
+  const int nch = H / 8;
+  for (int c = lane; c < nch; c += 32) {
+    float acc[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) acc[q] = 0.f;
+#pragma unroll 8
+    for (int j = 0; j < k; ++j) {
+      const int row = __shfl_sync(0xffffffffu, my_row, j);
+      const float wj = __shfl_sync(0xffffffffu, my_w, j);
+      const uint4 v = __ldg(reinterpret_cast<const uint4*>(y_perm + (int64_t)row * H) + c);
+      float f[8];
+      unpack8(v, f);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) acc[q] = fmaf(wj, f[q], acc[q]);
+    }
+    if (y_shared) {
+      const uint4 v = __ldg(reinterpret_cast<const uint4*>(y_shared + (int64_t)t * H) + c);
+      float f[8];
+      unpack8(v, f);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) acc[q] += f[q];
+    }
+    reinterpret_cast<uint4*>(y + (int64_t)t * H)[c] = pack8(acc);
+  }
+}
+
+__global__ void __launch_bounds__(256) combine_bwd_kernel(const uint16_t* __restrict__ dy,
+                                                          const uint16_t* __restrict__ y_perm,
+                                                          const int32_t* __restrict__ row_map,
+                                                          const float* __restrict__ w, int T, int H,
+                                                          int k, uint16_t* __restrict__ dy_perm,
+                                                          float* __restrict__ dw) {
+  const int lane = threadIdx.x & 31;
+  const int t = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
+  if (t >= T) return;
+  const int nch = H / 8;
+  const uint4* dyr = reinterpret_cast<const uint4*>(dy + (int64_t)t * H);
+  for (int j = 0; j < k; ++j) {
+    const int row = row_map[(int64_t)t * k + j];
+    const float wj = w[(int64_t)t * k + j];
+    const uint4* yr = reinterpret_cast<const uint4*>(y_perm + (int64_t)row * H);
+    uint4* out = reinterpret_cast<uint4*>(dy_perm + (int64_t)row * H);
+    float dot = 0.f;
+    for (int c = lane; c < nch; c += 32) {
+      float a[8], b[8];
+      unpack8(dyr[c], a);
+      unpack8(__ldg(yr + c), b);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) dot = fmaf(a[q], b[q], dot);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) a[q] *= wj;
+      out[c] = pack8(a);
+    }
+    dot = warp_sum(dot);
+    if (lane == 0) dw[(int64_t)t * k + j] = dot;
+  }
+}
+
+__global__ void __launch_bounds__(256) route_bwd_kernel(const float* __restrict__ dw,
+                                                        const float* __restrict__ w,
+                                                        const int32_t* __restrict__ ids, int T,
+                                                        int E, int k,
+                                                        float* __restrict__ d_logits) {
+  const int lane = threadIdx.x & 31;
+  const int t = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
+  if (t >= T) return;
+  float my_w = 0.f, my_dw = 0.f;
+  int my_id = -1;
+  if (lane < k) {
+    my_w = w[(int64_t)t * k + lane];
+    my_dw = dw[(int64_t)t * k + lane];
+    my_id = ids[(int64_t)t * k + lane];
+  }
+  const float mean = warp_sum(my_w * my_dw);   // sum_i w_i dw_i
+  const float my_dz = my_w * (my_dw - mean);
+  for (int e0 = 0; e0 < E; e0 += 32) {
+    const int e = e0 + lane;
+    float v = 0.f;
+    for (int j = 0; j < k; ++j) {
+      const int idj = __shfl_sync(0xffffffffu, my_id, j);
+      const float dzj = __shfl_sync(0xffffffffu, my_dz, j);
+      if (idj == e) v = dzj;
+    }
+    if (e < E) d_logits[(int64_t)t * E + e] = v;
+  }
+}
+
+__global__ void transpose_f32_kernel(const float* __restrict__ in, int rows, int cols,
+                                     float* __restrict__ out) {
+  __shared__ float tile[32][33];
+  const int c0 = blockIdx.x * 32, r0 = blockIdx.y * 32;
+  for (int q = threadIdx.y; q < 32; q += blockDim.y) {
+    const int r = r0 + q, c = c0 + threadIdx.x;
+    if (r < rows && c < cols) tile[q][threadIdx.x] = in[(int64_t)r * cols + c];
+  }
+  __syncthreads();
+  for (int q = threadIdx.y; q < 32; q += blockDim.y) {
+    const int c = c0 + q, r = r0 + threadIdx.x;
+    if (r < rows && c < cols) out[(int64_t)c * rows + r] = tile[threadIdx.x][q];
+  }
+}
+
+__global__ void __launch_bounds__(256) gather_dx_kernel(const uint16_t* __restrict__ dx_perm,
+                                                        const int32_t* __restrict__ row_map,
+                                                        const float* __restrict__ d_logits,
+                                                        const int32_t* __restrict__ ids,
+                                                        const float* __restrict__ wr_t, int T,
+                                                        int H, int E, int k,
+                                                        uint16_t* __restrict__ dx) {
+  const int lane = threadIdx.x & 31;
+  const int t = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
+  if (t >= T) return;
+  int my_row = 0, my_id = 0;
+  float my_dz = 0.f;
+  if (lane < k) {
+    my_row = row_map[(int64_t)t * k + lane];
+    if (d_logits) {
+      my_id = ids[(int64_t)t * k + lane];
+      my_dz = d_logits[(int64_t)t * E + my_id];
+    }
+  }
+  const int nch = H / 8;
+  for (int c = lane; c < nch; c += 32) {
+    float acc[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) acc[q] = 0.f;
+#pragma unroll 8
+    for (int j = 0; j < k; ++j) {
+      const int row = __shfl_sync(0xffffffffu, my_row, j);
+      float f[8];
+      unpack8(__ldg(reinterpret_cast<const uint4*>(dx_perm + (int64_t)row * H) + c), f);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) acc[q] += f[q];
+    }
+    if (d_logits) {
+      for (int j = 0; j < k; ++j) {
+        const int e = __shfl_sync(0xffffffffu, my_id, j);
+        const float dz = __shfl_sync(0xffffffffu, my_dz, j);
+        const float4* wr = reinterpret_cast<const float4*>(wr_t + (int64_t)e * H) + 2 * c;
+        const float4 a = __ldg(wr), b = __ldg(wr + 1);
+        acc[0] = fmaf(dz, a.x, acc[0]); acc[1] = fmaf(dz, a.y, acc[1]);
+        acc[2] = fmaf(dz, a.z, acc[2]); acc[3] = fmaf(dz, a.w, acc[3]);
+        acc[4] = fmaf(dz, b.x, acc[4]); acc[5] = fmaf(dz, b.y, acc[5]);
+        acc[6] = fmaf(dz, b.z, acc[6]); acc[7] = fmaf(dz, b.w, acc[7]);
+      }
+    }
+    reinterpret_cast<uint4*>(dx + (int64_t)t * H)[c] = pack8(acc);
+  }
+}
+
+// d_w_r[h, e] = sum_t x[t, h] * d_logits[t, e]; block tile 32 h x 64 e,
+// each thread 2 x 4, T staged 32 at a time (summed in increasing t).
+__global__ void __launch_bounds__(256) route_bwd_weight_kernel(const uint16_t* __restrict__ x,
+                                                               const float* __restrict__ dl, int T,
+                                                               int H, int E,
+                                                               float* __restrict__ dwr) {
+  __shared__ __align__(16) float xs[32][32];  // [t][h]
+  __shared__ __align__(16) float ds[32][64];  // [t][e]
+  const int tid = threadIdx.x, ty = tid / 16, tx = tid % 16;
+  const int h0 = blockIdx.x * 32, e0 = blockIdx.y * 64;
+  float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+  for (int t0 = 0; t0 < T; t0 += 32) {
+    for (int q = tid; q < 32 * 32; q += 256) {
+      const int tl = q / 32, hl = q % 32;
+      const int t = t0 + tl, h = h0 + hl;
+      xs[tl][hl] = (t < T && h < H) ? __uint_as_float((uint32_t)x[(int64_t)t * H + h] << 16) : 0.f;
+    }
+    for (int q = tid; q < 32 * 64; q += 256) {
+      const int tl = q / 64, el = q % 64;
+      const int t = t0 + tl, e = e0 + el;
+      ds[tl][el] = (t < T && e < E) ? dl[(int64_t)t * E + e] : 0.f;
+    }
+    __syncthreads();
+#pragma unroll 8
+    for (int tl = 0; tl < 32; ++tl) {
+      const float2 xv = *reinterpret_cast<const float2*>(&xs[tl][ty * 2]);
+      const float4 dv = *reinterpret_cast<const float4*>(&ds[tl][tx * 4]);
+      acc[0][0] = fmaf(xv.x, dv.x, acc[0][0]); acc[0][1] = fmaf(xv.x, dv.y, acc[0][1]);
+      acc[0][2] = fmaf(xv.x, dv.z, acc[0][2]); acc[0][3] = fmaf(xv.x, dv.w, acc[0][3]);
+      acc[1][0] = fmaf(xv.y, dv.x, acc[1][0]); acc[1][1] = fmaf(xv.y, dv.y, acc[1][1]);
+      acc[1][2] = fmaf(xv.y, dv.z, acc[1][2]); acc[1][3] = fmaf(xv.y, dv.w, acc[1][3]);
+    }
+    __syncthreads();
+  }
+  for (int a = 0; a < 2; ++a) {
+    const int h = h0 + ty * 2 + a;
+    if (h >= H) continue;
+    for (int b = 0; b < 4; ++b) {
+      const int e = e0 + tx * 4 + b;
+      if (e < E) dwr[(int64_t)h * E + e] = acc[a][b];
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_combine(const uint16_t* y_perm, const int32_t* row_map, const float* w,
+                           const uint16_t* y_shared, int64_t T, int64_t H, int64_t k, uint16_t* y,
+                           cudaStream_t stream) {
+  if (T == 0) return cudaSuccess;
+  combine_kernel<<<(unsigned)((T + kWarpsPerBlock - 1) / kWarpsPerBlock), 256, 0, stream>>>(
+      y_perm, row_map, w, y_shared, (int)T, (int)H, (int)k, y);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_combine_bwd(const uint16_t* dy, const uint16_t* y_perm, const int32_t* row_map,
+                               const float* w, int64_t T, int64_t H, int64_t k, uint16_t* dy_perm,
+                               float* dw, cudaStream_t stream) {
+  if (T == 0) return cudaSuccess;
+  combine_bwd_kernel<<<(unsigned)((T + kWarpsPerBlock - 1) / kWarpsPerBlock), 256, 0, stream>>>(
+      dy, y_perm, row_map, w, (int)T, (int)H, (int)k, dy_perm, dw);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_route_bwd(const float* dw, const float* w, const int32_t* ids, int64_t T,
+                             int64_t E, int64_t k, float* d_logits, cudaStream_t stream) {
+  if (T == 0) return cudaSuccess;
+  route_bwd_kernel<<<(unsigned)((T + kWarpsPerBlock - 1) / kWarpsPerBlock), 256, 0, stream>>>(
+      dw, w, ids, (int)T, (int)E, (int)k, d_logits);
+  return cudaGetLastError();
+}
+
+size_t gather_dx_workspace_bytes(int64_t H, int64_t E) { return (size_t)(H * E * sizeof(float)); }
+
+cudaError_t launch_gather_dx(const uint16_t* dx_perm, const int32_t* row_map, const float* d_logits,
+                             const int32_t* ids, const float* w_router, int64_t T, int64_t H,
+                             int64_t E, int64_t k, uint16_t* dx, void* ws, cudaStream_t stream) {
+  if (T == 0) return cudaSuccess;
+  float* wr_t = nullptr;
+  if (d_logits) {
+    wr_t = static_cast<float*>(ws);
+    dim3 g((unsigned)((E + 31) / 32), (unsigned)((H + 31) / 32));
+    transpose_f32_kernel<<<g, dim3(32, 8), 0, stream>>>(w_router, (int)H, (int)E, wr_t);
+  }
+  gather_dx_kernel<<<(unsigned)((T + kWarpsPerBlock - 1) / kWarpsPerBlock), 256, 0, stream>>>(
+      dx_perm, row_map, d_logits, ids, wr_t, (int)T, (int)H, (int)E, (int)k, dx);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_route_bwd_weight(const uint16_t* x, const float* d_logits, int64_t T, int64_t H,
+                                    int64_t E, float* d_w_router, cudaStream_t stream) {
+  dim3 g((unsigned)((H + 31) / 32), (unsigned)((E + 63) / 64));
+  route_bwd_weight_kernel<<<g, 256, 0, stream>>>(x, d_logits, (int)T, (int)H, (int)E, d_w_router);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,697 @@
+// Grouped GEMMs of the MoE expert layer on the sm_103a tensor cores.
+//
+// What they compute ("InternVL3.5 接入 pure FSDP2 后端开发实践", MindSpeed-MM
+// issue 625, §2 fused expert layout gate_up_proj [E*H, 2I] / down_proj
+// [E*I, H], §8.3 permute -> grouped_matmul -> SwiGLU -> grouped_matmul ->
+// unpermute; "InternVL3.5 pure FSDP2 训练性能优化实践" §2.1: one grouped call
+// over all experts instead of one call per expert):
+//
+//   FWD_GATEUP    h[r]      = silu(x[src_row[r]] . Wg_e) * (x[src_row[r]] . Wu_e)
+//   FWD_DOWN      y_perm[r] = h[r] . Wd_e
+//   DGRAD_DOWN    dgu[r]    = SwiGLU'(dy_perm[r] . Wd_e^T, gu_pre[r])
+//   DGRAD_GATEUP  dx_perm[r]= dgu[r] . Wgu_e^T
+//   WGRAD_DOWN    d_down_e  = h_e^T . dy_perm_e
+//   WGRAD_GATEUP  d_gu_e    = x[src_rows of e]^T . dgu_e
+//
+// One persistent, warp-specialised kernel template serves all six (grid =
+// the SM count, 192 threads, one CTA per SM):
+//   warp 0      TMA producer: per 64-wide K block one A tile (128 rows) and
+//               one B tile (256 columns) into a 4-stage shared-memory ring,
+//               128-byte swizzled.  Gathered A rows (the permute fused into
+//               the load) use cp.async.bulk.tensor ... tile::gather4, four
+//               token rows per instruction spread over the warp's lanes.
+//   warp 1      allocates 512 TMEM columns (two 128 x 256 fp32 accumulators)
+//               and, from one lane, issues tcgen05.mma (M=128, N=256, K=16,
+//               bf16 x bf16 -> fp32); tcgen05.commit frees ring stages and
+//               hands finished accumulators to the epilogue.
+//   warps 2..5  epilogue: tcgen05.ld of the accumulator (one TMEM lane = one
+//               output row per thread), fused SwiGLU / SwiGLU-backward in
+//               fp32, bf16 stores.  Double-buffered accumulators let the
+//               epilogue of tile i overlap the main loop of tile i+1.
+//
+// The tile list is derived on the device from expert_offsets (no host read
+// back): forward and dgrad GEMMs are grouped along M (each expert's rows form
+// ceil(M_e/128) row tiles, empty experts none); wgrad GEMMs are grouped along
+// K (every expert owns a fixed grid of output tiles; its K extent is M_e,
+// and an empty expert's tiles are written as zeros).  Within a wgrad tile,
+// K rows past the expert's last row are zeroed in shared memory before the
+// MMA so no other expert's rows leak in.  The K order inside a tile is fixed
+// and there is no split-K: results are deterministic.
+//
+// Every spin wait is bounded (globaltimer); on expiry the kernel records
+// MOE_ERR_TIMEOUT in the status word, lets the other roles stop, waits
+// (bounded) for its TMA copies and MMAs in flight, frees its TMEM and
+// returns.
+#include "kernels.h"
+
+namespace moe {
+
+namespace {
+
+constexpr int BM = 128;
+constexpr int BN = 256;
+constexpr int BK = 64;
+constexpr int STAGES = 4;
+constexpr int A_BYTES = BM * BK * 2;               // 16 KB
+constexpr int B_BYTES = BN * BK * 2;               // 32 KB
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;     // 48 KB
+constexpr int kThreads = 192;
+constexpr uint32_t TMEM_COLS = 512;
+constexpr int MN_CHUNK_BYTES = 64 * 128;           // one 64-wide MN chunk x 64 K rows
+
+enum Mode { FWD_GATEUP = 0, FWD_DOWN = 1, DGRAD_DOWN = 2, DGRAD_GATEUP = 3, WGRAD_DOWN = 4,
+            WGRAD_GATEUP = 5 };
+
+template <int MODE>
+struct Traits {
+  static constexpr bool kAMN = (MODE == WGRAD_DOWN || MODE == WGRAD_GATEUP);
+  static constexpr bool kBMN = (MODE == FWD_GATEUP || MODE == FWD_DOWN || MODE == WGRAD_DOWN ||
+                                MODE == WGRAD_GATEUP);
+  static constexpr bool kKGrouped = (MODE == WGRAD_DOWN || MODE == WGRAD_GATEUP);
+};
+
+struct GemmParams {   // 64-byte aligned through its CUtensorMap members
+  CUtensorMap tmA;
+  CUtensorMap tmB;
+  const int32_t* offsets;   // [E+1] expert row offsets, or nullptr: one group of `rows`
+  const int32_t* gidx;      // gather indices (src_row), or nullptr: identity
+  const uint16_t* aux;      // gu_pre for DGRAD_DOWN
+  uint16_t* out;
+  uint16_t* out2;           // gu_pre output of FWD_GATEUP (nullable)
+  uint32_t* status;
+  uint64_t wait_limit_ns;
+  int rows;                 // permuted rows R
+  int E;
+  int K;                    // contraction length (M-grouped modes)
+  int I;
+  int n_out;                // valid output columns
+  int m_w;                  // output rows per expert (K-grouped modes)
+  int nt;                   // n tiles
+  int mt_w;                 // m tiles per expert (K-grouped modes)
+  int64_t ldo;              // leading dimension of out
+};
+
+// UMMA shared-memory descriptor, 128-byte swizzle, sm_100-family version bits.
+__device__ __forceinline__ uint64_t umma_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+  d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;
+  return d;
+}
+
+template <int MODE>
+__device__ __forceinline__ uint32_t make_idesc() {
+  using Tr = Traits<MODE>;
+  return (1u << 4)                       // D: fp32
+         | (1u << 7)                     // A: bf16
+         | (1u << 10)                    // B: bf16
+         | ((Tr::kAMN ? 1u : 0u) << 15)  // A major: 0 = K, 1 = MN
+         | ((Tr::kBMN ? 1u : 0u) << 16)  // B major
+         | ((uint32_t)(BN >> 3) << 17)   // N
+         | ((uint32_t)(BM >> 4) << 24);  // M
+}
+
+struct Tile {
+  int e, mt, nt;
+  int row0;       // M-grouped: first permuted row; K-grouped: first K row of the expert
+  int rows;       // M-grouped: valid rows in the tile; K-grouped: K extent of the expert
+  int kblocks;
+};
+
+__device__ __forceinline__ void group_range(const GemmParams& p, int e, int& start, int& count) {
+  if (p.offsets) {
+    start = p.offsets[e];
+    count = p.offsets[e + 1] - start;
+  } else {
+    start = 0;
+    count = p.rows;
+  }
+}
+
+template <int MODE>
+__device__ __forceinline__ Tile decode_tile(const GemmParams& p, const int* prefix, int tile) {
+  Tile t;
+  if (Traits<MODE>::kKGrouped) {
+    const int per = p.mt_w * p.nt;
+    t.e = tile / per;
+    const int local = tile - t.e * per;
+    t.mt = local / p.nt;
+    t.nt = local - t.mt * p.nt;
+    group_range(p, t.e, t.row0, t.rows);
+    t.kblocks = (t.rows + BK - 1) / BK;
+  } else {
+    int lo = 0, hi = p.E - 1;    // largest e with prefix[e] <= tile
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (prefix[mid] <= tile) lo = mid; else hi = mid - 1;
+    }
+    t.e = lo;
+    const int local = tile - prefix[lo];
+    t.mt = local / p.nt;
+    t.nt = local - t.mt * p.nt;
+    int start, count;
+    group_range(p, t.e, start, count);
+    t.row0 = start + t.mt * BM;
+    t.rows = min(BM, count - t.mt * BM);
+    t.kblocks = p.K / BK;
+  }
+  return t;
+}
+
+template <int MODE>
+__device__ __forceinline__ void store_zero_tile(const GemmParams& p, const Tile& t, int r) {
+  const int m = t.mt * BM + r;
+  if (m >= p.m_w) return;
+  uint16_t* orow = p.out + ((int64_t)t.e * p.m_w + m) * p.ldo + (int64_t)t.nt * BN;
+  const uint4 z = make_uint4(0, 0, 0, 0);
+  for (int c = 0; c < BN; c += 8)
+    if (t.nt * BN + c < p.n_out) *reinterpret_cast<uint4*>(orow + c) = z;
+}
+
+__device__ __forceinline__ void store32(uint16_t* dst, const float* v) {
+  uint4* d = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) d[q] = pack8(v + 8 * q);
+}
+
+__device__ __forceinline__ void load32_bf16(const uint16_t* src, float* v) {
+  const uint4* s = reinterpret_cast<const uint4*>(src);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) unpack8(__ldg(s + q), v + 8 * q);
+}
+
+template <int MODE>
+__global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_constant__ GemmParams p) {
+  using Tr = Traits<MODE>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* ring = smem;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+  // bars: full[STAGES], empty[STAGES], acc_full[2], acc_empty[2], drain
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  int* prefix = reinterpret_cast<int*>(tmem_slot + 2);   // [E+1]
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t ring_u32 = smem_u32(ring);
+  const uint32_t bar_u32 = smem_u32(bars);
+  auto full_bar = [&](int s) { return bar_u32 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar_u32 + 8u * (STAGES + s); };
+  auto accf_bar = [&](int b) { return bar_u32 + 8u * (2 * STAGES + b); };
+  auto acce_bar = [&](int b) { return bar_u32 + 8u * (2 * STAGES + 2 + b); };
+  const uint32_t drain_bar = bar_u32 + 8u * (2 * STAGES + 4);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(accf_bar(b), 1);
+      mbar_init(acce_bar(b), 128);
+    }
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&p.tmA);
+    tma_prefetch_desc(&p.tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+    tmem_relinquish();
+  }
+  // Tile prefix over experts (M-grouped modes): prefix[e] = sum_{e'<e} ceil(M_e'/BM) * nt
+  int total_tiles;
+  if (Tr::kKGrouped) {
+    total_tiles = p.E * p.mt_w * p.nt;
+  } else {
+    if (warp == 2) {
+      int carry = 0;
+      for (int e0 = 0; e0 < p.E; e0 += 32) {
+        const int e = e0 + lane;
+        int v = 0;
+        if (e < p.E) {
+          int start, count;
+          group_range(p, e, start, count);
+          v = ((count + BM - 1) / BM) * p.nt;
+        }
+        int incl = v;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int n = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += n;
+        }
+        if (e < p.E) prefix[e] = carry + incl - v;
+        carry += __shfl_sync(0xffffffffu, incl, 31);
+      }
+      if (lane == 0) prefix[p.E] = carry;
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  if (!Tr::kKGrouped) total_tiles = prefix[p.E];
+
+  if (warp == 0) {
+    // ------------------------------------------------------ TMA producer
+    int stage = 0;
+    uint32_t phase = 0;
+    uint32_t issued_mask = 0;       // stages that ever received a load
+    uint32_t last_parity = 0;       // bit s: parity of the last load into stage s
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x) {
+      const Tile t = decode_tile<MODE>(p, prefix, tile);
+      if (t.kblocks == 0) continue;
+      int gi[4] = {0, 0, 0, 0};
+      if (MODE == FWD_GATEUP) {      // this lane gathers tile rows 4*lane .. 4*lane+3
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const int r = min(4 * lane + q, t.rows - 1);
+          gi[q] = p.gidx ? p.gidx[t.row0 + r] : t.row0 + r;
+        }
+      }
+      for (int kb = 0; kb < t.kblocks; ++kb) {
+        bool w = true;
+        if (lane == 0)
+          w = mbar_wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, p.wait_limit_ns, p.status, 1);
+        ok = __shfl_sync(0xffffffffu, w ? 1 : 0, 0) != 0;
+        if (!ok) break;
+        const uint32_t sA = ring_u32 + stage * STAGE_BYTES;
+        const uint32_t sB = sA + A_BYTES;
+        const uint32_t fb = full_bar(stage);
+        if (lane == 0) mbar_arrive_expect_tx(fb, STAGE_BYTES);
+        __syncwarp();
+        const int k0 = kb * BK;
+        if (MODE == FWD_GATEUP) {
+          tma_gather4(sA + 4 * lane * 128, &p.tmA, k0, gi[0], gi[1], gi[2], gi[3], fb);
+          if (lane == 0) {
+            const int brow = t.e * p.K + k0;               // gate_up rows of expert e
+            const int n0 = t.nt * 128;
+            tma_load_2d(sB + 0 * MN_CHUNK_BYTES, &p.tmB, n0, brow, fb);
+            tma_load_2d(sB + 1 * MN_CHUNK_BYTES, &p.tmB, n0 + 64, brow, fb);
+            tma_load_2d(sB + 2 * MN_CHUNK_BYTES, &p.tmB, p.I + n0, brow, fb);
+            tma_load_2d(sB + 3 * MN_CHUNK_BYTES, &p.tmB, p.I + n0 + 64, brow, fb);
+          }
+        } else if (MODE == FWD_DOWN) {
+          if (lane == 0) {
+            tma_load_2d(sA, &p.tmA, k0, t.row0, fb);
+            const int brow = t.e * p.K + k0;               // down rows of expert e
+            const int n0 = t.nt * BN;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) tma_load_2d(sB + c * MN_CHUNK_BYTES, &p.tmB, n0 + 64 * c, brow, fb);
+          }
+        } else if (MODE == DGRAD_DOWN || MODE == DGRAD_GATEUP) {
+          if (lane == 0) {
+            tma_load_2d(sA, &p.tmA, k0, t.row0, fb);
+            // B^T rows: expert e's block of n_rows_per_expert rows, K-major
+            const int rows_per_e = (MODE == DGRAD_DOWN) ? p.I : p.n_out;
+            tma_load_2d(sB, &p.tmB, k0, t.e * rows_per_e + t.nt * BN, fb);
+          }
+        } else if (MODE == WGRAD_DOWN) {
+          if (lane == 0) {
+            const int krow = t.row0 + k0;
+            const int m0 = t.mt * BM;
+            tma_load_2d(sA + 0 * MN_CHUNK_BYTES, &p.tmA, m0, krow, fb);
+            tma_load_2d(sA + 1 * MN_CHUNK_BYTES, &p.tmA, m0 + 64, krow, fb);
+            const int n0 = t.nt * BN;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) tma_load_2d(sB + c * MN_CHUNK_BYTES, &p.tmB, n0 + 64 * c, krow, fb);
+          }
+        } else {  // WGRAD_GATEUP: A = gathered x rows (K = tokens), MN-major
+          const int c = lane >> 4;           // MN chunk 0/1
+          const int g = lane & 15;           // k rows 4g .. 4g+3
+          int r4[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const int kr = min(k0 + 4 * g + q, t.rows - 1);
+            r4[q] = p.gidx ? p.gidx[t.row0 + kr] : t.row0 + kr;
+          }
+          tma_gather4(sA + c * MN_CHUNK_BYTES + 4 * g * 128, &p.tmA, t.mt * BM + 64 * c, r4[0], r4[1],
+                      r4[2], r4[3], fb);
+          if (lane == 0) {
+            const int n0 = t.nt * BN;
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc)
+              tma_load_2d(sB + cc * MN_CHUNK_BYTES, &p.tmB, n0 + 64 * cc, t.row0 + k0, fb);
+          }
+        }
+        issued_mask |= 1u << stage;
+        last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+    if (!ok && lane == 0) {
+      // stopped early: wait (bounded) for the copies still in flight
+      for (int s = 0; s < STAGES; ++s)
+        if (issued_mask & (1u << s)) {
+          const uint64_t t0 = globaltimer_ns();
+          while (!mbar_try_wait(full_bar(s), (last_parity >> s) & 1u) &&
+                 globaltimer_ns() - t0 < p.wait_limit_ns) {
+          }
+        }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------- MMA issuer
+    const uint32_t idesc = make_idesc<MODE>();
+    int stage = 0;
+    uint32_t phase = 0;
+    int buf = 0;
+    uint32_t acc_phase = 0;
+    bool ok = true;
+    bool issued_any = false;
+    for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x) {
+      const Tile t = decode_tile<MODE>(p, prefix, tile);
+      if (t.kblocks == 0) continue;
+      bool w = true;
+      if (lane == 0)
+        w = mbar_wait_bounded(acce_bar(buf), acc_phase ^ 1u, abort_flag, p.wait_limit_ns, p.status, 2);
+      ok = __shfl_sync(0xffffffffu, w ? 1 : 0, 0) != 0;
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t d_tmem = tmem_base + (uint32_t)(buf * BN);
+      for (int kb = 0; kb < t.kblocks; ++kb) {
+        if (lane == 0)
+          w = mbar_wait_bounded(full_bar(stage), phase, abort_flag, p.wait_limit_ns, p.status, 3);
+        ok = __shfl_sync(0xffffffffu, w ? 1 : 0, 0) != 0;
+        if (!ok) break;
+        const uint32_t sA = ring_u32 + stage * STAGE_BYTES;
+        const uint32_t sB = sA + A_BYTES;
+        if (Tr::kKGrouped) {
+          const int kvalid = t.rows - kb * BK;
+          if (kvalid < BK) {   // zero the K rows past the expert's last row (A: 2 chunks, B: 4)
+            uint8_t* gA = ring + stage * STAGE_BYTES;
+            const int nrow = BK - kvalid;
+            for (int q = lane; q < nrow * 8 * 6; q += 32) {
+              const int chunk = q / (nrow * 8);
+              const int rem = q - chunk * nrow * 8;
+              const int row = kvalid + rem / 8;
+              const int u = rem & 7;
+              *reinterpret_cast<uint4*>(gA + chunk * MN_CHUNK_BYTES + row * 128 + u * 16) =
+                  make_uint4(0, 0, 0, 0);
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+          }
+        }
+        tc_fence_after();
+        if (lane == 0) {
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            const uint64_t ad = Tr::kAMN ? umma_desc(sA + kk * 2048, MN_CHUNK_BYTES, 1024)
+                                         : umma_desc(sA + kk * 32, 16, 1024);
+            const uint64_t bd = Tr::kBMN ? umma_desc(sB + kk * 2048, MN_CHUNK_BYTES, 1024)
+                                         : umma_desc(sB + kk * 32, 16, 1024);
+            tc_mma_bf16(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+          }
+          tc_commit(empty_bar(stage));
+        }
+        issued_any = true;
+        __syncwarp();
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+      if (!ok) break;
+      if (lane == 0) tc_commit(accf_bar(buf));
+      __syncwarp();
+      buf ^= 1;
+      if (buf == 0) acc_phase ^= 1u;
+    }
+    if (!ok && issued_any && lane == 0) {
+      // stopped early: make sure every MMA issued has finished before TMEM is freed
+      tc_commit(drain_bar);
+      const uint64_t t0 = globaltimer_ns();
+      while (!mbar_try_wait(drain_bar, 0) && globaltimer_ns() - t0 < p.wait_limit_ns) {
+      }
+    }
+  } else {
+    // ---------------------------------------------------------- epilogue
+    const int quarter = warp & 3;            // TMEM lanes 32*quarter .. +31
+    const int r = quarter * 32 + lane;       // accumulator row of this thread
+    int buf = 0;
+    uint32_t acc_phase = 0;
+    for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
+      const Tile t = decode_tile<MODE>(p, prefix, tile);
+      if (t.kblocks == 0) {
+        if (Tr::kKGrouped) store_zero_tile<MODE>(p, t, r);
+        continue;
+      }
+      bool w = true;
+      if (lane == 0)
+        w = mbar_wait_bounded(accf_bar(buf), acc_phase, abort_flag, p.wait_limit_ns, p.status, 4);
+      if (__shfl_sync(0xffffffffu, w ? 1 : 0, 0) == 0) break;
+      tc_fence_after();
+      const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(buf * BN);
+      float v[32];
+      if (MODE == FWD_GATEUP) {
+        const bool row_ok = r < t.rows;
+        const int64_t row = t.row0 + r;
+        const int n0 = t.nt * 128;
+#pragma unroll 1
+        for (int c0 = 0; c0 < 128; c0 += 32) {
+          if (n0 + c0 >= p.n_out) break;                 // warp-uniform
+          float u[32];
+          tmem_ld32(taddr + c0, v);                      // gate columns
+          tmem_ld32(taddr + 128 + c0, u);                // up columns
+          if (row_ok) {
+            if (p.out2) {
+              store32(p.out2 + row * 2 * p.I + n0 + c0, v);
+              store32(p.out2 + row * 2 * p.I + p.I + n0 + c0, u);
+            }
+#pragma unroll
+            for (int q = 0; q < 32; ++q) v[q] = v[q] / (1.0f + expf(-v[q])) * u[q];
+            store32(p.out + row * p.ldo + n0 + c0, v);
+          }
+        }
+      } else if (MODE == FWD_DOWN || MODE == DGRAD_GATEUP) {
+        const bool row_ok = r < t.rows;
+        const int64_t row = t.row0 + r;
+        const int n0 = t.nt * BN;
+#pragma unroll 1
+        for (int c0 = 0; c0 < BN; c0 += 32) {
+          if (n0 + c0 >= p.n_out) break;
+          tmem_ld32(taddr + c0, v);
+          if (row_ok) store32(p.out + row * p.ldo + n0 + c0, v);
+        }
+      } else if (MODE == DGRAD_DOWN) {
+        const bool row_ok = r < t.rows;
+        const int64_t row = t.row0 + r;
+        const int n0 = t.nt * BN;
+#pragma unroll 1
+        for (int c0 = 0; c0 < BN; c0 += 32) {
+          if (n0 + c0 >= p.n_out) break;
+          tmem_ld32(taddr + c0, v);                      // dh (fp32)
+          if (row_ok) {
+            float g[32], u[32];
+            load32_bf16(p.aux + row * 2 * p.I + n0 + c0, g);
+            load32_bf16(p.aux + row * 2 * p.I + p.I + n0 + c0, u);
+#pragma unroll
+            for (int q = 0; q < 32; ++q) {
+              const float s = 1.0f / (1.0f + expf(-g[q]));
+              const float dh = v[q];
+              const float dg = dh * u[q] * s * (1.0f + g[q] * (1.0f - s));
+              const float du = dh * g[q] * s;
+              g[q] = dg;
+              u[q] = du;
+            }
+            store32(p.out + row * 2 * p.I + n0 + c0, g);
+            store32(p.out + row * 2 * p.I + p.I + n0 + c0, u);
+          }
+        }
+      } else {  // WGRAD_*: output rows m = mt*BM + r of expert e's weight-gradient block
+        const int m = t.mt * BM + r;
+        const bool row_ok = m < p.m_w;
+        uint16_t* orow = p.out + ((int64_t)t.e * p.m_w + m) * p.ldo;
+        const int n0 = t.nt * BN;
+#pragma unroll 1
+        for (int c0 = 0; c0 < BN; c0 += 32) {
+          if (n0 + c0 >= p.n_out) break;
+          tmem_ld32(taddr + c0, v);
+          if (row_ok) store32(orow + n0 + c0, v);
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(acce_bar(buf));
+      buf ^= 1;
+      if (buf == 0) acc_phase ^= 1u;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+size_t gemm_smem_bytes(int E) {
+  return 1024 + (size_t)STAGES * STAGE_BYTES + 8 * (2 * STAGES + 5) + 16 + 4 * (size_t)(E + 1) + 64;
+}
+
+template <int MODE>
+cudaError_t run_gemm(const GemmParams& p, int64_t tiles_upper_bound, const DeviceInfo& dev,
+                     cudaStream_t stream) {
+  const size_t smem = gemm_smem_bytes(p.E);
+  static int configured[kMaxDevices] = {0};
+  if (!configured[dev.ordinal]) {
+    cudaError_t err = cudaFuncSetAttribute(grouped_gemm_kernel<MODE>,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           (int)gemm_smem_bytes(kMaxExperts));
+    if (err != cudaSuccess) return err;
+    configured[dev.ordinal] = 1;
+  }
+  int64_t grid = tiles_upper_bound < dev.num_sms ? tiles_upper_bound : dev.num_sms;
+  if (grid < 1) grid = 1;
+  grouped_gemm_kernel<MODE><<<(unsigned)grid, kThreads, smem, stream>>>(p);
+  return cudaGetLastError();
+}
+
+// 2-D bf16 tensor map over a row-major [rows, cols] matrix, 128-byte swizzle.
+bool make_map(CUtensorMap* map, const void* base, int64_t rows, int64_t cols, int box_cols,
+              int box_rows) {
+  const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)(cols * 2)};
+  const cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return encode_tensor_map_2d_bf16(map, base, dims, strides, box, estr);
+}
+
+void fill_common(GemmParams& p, const int32_t* offsets, int64_t R, int64_t E, int64_t I,
+                 const DeviceInfo& dev) {
+  p.offsets = offsets;
+  p.gidx = nullptr;
+  p.aux = nullptr;
+  p.out = nullptr;
+  p.out2 = nullptr;
+  p.status = dev.status;
+  p.wait_limit_ns = dev.wait_limit_ns;
+  p.rows = (int)R;
+  p.E = (int)E;
+  p.I = (int)I;
+  p.K = 0;
+  p.n_out = 0;
+  p.m_w = 0;
+  p.nt = 0;
+  p.mt_w = 0;
+  p.ldo = 0;
+}
+
+int64_t mgrouped_tile_bound(int64_t R, int64_t E, int nt) { return ((R + BM - 1) / BM + E) * nt; }
+
+}  // namespace
+
+int launch_gemm_gate_up(const uint16_t* x, const int32_t* src_row, const int32_t* offsets,
+                        const uint16_t* gate_up, int64_t T, int64_t R, int64_t H, int64_t E,
+                        int64_t I, uint16_t* h, uint16_t* gu_pre, const DeviceInfo& dev,
+                        cudaStream_t stream) {
+  if (R == 0) return 0;
+  GemmParams p;
+  fill_common(p, offsets, R, E, I, dev);
+  if (!make_map(&p.tmA, x, T, H, 64, 1) || !make_map(&p.tmB, gate_up, E * H, 2 * I, 64, 64))
+    return -1;
+  p.gidx = src_row;
+  p.out = h;
+  p.out2 = gu_pre;
+  p.K = (int)H;
+  p.n_out = (int)I;
+  p.nt = (int)((I + 127) / 128);
+  p.ldo = I;
+  return run_gemm<FWD_GATEUP>(p, mgrouped_tile_bound(R, E, p.nt), dev, stream) == cudaSuccess ? 0 : 1;
+}
+
+int launch_gemm_down(const uint16_t* h, const int32_t* offsets, const uint16_t* down, int64_t R,
+                     int64_t H, int64_t E, int64_t I, uint16_t* y_perm, const DeviceInfo& dev,
+                     cudaStream_t stream) {
+  if (R == 0) return 0;
+  GemmParams p;
+  fill_common(p, offsets, R, E, I, dev);
+  if (!make_map(&p.tmA, h, R, I, 64, 128) || !make_map(&p.tmB, down, E * I, H, 64, 64)) return -1;
+  p.out = y_perm;
+  p.K = (int)I;
+  p.n_out = (int)H;
+  p.nt = (int)((H + BN - 1) / BN);
+  p.ldo = H;
+  return run_gemm<FWD_DOWN>(p, mgrouped_tile_bound(R, E, p.nt), dev, stream) == cudaSuccess ? 0 : 1;
+}
+
+int launch_gemm_down_bwd(const uint16_t* dy_perm, const uint16_t* h, const uint16_t* gu_pre,
+                         const int32_t* offsets, const uint16_t* down, int64_t R, int64_t H,
+                         int64_t E, int64_t I, uint16_t* dgu, uint16_t* d_down,
+                         const DeviceInfo& dev, cudaStream_t stream) {
+  if (R > 0) {  // dgu = SwiGLU'(dy_perm . Wd_e^T)
+    GemmParams p;
+    fill_common(p, offsets, R, E, I, dev);
+    if (!make_map(&p.tmA, dy_perm, R, H, 64, 128) || !make_map(&p.tmB, down, E * I, H, 64, 256))
+      return -1;
+    p.aux = gu_pre;
+    p.out = dgu;
+    p.K = (int)H;
+    p.n_out = (int)I;
+    p.nt = (int)((I + BN - 1) / BN);
+    p.ldo = 2 * I;
+    if (run_gemm<DGRAD_DOWN>(p, mgrouped_tile_bound(R, E, p.nt), dev, stream) != cudaSuccess) return 1;
+  }
+  {  // d_down_e = h_e^T . dy_perm_e
+    GemmParams p;
+    fill_common(p, offsets, R, E, I, dev);
+    const int64_t rows = R > 0 ? R : 1;
+    if (!make_map(&p.tmA, h, rows, I, 64, 64) || !make_map(&p.tmB, dy_perm, rows, H, 64, 64))
+      return -1;
+    p.out = d_down;
+    p.m_w = (int)I;
+    p.n_out = (int)H;
+    p.mt_w = (int)((I + BM - 1) / BM);
+    p.nt = (int)((H + BN - 1) / BN);
+    p.ldo = H;
+    if (run_gemm<WGRAD_DOWN>(p, E * p.mt_w * p.nt, dev, stream) != cudaSuccess) return 1;
+  }
+  return 0;
+}
+
+int launch_gemm_gate_up_bwd(const uint16_t* dgu, const uint16_t* x, const int32_t* src_row,
+                            const int32_t* offsets, const uint16_t* gate_up, int64_t T, int64_t R,
+                            int64_t H, int64_t E, int64_t I, uint16_t* dx_perm,
+                            uint16_t* d_gate_up, const DeviceInfo& dev, cudaStream_t stream) {
+  if (R > 0) {  // dx_perm = dgu . Wgu_e^T
+    GemmParams p;
+    fill_common(p, offsets, R, E, I, dev);
+    if (!make_map(&p.tmA, dgu, R, 2 * I, 64, 128) || !make_map(&p.tmB, gate_up, E * H, 2 * I, 64, 256))
+      return -1;
+    p.out = dx_perm;
+    p.K = (int)(2 * I);
+    p.n_out = (int)H;
+    p.nt = (int)((H + BN - 1) / BN);
+    p.ldo = H;
+    if (run_gemm<DGRAD_GATEUP>(p, mgrouped_tile_bound(R, E, p.nt), dev, stream) != cudaSuccess) return 1;
+  }
+  {  // d_gate_up_e = x[src rows of e]^T . dgu_e
+    GemmParams p;
+    fill_common(p, offsets, R, E, I, dev);
+    const int64_t rows = R > 0 ? R : 1;
+    if (!make_map(&p.tmA, x, T > 0 ? T : 1, H, 64, 1) || !make_map(&p.tmB, dgu, rows, 2 * I, 64, 64))
+      return -1;
+    p.gidx = src_row;
+    p.out = d_gate_up;
+    p.m_w = (int)H;
+    p.n_out = (int)(2 * I);
+    p.mt_w = (int)((H + BM - 1) / BM);
+    p.nt = (int)((2 * I + BN - 1) / BN);
+    p.ldo = 2 * I;
+    if (run_gemm<WGRAD_GATEUP>(p, E * p.mt_w * p.nt, dev, stream) != cudaSuccess) return 1;
+  }
+  return 0;
+}
+
+}  // namespace moe

@@ -1,0 +1,185 @@
+// Permute: group the R = T*k (token, slot) assignments by expert
+// ("Awesome-ML-SYS-Tutorial" MoE/EP guide, gsyq.cn, "Expert Parallelism":
+// per-expert token counts, then permute so each expert's tokens are
+// contiguous; "InternVL3.5 接入 pure FSDP2 后端开发实践" §8.3: permute).
+//
+// Deterministic three-pass counting sort, no order-dependent atomics:
+//   1. permute_hist_kernel   block b counts the ids of its chunk of
+//                            kChunk assignments -> hist[b][e]
+//   2. permute_scan_kernel   one block: counts[e] = sum_b hist[b][e];
+//                            offsets = exclusive scan; hist[b][e] becomes
+//                            offsets[e] + sum_{b'<b} hist[b'][e]
+//   3. permute_scatter_kernel block b ranks its chunk stably: warp w owns a
+//                            contiguous slice, warp bases come from a scan of
+//                            per-warp counts, and inside a warp step the
+//                            lanes holding the same expert rank themselves
+//                            with __match_any_sync (lower lane = lower i).
+// Outputs: counts, offsets, row_map[i] (permuted row of assignment i) and
+// src_row[row] = i / k.  Workspace: hist, nblocks * E int32.
+#include "kernels.h"
+
+namespace moe {
+
+namespace {
+
+constexpr int kChunk = 2048;     // assignments per block
+constexpr int kPermThreads = 256;
+constexpr int kPermWarps = kPermThreads / 32;
+constexpr int kPerWarp = kChunk / kPermWarps;   // 256 = 8 steps of 32
+
+__global__ void __launch_bounds__(kPermThreads) permute_hist_kernel(const int32_t* __restrict__ ids,
+                                                                    int64_t R, int E,
+                                                                    int32_t* __restrict__ hist,
+                                                                    uint32_t* status) {
+  extern __shared__ int32_t sh[];  // [E]
+  for (int e = threadIdx.x; e < E; e += blockDim.x) sh[e] = 0;
+  __syncthreads();
+  const int64_t base = (int64_t)blockIdx.x * kChunk;
+  for (int q = threadIdx.x; q < kChunk; q += blockDim.x) {
+    const int64_t i = base + q;
+    if (i < R) {
+      const int e = ids[i];
+      if (e < 0 || e >= E) {
+        report_status(status, kStatusDevice, kKernPermute, 1);
+      } else {
+        atomicAdd(&sh[e], 1);   // counts only: the order of increments is irrelevant
+      }
+    }
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) hist[(int64_t)blockIdx.x * E + e] = sh[e];
+}
+
+__global__ void __launch_bounds__(1024) permute_scan_kernel(int32_t* __restrict__ hist, int nblocks,
+                                                            int E, int32_t* __restrict__ counts,
+                                                            int32_t* __restrict__ offsets) {
+  __shared__ int32_t warp_tot[32];
+  const int e = threadIdx.x;
+  int32_t c = 0;
+  if (e < E)
+    for (int b = 0; b < nblocks; ++b) c += hist[(int64_t)b * E + e];
+  // exclusive scan of c over e (block of 1024 threads = 32 warps)
+  const int lane = e & 31, wid = e >> 5;
+  int32_t incl = c;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int32_t n = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += n;
+  }
+  if (lane == 31) warp_tot[wid] = incl;
+  __syncthreads();
+  if (wid == 0) {
+    int32_t v = warp_tot[lane];
+    int32_t s = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int32_t n = __shfl_up_sync(0xffffffffu, s, o);
+      if (lane >= o) s += n;
+    }
+    warp_tot[lane] = s - v;   // exclusive prefix of warp totals
+  }
+  __syncthreads();
+  const int32_t excl = incl - c + warp_tot[wid];
+  if (e < E) {
+    counts[e] = c;
+    offsets[e] = excl;
+    if (e == E - 1) offsets[E] = excl + c;
+    int32_t run = excl;
+    for (int b = 0; b < nblocks; ++b) {
+      const int32_t h = hist[(int64_t)b * E + e];
+      hist[(int64_t)b * E + e] = run;
+      run += h;
+    }
+  }
+}
+
+__global__ void __launch_bounds__(kPermThreads) permute_scatter_kernel(
+    const int32_t* __restrict__ ids, int64_t R, int k, int E, const int32_t* __restrict__ base_be,
+    int32_t* __restrict__ row_map, int32_t* __restrict__ src_row) {
+  extern __shared__ int32_t sh[];              // [kPermWarps][E] counts, then bases
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  const int64_t chunk0 = (int64_t)blockIdx.x * kChunk;
+  const int64_t slice0 = chunk0 + (int64_t)wid * kPerWarp;
+  for (int q = threadIdx.x; q < kPermWarps * E; q += blockDim.x) sh[q] = 0;
+  __syncthreads();
+  // per-warp counts of its slice
+  for (int s = 0; s < kPerWarp; s += 32) {
+    const int64_t i = slice0 + s + lane;
+    if (i < R) {
+      const int e = ids[i];
+      if (e >= 0 && e < E) atomicAdd(&sh[wid * E + e], 1);
+    }
+  }
+  __syncthreads();
+  // per expert: exclusive scan over warps, plus the block's global base
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int32_t run = base_be[(int64_t)blockIdx.x * E + e];
+    for (int w = 0; w < kPermWarps; ++w) {
+      const int32_t c = sh[w * E + e];
+      sh[w * E + e] = run;
+      run += c;
+    }
+  }
+  __syncthreads();
+  // stable ranking inside the warp's slice, 32 assignments per step
+  int32_t* my = sh + wid * E;
+  for (int s = 0; s < kPerWarp; s += 32) {
+    const int64_t i = slice0 + s + lane;
+    const bool valid = i < R;
+    int e = valid ? ids[i] : -1;
+    if (e < 0 || e >= E) e = E + lane;        // unique key: matches no other lane
+    const uint32_t peers = __match_any_sync(0xffffffffu, e);
+    const uint32_t lower = peers & ((1u << lane) - 1u);
+    if (e < E) {
+      const int32_t row = my[e] + __popc(lower);
+      row_map[i] = row;
+      src_row[row] = (int32_t)(i / k);
+    }
+    __syncwarp();
+    // the highest lane of each group advances that expert's running base
+    if (e < E && (peers >> lane) == 1u) my[e] += __popc(peers);
+    __syncwarp();
+  }
+}
+
+__global__ void permute_rows_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ src_row,
+                                    int64_t R, int H, uint16_t* __restrict__ x_perm) {
+  const int64_t row = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= R) return;
+  const uint4* src = reinterpret_cast<const uint4*>(x + (int64_t)src_row[row] * H);
+  uint4* dst = reinterpret_cast<uint4*>(x_perm + row * H);
+  for (int c = lane; c < H / 8; c += 32) dst[c] = src[c];
+}
+
+}  // namespace
+
+size_t permute_workspace_bytes(int64_t R, int64_t E) {
+  const int64_t nb = (R + kChunk - 1) / kChunk;
+  return (size_t)((nb > 0 ? nb : 1) * E * sizeof(int32_t));
+}
+
+cudaError_t launch_permute(const int32_t* ids, int64_t T, int64_t k, int64_t E, int32_t* counts,
+                           int32_t* offsets, int32_t* row_map, int32_t* src_row, void* ws,
+                           uint32_t* status, cudaStream_t stream) {
+  const int64_t R = T * k;
+  const int nb = (int)((R + kChunk - 1) / kChunk);
+  int32_t* hist = static_cast<int32_t*>(ws);
+  if (nb > 0)
+    permute_hist_kernel<<<nb, kPermThreads, E * sizeof(int32_t), stream>>>(ids, R, (int)E, hist,
+                                                                           status);
+  permute_scan_kernel<<<1, 1024, 0, stream>>>(hist, nb, (int)E, counts, offsets);
+  if (nb > 0)
+    permute_scatter_kernel<<<nb, kPermThreads, kPermWarps * E * sizeof(int32_t), stream>>>(
+        ids, R, (int)k, (int)E, hist, row_map, src_row);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_permute_rows(const uint16_t* x, const int32_t* src_row, int64_t R, int64_t H,
+                                uint16_t* x_perm, cudaStream_t stream) {
+  if (R == 0) return cudaSuccess;
+  permute_rows_kernel<<<(unsigned)((R + 7) / 8), 256, 0, stream>>>(x, src_row, R, (int)H, x_perm);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,109 @@
+"""The MoE expert layer as a sequence of library calls, plus a torch autograd
+Function around it.
+
+Forward ("InternVL3.5 接入 pure FSDP2 后端开发实践", MindSpeed-MM issue 625,
+§8.2-§8.3): route -> permute -> grouped gate_up GEMM + SwiGLU -> grouped down
+GEMM -> unpermute-combine (+ the shared expert, "Awesome-ML-SYS-Tutorial"
+MoE/EP guide: shared experts are always active).  All calls are enqueued on
+the current stream with no host synchronisation: expert_offsets stay on the
+device and the grouped GEMMs read them there.
+
+Backward: combine_bwd -> route_bwd -> down_bwd -> gate_up_bwd -> gather_dx.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+import torch
+
+from . import ops
+
+
+@dataclass
+class ForwardState:
+    """What the forward keeps for the backward."""
+    x: torch.Tensor
+    ids: torch.Tensor
+    w: torch.Tensor
+    counts: torch.Tensor
+    offsets: torch.Tensor
+    row_map: torch.Tensor
+    src_row: torch.Tensor
+    gu_pre: torch.Tensor | None
+    h: torch.Tensor
+    y_perm: torch.Tensor
+    y_shared: torch.Tensor | None = None
+
+
+def moe_forward(x, w_router, gate_up, down, k, bias=None, sh_gate_up=None, sh_down=None,
+                save_for_backward=False):
+    """y [T, H] bf16 and the ForwardState."""
+    T, H = x.shape
+    E = w_router.shape[1]
+    I = down.shape[0] // E
+    ids, w = ops.route(x, w_router, k, bias)
+    counts, offsets, row_map, src_row = ops.permute(ids, E)
+    h, gu_pre = ops.grouped_gemm_gate_up_swiglu(x, src_row, offsets, gate_up, I,
+                                                save_gu_pre=save_for_backward)
+    y_perm = ops.grouped_gemm_down(h, offsets, down, H)
+    y_shared = None
+    if sh_gate_up is not None:
+        I_s = sh_down.shape[0]
+        hs, _ = ops.grouped_gemm_gate_up_swiglu(x, None, None, sh_gate_up, I_s)
+        y_shared = ops.grouped_gemm_down(hs, None, sh_down, H)
+    y = ops.unpermute_combine(y_perm, row_map, w, y_shared)
+    st = ForwardState(x, ids, w, counts, offsets, row_map, src_row, gu_pre, h, y_perm, y_shared)
+    return y, st
+
+
+def moe_backward(dy, st: ForwardState, w_router, gate_up, down, want_dw_router=False):
+    """dict(dx, d_logits, d_gate_up, d_down[, d_w_router]) for upstream gradient dy."""
+    if st.gu_pre is None:
+        raise ValueError("the forward ran without save_for_backward=True")
+    T, H = st.x.shape
+    E = w_router.shape[1]
+    k = st.w.shape[1]
+    dy_perm, dw = ops.unpermute_combine_bwd(dy, st.y_perm, st.row_map, st.w)
+    d_logits = ops.route_bwd(dw, st.w, st.ids, E)
+    dgu, d_down = ops.grouped_gemm_down_bwd(dy_perm, st.h, st.gu_pre, st.offsets, down)
+    dx_perm, d_gate_up = ops.grouped_gemm_gate_up_bwd(dgu, st.x, st.src_row, st.offsets, gate_up)
+    dx = ops.gather_dx(dx_perm, st.row_map, T, k, d_logits, st.ids, w_router)
+    out = dict(dx=dx, d_logits=d_logits, d_gate_up=d_gate_up, d_down=d_down, dw=dw)
+    if want_dw_router:
+        out["d_w_router"] = ops.route_bwd_weight(st.x, d_logits)
+    return out
+
+
+class MoELayerFunction(torch.autograd.Function):
+    """y = MoE(x); gradients for x, W_r, gate_up and down (fp32 W_r grad)."""
+
+    @staticmethod
+    def forward(ctx, x, w_router, gate_up, down, k, bias):
+        y, st = moe_forward(x.contiguous(), w_router.contiguous(), gate_up.contiguous(),
+                            down.contiguous(), k, bias, save_for_backward=True)
+        ctx.st = st
+        ctx.save_for_backward(w_router, gate_up, down)
+        return y
+
+    @staticmethod
+    def backward(ctx, dy):
+        w_router, gate_up, down = ctx.saved_tensors
+        g = moe_backward(dy.contiguous(), ctx.st, w_router, gate_up, down,
+                         want_dw_router=ctx.needs_input_grad[1])
+        return (g["dx"], g.get("d_w_router"), g["d_gate_up"], g["d_down"], None, None)
+
+
+class MoELayer(torch.nn.Module):
+    """Routed SwiGLU experts over the fused layout gate_up [E*H, 2I], down [E*I, H]."""
+
+    def __init__(self, hidden: int, n_experts: int, top_k: int, inter: int, device="cuda"):
+        super().__init__()
+        self.k = top_k
+        self.w_router = torch.nn.Parameter(torch.empty(hidden, n_experts, dtype=torch.float32, device=device))
+        self.gate_up = torch.nn.Parameter(torch.empty(n_experts * hidden, 2 * inter, dtype=torch.bfloat16,
+                                                      device=device))
+        self.down = torch.nn.Parameter(torch.empty(n_experts * inter, hidden, dtype=torch.bfloat16,
+                                                   device=device))
+
+    def forward(self, x, bias=None):
+        return MoELayerFunction.apply(x, self.w_router, self.gate_up, self.down, self.k, bias)

@@ -1,0 +1,249 @@
+"""Per-step entry points of the MoE layer on torch CUDA tensors.
+
+Argument marshalling only: each function checks dtypes and shapes, allocates
+its outputs with torch (device memory), and calls the matching C entry point
+of libmoe_gb300.so on the current torch stream.  Every step runs in the
+library's CUDA kernels; there is no CPU or PyTorch fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+
+import torch
+
+from ._lib import call
+
+_BF16 = torch.bfloat16
+
+
+def _stream():
+    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+
+def _p(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _need(t, name, dtype, ndim=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("%s must be a torch.Tensor" % name)
+    if not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor (the path runs only on the GPU)" % name)
+    if t.dtype != dtype:
+        raise TypeError("%s must be %s, got %s" % (name, dtype, t.dtype))
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError("%s must have %d dims" % (name, ndim))
+    return t
+
+
+def _ws(nbytes, device):
+    return torch.empty(max(int(nbytes), 16), dtype=torch.uint8, device=device)
+
+
+def sync_status():
+    """Synchronise the current stream and raise if a kernel reported a device-side error."""
+    detail = ctypes.c_uint32(0)
+    call("moe_sync_status", _stream(), ctypes.byref(detail))
+    return detail.value
+
+
+def set_wait_limit_ns(ns: int):
+    call("moe_set_wait_limit_ns", int(ns))
+
+
+# ----------------------------------------------------------------- forward
+
+def route(x, w_router, k, bias=None, return_logits=False):
+    """ids [T,k] int32, w [T,k] fp32 (and logits [T,E] fp32)."""
+    _need(x, "x", _BF16, 2)
+    _need(w_router, "w_router", torch.float32, 2)
+    if bias is not None:
+        _need(bias, "bias", torch.float32, 1)
+    T, H = x.shape
+    E = w_router.shape[1]
+    dev = x.device
+    ids = torch.empty((T, k), dtype=torch.int32, device=dev)
+    w = torch.empty((T, k), dtype=torch.float32, device=dev)
+    logits = torch.empty((T, E), dtype=torch.float32, device=dev)
+    call("moe_route", _p(x), _p(w_router), _p(bias), T, H, E, k, _p(ids), _p(w), _p(logits), None, 0,
+         _stream())
+    return (ids, w, logits) if return_logits else (ids, w)
+
+
+def permute(ids, E):
+    """counts [E], offsets [E+1], row_map [R], src_row [R] (all int32)."""
+    _need(ids, "ids", torch.int32, 2)
+    T, k = ids.shape
+    dev = ids.device
+    nbytes = ctypes.c_size_t(0)
+    call("moe_permute_workspace_size", T, k, E, ctypes.byref(nbytes))
+    ws = _ws(nbytes.value, dev)
+    counts = torch.empty(E, dtype=torch.int32, device=dev)
+    offsets = torch.empty(E + 1, dtype=torch.int32, device=dev)
+    row_map = torch.empty(T * k, dtype=torch.int32, device=dev)
+    src_row = torch.empty(T * k, dtype=torch.int32, device=dev)
+    call("moe_permute", _p(ids), T, k, E, _p(counts), _p(offsets), _p(row_map), _p(src_row), _p(ws),
+         ws.numel(), _stream())
+    return counts, offsets, row_map, src_row
+
+
+def permute_rows(x, src_row):
+    _need(x, "x", _BF16, 2)
+    _need(src_row, "src_row", torch.int32, 1)
+    R, H = src_row.shape[0], x.shape[1]
+    out = torch.empty((R, H), dtype=_BF16, device=x.device)
+    call("moe_permute_rows", _p(x), _p(src_row), R, H, _p(out), _stream())
+    return out
+
+
+def grouped_gemm_gate_up_swiglu(x, src_row, offsets, gate_up, I, R=None, save_gu_pre=False):
+    """h [R, I] bf16 (and gu_pre [R, 2I] bf16).  src_row/offsets None: dense (E = 1)."""
+    _need(x, "x", _BF16, 2)
+    _need(gate_up, "gate_up", _BF16, 2)
+    T, H = x.shape
+    E = gate_up.shape[0] // H
+    if gate_up.shape != (E * H, 2 * I):
+        raise ValueError("gate_up must be [E*H, 2I]")
+    if src_row is not None:
+        _need(src_row, "src_row", torch.int32, 1)
+        R = src_row.shape[0]
+    elif R is None:
+        R = T
+    if offsets is not None:
+        _need(offsets, "offsets", torch.int32, 1)
+    h = torch.empty((R, I), dtype=_BF16, device=x.device)
+    gu = torch.empty((R, 2 * I), dtype=_BF16, device=x.device) if save_gu_pre else None
+    call("moe_grouped_gemm_gate_up_swiglu", _p(x), _p(src_row), _p(offsets), _p(gate_up), T, R, H, E, I,
+         _p(h), _p(gu), _stream())
+    return h, gu
+
+
+def grouped_gemm_down(h, offsets, down, H):
+    """y_perm [R, H] bf16."""
+    _need(h, "h", _BF16, 2)
+    _need(down, "down", _BF16, 2)
+    R, I = h.shape
+    E = down.shape[0] // I
+    if down.shape != (E * I, H):
+        raise ValueError("down must be [E*I, H]")
+    if offsets is not None:
+        _need(offsets, "offsets", torch.int32, 1)
+    y = torch.empty((R, H), dtype=_BF16, device=h.device)
+    call("moe_grouped_gemm_down", _p(h), _p(offsets), _p(down), R, H, E, I, _p(y), _stream())
+    return y
+
+
+def unpermute_combine(y_perm, row_map, w, y_shared=None):
+    """y [T, H] bf16."""
+    _need(y_perm, "y_perm", _BF16, 2)
+    _need(row_map, "row_map", torch.int32, 1)
+    _need(w, "w", torch.float32, 2)
+    if y_shared is not None:
+        _need(y_shared, "y_shared", _BF16, 2)
+    T, k = w.shape
+    H = y_perm.shape[1]
+    y = torch.empty((T, H), dtype=_BF16, device=y_perm.device)
+    call("moe_unpermute_combine", _p(y_perm), _p(row_map), _p(w), _p(y_shared), T, H, k, _p(y), _stream())
+    return y
+
+
+# ---------------------------------------------------------------- backward
+
+def unpermute_combine_bwd(dy, y_perm, row_map, w):
+    """dy_perm [R, H] bf16, dw [T, k] fp32."""
+    _need(dy, "dy", _BF16, 2)
+    _need(y_perm, "y_perm", _BF16, 2)
+    _need(row_map, "row_map", torch.int32, 1)
+    _need(w, "w", torch.float32, 2)
+    T, k = w.shape
+    H = dy.shape[1]
+    dy_perm = torch.empty((T * k, H), dtype=_BF16, device=dy.device)
+    dw = torch.empty((T, k), dtype=torch.float32, device=dy.device)
+    call("moe_unpermute_combine_bwd", _p(dy), _p(y_perm), _p(row_map), _p(w), T, H, k, _p(dy_perm), _p(dw),
+         _stream())
+    return dy_perm, dw
+
+
+def route_bwd(dw, w, ids, E):
+    """d_logits [T, E] fp32."""
+    _need(dw, "dw", torch.float32, 2)
+    _need(w, "w", torch.float32, 2)
+    _need(ids, "ids", torch.int32, 2)
+    T, k = w.shape
+    dl = torch.empty((T, E), dtype=torch.float32, device=w.device)
+    call("moe_route_bwd", _p(dw), _p(w), _p(ids), T, E, k, _p(dl), _stream())
+    return dl
+
+
+def grouped_gemm_down_bwd(dy_perm, h, gu_pre, offsets, down):
+    """dgu [R, 2I] bf16, d_down [E*I, H] bf16."""
+    _need(dy_perm, "dy_perm", _BF16, 2)
+    _need(h, "h", _BF16, 2)
+    _need(gu_pre, "gu_pre", _BF16, 2)
+    _need(down, "down", _BF16, 2)
+    R, I = h.shape
+    H = dy_perm.shape[1]
+    E = down.shape[0] // I
+    if offsets is not None:
+        _need(offsets, "offsets", torch.int32, 1)
+    dgu = torch.empty((R, 2 * I), dtype=_BF16, device=h.device)
+    d_down = torch.empty((E * I, H), dtype=_BF16, device=h.device)
+    call("moe_grouped_gemm_down_bwd", _p(dy_perm), _p(h), _p(gu_pre), _p(offsets), _p(down), R, H, E, I,
+         _p(dgu), _p(d_down), _stream())
+    return dgu, d_down
+
+
+def grouped_gemm_gate_up_bwd(dgu, x, src_row, offsets, gate_up):
+    """dx_perm [R, H] bf16, d_gate_up [E*H, 2I] bf16."""
+    _need(dgu, "dgu", _BF16, 2)
+    _need(x, "x", _BF16, 2)
+    _need(gate_up, "gate_up", _BF16, 2)
+    R, I2 = dgu.shape
+    I = I2 // 2
+    T, H = x.shape
+    E = gate_up.shape[0] // H
+    if src_row is not None:
+        _need(src_row, "src_row", torch.int32, 1)
+    if offsets is not None:
+        _need(offsets, "offsets", torch.int32, 1)
+    dx_perm = torch.empty((R, H), dtype=_BF16, device=x.device)
+    d_gu = torch.empty((E * H, 2 * I), dtype=_BF16, device=x.device)
+    call("moe_grouped_gemm_gate_up_bwd", _p(dgu), _p(x), _p(src_row), _p(offsets), _p(gate_up), T, R, H, E,
+         I, _p(dx_perm), _p(d_gu), _stream())
+    return dx_perm, d_gu
+
+
+def gather_dx(dx_perm, row_map, T, k, d_logits=None, ids=None, w_router=None):
+    """dX [T, H] bf16 = sum_j dx_perm[row_map] (+ d_logits . W_r^T on the chosen experts)."""
+    _need(dx_perm, "dx_perm", _BF16, 2)
+    _need(row_map, "row_map", torch.int32, 1)
+    H = dx_perm.shape[1]
+    E = 1
+    ws = None
+    if d_logits is not None:
+        _need(d_logits, "d_logits", torch.float32, 2)
+        _need(ids, "ids", torch.int32, 2)
+        _need(w_router, "w_router", torch.float32, 2)
+        E = w_router.shape[1]
+        nbytes = ctypes.c_size_t(0)
+        call("moe_gather_dx_workspace_size", H, E, ctypes.byref(nbytes))
+        ws = _ws(nbytes.value, dx_perm.device)
+    else:
+        E = max(k, 1)
+    dx = torch.empty((T, H), dtype=_BF16, device=dx_perm.device)
+    call("moe_gather_dx", _p(dx_perm), _p(row_map), _p(d_logits), _p(ids), _p(w_router), T, H, E, k, _p(dx),
+         _p(ws), 0 if ws is None else ws.numel(), _stream())
+    return dx
+
+
+def route_bwd_weight(x, d_logits):
+    """d_w_router [H, E] fp32 = x^T . d_logits."""
+    _need(x, "x", _BF16, 2)
+    _need(d_logits, "d_logits", torch.float32, 2)
+    T, H = x.shape
+    E = d_logits.shape[1]
+    out = torch.empty((H, E), dtype=torch.float32, device=x.device)
+    call("moe_route_bwd_weight", _p(x), _p(d_logits), T, H, E, _p(out), _stream())
+    return out
