@@ -1,0 +1,488 @@
+"""Benchmark of the MoE expert layer on GB300 (one JSON line on rank 0).
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+                  [--workload qwen3_moe] [--no-fwd-bwd] [--no-cpu-baseline]
+
+A step is one pass of the layer over one batch of synthetic input: route ->
+permute -> grouped gate_up GEMM + SwiGLU -> grouped down GEMM -> combine, on
+the Qwen3-MoE-shaped workload (T=4096, H=2048, E=128, k=8, I=768) unless
+--workload names another.  Inputs and weights are resident in HBM; L2 is
+flushed (256 MB write) before every step, outside the timed events.  `value`
+is tokens/s over exactly K device-timed steps (CUDA events on the launching
+stream), max over ranks; `e2e` repeats the step through the public API with
+the tokens copied from pinned host memory and the output copied back inside
+the timed region.  A training step (forward + backward) at the training
+workload (T=8192) is reported under `fwd_bwd`.
+
+Under torchrun (N > 1) every rank runs an independent replica on its own GPU
+(the layer has no data-path exchange on one node here: "replicas only");
+ranks meet only at the timing barriers.
+
+--impl reference times the fp64 CPU oracle (the reference arm: a plain, slow
+restatement of the layer) on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "MoE layer tokens/s (fwd; fwd+bwd) and grouped-GEMM % of GB300 bf16 peak"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--workload", default="qwen3_moe")
+    ap.add_argument("--no-fwd-bwd", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--gather", default="rows", choices=["fused", "rows"],
+                    help="fused: the gate_up GEMM gathers token rows itself (TMA row gather); "
+                         "rows: materialise the permuted rows first and stream them with tile loads")
+    return ap.parse_args()
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+# --------------------------------------------------------------- distributed
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def init_dist(backend):
+    import torch.distributed as dist
+
+    ws, rank, _ = dist_env()
+    if ws > 1 and not dist.is_initialized():
+        dist.init_process_group(backend=backend)
+    return dist if ws > 1 else None
+
+
+def barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+def max_over_ranks(dist, value, device=None):
+    if dist is None:
+        return value
+    import torch
+
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+        self.t = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def stop(self, t0, t1):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        mhz, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ts, line in self.lines:
+            if not (t0 - 0.05 <= ts <= t1 + 0.05):
+                continue
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                mhz.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not mhz:
+            return {"sm_mhz": None, "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": 0}
+        mhz.sort()
+        return {"sm_mhz": mhz[len(mhz) // 2], "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(mhz)}
+
+
+# ------------------------------------------------------------ native arm
+
+def traffic_for(kernel_src):
+    """dram bytes (read + write) per launch of the dominant kernel from the
+    committed ncu summary, or None when the kernel source changed since it was
+    captured (the summary records the sha256 of the source it profiled)."""
+    path = os.path.join(ROOT, "profiles", "grouped_gemm_qwen3_moe.md")
+    if not os.path.exists(path):
+        return None
+    fields = {}
+    with open(path) as f:
+        for line in f:
+            if ":" in line and line.split(":")[0] in ("source_sha256", "dram_bytes_per_launch"):
+                k, v = line.split(":", 1)
+                fields[k.strip()] = v.strip()
+    h = hashlib.sha256(open(kernel_src, "rb").read()).hexdigest()
+    if fields.get("source_sha256") != h or "dram_bytes_per_launch" not in fields:
+        return None
+    return int(fields["dram_bytes_per_launch"])
+
+
+def device_inputs(cfg, torch, device):
+    import numpy as np
+
+    import synth
+
+    inp = synth.make_inputs(cfg, with_dy=cfg.train)
+
+    def bf(a):
+        return torch.from_numpy(a.view(np.int16)).to(device).view(torch.bfloat16)
+
+    d = dict(x=bf(inp.x), w_router=torch.from_numpy(inp.w_router).to(device), gate_up=bf(inp.gate_up),
+             down=bf(inp.down))
+    d["bias"] = torch.from_numpy(inp.bias).to(device) if inp.bias is not None else None
+    d["sh_gate_up"] = bf(inp.sh_gate_up) if inp.sh_gate_up is not None else None
+    d["sh_down"] = bf(inp.sh_down) if inp.sh_down is not None else None
+    d["dy"] = bf(inp.dy) if inp.dy is not None else None
+    d["x_host"] = torch.from_numpy(inp.x.view(np.int16)).view(torch.bfloat16).pin_memory()
+    return d
+
+
+def run_native(args):
+    import torch
+
+    import synth
+    import token_dispatch_grouped_softmax_gb300 as moe
+
+    ws, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    dist = init_dist("nccl")
+    moe.build()
+    moe.load()
+    cfg = synth.CONFIGS[args.workload]
+    pk, pk_kind = peaks()
+    d = device_inputs(cfg, torch, device)
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=device)
+    stream = torch.cuda.current_stream()
+    T, H, E, k, I = cfg.T, cfg.H, cfg.E, cfg.k, cfg.I
+    I_s = cfg.I_shared
+
+    fused = args.gather == "fused"
+    names = ["route", "permute"] + ([] if fused else ["permute_rows"]) + ["gate_up", "down"] + \
+        (["shared"] if I_s else []) + ["combine"]
+
+    def step(ev=None):
+        j = [0]
+
+        def mark():
+            if ev is not None:
+                ev[j[0]].record(stream)
+            j[0] += 1
+        mark()
+        ids, w = moe.route(d["x"], d["w_router"], k, d["bias"])
+        mark()
+        counts, offsets, row_map, src_row = moe.permute(ids, E)
+        mark()
+        if fused:
+            h, _, _ = moe.grouped_gemm_gate_up_swiglu(d["x"], src_row, offsets, d["gate_up"], I)
+        else:
+            x_perm = moe.permute_rows(d["x"], src_row)
+            mark()
+            h, _, _ = moe.grouped_gemm_gate_up_swiglu(x_perm, None, offsets, d["gate_up"], I)
+        mark()
+        y_perm = moe.grouped_gemm_down(h, offsets, d["down"], H)
+        mark()
+        y_sh = None
+        if I_s:
+            hs, _, _ = moe.grouped_gemm_gate_up_swiglu(d["x"], None, None, d["sh_gate_up"], I_s)
+            y_sh = moe.grouped_gemm_down(hs, None, d["sh_down"], H)
+            mark()
+        y = moe.unpermute_combine(y_perm, row_map, w, y_sh)
+        mark()
+        return y
+
+    launches_per_step = 2 + 3 + (0 if fused else 1) + 1 + 1 + (2 if I_s else 0) + 1
+    for _ in range(max(args.warmup, 3)):
+        step()
+    moe.sync_status()
+    torch.cuda.synchronize()
+
+    K = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)] for _ in range(K)]
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    barrier(dist)
+    torch.cuda.synchronize()
+    t0 = time.time()
+    for i in range(K):
+        flush.zero_()
+        step(evs[i])
+    torch.cuda.synchronize()
+    barrier(dist)
+    t1 = time.time()
+    clk = clocks.stop(t0, t1)
+    moe.sync_status()
+
+    step_ms = [evs[i][0].elapsed_time(evs[i][-1]) for i in range(K)]
+    per_kernel = {n: sum(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(K)) / K
+                  for j, n in enumerate(names)}
+    total_s = sum(step_ms) / 1e3
+    total_s = max_over_ranks(dist, total_s, device)
+    value = ws * T * K / total_s
+    ms_per_step = 1e3 * total_s / K
+
+    # rooflines
+    f_gate_up = 2.0 * cfg.R * H * 2 * I
+    f_down = 2.0 * cfg.R * I * H
+    gemm_ms = per_kernel["gate_up"] + per_kernel["down"] + per_kernel.get("shared", 0.0)
+    gemm_flops = cfg.flops_fwd()
+    peak_tf = pk["bf16_tflops"]
+    achieved = f_gate_up / (per_kernel["gate_up"] * 1e-3) / 1e12
+    src = os.path.join(ROOT, "token_dispatch_grouped_softmax_gb300", "csrc", "grouped_gemm.cu")
+    roofline = {"bound": "tensor", "kernel": "grouped_gemm_kernel<FWD_GATEUP>",
+                "achieved": round(achieved, 1), "peak": peak_tf, "unit": "TFLOP/s",
+                "frac": round(achieved / peak_tf, 4), "traffic": traffic_for(src),
+                "peak_kind": "%s burst bf16 (MEASURED_PEAKS.json)" % pk_kind,
+                "algorithmic_flops_per_launch": f_gate_up}
+    comb_bytes = cfg.R * H * 2 + T * H * 2 + cfg.R * 8
+    out = {
+        "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": ws, "steps": K,
+        "warmup": max(args.warmup, 3), "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": cfg.name, "T": T, "H": H, "E": E, "k": k, "I": I, "I_shared": I_s,
+                   "seed": cfg.seed, "description": cfg.description,
+                   "l2": "flushed before every step (256 MB write), outside the timed events",
+                   "parallelism": "replicas" if ws > 1 else "single",
+                   "gather": args.gather},
+        "roofline": roofline,
+        "kernels_us": {n: round(v * 1e3, 2) for n, v in per_kernel.items()},
+        "gemm": {"tflops": round(gemm_flops / (gemm_ms * 1e-3) / 1e12, 1),
+                 "frac_of_peak": round(gemm_flops / (gemm_ms * 1e-3) / 1e12 / peak_tf, 4),
+                 "down_tflops": round(f_down / (per_kernel["down"] * 1e-3) / 1e12, 1)},
+        "combine": {"gbs": round(comb_bytes / (per_kernel["combine"] * 1e-3) / 1e9, 1),
+                    "frac_of_hbm": round(comb_bytes / (per_kernel["combine"] * 1e-3) / 1e9 / pk["hbm_gbs"], 4),
+                    "algorithmic_bytes": comb_bytes},
+        "gpu_launches": launches_per_step * K,
+        "clocks": clk,
+        "wall_s": round(t1 - t0, 3),
+    }
+
+    if not args.no_e2e:
+        out["e2e"] = e2e(moe, d, cfg, torch, stream, dist, device, ws, min(K, 100), fused)
+    if not args.no_fwd_bwd:
+        del d
+        torch.cuda.empty_cache()
+        out["fwd_bwd"] = fwd_bwd(moe, torch, stream, dist, device, ws, flush, pk, fused)
+    if rank == 0 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(cfg, target_s=15.0)
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+
+
+def e2e(moe, d, cfg, torch, stream, dist, device, ws, K, fused):
+    """Tokens from pinned host memory -> layer -> output back to pinned host memory."""
+    T, H = cfg.T, cfg.H
+    x_dev = torch.empty_like(d["x"])
+    y_host = torch.empty((T, H), dtype=torch.bfloat16).pin_memory()
+
+    def step():
+        x_dev.copy_(d["x_host"], non_blocking=True)
+        y, _ = moe.moe_forward(x_dev, d["w_router"], d["gate_up"], d["down"], cfg.k, d["bias"],
+                               d["sh_gate_up"], d["sh_down"], fused_gather=fused)
+        y_host.copy_(y, non_blocking=True)
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    barrier(dist)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(K):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(dist)
+    s = max_over_ranks(dist, e0.elapsed_time(e1) / 1e3, device)
+    return {"value": round(ws * T * K / s, 1), "unit": "tokens/s", "h2d_bytes_per_step": T * H * 2,
+            "d2h_bytes_per_step": T * H * 2, "steps": K,
+            "note": "weights resident; x H2D from pinned host + y D2H to pinned host inside the timed region"}
+
+
+def fwd_bwd(moe, torch, stream, dist, device, ws, flush, pk, fused):
+    """Training step (forward with saved activations + backward) on the training workload."""
+    import synth
+
+    cfg = synth.CONFIGS["qwen3_moe_train"]
+    d = device_inputs(cfg, torch, device)
+    K = 30
+
+    def step():
+        y, st = moe.moe_forward(d["x"], d["w_router"], d["gate_up"], d["down"], cfg.k, save_for_backward=True,
+                                fused_gather=fused)
+        g = moe.moe_backward(d["dy"], st, d["w_router"], d["gate_up"], d["down"])
+        return g
+
+    for _ in range(3):
+        step()
+    moe.sync_status()
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    barrier(dist)
+    for i in range(K):
+        flush.zero_()
+        evs[i][0].record(stream)
+        step()
+        evs[i][1].record(stream)
+    torch.cuda.synchronize()
+    barrier(dist)
+    moe.sync_status()
+    s = sum(a.elapsed_time(b) for a, b in evs) / 1e3
+    s = max_over_ranks(dist, s, device)
+    flops = 3.0 * cfg.flops_fwd()
+    return {"workload": cfg.name, "T": cfg.T, "value": round(ws * cfg.T * K / s, 1), "unit": "tokens/s",
+            "ms_per_step": round(1e3 * s / K, 4), "gemm_flops_per_step": flops,
+            "layer_tflops": round(flops * K / s / 1e12, 1), "steps": K,
+            "launches_per_step": 8 + (0 if fused else 1) + 1 + 1 + 2 + 2 + 2}
+
+
+# -------------------------------------------------------------- CPU oracle
+
+def cpu_baseline(cfg, target_s=15.0, max_tokens=None):
+    """The fp64 oracle as it stands, on a bounded token sample of the workload:
+    route + per-token expert FFNs + combine for n tokens; tokens/s."""
+    import numpy as np
+
+    import oracle
+    import synth
+
+    inp = synth.make_inputs(cfg)
+    cores = os.cpu_count() or 1
+
+    def run(n):
+        x = np.ascontiguousarray(inp.x[:n])
+        t = time.perf_counter()
+        r = oracle.route(x, inp.w_router, inp.bias, cfg.k)
+        oracle.forward_tokens(np.arange(n), x, inp.gate_up, inp.down, r["ids"], r["w"], inp.sh_gate_up,
+                              inp.sh_down)
+        return time.perf_counter() - t
+
+    n0 = 32
+    t_pilot = run(n0)
+    n = int(min(cfg.T if max_tokens is None else max_tokens, max(n0, n0 * target_s / max(t_pilot, 1e-6))))
+    dt = run(n) if n != n0 else t_pilot
+    return {"value": round(n / dt, 2), "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": "first %d of %d tokens of %s (route + per-token expert FFNs + combine, fp64), %.1f s"
+                      % (n, cfg.T, cfg.name, dt)}
+
+
+def run_reference(args):
+    ws, rank, local = dist_env()
+    if rank != 0:
+        return
+    import synth
+
+    cfg = synth.CONFIGS[args.workload]
+    K, W = args.steps, max(args.warmup, 0)
+    # bounded: each step a sample sized so that the whole run ends within minutes
+    per_step_s = max(1.0, 60.0 / max(K + W, 1))
+    base = cpu_baseline(cfg, target_s=per_step_s)
+    n = int(base["sample"].split()[1])
+    import numpy as np
+
+    import oracle
+
+    inp = synth.make_inputs(cfg)
+    x = np.ascontiguousarray(inp.x[:n])
+
+    def step():
+        r = oracle.route(x, inp.w_router, inp.bias, cfg.k)
+        oracle.forward_tokens(np.arange(n), x, inp.gate_up, inp.down, r["ids"], r["w"], inp.sh_gate_up,
+                              inp.sh_down)
+
+    for _ in range(W):
+        step()
+    t = time.perf_counter()
+    for _ in range(K):
+        step()
+    dt = time.perf_counter() - t
+    value = n * K / dt
+    out = {"impl": "reference", "metric": METRIC, "value": round(value, 2), "unit": "tokens/s", "n_gpus": ws,
+           "steps": K, "warmup": W, "ms_per_step": round(1e3 * dt / K, 3), "higher_is_better": True,
+           "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+           "config": {"workload": cfg.name, "T": cfg.T, "H": cfg.H, "E": cfg.E, "k": cfg.k, "I": cfg.I,
+                      "I_shared": cfg.I_shared, "seed": cfg.seed},
+           "cpu_baseline": {"value": round(value, 2), "unit": "tokens/s", "cores": os.cpu_count() or 1,
+                            "kind": "oracle",
+                            "sample": "first %d of %d tokens per step (fp64 oracle, route + experts + combine)"
+                                      % (n, cfg.T)},
+           "e2e": {"value": round(value, 2), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                   "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_native(args)
+
+
+if __name__ == "__main__":
+    main()

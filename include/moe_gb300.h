@@ -73,9 +73,11 @@ int moe_set_wait_limit_ns(uint64_t ns);
 
 /* ------------------------------------------------------------------ route */
 
-/* Bytes of workspace moe_route needs: T*E*4 when `logits` is NULL (the logits
- * are staged there), else 0. */
-int moe_route_workspace_size(int64_t T, int64_t E, int has_logits_out, size_t* bytes);
+/* Bytes of workspace moe_route needs.  With E % 8 == 0 and H % 64 == 0 the
+ * logits run on the tensor cores: the workspace holds the exact three-term
+ * bf16 split of W_r (3*H*E*2 bytes) and fp32 partial logits of a split-K
+ * GEMM (parts*T*E*4 bytes); otherwise it holds the fp32 logits (T*E*4). */
+int moe_route_workspace_size(int64_t T, int64_t H, int64_t E, size_t* bytes);
 
 /* Router (MindSpeed page §8.2: gate -> FP32 softmax -> top-k -> renormalise).
  *   x        [T, H] bf16         tokens
@@ -85,8 +87,11 @@ int moe_route_workspace_size(int64_t T, int64_t E, int has_logits_out, size_t* b
  *                                equal fp32 logits go to the lower index
  *   w        [T, k] fp32 (out)   p_j / sum of the chosen p (sums to 1)
  *   logits   [T, E] fp32 (out, nullable) x . W_r + bias
- * Limits: 1 <= k <= min(E, 32), E <= 1024, H % 8 == 0.  The dot products
- * accumulate in fp32 from the exact bf16 x; the softmax is fp32. */
+ *   workspace                    device scratch, moe_route_workspace_size bytes
+ * Limits: 1 <= k <= min(E, 32), E <= 1024, H % 8 == 0.  The logits are the
+ * fp32-accumulated dot products of the exact bf16 x with the fp32 W_r (on
+ * the tensor cores through an exact three-term bf16 split of W_r, or on the
+ * CUDA cores); the softmax is fp32. */
 int moe_route(const uint16_t* x, const float* w_router, const float* bias, int64_t T, int64_t H,
               int64_t E, int64_t k, int32_t* ids, float* w, float* logits, void* workspace,
               size_t workspace_bytes, void* stream);
@@ -99,16 +104,18 @@ int moe_permute_workspace_size(int64_t T, int64_t k, int64_t E, size_t* bytes);
 /* Group the R = T*k assignments by expert ("Awesome-ML-SYS-Tutorial" guide:
  * per-expert token counts, then permute by expert; MindSpeed page §8.3).
  *   ids      [T, k] int32  expert of each (token, slot); i = t*k + j
+ *   w        [T, k] fp32 or NULL   gate weights to carry along (with w_perm)
  *   counts   [E] int32 (out)     rows per expert (empty experts give 0)
  *   offsets  [E+1] int32 (out)   exclusive scan of counts, offsets[E] = R
  *   row_map  [R] int32 (out)     permuted row of assignment i; stable: the
  *                                rows of one expert keep increasing i
  *   src_row  [R] int32 (out)     token of each permuted row (= i / k)
+ *   w_perm   [R] fp32 (out) or NULL   w_perm[row_map[i]] = w[i]
  * Deterministic (no order-dependent atomics).  An id outside [0, E) sets
  * MOE_ERR_DEVICE in the status word; the outputs are then undefined.
  * Limits: E <= 1024, R < 2^31. */
-int moe_permute(const int32_t* ids, int64_t T, int64_t k, int64_t E, int32_t* counts,
-                int32_t* offsets, int32_t* row_map, int32_t* src_row, void* workspace,
+int moe_permute(const int32_t* ids, const float* w, int64_t T, int64_t k, int64_t E, int32_t* counts,
+                int32_t* offsets, int32_t* row_map, int32_t* src_row, float* w_perm, void* workspace,
                 size_t workspace_bytes, void* stream);
 
 /* The materialised permute: x_perm[row] = x[src_row[row]] for R rows of H
@@ -121,20 +128,25 @@ int moe_permute_rows(const uint16_t* x, const int32_t* src_row, int64_t R, int64
 /* Grouped gate_up GEMM with the SwiGLU fused into its epilogue (MindSpeed
  * page §2 layout, §8.3 "grouped_matmul -> SwiGLU").  For each expert e and
  * each permuted row r in [offsets[e], offsets[e+1]):
- *   g = x[src_row[r]] . gate_up[e*H:(e+1)*H, 0:I]
- *   u = x[src_row[r]] . gate_up[e*H:(e+1)*H, I:2I]
- *   h[r] = silu(g) * u                        (fp32, stored bf16)
- *   gu_pre[r] = [g | u]                        (bf16, when not NULL)
- *   x        [T, H] bf16;  gate_up [E*H, 2I] bf16;  h [R, I] bf16
- *   src_row  [R] int32, or NULL for rows taken in order (x has R rows)
+ *   a = x[src_row[r]]  (or x[r] when src_row is NULL)
+ *   g = a . gate_up[e*H:(e+1)*H, 0:I],   u = a . gate_up[e*H:(e+1)*H, I:2I]
+ *   h[r] = silu(g) * u                          (fp32, stored bf16)
+ *   gu_pre[r] = [g | u]                          (fp32, when not NULL)
+ *   h_w[r] = w_perm[r] * silu(g) * u             (bf16, when not NULL)
+ *   x        [T, H] bf16 (or [R, H] already permuted, src_row NULL)
+ *   gate_up  [E*H, 2I] bf16;  h, h_w [R, I] bf16;  gu_pre [R, 2I] fp32
+ *   src_row  [R] int32: the permute is fused into the A-operand load (TMA
+ *            row gather); NULL: rows are read in order
  *   offsets  [E+1] int32 on the device (never read back to the host), or
  *            NULL for one group of all R rows (E must be 1): the dense mode
  *            used for the shared expert
- * bf16 inputs, fp32 accumulation (tcgen05 tensor cores), bf16 outputs. */
+ *   w_perm   [R] fp32 (from moe_permute), needed only for h_w
+ * The training forward saves gu_pre and h_w for the backward.
+ * bf16 inputs, fp32 accumulation (tcgen05 tensor cores). */
 int moe_grouped_gemm_gate_up_swiglu(const uint16_t* x, const int32_t* src_row,
                                     const int32_t* offsets, const uint16_t* gate_up, int64_t T,
                                     int64_t R, int64_t H, int64_t E, int64_t I, uint16_t* h,
-                                    uint16_t* gu_pre, void* stream);
+                                    const float* w_perm, float* gu_pre, uint16_t* h_w, void* stream);
 
 /* Grouped down GEMM (MindSpeed page §2 layout, §8.3):
  *   y_perm[r] = h[r] . down[e*I:(e+1)*I, :]   for r in expert e's rows
@@ -160,40 +172,53 @@ int moe_unpermute_combine(const uint16_t* y_perm, const int32_t* row_map, const 
 /* --------------------------------------------------------------- backward */
 /* The backward of L with upstream gradient dY, the chosen experts held fixed
  * (the gradient reaches the router only through the renormalised weights).
- * Call order: combine_bwd -> route_bwd -> down_bwd -> gate_up_bwd -> gather_dx. */
+ * Call order: combine_bwd -> down_bwd -> route_bwd -> gate_up_bwd -> gather_dx. */
 
-/* Backward of the combine:
- *   dy_perm[row_map[t*k+j]] = w[t,j] * dY[t]            (bf16)
- *   dw[t,j] = <dY[t], y_perm[row_map[t*k+j]]>           (fp32)
- *   dy [T, H] bf16; y_perm [R, H] bf16 (saved forward output). */
-int moe_unpermute_combine_bwd(const uint16_t* dy, const uint16_t* y_perm, const int32_t* row_map,
-                              const float* w, int64_t T, int64_t H, int64_t k, uint16_t* dy_perm,
-                              float* dw, void* stream);
+/* Backward of the combine with respect to the expert outputs, before the
+ * gate weights (which the grouped GEMMs apply in fp32):
+ *   dy_perm[row] = dY[src_row[row]]         (an exact bf16 copy; R = T*k rows)
+ * The gate-weight gradient dw[t,j] = <dY[t], y_perm[row_map[t*k+j]]> is
+ * produced by moe_grouped_gemm_down_bwd (as <dY . Wd^T, h>) and summed by
+ * moe_route_bwd.  dy [T, H] bf16; src_row [R] int32; dy_perm [R, H] bf16. */
+int moe_unpermute_combine_bwd(const uint16_t* dy, const int32_t* src_row, int64_t T, int64_t H,
+                              int64_t k, uint16_t* dy_perm, void* stream);
 
-/* Backward of the renormalised softmax (w = softmax over the chosen logits):
- *   d_logits[t, ids[t,j]] = w[t,j] * (dw[t,j] - sum_i w[t,i] dw[t,i])
- *   d_logits[t, e] = 0 for every expert not chosen by t
- *   d_logits [T, E] fp32 (out). */
-int moe_route_bwd(const float* dw, const float* w, const int32_t* ids, int64_t T, int64_t E,
-                  int64_t k, float* d_logits, void* stream);
+/* Number of partial sums per permuted row that moe_grouped_gemm_down_bwd
+ * writes into dw_part (one per 256-column tile of I). */
+int moe_grouped_gemm_down_bwd_parts(int64_t I, int64_t* nparts);
 
 /* Backward of the down GEMM and of the SwiGLU, per expert e:
- *   dh = dy_perm[r] . down_e^T                       (fp32)
- *   g, u = gu_pre[r];  s = sigmoid(g)
+ *   a = dy_perm[r] . down_e^T                         (fp32)
+ *   dh = w_perm[r] * a;  g, u = gu_pre[r];  s = sigmoid(g)
  *   dgu[r] = [ dh * u * s * (1 + g*(1-s))  |  dh * g * s ]   (bf16)
- *   d_down_e = h_e^T . dy_perm_e                     (fp32 accumulate, bf16;
- *                                                     0 for an empty expert)
- *   dy_perm [R, H]; h [R, I]; gu_pre [R, 2I]; down [E*I, H];
- *   dgu [R, 2I] (out); d_down [E*I, H] (out). */
-int moe_grouped_gemm_down_bwd(const uint16_t* dy_perm, const uint16_t* h, const uint16_t* gu_pre,
-                              const int32_t* offsets, const uint16_t* down, int64_t R, int64_t H,
-                              int64_t E, int64_t I, uint16_t* dgu, uint16_t* d_down, void* stream);
+ *   dw_part[r, n] = sum over tile n's columns of a * silu(g) * u   (fp32;
+ *                   summed over n this is <dY[t], y_perm[r]>, the gradient
+ *                   of the gate weight of row r)
+ *   d_down_e = h_w_e^T . dy_perm_e                    (fp32 accumulate, bf16;
+ *                                                      0 for an empty expert)
+ *   dy_perm [R, H] bf16 (unweighted); h_w [R, I] bf16 (w * h, saved forward);
+ *   gu_pre [R, 2I] fp32; w_perm [R] fp32; down [E*I, H] bf16;
+ *   dgu [R, 2I] bf16 (out); d_down [E*I, H] bf16 (out);
+ *   dw_part [R, nparts] fp32 (out), nparts from moe_grouped_gemm_down_bwd_parts. */
+int moe_grouped_gemm_down_bwd(const uint16_t* dy_perm, const uint16_t* h_w, const float* gu_pre,
+                              const float* w_perm, const int32_t* offsets, const uint16_t* down,
+                              int64_t R, int64_t H, int64_t E, int64_t I, uint16_t* dgu,
+                              uint16_t* d_down, float* dw_part, void* stream);
+
+/* Backward of the renormalised softmax (w = softmax over the chosen logits):
+ *   dw[t,j] = sum_n dw_part[row_map[t*k+j], n]          (fixed order)
+ *   d_logits[t, ids[t,j]] = w[t,j] * (dw[t,j] - sum_i w[t,i] dw[t,i])
+ *   d_logits[t, e] = 0 for every expert not chosen by t
+ *   d_logits [T, E] fp32 (out); dw [T, k] fp32 (out, nullable). */
+int moe_route_bwd(const float* dw_part, int64_t nparts, const int32_t* row_map, const float* w,
+                  const int32_t* ids, int64_t T, int64_t E, int64_t k, float* d_logits, float* dw,
+                  void* stream);
 
 /* Backward of the gate_up GEMM, per expert e:
  *   dx_perm[r] = dgu[r] . gate_up_e^T                (bf16)
  *   d_gate_up_e = x[src_rows of e]^T . dgu_e         (fp32 accumulate, bf16;
  *                                                     0 for an empty expert)
- *   dgu [R, 2I]; x [T, H]; src_row [R] (NULL: rows in order, T == R);
+ *   dgu [R, 2I]; x [T, H]; src_row [R] (NULL: x is already permuted, [R, H]);
  *   gate_up [E*H, 2I]; dx_perm [R, H] (out); d_gate_up [E*H, 2I] (out). */
 int moe_grouped_gemm_gate_up_bwd(const uint16_t* dgu, const uint16_t* x, const int32_t* src_row,
                                  const int32_t* offsets, const uint16_t* gate_up, int64_t T,

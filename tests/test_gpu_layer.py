@@ -34,29 +34,35 @@ def _inputs(T, H, E, k, I, seed, **kw):
     return cfg, synth.make_inputs(cfg, with_dy=True)
 
 
-def _forward(moe, inp, save=False):
+def _forward(moe, inp, save=False, fused=True):
     x, wr = bf(inp.x), f32(inp.w_router)
     gu, dn = bf(inp.gate_up), bf(inp.down)
     bias = f32(inp.bias) if inp.bias is not None else None
     sgu = bf(inp.sh_gate_up) if inp.sh_gate_up is not None else None
     sdn = bf(inp.sh_down) if inp.sh_down is not None else None
-    y, st = moe.moe_forward(x, wr, gu, dn, inp.cfg.k, bias, sgu, sdn, save_for_backward=save)
+    y, st = moe.moe_forward(x, wr, gu, dn, inp.cfg.k, bias, sgu, sdn, save_for_backward=save,
+                            fused_gather=fused)
     moe.sync_status()
     return (x, wr, gu, dn), y, st
 
 
+@pytest.mark.parametrize("fused", [True, False], ids=["gather_fused", "rows_materialised"])
 @pytest.mark.parametrize("T,H,E,k,I", SMALL)
-def test_forward_elementwise(T, H, E, k, I):
+def test_forward_elementwise(T, H, E, k, I, fused):
     moe = lib()
     cfg, inp = _inputs(T, H, E, k, I, seed=T + H + I)
-    _, y, st = _forward(moe, inp, save=True)
+    _, y, st = _forward(moe, inp, save=True, fused=fused)
     ref = oracle.layer_forward(inp, want_intermediates=True)
     same, tol = compare_ids(npi(st.ids), ref["route"])
     assert tol == 0 and same.all()
     for key in ("counts", "offsets", "row_map", "src_row"):
         np.testing.assert_array_equal(npi(getattr(st, key)), ref["perm"][key], err_msg=key)
-    assert_close("gu_pre", f64(st.gu_pre), ref["gu_perm"])
+    w_perm_ref = np.empty(cfg.R)
+    w_perm_ref[ref["perm"]["row_map"]] = ref["route"]["w"].reshape(-1)
+    assert_close("w_perm", f64(st.w_perm), w_perm_ref, bf16_out=False)
+    assert_close("gu_pre", f64(st.gu_pre), ref["gu_perm"], bf16_out=False)
     assert_close("h", f64(st.h), ref["h_perm"])
+    assert_close("h_w", f64(st.h_w), w_perm_ref[:, None] * ref["h_perm"])
     assert_close("y_perm", f64(st.y_perm), ref["y_perm"])
     assert_close("y", f64(y), ref["y"])
 
@@ -68,7 +74,7 @@ def test_dense_mode_is_one_swiglu_ffn(T, H, I):
     x = synth.normal_bf16(T, synth.TID_X, (T, H), 1.0)
     gu = synth.normal_bf16(T, synth.TID_SH_GATE_UP, (H, 2 * I), H ** -0.5)
     dn = synth.normal_bf16(T, synth.TID_SH_DOWN, (I, H), I ** -0.5)
-    h, _ = moe.grouped_gemm_gate_up_swiglu(bf(x), None, None, bf(gu), I)
+    h, _, _ = moe.grouped_gemm_gate_up_swiglu(bf(x), None, None, bf(gu), I)
     y = moe.grouped_gemm_down(h, None, bf(dn), H)
     moe.sync_status()
     assert_close("dense ffn", f64(y), oracle.dense_ffn(x, gu, dn))
@@ -84,11 +90,12 @@ def test_shared_expert_layer():
     assert_close("y", f64(y), ref["y"])
 
 
+@pytest.mark.parametrize("fused", [True, False], ids=["gather_fused", "rows_materialised"])
 @pytest.mark.parametrize("T,H,E,k,I", SMALL)
-def test_backward_elementwise(T, H, E, k, I):
+def test_backward_elementwise(T, H, E, k, I, fused):
     moe = lib()
     cfg, inp = _inputs(T, H, E, k, I, seed=3 * T + I)
-    (x, wr, gu, dn), y, st = _forward(moe, inp, save=True)
+    (x, wr, gu, dn), y, st = _forward(moe, inp, save=True, fused=fused)
     g = moe.moe_backward(bf(inp.dy), st, wr, gu, dn, want_dw_router=True)
     moe.sync_status()
     r = oracle.route(inp.x, inp.w_router, None, k)
@@ -96,12 +103,12 @@ def test_backward_elementwise(T, H, E, k, I):
     assert tol == 0 and same.all()
     b = oracle.backward(inp.x, inp.w_router, inp.gate_up, inp.down, r["ids"], r["w"], inp.dy,
                         want_dw=True, want_dwr=True)
-    assert_close("dw", f64(g["dw"]), b["dw"])
-    assert_close("d_logits", f64(g["d_logits"]), b["dlogits"])
+    assert_close("dw", f64(g["dw"]), b["dw"], bf16_out=False)
+    assert_close("d_logits", f64(g["d_logits"]), b["dlogits"], bf16_out=False)
     assert_close("dX", f64(g["dx"]), b["dX"])
     assert_close("d_gate_up", f64(g["d_gate_up"]), b["d_gate_up"])
     assert_close("d_down", f64(g["d_down"]), b["d_down"])
-    assert_close("d_w_router", f64(g["d_w_router"]), b["d_w_r"])
+    assert_close("d_w_router", f64(g["d_w_router"]), b["d_w_r"], bf16_out=False)
 
 
 def test_backward_empty_experts_get_zero_weight_grads():
@@ -125,7 +132,7 @@ def _sampled_forward_check(cfg_name, n_tokens=192):
     _, y, st = _forward(moe, inp)
     r = oracle.route(inp.x, inp.w_router, inp.bias, cfg.k)
     same, tol = compare_ids(npi(st.ids), r)
-    assert tol <= 2
+    assert tol <= max(4, cfg.T // 2000)   # every one of them checked to be a near tie
     if same.all():
         perm = oracle.permute(r["ids"], cfg.E)
         for key in ("counts", "offsets", "row_map", "src_row"):
@@ -161,13 +168,13 @@ def test_training_step_backward_sampled():
     moe.sync_status()
     r = oracle.route(inp.x, inp.w_router, None, cfg.k)
     same, tol = compare_ids(npi(st.ids), r)
-    assert tol <= 2
+    assert tol <= max(4, cfg.T // 2000)
     tok = sample_tokens(cfg.T, 96, 33)
     tok = tok[same[tok]]
     b = oracle.backward_tokens(tok, inp.x, inp.w_router, inp.gate_up, inp.down, r["ids"], r["w"], inp.dy)
     assert_close("dX[sample]", f64(g["dx"])[tok], b["dX"])
-    assert_close("d_logits[sample]", f64(g["d_logits"])[tok], b["dlogits"])
-    assert_close("dw[sample]", f64(g["dw"])[tok], b["dw"])
+    assert_close("d_logits[sample]", f64(g["d_logits"])[tok], b["dlogits"], bf16_out=False)
+    assert_close("dw[sample]", f64(g["dw"])[tok], b["dw"], bf16_out=False)
     if same.all():
         H, I = cfg.H, cfg.I
         dgu = g["d_gate_up"]

@@ -21,8 +21,8 @@ def test_route_matches_oracle(T, H, E, k):
     ref = oracle.route(inp.x, inp.w_router, None, k)
     same, tolerated = compare_ids(npi(ids), ref)
     assert tolerated <= max(1, T // 1000)
-    assert_close("logits", f64(logits), ref["logits"])
-    assert_close("w", f64(w)[same], ref["w"][same])
+    assert_close("logits", f64(logits), ref["logits"], bf16_out=False)
+    assert_close("w", f64(w)[same], ref["w"][same], bf16_out=False)
     np.testing.assert_allclose(f64(w).sum(1), 1.0, atol=1e-5)
 
 
@@ -34,8 +34,8 @@ def test_route_bias_and_skewed_workload():
     moe.sync_status()
     ref = oracle.route(inp.x, inp.w_router, inp.bias, cfg.k)
     same, tolerated = compare_ids(npi(ids), ref)
-    assert tolerated <= 2
-    assert_close("w", f64(w)[same], ref["w"][same])
+    assert tolerated <= 4
+    assert_close("w", f64(w)[same], ref["w"][same], bf16_out=False)
     counts = np.bincount(npi(ids).reshape(-1), minlength=cfg.E)
     assert (counts == 0).sum() >= 8 and counts.max() > 0.10 * cfg.R   # hotspot + empty experts
 

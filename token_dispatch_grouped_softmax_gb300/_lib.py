@@ -25,17 +25,18 @@ SIGNATURES = {
     "moe_version": [],
     "moe_sync_status": [P, ctypes.POINTER(ctypes.c_uint32)],
     "moe_set_wait_limit_ns": [ctypes.c_uint64],
-    "moe_route_workspace_size": [I64, I64, INT, ctypes.POINTER(SZ)],
+    "moe_route_workspace_size": [I64, I64, I64, ctypes.POINTER(SZ)],
     "moe_route": [P, P, P, I64, I64, I64, I64, P, P, P, P, SZ, P],
     "moe_permute_workspace_size": [I64, I64, I64, ctypes.POINTER(SZ)],
-    "moe_permute": [P, I64, I64, I64, P, P, P, P, P, SZ, P],
+    "moe_permute": [P, P, I64, I64, I64, P, P, P, P, P, P, SZ, P],
     "moe_permute_rows": [P, P, I64, I64, P, P],
-    "moe_grouped_gemm_gate_up_swiglu": [P, P, P, P, I64, I64, I64, I64, I64, P, P, P],
+    "moe_grouped_gemm_gate_up_swiglu": [P, P, P, P, I64, I64, I64, I64, I64, P, P, P, P, P],
     "moe_grouped_gemm_down": [P, P, P, I64, I64, I64, I64, P, P],
     "moe_unpermute_combine": [P, P, P, P, I64, I64, I64, P, P],
-    "moe_unpermute_combine_bwd": [P, P, P, P, I64, I64, I64, P, P, P],
-    "moe_route_bwd": [P, P, P, I64, I64, I64, P, P],
-    "moe_grouped_gemm_down_bwd": [P, P, P, P, P, I64, I64, I64, I64, P, P, P],
+    "moe_unpermute_combine_bwd": [P, P, I64, I64, I64, P, P],
+    "moe_route_bwd": [P, I64, P, P, P, I64, I64, I64, P, P, P],
+    "moe_grouped_gemm_down_bwd_parts": [I64, ctypes.POINTER(I64)],
+    "moe_grouped_gemm_down_bwd": [P, P, P, P, P, P, I64, I64, I64, I64, P, P, P, P],
     "moe_grouped_gemm_gate_up_bwd": [P, P, P, P, P, I64, I64, I64, I64, I64, P, P, P],
     "moe_gather_dx_workspace_size": [I64, I64, ctypes.POINTER(SZ)],
     "moe_gather_dx": [P, P, P, P, P, I64, I64, I64, I64, P, P, SZ, P],

@@ -115,9 +115,9 @@ int moe_sync_status(void* stream, uint32_t* detail) {
 
 /* ------------------------------------------------------------------ route */
 
-int moe_route_workspace_size(int64_t T, int64_t E, int has_logits_out, size_t* bytes) {
-  if (!bytes || T < 0 || E < 1) return MOE_ERR_INVALID_ARG;
-  *bytes = has_logits_out ? 0 : (size_t)(T * E * (int64_t)sizeof(float));
+int moe_route_workspace_size(int64_t T, int64_t H, int64_t E, size_t* bytes) {
+  if (!bytes || T < 0 || H < 1 || E < 1) return MOE_ERR_INVALID_ARG;
+  *bytes = moe::route_workspace_bytes(T, H, E);
   return MOE_OK;
 }
 
@@ -129,13 +129,14 @@ int moe_route(const uint16_t* x, const float* w_router, const float* bias, int64
   if (T > 0 && (!x || !w_router || !ids || !w)) return MOE_ERR_INVALID_ARG;
   if (E > moe::kMaxExperts || k > 32 || H % 8 != 0) return MOE_ERR_UNSUPPORTED;
   if ((x && !aligned16(x)) || (w_router && !aligned16(w_router))) return MOE_ERR_INVALID_ARG;
-  float* lg = logits;
-  if (!lg) {
-    if (T > 0 && (!workspace || workspace_bytes < (size_t)(T * E * 4))) return MOE_ERR_WORKSPACE;
-    lg = static_cast<float*>(workspace);
-  }
+  if (T > 0 && (!workspace || !aligned16(workspace) ||
+                workspace_bytes < moe::route_workspace_bytes(T, H, E)))
+    return MOE_ERR_WORKSPACE;
   if (T == 0) return MOE_OK;
-  return cuda_status(moe::launch_route(x, w_router, bias, T, H, E, k, ids, w, lg,
+  moe::DeviceInfo dev;
+  int rc = moe::current_device(&dev);
+  if (rc != MOE_OK) return rc;
+  return cuda_status(moe::launch_route(x, w_router, bias, T, H, E, k, ids, w, logits, workspace, dev,
                                        static_cast<cudaStream_t>(stream)));
 }
 
@@ -147,18 +148,19 @@ int moe_permute_workspace_size(int64_t T, int64_t k, int64_t E, size_t* bytes) {
   return MOE_OK;
 }
 
-int moe_permute(const int32_t* ids, int64_t T, int64_t k, int64_t E, int32_t* counts,
-                int32_t* offsets, int32_t* row_map, int32_t* src_row, void* workspace,
+int moe_permute(const int32_t* ids, const float* w, int64_t T, int64_t k, int64_t E, int32_t* counts,
+                int32_t* offsets, int32_t* row_map, int32_t* src_row, float* w_perm, void* workspace,
                 size_t workspace_bytes, void* stream) {
   if (T < 0 || k < 1 || E < 1 || T * k > kMaxI32) return MOE_ERR_INVALID_ARG;
   if (!counts || !offsets || (T > 0 && (!ids || !row_map || !src_row))) return MOE_ERR_INVALID_ARG;
+  if ((w == nullptr) != (w_perm == nullptr)) return MOE_ERR_INVALID_ARG;
   if (E > moe::kMaxExperts) return MOE_ERR_UNSUPPORTED;
   if (!workspace || workspace_bytes < moe::permute_workspace_bytes(T * k, E)) return MOE_ERR_WORKSPACE;
   moe::DeviceInfo dev;
   int rc = moe::current_device(&dev);
   if (rc != MOE_OK) return rc;
-  return cuda_status(moe::launch_permute(ids, T, k, E, counts, offsets, row_map, src_row, workspace,
-                                         dev.status, static_cast<cudaStream_t>(stream)));
+  return cuda_status(moe::launch_permute(ids, w, T, k, E, counts, offsets, row_map, src_row, w_perm,
+                                         workspace, dev.status, static_cast<cudaStream_t>(stream)));
 }
 
 int moe_permute_rows(const uint16_t* x, const int32_t* src_row, int64_t R, int64_t H,
@@ -182,20 +184,23 @@ static int gemm_shape_check(int64_t R, int64_t H, int64_t E, int64_t I) {
 int moe_grouped_gemm_gate_up_swiglu(const uint16_t* x, const int32_t* src_row,
                                     const int32_t* offsets, const uint16_t* gate_up, int64_t T,
                                     int64_t R, int64_t H, int64_t E, int64_t I, uint16_t* h,
-                                    uint16_t* gu_pre, void* stream) {
+                                    const float* w_perm, float* gu_pre, uint16_t* h_w, void* stream) {
   int rc = gemm_shape_check(R, H, E, I);
   if (rc != MOE_OK) return rc;
   if (T < 0 || T > kMaxI32) return MOE_ERR_INVALID_ARG;
   if (!offsets && E != 1) return MOE_ERR_INVALID_ARG;
   if (!src_row && T < R) return MOE_ERR_INVALID_ARG;
+  if (h_w && !w_perm) return MOE_ERR_INVALID_ARG;
   if (R == 0) return MOE_OK;
   if (!x || !gate_up || !h || T < 1) return MOE_ERR_INVALID_ARG;
-  if (!aligned16(x) || !aligned16(gate_up) || !aligned16(h) || (gu_pre && !aligned16(gu_pre)))
+  if (!aligned16(x) || !aligned16(gate_up) || !aligned16(h) || (gu_pre && !aligned16(gu_pre)) ||
+      (h_w && !aligned16(h_w)))
     return MOE_ERR_INVALID_ARG;
   moe::DeviceInfo dev;
   if ((rc = moe::current_device(&dev)) != MOE_OK) return rc;
   return moe::gemm_status(moe::launch_gemm_gate_up(x, src_row, offsets, gate_up, T, R, H, E, I, h,
-                                                   gu_pre, dev, static_cast<cudaStream_t>(stream)));
+                                                   w_perm, gu_pre, h_w, dev,
+                                                   static_cast<cudaStream_t>(stream)));
 }
 
 int moe_grouped_gemm_down(const uint16_t* h, const int32_t* offsets, const uint16_t* down, int64_t R,
@@ -228,42 +233,53 @@ int moe_unpermute_combine(const uint16_t* y_perm, const int32_t* row_map, const 
 
 /* --------------------------------------------------------------- backward */
 
-int moe_unpermute_combine_bwd(const uint16_t* dy, const uint16_t* y_perm, const int32_t* row_map,
-                              const float* w, int64_t T, int64_t H, int64_t k, uint16_t* dy_perm,
-                              float* dw, void* stream) {
+int moe_unpermute_combine_bwd(const uint16_t* dy, const int32_t* src_row, int64_t T, int64_t H,
+                              int64_t k, uint16_t* dy_perm, void* stream) {
   if (T < 0 || H < 1 || k < 1 || T > kMaxI32 || T * k > kMaxI32) return MOE_ERR_INVALID_ARG;
-  if (k > 32 || H % 8 != 0) return MOE_ERR_UNSUPPORTED;
+  if (H % 8 != 0) return MOE_ERR_UNSUPPORTED;
   if (T == 0) return MOE_OK;
-  if (!dy || !y_perm || !row_map || !w || !dy_perm || !dw) return MOE_ERR_INVALID_ARG;
-  if (!aligned16(dy) || !aligned16(y_perm) || !aligned16(dy_perm)) return MOE_ERR_INVALID_ARG;
-  return cuda_status(moe::launch_combine_bwd(dy, y_perm, row_map, w, T, H, k, dy_perm, dw,
-                                             static_cast<cudaStream_t>(stream)));
+  if (!dy || !src_row || !dy_perm) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(dy) || !aligned16(dy_perm)) return MOE_ERR_INVALID_ARG;
+  return cuda_status(moe::launch_permute_rows(dy, src_row, T * k, H, dy_perm,
+                                              static_cast<cudaStream_t>(stream)));
 }
 
-int moe_route_bwd(const float* dw, const float* w, const int32_t* ids, int64_t T, int64_t E,
-                  int64_t k, float* d_logits, void* stream) {
-  if (T < 0 || E < 1 || k < 1 || k > E || T > kMaxI32 || T * k > kMaxI32) return MOE_ERR_INVALID_ARG;
-  if (k > 32) return MOE_ERR_UNSUPPORTED;
+int moe_route_bwd(const float* dw_part, int64_t nparts, const int32_t* row_map, const float* w,
+                  const int32_t* ids, int64_t T, int64_t E, int64_t k, float* d_logits, float* dw,
+                  void* stream) {
+  if (T < 0 || E < 1 || k < 1 || k > E || nparts < 1 || T > kMaxI32 || T * k > kMaxI32)
+    return MOE_ERR_INVALID_ARG;
+  if (k > 32 || nparts > 64) return MOE_ERR_UNSUPPORTED;
   if (T == 0) return MOE_OK;
-  if (!dw || !w || !ids || !d_logits) return MOE_ERR_INVALID_ARG;
-  return cuda_status(moe::launch_route_bwd(dw, w, ids, T, E, k, d_logits, static_cast<cudaStream_t>(stream)));
+  if (!dw_part || !row_map || !w || !ids || !d_logits) return MOE_ERR_INVALID_ARG;
+  return cuda_status(moe::launch_route_bwd(dw_part, (int)nparts, row_map, w, ids, T, E, k, d_logits, dw,
+                                           static_cast<cudaStream_t>(stream)));
 }
 
-int moe_grouped_gemm_down_bwd(const uint16_t* dy_perm, const uint16_t* h, const uint16_t* gu_pre,
-                              const int32_t* offsets, const uint16_t* down, int64_t R, int64_t H,
-                              int64_t E, int64_t I, uint16_t* dgu, uint16_t* d_down, void* stream) {
+int moe_grouped_gemm_down_bwd_parts(int64_t I, int64_t* nparts) {
+  if (!nparts || I < 1) return MOE_ERR_INVALID_ARG;
+  *nparts = moe::down_bwd_parts(I);
+  return MOE_OK;
+}
+
+int moe_grouped_gemm_down_bwd(const uint16_t* dy_perm, const uint16_t* h_w, const float* gu_pre,
+                              const float* w_perm, const int32_t* offsets, const uint16_t* down,
+                              int64_t R, int64_t H, int64_t E, int64_t I, uint16_t* dgu,
+                              uint16_t* d_down, float* dw_part, void* stream) {
   int rc = gemm_shape_check(R, H, E, I);
   if (rc != MOE_OK) return rc;
   if (!offsets && E != 1) return MOE_ERR_INVALID_ARG;
-  if (!down || !d_down || (R > 0 && (!dy_perm || !h || !gu_pre || !dgu))) return MOE_ERR_INVALID_ARG;
+  if (!down || !d_down || (R > 0 && (!dy_perm || !h_w || !gu_pre || !w_perm || !dgu || !dw_part)))
+    return MOE_ERR_INVALID_ARG;
   if (!aligned16(down) || !aligned16(d_down) ||
-      (R > 0 && (!aligned16(dy_perm) || !aligned16(h) || !aligned16(gu_pre) || !aligned16(dgu))))
+      (R > 0 && (!aligned16(dy_perm) || !aligned16(h_w) || !aligned16(gu_pre) || !aligned16(dgu))))
     return MOE_ERR_INVALID_ARG;
   if (R == 0) return cuda_status(cudaMemsetAsync(d_down, 0, (size_t)(E * I * H * 2), static_cast<cudaStream_t>(stream)));
   moe::DeviceInfo dev;
   if ((rc = moe::current_device(&dev)) != MOE_OK) return rc;
-  return moe::gemm_status(moe::launch_gemm_down_bwd(dy_perm, h, gu_pre, offsets, down, R, H, E, I,
-                                                    dgu, d_down, dev, static_cast<cudaStream_t>(stream)));
+  return moe::gemm_status(moe::launch_gemm_down_bwd(dy_perm, h_w, gu_pre, w_perm, offsets, down, R, H,
+                                                    E, I, dgu, d_down, dw_part, dev,
+                                                    static_cast<cudaStream_t>(stream)));
 }
 
 int moe_grouped_gemm_gate_up_bwd(const uint16_t* dgu, const uint16_t* x, const int32_t* src_row,

@@ -9,9 +9,13 @@
 // launch shape (a gather, not a scatter-add: deterministic).
 //
 // Backward (the gradient of the same expression, experts held fixed):
-//   combine_bwd   dy_perm[row_map[t*k+j]] = w[t,j] * dY[t];
-//                 dw[t,j] = <dY[t], y_perm[row]>   (warp-shuffle reduction)
-//   route_bwd     d_logits[t, ids_j] = w_j (dw_j - sum_i w_i dw_i), 0 elsewhere
+//   combine_bwd   dy_perm[row] = dY[src_row[row]]: an exact copy (the rows
+//                 permute of dY); the gate weight w[t,j] is applied in fp32
+//                 by the GEMM epilogues, so it is never rounded into a bf16
+//                 operand.  dw[t,j] = <dY[t], y_perm[row]> is computed by the
+//                 down GEMM's backward as <dY . Wd^T, h> in fp32.
+//   route_bwd     dw[t,j] = sum of its per-tile partials (fixed order);
+//                 d_logits[t, ids_j] = w_j (dw_j - sum_i w_i dw_i), 0 elsewhere
 //   gather_dx     dX[t] = sum_j dx_perm[row_map[t*k+j]]
 //                         + sum_j d_logits[t, ids_j] * W_r[:, ids_j]
 //                 (W_r read through a transposed copy [E, H] so the router
@@ -66,43 +70,13 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict
   }
 }
 
-__global__ void __launch_bounds__(256) combine_bwd_kernel(const uint16_t* __restrict__ dy,
-                                                          const uint16_t* __restrict__ y_perm,
-                                                          const int32_t* __restrict__ row_map,
-                                                          const float* __restrict__ w, int T, int H,
-                                                          int k, uint16_t* __restrict__ dy_perm,
-                                                          float* __restrict__ dw) {
-  const int lane = threadIdx.x & 31;
-  const int t = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
-  if (t >= T) return;
-  const int nch = H / 8;
-  const uint4* dyr = reinterpret_cast<const uint4*>(dy + (int64_t)t * H);
-  for (int j = 0; j < k; ++j) {
-    const int row = row_map[(int64_t)t * k + j];
-    const float wj = w[(int64_t)t * k + j];
-    const uint4* yr = reinterpret_cast<const uint4*>(y_perm + (int64_t)row * H);
-    uint4* out = reinterpret_cast<uint4*>(dy_perm + (int64_t)row * H);
-    float dot = 0.f;
-    for (int c = lane; c < nch; c += 32) {
-      float a[8], b[8];
-      unpack8(dyr[c], a);
-      unpack8(__ldg(yr + c), b);
-#pragma unroll
-      for (int q = 0; q < 8; ++q) dot = fmaf(a[q], b[q], dot);
-#pragma unroll
-      for (int q = 0; q < 8; ++q) a[q] *= wj;
-      out[c] = pack8(a);
-    }
-    dot = warp_sum(dot);
-    if (lane == 0) dw[(int64_t)t * k + j] = dot;
-  }
-}
-
-__global__ void __launch_bounds__(256) route_bwd_kernel(const float* __restrict__ dw,
+__global__ void __launch_bounds__(256) route_bwd_kernel(const float* __restrict__ dw_part, int nparts,
+                                                        const int32_t* __restrict__ row_map,
                                                         const float* __restrict__ w,
                                                         const int32_t* __restrict__ ids, int T,
                                                         int E, int k,
-                                                        float* __restrict__ d_logits) {
+                                                        float* __restrict__ d_logits,
+                                                        float* __restrict__ dw) {
   const int lane = threadIdx.x & 31;
   const int t = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
   if (t >= T) return;
@@ -110,8 +84,10 @@ __global__ void __launch_bounds__(256) route_bwd_kernel(const float* __restrict_
   int my_id = -1;
   if (lane < k) {
     my_w = w[(int64_t)t * k + lane];
-    my_dw = dw[(int64_t)t * k + lane];
     my_id = ids[(int64_t)t * k + lane];
+    const int64_t row = row_map[(int64_t)t * k + lane];
+    for (int n = 0; n < nparts; ++n) my_dw += dw_part[row * nparts + n];   // fixed order
+    if (dw) dw[(int64_t)t * k + lane] = my_dw;
   }
   const float mean = warp_sum(my_w * my_dw);   // sum_i w_i dw_i
   const float my_dz = my_w * (my_dw - mean);
@@ -245,20 +221,12 @@ cudaError_t launch_combine(const uint16_t* y_perm, const int32_t* row_map, const
   return cudaGetLastError();
 }
 
-cudaError_t launch_combine_bwd(const uint16_t* dy, const uint16_t* y_perm, const int32_t* row_map,
-                               const float* w, int64_t T, int64_t H, int64_t k, uint16_t* dy_perm,
-                               float* dw, cudaStream_t stream) {
-  if (T == 0) return cudaSuccess;
-  combine_bwd_kernel<<<(unsigned)((T + kWarpsPerBlock - 1) / kWarpsPerBlock), 256, 0, stream>>>(
-      dy, y_perm, row_map, w, (int)T, (int)H, (int)k, dy_perm, dw);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_route_bwd(const float* dw, const float* w, const int32_t* ids, int64_t T,
-                             int64_t E, int64_t k, float* d_logits, cudaStream_t stream) {
+cudaError_t launch_route_bwd(const float* dw_part, int nparts, const int32_t* row_map, const float* w,
+                             const int32_t* ids, int64_t T, int64_t E, int64_t k, float* d_logits,
+                             float* dw, cudaStream_t stream) {
   if (T == 0) return cudaSuccess;
   route_bwd_kernel<<<(unsigned)((T + kWarpsPerBlock - 1) / kWarpsPerBlock), 256, 0, stream>>>(
-      dw, w, ids, (int)T, (int)E, (int)k, d_logits);
+      dw_part, nparts, row_map, w, ids, (int)T, (int)E, (int)k, d_logits, dw);
   return cudaGetLastError();
 }
 

@@ -8,7 +8,10 @@
 //
 //   FWD_GATEUP    h[r]      = silu(x[src_row[r]] . Wg_e) * (x[src_row[r]] . Wu_e)
 //   FWD_DOWN      y_perm[r] = h[r] . Wd_e
-//   DGRAD_DOWN    dgu[r]    = SwiGLU'(dy_perm[r] . Wd_e^T, gu_pre[r])
+//   DGRAD_DOWN    dgu[r]    = SwiGLU'(w[r] * (dy_perm[r] . Wd_e^T), gu_pre[r]), and
+//                 the gate-weight gradient dw[r] = <dy_perm[r] . Wd_e^T, h[r]>
+//                 (= <dY, y_perm[r]>) as per-tile partials, h recomputed in
+//                 fp32 from the saved fp32 pre-activations
 //   DGRAD_GATEUP  dx_perm[r]= dgu[r] . Wgu_e^T
 //   WGRAD_DOWN    d_down_e  = h_e^T . dy_perm_e
 //   WGRAD_GATEUP  d_gu_e    = x[src_rows of e]^T . dgu_e
@@ -60,14 +63,15 @@ constexpr uint32_t TMEM_COLS = 512;
 constexpr int MN_CHUNK_BYTES = 64 * 128;           // one 64-wide MN chunk x 64 K rows
 
 enum Mode { FWD_GATEUP = 0, FWD_DOWN = 1, DGRAD_DOWN = 2, DGRAD_GATEUP = 3, WGRAD_DOWN = 4,
-            WGRAD_GATEUP = 5 };
+            WGRAD_GATEUP = 5, ROUTER = 6 };
 
 template <int MODE>
 struct Traits {
   static constexpr bool kAMN = (MODE == WGRAD_DOWN || MODE == WGRAD_GATEUP);
   static constexpr bool kBMN = (MODE == FWD_GATEUP || MODE == FWD_DOWN || MODE == WGRAD_DOWN ||
-                                MODE == WGRAD_GATEUP);
+                                MODE == WGRAD_GATEUP || MODE == ROUTER);
   static constexpr bool kKGrouped = (MODE == WGRAD_DOWN || MODE == WGRAD_GATEUP);
+  static constexpr bool kRouter = (MODE == ROUTER);
 };
 
 struct GemmParams {   // 64-byte aligned through its CUtensorMap members
@@ -75,9 +79,13 @@ struct GemmParams {   // 64-byte aligned through its CUtensorMap members
   CUtensorMap tmB;
   const int32_t* offsets;   // [E+1] expert row offsets, or nullptr: one group of `rows`
   const int32_t* gidx;      // gather indices (src_row), or nullptr: identity
-  const uint16_t* aux;      // gu_pre for DGRAD_DOWN
+  const float* aux;         // fp32 gu_pre [R, 2I] read by DGRAD_DOWN
+  const float* wrow;        // gate weight of each permuted row [R] (nullable)
   uint16_t* out;
-  uint16_t* out2;           // gu_pre output of FWD_GATEUP (nullable)
+  float* out_gu;            // FWD_GATEUP: fp32 pre-activations g | u [R, 2I] (nullable)
+  uint16_t* out_hw;         // FWD_GATEUP: bf16(w_row * h) [R, I] (nullable, needs wrow)
+  float* out_part;          // DGRAD_DOWN: per (row, n tile) partial of <dY . Wd^T, h> [R, nt]
+                            // ROUTER: fp32 partial logits [parts, rows, n_out]
   uint32_t* status;
   uint64_t wait_limit_ns;
   int rows;                 // permuted rows R
@@ -134,7 +142,16 @@ __device__ __forceinline__ void group_range(const GemmParams& p, int e, int& sta
 template <int MODE>
 __device__ __forceinline__ Tile decode_tile(const GemmParams& p, const int* prefix, int tile) {
   Tile t;
-  if (Traits<MODE>::kKGrouped) {
+  if (Traits<MODE>::kRouter) {   // e = K part; rows of x in order; K range [e*K, (e+1)*K)
+    const int per = p.mt_w * p.nt;
+    t.e = tile / per;
+    const int local = tile - t.e * per;
+    t.mt = local / p.nt;
+    t.nt = local - t.mt * p.nt;
+    t.row0 = t.mt * BM;
+    t.rows = min(BM, p.rows - t.row0);
+    t.kblocks = p.K / BK;
+  } else if (Traits<MODE>::kKGrouped) {
     const int per = p.mt_w * p.nt;
     t.e = tile / per;
     const int local = tile - t.e * per;
@@ -177,10 +194,19 @@ __device__ __forceinline__ void store32(uint16_t* dst, const float* v) {
   for (int q = 0; q < 4; ++q) d[q] = pack8(v + 8 * q);
 }
 
-__device__ __forceinline__ void load32_bf16(const uint16_t* src, float* v) {
-  const uint4* s = reinterpret_cast<const uint4*>(src);
+__device__ __forceinline__ void store32_f32(float* dst, const float* v) {
+  float4* d = reinterpret_cast<float4*>(dst);
 #pragma unroll
-  for (int q = 0; q < 4; ++q) unpack8(__ldg(s + q), v + 8 * q);
+  for (int q = 0; q < 8; ++q) d[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+}
+
+__device__ __forceinline__ void load32_f32(const float* src, float* v) {
+  const float4* s = reinterpret_cast<const float4*>(src);
+#pragma unroll
+  for (int q = 0; q < 8; ++q) {
+    const float4 a = __ldg(s + q);
+    v[4 * q] = a.x; v[4 * q + 1] = a.y; v[4 * q + 2] = a.z; v[4 * q + 3] = a.w;
+  }
 }
 
 template <int MODE>
@@ -228,7 +254,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
   }
   // Tile prefix over experts (M-grouped modes): prefix[e] = sum_{e'<e} ceil(M_e'/BM) * nt
   int total_tiles;
-  if (Tr::kKGrouped) {
+  if (Tr::kKGrouped || Tr::kRouter) {
     total_tiles = p.E * p.mt_w * p.nt;
   } else {
     if (warp == 2) {
@@ -257,7 +283,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  if (!Tr::kKGrouped) total_tiles = prefix[p.E];
+  if (!Tr::kKGrouped && !Tr::kRouter) total_tiles = prefix[p.E];
 
   if (warp == 0) {
     // ------------------------------------------------------ TMA producer
@@ -270,12 +296,9 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
       const Tile t = decode_tile<MODE>(p, prefix, tile);
       if (t.kblocks == 0) continue;
       int gi[4] = {0, 0, 0, 0};
-      if (MODE == FWD_GATEUP) {      // this lane gathers tile rows 4*lane .. 4*lane+3
+      if (MODE == FWD_GATEUP && p.gidx) {   // this lane gathers tile rows 4*lane .. 4*lane+3
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const int r = min(4 * lane + q, t.rows - 1);
-          gi[q] = p.gidx ? p.gidx[t.row0 + r] : t.row0 + r;
-        }
+        for (int q = 0; q < 4; ++q) gi[q] = p.gidx[t.row0 + min(4 * lane + q, t.rows - 1)];
       }
       for (int kb = 0; kb < t.kblocks; ++kb) {
         bool w = true;
@@ -290,7 +313,10 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
         __syncwarp();
         const int k0 = kb * BK;
         if (MODE == FWD_GATEUP) {
-          tma_gather4(sA + 4 * lane * 128, &p.tmA, k0, gi[0], gi[1], gi[2], gi[3], fb);
+          if (p.gidx)                                      // permute fused into the load
+            tma_gather4(sA + 4 * lane * 128, &p.tmA, k0, gi[0], gi[1], gi[2], gi[3], fb);
+          else if (lane == 0)                              // rows already in permuted order
+            tma_load_2d(sA, &p.tmA, k0, t.row0, fb);
           if (lane == 0) {
             const int brow = t.e * p.K + k0;               // gate_up rows of expert e
             const int n0 = t.nt * 128;
@@ -298,6 +324,14 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
             tma_load_2d(sB + 1 * MN_CHUNK_BYTES, &p.tmB, n0 + 64, brow, fb);
             tma_load_2d(sB + 2 * MN_CHUNK_BYTES, &p.tmB, p.I + n0, brow, fb);
             tma_load_2d(sB + 3 * MN_CHUNK_BYTES, &p.tmB, p.I + n0 + 64, brow, fb);
+          }
+        } else if (MODE == ROUTER) {
+          if (lane == 0) {
+            const int kg = t.e * p.K + k0;                 // row of the stacked [W0; W1; W2]
+            tma_load_2d(sA, &p.tmA, kg % p.I, t.row0, fb); // x repeats along the stacked K
+            const int n0 = t.nt * BN;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) tma_load_2d(sB + c * MN_CHUNK_BYTES, &p.tmB, n0 + 64 * c, kg, fb);
           }
         } else if (MODE == FWD_DOWN) {
           if (lane == 0) {
@@ -324,17 +358,19 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
 #pragma unroll
             for (int c = 0; c < 4; ++c) tma_load_2d(sB + c * MN_CHUNK_BYTES, &p.tmB, n0 + 64 * c, krow, fb);
           }
-        } else {  // WGRAD_GATEUP: A = gathered x rows (K = tokens), MN-major
-          const int c = lane >> 4;           // MN chunk 0/1
-          const int g = lane & 15;           // k rows 4g .. 4g+3
-          int r4[4];
+        } else {  // WGRAD_GATEUP: A = x rows of the expert (K = tokens), MN-major
+          if (p.gidx) {                       // gathered through src_row
+            const int c = lane >> 4;          // MN chunk 0/1
+            const int g = lane & 15;          // k rows 4g .. 4g+3
+            int r4[4];
 #pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const int kr = min(k0 + 4 * g + q, t.rows - 1);
-            r4[q] = p.gidx ? p.gidx[t.row0 + kr] : t.row0 + kr;
+            for (int q = 0; q < 4; ++q) r4[q] = p.gidx[t.row0 + min(k0 + 4 * g + q, t.rows - 1)];
+            tma_gather4(sA + c * MN_CHUNK_BYTES + 4 * g * 128, &p.tmA, t.mt * BM + 64 * c, r4[0], r4[1],
+                        r4[2], r4[3], fb);
+          } else if (lane == 0) {             // rows already in permuted order
+            tma_load_2d(sA + 0 * MN_CHUNK_BYTES, &p.tmA, t.mt * BM, t.row0 + k0, fb);
+            tma_load_2d(sA + 1 * MN_CHUNK_BYTES, &p.tmA, t.mt * BM + 64, t.row0 + k0, fb);
           }
-          tma_gather4(sA + c * MN_CHUNK_BYTES + 4 * g * 128, &p.tmA, t.mt * BM + 64 * c, r4[0], r4[1],
-                      r4[2], r4[3], fb);
           if (lane == 0) {
             const int n0 = t.nt * BN;
 #pragma unroll
@@ -465,13 +501,35 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
           tmem_ld32(taddr + c0, v);                      // gate columns
           tmem_ld32(taddr + 128 + c0, u);                // up columns
           if (row_ok) {
-            if (p.out2) {
-              store32(p.out2 + row * 2 * p.I + n0 + c0, v);
-              store32(p.out2 + row * 2 * p.I + p.I + n0 + c0, u);
+            if (p.out_gu) {
+              store32_f32(p.out_gu + row * 2 * p.I + n0 + c0, v);
+              store32_f32(p.out_gu + row * 2 * p.I + p.I + n0 + c0, u);
             }
 #pragma unroll
             for (int q = 0; q < 32; ++q) v[q] = v[q] / (1.0f + expf(-v[q])) * u[q];
             store32(p.out + row * p.ldo + n0 + c0, v);
+            if (p.out_hw) {
+              const float wr = p.wrow[row];
+#pragma unroll
+              for (int q = 0; q < 32; ++q) v[q] *= wr;
+              store32(p.out_hw + row * p.ldo + n0 + c0, v);
+            }
+          }
+        }
+      } else if (MODE == ROUTER) {
+        const bool row_ok = r < t.rows;
+        float* orow = p.out_part + ((int64_t)t.e * p.rows + t.row0 + r) * p.ldo;
+        const int n0 = t.nt * BN;
+#pragma unroll 1
+        for (int c0 = 0; c0 < BN; c0 += 32) {
+          if (n0 + c0 >= p.n_out) break;
+          tmem_ld32(taddr + c0, v);
+          if (row_ok) {
+            if (n0 + c0 + 32 <= p.n_out && (p.ldo & 3) == 0) {
+              store32_f32(orow + n0 + c0, v);
+            } else {
+              for (int q = 0; q < 32 && n0 + c0 + q < p.n_out; ++q) orow[n0 + c0 + q] = v[q];
+            }
           }
         }
       } else if (MODE == FWD_DOWN || MODE == DGRAD_GATEUP) {
@@ -488,18 +546,21 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
         const bool row_ok = r < t.rows;
         const int64_t row = t.row0 + r;
         const int n0 = t.nt * BN;
+        float dot = 0.f;                                 // <dY . Wd^T, h> over this tile's columns
 #pragma unroll 1
         for (int c0 = 0; c0 < BN; c0 += 32) {
           if (n0 + c0 >= p.n_out) break;
-          tmem_ld32(taddr + c0, v);                      // dh (fp32)
+          tmem_ld32(taddr + c0, v);                      // dY . Wd^T (fp32)
           if (row_ok) {
             float g[32], u[32];
-            load32_bf16(p.aux + row * 2 * p.I + n0 + c0, g);
-            load32_bf16(p.aux + row * 2 * p.I + p.I + n0 + c0, u);
+            load32_f32(p.aux + row * 2 * p.I + n0 + c0, g);
+            load32_f32(p.aux + row * 2 * p.I + p.I + n0 + c0, u);
+            const float wr = p.wrow[row];                // dh = w * (dY . Wd^T)
 #pragma unroll
             for (int q = 0; q < 32; ++q) {
               const float s = 1.0f / (1.0f + expf(-g[q]));
-              const float dh = v[q];
+              dot = fmaf(v[q], g[q] * s * u[q], dot);    // h = silu(g) * u from the fp32 pre-activations
+              const float dh = wr * v[q];
               const float dg = dh * u[q] * s * (1.0f + g[q] * (1.0f - s));
               const float du = dh * g[q] * s;
               g[q] = dg;
@@ -509,6 +570,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
             store32(p.out + row * 2 * p.I + p.I + n0 + c0, u);
           }
         }
+        if (row_ok && p.out_part) p.out_part[row * p.nt + t.nt] = dot;
       } else {  // WGRAD_*: output rows m = mt*BM + r of expert e's weight-gradient block
         const int m = t.mt * BM + r;
         const bool row_ok = m < p.m_w;
@@ -573,8 +635,11 @@ void fill_common(GemmParams& p, const int32_t* offsets, int64_t R, int64_t E, in
   p.offsets = offsets;
   p.gidx = nullptr;
   p.aux = nullptr;
+  p.wrow = nullptr;
   p.out = nullptr;
-  p.out2 = nullptr;
+  p.out_gu = nullptr;
+  p.out_hw = nullptr;
+  p.out_part = nullptr;
   p.status = dev.status;
   p.wait_limit_ns = dev.wait_limit_ns;
   p.rows = (int)R;
@@ -594,21 +659,54 @@ int64_t mgrouped_tile_bound(int64_t R, int64_t E, int nt) { return ((R + BM - 1)
 
 int launch_gemm_gate_up(const uint16_t* x, const int32_t* src_row, const int32_t* offsets,
                         const uint16_t* gate_up, int64_t T, int64_t R, int64_t H, int64_t E,
-                        int64_t I, uint16_t* h, uint16_t* gu_pre, const DeviceInfo& dev,
-                        cudaStream_t stream) {
+                        int64_t I, uint16_t* h, const float* w_perm, float* gu_pre, uint16_t* h_w,
+                        const DeviceInfo& dev, cudaStream_t stream) {
   if (R == 0) return 0;
   GemmParams p;
   fill_common(p, offsets, R, E, I, dev);
-  if (!make_map(&p.tmA, x, T, H, 64, 1) || !make_map(&p.tmB, gate_up, E * H, 2 * I, 64, 64))
-    return -1;
+  // gathered rows: one-row boxes for tile::gather4; rows in order: 128-row tiles
+  const bool ok_a = src_row ? make_map(&p.tmA, x, T, H, 64, 1) : make_map(&p.tmA, x, R, H, 64, 128);
+  if (!ok_a || !make_map(&p.tmB, gate_up, E * H, 2 * I, 64, 64)) return -1;
   p.gidx = src_row;
   p.out = h;
-  p.out2 = gu_pre;
+  p.wrow = w_perm;
+  p.out_gu = gu_pre;
+  p.out_hw = h_w;
   p.K = (int)H;
   p.n_out = (int)I;
   p.nt = (int)((I + 127) / 128);
   p.ldo = I;
   return run_gemm<FWD_GATEUP>(p, mgrouped_tile_bound(R, E, p.nt), dev, stream) == cudaSuccess ? 0 : 1;
+}
+
+// K split of the router GEMM: the smallest divisor of its 64-wide K blocks
+// giving at least 228 tiles (1.5 waves on the 152 SMs of a GB300); fixed by
+// the shape alone so that workspace sizes do not depend on the device.
+int router_parts(int64_t T, int64_t H, int64_t E) {
+  const int64_t tiles = ((T + BM - 1) / BM) * ((E + BN - 1) / BN);
+  const int64_t kb = 3 * H / BK;          // 64-wide K blocks of the stacked split weight
+  int parts = 1;
+  for (int cand = 1; cand <= 48; ++cand) {
+    if (kb % cand) continue;
+    parts = cand;
+    if (tiles * cand >= 228) break;
+  }
+  return parts;
+}
+
+int launch_router_logits(const uint16_t* x, const uint16_t* w_split, int64_t T, int64_t H, int64_t E,
+                         int parts, float* part_out, const DeviceInfo& dev, cudaStream_t stream) {
+  if (T == 0) return 0;
+  GemmParams p;
+  fill_common(p, nullptr, T, parts, H, dev);
+  if (!make_map(&p.tmA, x, T, H, 64, 128) || !make_map(&p.tmB, w_split, 3 * H, E, 64, 64)) return -1;
+  p.out_part = part_out;
+  p.K = (int)(3 * H / parts);   // K extent of one part
+  p.n_out = (int)E;
+  p.mt_w = (int)((T + BM - 1) / BM);
+  p.nt = (int)((E + BN - 1) / BN);
+  p.ldo = E;
+  return run_gemm<ROUTER>(p, (int64_t)parts * p.mt_w * p.nt, dev, stream) == cudaSuccess ? 0 : 1;
 }
 
 int launch_gemm_down(const uint16_t* h, const int32_t* offsets, const uint16_t* down, int64_t R,
@@ -626,28 +724,32 @@ int launch_gemm_down(const uint16_t* h, const int32_t* offsets, const uint16_t* 
   return run_gemm<FWD_DOWN>(p, mgrouped_tile_bound(R, E, p.nt), dev, stream) == cudaSuccess ? 0 : 1;
 }
 
-int launch_gemm_down_bwd(const uint16_t* dy_perm, const uint16_t* h, const uint16_t* gu_pre,
-                         const int32_t* offsets, const uint16_t* down, int64_t R, int64_t H,
-                         int64_t E, int64_t I, uint16_t* dgu, uint16_t* d_down,
-                         const DeviceInfo& dev, cudaStream_t stream) {
-  if (R > 0) {  // dgu = SwiGLU'(dy_perm . Wd_e^T)
+int down_bwd_parts(int64_t I) { return (int)((I + BN - 1) / BN); }
+
+int launch_gemm_down_bwd(const uint16_t* dy_perm, const uint16_t* h_w, const float* gu_pre,
+                         const float* w_perm, const int32_t* offsets, const uint16_t* down, int64_t R,
+                         int64_t H, int64_t E, int64_t I, uint16_t* dgu, uint16_t* d_down,
+                         float* dw_part, const DeviceInfo& dev, cudaStream_t stream) {
+  if (R > 0) {  // dgu = SwiGLU'(w * (dy_perm . Wd_e^T), gu_pre)
     GemmParams p;
     fill_common(p, offsets, R, E, I, dev);
     if (!make_map(&p.tmA, dy_perm, R, H, 64, 128) || !make_map(&p.tmB, down, E * I, H, 64, 256))
       return -1;
     p.aux = gu_pre;
+    p.wrow = w_perm;
     p.out = dgu;
+    p.out_part = dw_part;
     p.K = (int)H;
     p.n_out = (int)I;
     p.nt = (int)((I + BN - 1) / BN);
     p.ldo = 2 * I;
     if (run_gemm<DGRAD_DOWN>(p, mgrouped_tile_bound(R, E, p.nt), dev, stream) != cudaSuccess) return 1;
   }
-  {  // d_down_e = h_e^T . dy_perm_e
+  {  // d_down_e = (w h)_e^T . dy_perm_e
     GemmParams p;
     fill_common(p, offsets, R, E, I, dev);
     const int64_t rows = R > 0 ? R : 1;
-    if (!make_map(&p.tmA, h, rows, I, 64, 64) || !make_map(&p.tmB, dy_perm, rows, H, 64, 64))
+    if (!make_map(&p.tmA, h_w, rows, I, 64, 64) || !make_map(&p.tmB, dy_perm, rows, H, 64, 64))
       return -1;
     p.out = d_down;
     p.m_w = (int)I;
@@ -676,12 +778,13 @@ int launch_gemm_gate_up_bwd(const uint16_t* dgu, const uint16_t* x, const int32_
     p.ldo = H;
     if (run_gemm<DGRAD_GATEUP>(p, mgrouped_tile_bound(R, E, p.nt), dev, stream) != cudaSuccess) return 1;
   }
-  {  // d_gate_up_e = x[src rows of e]^T . dgu_e
+  {  // d_gate_up_e = x[rows of e]^T . dgu_e
     GemmParams p;
     fill_common(p, offsets, R, E, I, dev);
     const int64_t rows = R > 0 ? R : 1;
-    if (!make_map(&p.tmA, x, T > 0 ? T : 1, H, 64, 1) || !make_map(&p.tmB, dgu, rows, 2 * I, 64, 64))
-      return -1;
+    const bool ok_a = src_row ? make_map(&p.tmA, x, T > 0 ? T : 1, H, 64, 1)
+                              : make_map(&p.tmA, x, rows, H, 64, 64);
+    if (!ok_a || !make_map(&p.tmB, dgu, rows, 2 * I, 64, 64)) return -1;
     p.gidx = src_row;
     p.out = d_gate_up;
     p.m_w = (int)H;

@@ -27,25 +27,24 @@ bool encode_tensor_map_2d_bf16(CUtensorMap* map, const void* base, const cuuint6
                                const cuuint64_t* strides, const cuuint32_t* box,
                                const cuuint32_t* estr);
 
+size_t route_workspace_bytes(int64_t T, int64_t H, int64_t E);
 cudaError_t launch_route(const uint16_t* x, const float* w_router, const float* bias, int64_t T,
                          int64_t H, int64_t E, int64_t k, int32_t* ids, float* w, float* logits,
-                         cudaStream_t stream);
+                         void* ws, const DeviceInfo& dev, cudaStream_t stream);
 
 size_t permute_workspace_bytes(int64_t R, int64_t E);
-cudaError_t launch_permute(const int32_t* ids, int64_t T, int64_t k, int64_t E, int32_t* counts,
-                           int32_t* offsets, int32_t* row_map, int32_t* src_row, void* ws,
-                           uint32_t* status, cudaStream_t stream);
+cudaError_t launch_permute(const int32_t* ids, const float* w, int64_t T, int64_t k, int64_t E,
+                           int32_t* counts, int32_t* offsets, int32_t* row_map, int32_t* src_row,
+                           float* w_perm, void* ws, uint32_t* status, cudaStream_t stream);
 cudaError_t launch_permute_rows(const uint16_t* x, const int32_t* src_row, int64_t R, int64_t H,
                                 uint16_t* x_perm, cudaStream_t stream);
 
 cudaError_t launch_combine(const uint16_t* y_perm, const int32_t* row_map, const float* w,
                            const uint16_t* y_shared, int64_t T, int64_t H, int64_t k, uint16_t* y,
                            cudaStream_t stream);
-cudaError_t launch_combine_bwd(const uint16_t* dy, const uint16_t* y_perm, const int32_t* row_map,
-                               const float* w, int64_t T, int64_t H, int64_t k, uint16_t* dy_perm,
-                               float* dw, cudaStream_t stream);
-cudaError_t launch_route_bwd(const float* dw, const float* w, const int32_t* ids, int64_t T,
-                             int64_t E, int64_t k, float* d_logits, cudaStream_t stream);
+cudaError_t launch_route_bwd(const float* dw_part, int nparts, const int32_t* row_map, const float* w,
+                             const int32_t* ids, int64_t T, int64_t E, int64_t k, float* d_logits,
+                             float* dw, cudaStream_t stream);
 size_t gather_dx_workspace_bytes(int64_t H, int64_t E);
 cudaError_t launch_gather_dx(const uint16_t* dx_perm, const int32_t* row_map, const float* d_logits,
                              const int32_t* ids, const float* w_router, int64_t T, int64_t H,
@@ -54,17 +53,21 @@ cudaError_t launch_route_bwd_weight(const uint16_t* x, const float* d_logits, in
                                     int64_t E, float* d_w_router, cudaStream_t stream);
 
 // Grouped GEMMs: 0 = enqueued, -1 = tensor map rejected, 1 = launch failed.
+int router_parts(int64_t T, int64_t H, int64_t E);
+int launch_router_logits(const uint16_t* x, const uint16_t* w_split, int64_t T, int64_t H, int64_t E,
+                         int parts, float* part_out, const DeviceInfo& dev, cudaStream_t stream);
 int launch_gemm_gate_up(const uint16_t* x, const int32_t* src_row, const int32_t* offsets,
                         const uint16_t* gate_up, int64_t T, int64_t R, int64_t H, int64_t E,
-                        int64_t I, uint16_t* h, uint16_t* gu_pre, const DeviceInfo& dev,
-                        cudaStream_t stream);
+                        int64_t I, uint16_t* h, const float* w_perm, float* gu_pre, uint16_t* h_w,
+                        const DeviceInfo& dev, cudaStream_t stream);
 int launch_gemm_down(const uint16_t* h, const int32_t* offsets, const uint16_t* down, int64_t R,
                      int64_t H, int64_t E, int64_t I, uint16_t* y_perm, const DeviceInfo& dev,
                      cudaStream_t stream);
-int launch_gemm_down_bwd(const uint16_t* dy_perm, const uint16_t* h, const uint16_t* gu_pre,
-                         const int32_t* offsets, const uint16_t* down, int64_t R, int64_t H,
-                         int64_t E, int64_t I, uint16_t* dgu, uint16_t* d_down,
-                         const DeviceInfo& dev, cudaStream_t stream);
+int down_bwd_parts(int64_t I);   // n tiles of the dgrad: partial dot products per row
+int launch_gemm_down_bwd(const uint16_t* dy_perm, const uint16_t* h_w, const float* gu_pre,
+                         const float* w_perm, const int32_t* offsets, const uint16_t* down, int64_t R,
+                         int64_t H, int64_t E, int64_t I, uint16_t* dgu, uint16_t* d_down,
+                         float* dw_part, const DeviceInfo& dev, cudaStream_t stream);
 int launch_gemm_gate_up_bwd(const uint16_t* dgu, const uint16_t* x, const int32_t* src_row,
                             const int32_t* offsets, const uint16_t* gate_up, int64_t T, int64_t R,
                             int64_t H, int64_t E, int64_t I, uint16_t* dx_perm,

@@ -14,8 +14,9 @@
 //                            per-warp counts, and inside a warp step the
 //                            lanes holding the same expert rank themselves
 //                            with __match_any_sync (lower lane = lower i).
-// Outputs: counts, offsets, row_map[i] (permuted row of assignment i) and
-// src_row[row] = i / k.  Workspace: hist, nblocks * E int32.
+// Outputs: counts, offsets, row_map[i] (permuted row of assignment i),
+// src_row[row] = i / k, and optionally w_perm[row] = w[i] (the gate weight
+// travelling with its row).  Workspace: hist, nblocks * E int32.
 #include "kernels.h"
 
 namespace moe {
@@ -94,8 +95,9 @@ __global__ void __launch_bounds__(1024) permute_scan_kernel(int32_t* __restrict_
 }
 
 __global__ void __launch_bounds__(kPermThreads) permute_scatter_kernel(
-    const int32_t* __restrict__ ids, int64_t R, int k, int E, const int32_t* __restrict__ base_be,
-    int32_t* __restrict__ row_map, int32_t* __restrict__ src_row) {
+    const int32_t* __restrict__ ids, const float* __restrict__ w, int64_t R, int k, int E,
+    const int32_t* __restrict__ base_be, int32_t* __restrict__ row_map, int32_t* __restrict__ src_row,
+    float* __restrict__ w_perm) {
   extern __shared__ int32_t sh[];              // [kPermWarps][E] counts, then bases
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
   const int64_t chunk0 = (int64_t)blockIdx.x * kChunk;
@@ -134,6 +136,7 @@ __global__ void __launch_bounds__(kPermThreads) permute_scatter_kernel(
       const int32_t row = my[e] + __popc(lower);
       row_map[i] = row;
       src_row[row] = (int32_t)(i / k);
+      if (w_perm) w_perm[row] = w[i];
     }
     __syncwarp();
     // the highest lane of each group advances that expert's running base
@@ -159,9 +162,9 @@ size_t permute_workspace_bytes(int64_t R, int64_t E) {
   return (size_t)((nb > 0 ? nb : 1) * E * sizeof(int32_t));
 }
 
-cudaError_t launch_permute(const int32_t* ids, int64_t T, int64_t k, int64_t E, int32_t* counts,
-                           int32_t* offsets, int32_t* row_map, int32_t* src_row, void* ws,
-                           uint32_t* status, cudaStream_t stream) {
+cudaError_t launch_permute(const int32_t* ids, const float* w, int64_t T, int64_t k, int64_t E,
+                           int32_t* counts, int32_t* offsets, int32_t* row_map, int32_t* src_row,
+                           float* w_perm, void* ws, uint32_t* status, cudaStream_t stream) {
   const int64_t R = T * k;
   const int nb = (int)((R + kChunk - 1) / kChunk);
   int32_t* hist = static_cast<int32_t*>(ws);
@@ -171,7 +174,7 @@ cudaError_t launch_permute(const int32_t* ids, int64_t T, int64_t k, int64_t E, 
   permute_scan_kernel<<<1, 1024, 0, stream>>>(hist, nb, (int)E, counts, offsets);
   if (nb > 0)
     permute_scatter_kernel<<<nb, kPermThreads, kPermWarps * E * sizeof(int32_t), stream>>>(
-        ids, R, (int)k, (int)E, hist, row_map, src_row);
+        ids, w, R, (int)k, (int)E, hist, row_map, src_row, w_perm);
   return cudaGetLastError();
 }
 

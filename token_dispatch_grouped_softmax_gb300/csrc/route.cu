@@ -2,19 +2,28 @@
 // renormalised weights ("InternVL3.5 接入 pure FSDP2 后端开发实践",
 // MindSpeed-MM issue 625, §8.2: gate -> FP32 softmax -> top-k -> 权重归一化).
 //
-// Kernel 1 (route_logits_kernel): a register-tiled fp32 GEMM on the CUDA
-// cores.  A 256-thread block owns 32 tokens x 64 experts; each thread 2 x 4
-// outputs; K (= H) is staged through shared memory 32 at a time, x widened
-// exactly from bf16.  The router is < 1% of the layer's FLOPs at the
-// Qwen3-MoE shape, and its fp32 precision decides the top-k, so it stays off
-// the bf16 tensor cores.
+// Logits on the tensor cores (E % 8 == 0, H % 64 == 0): W_r is split exactly
+// into three bf16 matrices, W_r = W0 + W1 + W2 (W0 = bf16(W_r), W1 =
+// bf16(W_r - W0), W2 = W_r - W0 - W1, which fits bf16 exactly: 24 = 3 x 8
+// significant bits; the split of an fp32 value into bf16 terms follows
+// Henry, Tang & Heinecke, "Leveraging the bfloat16 artificial intelligence
+// datatype for higher-precision computations", ARITH 2019).  x is exact in
+// bf16, so x . W_r = x . W0 + x . W1 + x . W2 with exact products and fp32
+// accumulation: the tcgen05 GEMM runs over the stacked [W0; W1; W2] (K = 3H)
+// with x repeated along K, split into `parts` K ranges (one CTA tile each)
+// whose fp32 partials the top-k kernel adds in a fixed order.
 //
-// Kernel 2 (route_topk_kernel): one warp per token.  The k largest logits are
-// picked by k rounds of a warp arg-max on (value desc, index asc), so equal
-// fp32 logits go to the lower expert index; picking on the logits orders the
-// experts exactly as their softmax probabilities.  With m the largest logit,
-// w_j = exp(z_j - m) / sum_{i chosen} exp(z_i - m), which is p_j / sum of
-// the chosen p (the softmax denominator cancels).
+// Other shapes use route_logits_kernel: a register-tiled fp32 GEMM on the
+// CUDA cores (32 tokens x 64 experts per 256-thread block).
+//
+// route_topk_kernel: one warp per token, NV logits per lane.  The k largest
+// logits are picked by k rounds of a warp arg-max on (value desc, index
+// asc), so equal fp32 logits go to the lower expert index; the logits order
+// the experts exactly as their softmax probabilities.  With m the largest
+// logit, w_j = exp(z_j - m) / sum_{i chosen} exp(z_i - m), which equals
+// p_j / sum of the chosen p (the softmax denominator cancels).
+#include <algorithm>
+
 #include "kernels.h"
 
 namespace moe {
@@ -114,29 +123,71 @@ __device__ __forceinline__ bool better(float v1, int i1, float v2, int i2) {
   return v1 > v2 || (v1 == v2 && i1 < i2);
 }
 
-__global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict__ logits, int T,
-                                                         int E, int k, int32_t* __restrict__ ids,
-                                                         float* __restrict__ w) {
+// W_r [H, E] fp32 -> [3, H, E] bf16 with W_r = W0 + W1 + W2 exactly.
+__global__ void split_router_weight_kernel(const float* __restrict__ wr, int64_t n,
+                                           uint16_t* __restrict__ out) {
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const float w = wr[i];
+    const __nv_bfloat16 w0 = __float2bfloat16_rn(w);
+    const float r1 = w - __bfloat162float(w0);
+    const __nv_bfloat16 w1 = __float2bfloat16_rn(r1);
+    const float r2 = r1 - __bfloat162float(w1);
+    const __nv_bfloat16 w2 = __float2bfloat16_rn(r2);
+    out[i] = __bfloat16_as_ushort(w0);
+    out[n + i] = __bfloat16_as_ushort(w1);
+    out[2 * n + i] = __bfloat16_as_ushort(w2);
+  }
+}
+
+// One warp per token.  z[e] = sum_p part[p][t][e] (+ bias[e]), p in
+// increasing order; NV = logits per lane (E <= 32 * NV).
+template <int NV>
+__global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict__ part, int nparts,
+                                                         const float* __restrict__ bias, int T, int E,
+                                                         int k, int32_t* __restrict__ ids,
+                                                         float* __restrict__ w,
+                                                         float* __restrict__ logits_out) {
   const int lane = threadIdx.x & 31;
   const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
   if (t >= T) return;
-  const float* z = logits + (int64_t)t * E;
-  float v[32];
   const float NEG = -INFINITY;
+  float v[NV];
+  // partials added in increasing part order; the NV loads of one part are
+  // independent, and the part loop is unrolled so the loads overlap
 #pragma unroll
-  for (int i = 0; i < 32; ++i) {
+  for (int i = 0; i < NV; ++i) {
     const int e = lane + 32 * i;
-    v[i] = (e < E) ? z[e] : NEG;
+    v[i] = (e < E) ? __ldg(part + (int64_t)t * E + e) : 0.f;
   }
-  uint32_t taken = 0;
+#pragma unroll 4
+  for (int q = 1; q < nparts; ++q) {
+    const float* pq = part + ((int64_t)q * T + t) * E;
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+      const int e = lane + 32 * i;
+      if (e < E) v[i] += __ldg(pq + e);
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < NV; ++i) {
+    const int e = lane + 32 * i;
+    if (e < E) {
+      if (bias) v[i] += bias[e];
+      if (logits_out) logits_out[(int64_t)t * E + e] = v[i];
+    } else {
+      v[i] = NEG;
+    }
+  }
   float zmax = 0.f, esum = 0.f;
   int my_id = 0;
   float my_e = 0.f;
+  uint32_t taken = 0;               // bit i: expert lane + 32 i already chosen
   for (int j = 0; j < k; ++j) {
     float bv = NEG;
     int bi = 0x7fffffff;
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
+    for (int i = 0; i < NV; ++i) {
       const int e = lane + 32 * i;
       if (e < E && !((taken >> i) & 1u) && better(v[i], e, bv, bi)) {
         bv = v[i];
@@ -167,16 +218,57 @@ __global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict
   }
 }
 
+template <int NV>
+void launch_topk(const float* part, int nparts, const float* bias, int64_t T, int64_t E, int64_t k,
+                 int32_t* ids, float* w, float* logits_out, cudaStream_t stream) {
+  route_topk_kernel<NV><<<(unsigned)((T + 7) / 8), 256, 0, stream>>>(part, nparts, bias, (int)T, (int)E,
+                                                                     (int)k, ids, w, logits_out);
+}
+
+void topk_dispatch(const float* part, int nparts, const float* bias, int64_t T, int64_t E, int64_t k,
+                   int32_t* ids, float* w, float* logits_out, cudaStream_t stream) {
+  if (E <= 32) launch_topk<1>(part, nparts, bias, T, E, k, ids, w, logits_out, stream);
+  else if (E <= 64) launch_topk<2>(part, nparts, bias, T, E, k, ids, w, logits_out, stream);
+  else if (E <= 128) launch_topk<4>(part, nparts, bias, T, E, k, ids, w, logits_out, stream);
+  else if (E <= 256) launch_topk<8>(part, nparts, bias, T, E, k, ids, w, logits_out, stream);
+  else if (E <= 512) launch_topk<16>(part, nparts, bias, T, E, k, ids, w, logits_out, stream);
+  else launch_topk<32>(part, nparts, bias, T, E, k, ids, w, logits_out, stream);
+}
+
 }  // namespace
+
+bool route_on_tensor_cores(int64_t H, int64_t E) { return E % 8 == 0 && H % 64 == 0; }
+
+size_t route_workspace_bytes(int64_t T, int64_t H, int64_t E) {
+  auto align = [](size_t b) { return (b + 255) & ~size_t(255); };
+  if (route_on_tensor_cores(H, E)) {
+    const int parts = router_parts(T, H, E);
+    return align((size_t)(3 * H * E * 2)) + align((size_t)(parts * T * E * 4));
+  }
+  return align((size_t)(T * E * 4));
+}
 
 cudaError_t launch_route(const uint16_t* x, const float* w_router, const float* bias, int64_t T,
                          int64_t H, int64_t E, int64_t k, int32_t* ids, float* w, float* logits,
-                         cudaStream_t stream) {
+                         void* ws, const DeviceInfo& dev, cudaStream_t stream) {
   if (T == 0) return cudaSuccess;
-  dim3 g1((unsigned)((T + kRT - 1) / kRT), (unsigned)((E + kRE - 1) / kRE));
-  route_logits_kernel<<<g1, 256, 0, stream>>>(x, w_router, bias, (int)T, (int)H, (int)E, logits);
-  route_topk_kernel<<<(unsigned)((T + 7) / 8), 256, 0, stream>>>(logits, (int)T, (int)E, (int)k,
-                                                                  ids, w);
+  auto align = [](size_t b) { return (b + 255) & ~size_t(255); };
+  uint8_t* wsb = static_cast<uint8_t*>(ws);
+  if (route_on_tensor_cores(H, E)) {
+    const int parts = router_parts(T, H, E);
+    uint16_t* w_split = reinterpret_cast<uint16_t*>(wsb);
+    float* part = reinterpret_cast<float*>(wsb + align((size_t)(3 * H * E * 2)));
+    const int64_t n = H * E;
+    split_router_weight_kernel<<<(unsigned)std::min<int64_t>((n + 255) / 256, 4096), 256, 0, stream>>>(
+        w_router, n, w_split);
+    if (launch_router_logits(x, w_split, T, H, E, parts, part, dev, stream) != 0) return cudaErrorInvalidValue;
+    topk_dispatch(part, parts, bias, T, E, k, ids, w, logits, stream);
+  } else {
+    float* lg = reinterpret_cast<float*>(wsb);
+    dim3 g1((unsigned)((T + kRT - 1) / kRT), (unsigned)((E + kRE - 1) / kRE));
+    route_logits_kernel<<<g1, 256, 0, stream>>>(x, w_router, nullptr, (int)T, (int)H, (int)E, lg);
+    topk_dispatch(lg, 1, bias, T, E, k, ids, w, logits, stream);
+  }
   return cudaGetLastError();
 }
 

@@ -66,15 +66,21 @@ def route(x, w_router, k, bias=None, return_logits=False):
     dev = x.device
     ids = torch.empty((T, k), dtype=torch.int32, device=dev)
     w = torch.empty((T, k), dtype=torch.float32, device=dev)
-    logits = torch.empty((T, E), dtype=torch.float32, device=dev)
-    call("moe_route", _p(x), _p(w_router), _p(bias), T, H, E, k, _p(ids), _p(w), _p(logits), None, 0,
-         _stream())
+    logits = torch.empty((T, E), dtype=torch.float32, device=dev) if return_logits else None
+    nbytes = ctypes.c_size_t(0)
+    call("moe_route_workspace_size", T, H, E, ctypes.byref(nbytes))
+    ws = _ws(nbytes.value, dev)
+    call("moe_route", _p(x), _p(w_router), _p(bias), T, H, E, k, _p(ids), _p(w), _p(logits), _p(ws),
+         ws.numel(), _stream())
     return (ids, w, logits) if return_logits else (ids, w)
 
 
-def permute(ids, E):
-    """counts [E], offsets [E+1], row_map [R], src_row [R] (all int32)."""
+def permute(ids, E, w=None):
+    """counts [E], offsets [E+1], row_map [R], src_row [R] (int32), and with w
+    [T,k] fp32 also w_perm [R] fp32 (the gate weight of each permuted row)."""
     _need(ids, "ids", torch.int32, 2)
+    if w is not None:
+        _need(w, "w", torch.float32, 2)
     T, k = ids.shape
     dev = ids.device
     nbytes = ctypes.c_size_t(0)
@@ -84,8 +90,11 @@ def permute(ids, E):
     offsets = torch.empty(E + 1, dtype=torch.int32, device=dev)
     row_map = torch.empty(T * k, dtype=torch.int32, device=dev)
     src_row = torch.empty(T * k, dtype=torch.int32, device=dev)
-    call("moe_permute", _p(ids), T, k, E, _p(counts), _p(offsets), _p(row_map), _p(src_row), _p(ws),
-         ws.numel(), _stream())
+    w_perm = torch.empty(T * k, dtype=torch.float32, device=dev) if w is not None else None
+    call("moe_permute", _p(ids), _p(w), T, k, E, _p(counts), _p(offsets), _p(row_map), _p(src_row),
+         _p(w_perm), _p(ws), ws.numel(), _stream())
+    if w is not None:
+        return counts, offsets, row_map, src_row, w_perm
     return counts, offsets, row_map, src_row
 
 
@@ -98,8 +107,9 @@ def permute_rows(x, src_row):
     return out
 
 
-def grouped_gemm_gate_up_swiglu(x, src_row, offsets, gate_up, I, R=None, save_gu_pre=False):
-    """h [R, I] bf16 (and gu_pre [R, 2I] bf16).  src_row/offsets None: dense (E = 1)."""
+def grouped_gemm_gate_up_swiglu(x, src_row, offsets, gate_up, I, R=None, w_perm=None, save_for_backward=False):
+    """h [R, I] bf16; with save_for_backward also gu_pre [R, 2I] fp32 and h_w = w_perm * h [R, I] bf16.
+    src_row None: x is already in permuted order (or the dense mode when offsets is None too)."""
     _need(x, "x", _BF16, 2)
     _need(gate_up, "gate_up", _BF16, 2)
     T, H = x.shape
@@ -113,11 +123,18 @@ def grouped_gemm_gate_up_swiglu(x, src_row, offsets, gate_up, I, R=None, save_gu
         R = T
     if offsets is not None:
         _need(offsets, "offsets", torch.int32, 1)
+    if w_perm is not None:
+        _need(w_perm, "w_perm", torch.float32, 1)
     h = torch.empty((R, I), dtype=_BF16, device=x.device)
-    gu = torch.empty((R, 2 * I), dtype=_BF16, device=x.device) if save_gu_pre else None
+    gu = hw = None
+    if save_for_backward:
+        if w_perm is None:
+            raise ValueError("save_for_backward needs w_perm (from permute(ids, E, w))")
+        gu = torch.empty((R, 2 * I), dtype=torch.float32, device=x.device)
+        hw = torch.empty((R, I), dtype=_BF16, device=x.device)
     call("moe_grouped_gemm_gate_up_swiglu", _p(x), _p(src_row), _p(offsets), _p(gate_up), T, R, H, E, I,
-         _p(h), _p(gu), _stream())
-    return h, gu
+         _p(h), _p(w_perm), _p(gu), _p(hw), _stream())
+    return h, gu, hw
 
 
 def grouped_gemm_down(h, offsets, down, H):
@@ -151,48 +168,56 @@ def unpermute_combine(y_perm, row_map, w, y_shared=None):
 
 # ---------------------------------------------------------------- backward
 
-def unpermute_combine_bwd(dy, y_perm, row_map, w):
-    """dy_perm [R, H] bf16, dw [T, k] fp32."""
+def unpermute_combine_bwd(dy, src_row):
+    """dy_perm [R, H] bf16: the dY row of each permuted row (unweighted, exact)."""
     _need(dy, "dy", _BF16, 2)
-    _need(y_perm, "y_perm", _BF16, 2)
-    _need(row_map, "row_map", torch.int32, 1)
-    _need(w, "w", torch.float32, 2)
-    T, k = w.shape
-    H = dy.shape[1]
-    dy_perm = torch.empty((T * k, H), dtype=_BF16, device=dy.device)
-    dw = torch.empty((T, k), dtype=torch.float32, device=dy.device)
-    call("moe_unpermute_combine_bwd", _p(dy), _p(y_perm), _p(row_map), _p(w), T, H, k, _p(dy_perm), _p(dw),
-         _stream())
-    return dy_perm, dw
+    _need(src_row, "src_row", torch.int32, 1)
+    T, H = dy.shape
+    R = src_row.shape[0]
+    k = R // max(T, 1)
+    dy_perm = torch.empty((R, H), dtype=_BF16, device=dy.device)
+    call("moe_unpermute_combine_bwd", _p(dy), _p(src_row), T, H, k, _p(dy_perm), _stream())
+    return dy_perm
 
 
-def route_bwd(dw, w, ids, E):
-    """d_logits [T, E] fp32."""
-    _need(dw, "dw", torch.float32, 2)
-    _need(w, "w", torch.float32, 2)
-    _need(ids, "ids", torch.int32, 2)
-    T, k = w.shape
-    dl = torch.empty((T, E), dtype=torch.float32, device=w.device)
-    call("moe_route_bwd", _p(dw), _p(w), _p(ids), T, E, k, _p(dl), _stream())
-    return dl
+def down_bwd_parts(I):
+    n = ctypes.c_int64(0)
+    call("moe_grouped_gemm_down_bwd_parts", I, ctypes.byref(n))
+    return n.value
 
 
-def grouped_gemm_down_bwd(dy_perm, h, gu_pre, offsets, down):
-    """dgu [R, 2I] bf16, d_down [E*I, H] bf16."""
+def grouped_gemm_down_bwd(dy_perm, h_w, gu_pre, w_perm, offsets, down):
+    """dgu [R, 2I] bf16, d_down [E*I, H] bf16, dw_part [R, nparts] fp32."""
     _need(dy_perm, "dy_perm", _BF16, 2)
-    _need(h, "h", _BF16, 2)
-    _need(gu_pre, "gu_pre", _BF16, 2)
+    _need(h_w, "h_w", _BF16, 2)
+    _need(gu_pre, "gu_pre", torch.float32, 2)
+    _need(w_perm, "w_perm", torch.float32, 1)
     _need(down, "down", _BF16, 2)
-    R, I = h.shape
+    R, I = h_w.shape
     H = dy_perm.shape[1]
     E = down.shape[0] // I
     if offsets is not None:
         _need(offsets, "offsets", torch.int32, 1)
-    dgu = torch.empty((R, 2 * I), dtype=_BF16, device=h.device)
-    d_down = torch.empty((E * I, H), dtype=_BF16, device=h.device)
-    call("moe_grouped_gemm_down_bwd", _p(dy_perm), _p(h), _p(gu_pre), _p(offsets), _p(down), R, H, E, I,
-         _p(dgu), _p(d_down), _stream())
-    return dgu, d_down
+    dgu = torch.empty((R, 2 * I), dtype=_BF16, device=h_w.device)
+    d_down = torch.empty((E * I, H), dtype=_BF16, device=h_w.device)
+    parts = torch.empty((R, down_bwd_parts(I)), dtype=torch.float32, device=h_w.device)
+    call("moe_grouped_gemm_down_bwd", _p(dy_perm), _p(h_w), _p(gu_pre), _p(w_perm), _p(offsets), _p(down), R,
+         H, E, I, _p(dgu), _p(d_down), _p(parts), _stream())
+    return dgu, d_down, parts
+
+
+def route_bwd(dw_part, row_map, w, ids, E):
+    """d_logits [T, E] fp32 and dw [T, k] fp32 from the per-row partials of the down backward."""
+    _need(dw_part, "dw_part", torch.float32, 2)
+    _need(row_map, "row_map", torch.int32, 1)
+    _need(w, "w", torch.float32, 2)
+    _need(ids, "ids", torch.int32, 2)
+    T, k = w.shape
+    dl = torch.empty((T, E), dtype=torch.float32, device=w.device)
+    dw = torch.empty((T, k), dtype=torch.float32, device=w.device)
+    call("moe_route_bwd", _p(dw_part), dw_part.shape[1], _p(row_map), _p(w), _p(ids), T, E, k, _p(dl), _p(dw),
+         _stream())
+    return dl, dw
 
 
 def grouped_gemm_gate_up_bwd(dgu, x, src_row, offsets, gate_up):
