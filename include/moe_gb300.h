@@ -51,6 +51,7 @@ extern "C" {
 #define MOE_ERR_TIMEOUT 4     /* a bounded device-side wait ran out */
 #define MOE_ERR_WORKSPACE 5   /* workspace missing or smaller than required */
 #define MOE_ERR_DEVICE 6      /* a device-side check failed (e.g. id out of range) */
+#define MOE_ERR_SCRATCH_LIMIT 7 /* beyond the fixed scratch of moe_permute_noalloc */
 
 /* Version of this ABI (major*10000 + minor*100 + patch). */
 int moe_version(void);
@@ -117,6 +118,28 @@ int moe_permute_workspace_size(int64_t T, int64_t k, int64_t E, size_t* bytes);
 int moe_permute(const int32_t* ids, const float* w, int64_t T, int64_t k, int64_t E, int32_t* counts,
                 int32_t* offsets, int32_t* row_map, int32_t* src_row, float* w_perm, void* workspace,
                 size_t workspace_bytes, void* stream);
+
+/* moe_permute without a workspace, for callers that cannot allocate device
+ * memory when they route: e.g. a plugin running inside an inference engine's
+ * enqueue step (which must not allocate), a runtime that has reserved all
+ * device memory for its own pool, or a latency-critical path that cannot pay
+ * for cudaMalloc's implicit device synchronisation.  The pages have no
+ * counterpart to this entry point; it computes exactly what moe_permute
+ * computes, with the same arguments minus the workspace.
+ *   Scratch: a fixed 4 MiB array in device memory inside this library
+ *   (every GPU that loads the library holds it until the process exits).
+ *   Limit: ceil(T*k / 2048) * E <= 2^20; larger sizes return
+ *   MOE_ERR_SCRATCH_LIMIT and enqueue nothing.
+ *   Allocation: none (no cudaMalloc, cudaFree or allocating library call).
+ *   Set-up: the first call on each device looks up the array's device
+ *   address (with that device current); make that first call before any
+ *   stream capture.
+ *   Concurrency: all calls share the one array; calls that overlap on the GPU
+ *   (different streams, or devices sharing a context) race.  Each call
+ *   overwrites the scratch it reads, so nothing carries over between calls. */
+int moe_permute_noalloc(const int32_t* ids, const float* w, int64_t T, int64_t k, int64_t E,
+                        int32_t* counts, int32_t* offsets, int32_t* row_map, int32_t* src_row,
+                        float* w_perm, void* stream);
 
 /* The materialised permute: x_perm[row] = x[src_row[row]] for R rows of H
  * bf16 (the grouped GEMMs gather rows themselves and do not need it). */

@@ -18,7 +18,8 @@ INT = ctypes.c_int
 
 MOE_OK = 0
 STATUS_NAMES = {0: "MOE_OK", 1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_CUDA",
-                4: "MOE_ERR_TIMEOUT", 5: "MOE_ERR_WORKSPACE", 6: "MOE_ERR_DEVICE"}
+                4: "MOE_ERR_TIMEOUT", 5: "MOE_ERR_WORKSPACE", 6: "MOE_ERR_DEVICE",
+                7: "MOE_ERR_SCRATCH_LIMIT"}
 
 # name -> argtypes (every entry point returns int)
 SIGNATURES = {
@@ -29,6 +30,7 @@ SIGNATURES = {
     "moe_route": [P, P, P, I64, I64, I64, I64, P, P, P, P, SZ, P],
     "moe_permute_workspace_size": [I64, I64, I64, ctypes.POINTER(SZ)],
     "moe_permute": [P, P, I64, I64, I64, P, P, P, P, P, P, SZ, P],
+    "moe_permute_noalloc": [P, P, I64, I64, I64, P, P, P, P, P, P],
     "moe_permute_rows": [P, P, I64, I64, P, P],
     "moe_grouped_gemm_gate_up_swiglu": [P, P, P, P, I64, I64, I64, I64, I64, P, P, P, P, P],
     "moe_grouped_gemm_down": [P, P, P, I64, I64, I64, I64, P, P],

@@ -50,6 +50,8 @@ constexpr int64_t kMaxI32 = 2147483647;
 
 }  // namespace
 
+int device_info(DeviceInfo* out) { return current_device(out); }
+
 bool encode_tensor_map_2d_bf16(CUtensorMap* map, const void* base, const cuuint64_t* dims,
                                const cuuint64_t* strides, const cuuint32_t* box,
                                const cuuint32_t* estr) {
@@ -91,6 +93,7 @@ const char* moe_error_string(int status) {
     case MOE_ERR_TIMEOUT: return "device-side wait timed out";
     case MOE_ERR_WORKSPACE: return "workspace missing or too small";
     case MOE_ERR_DEVICE: return "device-side check failed";
+    case MOE_ERR_SCRATCH_LIMIT: return "size exceeds the fixed scratch of moe_permute_noalloc";
     default: return "unknown status";
   }
 }

@@ -21,6 +21,9 @@ struct DeviceInfo {
   uint64_t wait_limit_ns;  // bound of every device-side spin wait
 };
 
+// Device information of the current device (status word address, SM count).
+int device_info(DeviceInfo* out);
+
 // Encodes a 2-D bf16 tensor map with 128-byte swizzle (driver entry point
 // looked up at run time); false when the driver rejects it.
 bool encode_tensor_map_2d_bf16(CUtensorMap* map, const void* base, const cuuint64_t* dims,

@@ -17,6 +17,9 @@
 // Outputs: counts, offsets, row_map[i] (permuted row of assignment i),
 // src_row[row] = i / k, and optionally w_perm[row] = w[i] (the gate weight
 // travelling with its row).  Workspace: hist, nblocks * E int32.
+#include <mutex>
+
+#include "../../include/moe_gb300.h"
 #include "kernels.h"
 
 namespace moe {
@@ -186,3 +189,56 @@ cudaError_t launch_permute_rows(const uint16_t* x, const int32_t* src_row, int64
 }
 
 }  // namespace moe
+
+// ------------------------------------------------------------------------
+// moe_permute_noalloc: the same permutation without a caller workspace.
+//
+// Some callers cannot allocate device memory at the moment they route
+// tokens: a plugin called from an inference engine's enqueue step, which
+// must not allocate; a runtime that has already reserved all device memory
+// for its own pool; or a latency-critical path that cannot afford
+// cudaMalloc's implicit device synchronisation.  For them the per-block
+// histograms live in a fixed array in device memory, declared here; every
+// GPU that loads this library keeps it until the process exits.
+namespace moe {
+
+constexpr int64_t kNoAllocScratchInts = int64_t(1) << 20;   // 4 MiB
+static __device__ __align__(256) int32_t g_permute_scratch[kNoAllocScratchInts];
+
+static std::mutex g_noalloc_mu;
+static int32_t* g_noalloc_scratch[kMaxDevices] = {nullptr};
+
+}  // namespace moe
+
+extern "C" int moe_permute_noalloc(const int32_t* ids, const float* w, int64_t T, int64_t k, int64_t E,
+                                   int32_t* counts, int32_t* offsets, int32_t* row_map,
+                                   int32_t* src_row, float* w_perm, void* stream) {
+  if (T < 0 || k < 1 || E < 1 || T * k > 2147483647) return MOE_ERR_INVALID_ARG;
+  if (!counts || !offsets || (T > 0 && (!ids || !row_map || !src_row))) return MOE_ERR_INVALID_ARG;
+  if ((w == nullptr) != (w_perm == nullptr)) return MOE_ERR_INVALID_ARG;
+  if (E > moe::kMaxExperts) return MOE_ERR_UNSUPPORTED;
+  if (moe::permute_workspace_bytes(T * k, E) > sizeof(moe::g_permute_scratch))
+    return MOE_ERR_SCRATCH_LIMIT;
+  moe::DeviceInfo dev;
+  int rc = moe::device_info(&dev);
+  if (rc != MOE_OK) return rc;
+  int32_t* scratch = nullptr;
+  {
+    // Set-up, once per device, with that device current: the device
+    // address of the array (in host code its name is only a host-side
+    // stand-in, which a kernel must never be given).
+    std::lock_guard<std::mutex> lock(moe::g_noalloc_mu);
+    if (!moe::g_noalloc_scratch[dev.ordinal]) {
+      void* addr = nullptr;
+      if (cudaGetSymbolAddress(&addr, moe::g_permute_scratch) != cudaSuccess || !addr) return MOE_ERR_CUDA;
+      moe::g_noalloc_scratch[dev.ordinal] = static_cast<int32_t*>(addr);
+    }
+    scratch = moe::g_noalloc_scratch[dev.ordinal];
+  }
+  // Every call fully overwrites the histogram entries it reads (the count
+  // pass writes all nblocks x E of them first), so nothing has to be cleared.
+  return moe::launch_permute(ids, w, T, k, E, counts, offsets, row_map, src_row, w_perm, scratch,
+                             dev.status, static_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? MOE_OK
+             : MOE_ERR_CUDA;
+}
