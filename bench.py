@@ -50,9 +50,12 @@ def parse():
     ap.add_argument("--no-fwd-bwd", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
-    ap.add_argument("--gather", default="rows", choices=["fused", "rows"],
-                    help="fused: the gate_up GEMM gathers token rows itself (TMA row gather); "
-                         "rows: materialise the permuted rows first and stream them with tile loads")
+    ap.add_argument("--train-only", action="store_true",
+                    help="time only the training step (forward + backward) for --steps steps")
+    ap.add_argument("--gather", default="rows", choices=["fused", "tma", "rows"],
+                    help="fused: the gate_up GEMM gathers token rows itself with cp.async; tma: the "
+                         "same with TMA tile::gather4; rows: materialise the permuted rows first and "
+                         "stream them with TMA tiles (default, fastest)")
     return ap.parse_args()
 
 
@@ -214,13 +217,23 @@ def run_native(args):
     moe.load()
     cfg = synth.CONFIGS[args.workload]
     pk, pk_kind = peaks()
-    d = device_inputs(cfg, torch, device)
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=device)
+    if args.train_only:
+        moe.set_gather_mode("tma" if args.gather == "tma" else "cpasync")
+        res = fwd_bwd(moe, torch, torch.cuda.current_stream(), dist, device, ws, flush, pk,
+                      args.gather != "rows", K=args.steps, W=max(args.warmup, 3))
+        if rank == 0:
+            print(json.dumps({"metric": METRIC, "fwd_bwd": res}), flush=True)
+        if dist is not None:
+            dist.destroy_process_group()
+        return
+    d = device_inputs(cfg, torch, device)
     stream = torch.cuda.current_stream()
     T, H, E, k, I = cfg.T, cfg.H, cfg.E, cfg.k, cfg.I
     I_s = cfg.I_shared
 
-    fused = args.gather == "fused"
+    fused = args.gather in ("fused", "tma")
+    moe.set_gather_mode("tma" if args.gather == "tma" else "cpasync")
     names = ["route", "permute"] + ([] if fused else ["permute_rows"]) + ["gate_up", "down"] + \
         (["shared"] if I_s else []) + ["combine"]
 
@@ -364,13 +377,12 @@ def e2e(moe, d, cfg, torch, stream, dist, device, ws, K, fused):
             "note": "weights resident; x H2D from pinned host + y D2H to pinned host inside the timed region"}
 
 
-def fwd_bwd(moe, torch, stream, dist, device, ws, flush, pk, fused):
+def fwd_bwd(moe, torch, stream, dist, device, ws, flush, pk, fused, K=30, W=3):
     """Training step (forward with saved activations + backward) on the training workload."""
     import synth
 
     cfg = synth.CONFIGS["qwen3_moe_train"]
     d = device_inputs(cfg, torch, device)
-    K = 30
 
     def step():
         y, st = moe.moe_forward(d["x"], d["w_router"], d["gate_up"], d["down"], cfg.k, save_for_backward=True,
@@ -378,7 +390,7 @@ def fwd_bwd(moe, torch, stream, dist, device, ws, flush, pk, fused):
         g = moe.moe_backward(d["dy"], st, d["w_router"], d["gate_up"], d["down"])
         return g
 
-    for _ in range(3):
+    for _ in range(W):
         step()
     moe.sync_status()
     torch.cuda.synchronize()

@@ -72,6 +72,20 @@ int moe_sync_status(void* stream, uint32_t* detail);
  * default.  Not thread-safe against concurrent launches. */
 int moe_set_wait_limit_ns(uint64_t ns);
 
+/* How the grouped gate_up GEMM gathers token rows when it is given src_row
+ * (the permute fused into the A-operand load): 0 (default) = 16-byte
+ * cp.async copies by four dedicated warps into the swizzled stage; 1 = TMA
+ * tile::gather4 (four rows per instruction).  Both give identical results.
+ * Applies to launches after the call; not thread-safe against them. */
+int moe_set_gather_mode(int mode);
+
+/* Test hook of the failure-detection path: while on (1), the grouped GEMMs
+ * launched afterwards issue no operand loads, so their MMA warp's bounded
+ * wait runs out; the kernel then records MOE_ERR_TIMEOUT, stops its other
+ * warps, frees its tensor memory and returns (outputs undefined), leaving
+ * the context usable.  Off (0) by default; not for production use. */
+int moe_test_stall_gemm_producer(int on);
+
 /* ------------------------------------------------------------------ route */
 
 /* Bytes of workspace moe_route needs.  With E % 8 == 0 and H % 64 == 0 the
@@ -207,14 +221,14 @@ int moe_unpermute_combine_bwd(const uint16_t* dy, const int32_t* src_row, int64_
                               int64_t k, uint16_t* dy_perm, void* stream);
 
 /* Number of partial sums per permuted row that moe_grouped_gemm_down_bwd
- * writes into dw_part (one per 256-column tile of I). */
+ * writes into dw_part (two per 256-column tile of I). */
 int moe_grouped_gemm_down_bwd_parts(int64_t I, int64_t* nparts);
 
 /* Backward of the down GEMM and of the SwiGLU, per expert e:
  *   a = dy_perm[r] . down_e^T                         (fp32)
  *   dh = w_perm[r] * a;  g, u = gu_pre[r];  s = sigmoid(g)
  *   dgu[r] = [ dh * u * s * (1 + g*(1-s))  |  dh * g * s ]   (bf16)
- *   dw_part[r, n] = sum over tile n's columns of a * silu(g) * u   (fp32;
+ *   dw_part[r, n] = sum over column block n of a * silu(g) * u    (fp32;
  *                   summed over n this is <dY[t], y_perm[r]>, the gradient
  *                   of the gate weight of row r)
  *   d_down_e = h_w_e^T . dy_perm_e                    (fp32 accumulate, bf16;

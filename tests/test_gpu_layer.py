@@ -34,19 +34,25 @@ def _inputs(T, H, E, k, I, seed, **kw):
     return cfg, synth.make_inputs(cfg, with_dy=True)
 
 
-def _forward(moe, inp, save=False, fused=True):
+def _forward(moe, inp, save=False, fused="rows"):
+    """fused: "cpasync" / "tma" gather the token rows inside the gate_up GEMM
+    (cp.async copies or TMA tile::gather4); "rows" materialises them first."""
     x, wr = bf(inp.x), f32(inp.w_router)
     gu, dn = bf(inp.gate_up), bf(inp.down)
     bias = f32(inp.bias) if inp.bias is not None else None
     sgu = bf(inp.sh_gate_up) if inp.sh_gate_up is not None else None
     sdn = bf(inp.sh_down) if inp.sh_down is not None else None
-    y, st = moe.moe_forward(x, wr, gu, dn, inp.cfg.k, bias, sgu, sdn, save_for_backward=save,
-                            fused_gather=fused)
-    moe.sync_status()
+    moe.set_gather_mode("tma" if fused == "tma" else "cpasync")
+    try:
+        y, st = moe.moe_forward(x, wr, gu, dn, inp.cfg.k, bias, sgu, sdn, save_for_backward=save,
+                                fused_gather=fused != "rows")
+        moe.sync_status()
+    finally:
+        moe.set_gather_mode("cpasync")
     return (x, wr, gu, dn), y, st
 
 
-@pytest.mark.parametrize("fused", [True, False], ids=["gather_fused", "rows_materialised"])
+@pytest.mark.parametrize("fused", ["cpasync", "tma", "rows"])
 @pytest.mark.parametrize("T,H,E,k,I", SMALL)
 def test_forward_elementwise(T, H, E, k, I, fused):
     moe = lib()
@@ -90,7 +96,7 @@ def test_shared_expert_layer():
     assert_close("y", f64(y), ref["y"])
 
 
-@pytest.mark.parametrize("fused", [True, False], ids=["gather_fused", "rows_materialised"])
+@pytest.mark.parametrize("fused", ["cpasync", "tma", "rows"])
 @pytest.mark.parametrize("T,H,E,k,I", SMALL)
 def test_backward_elementwise(T, H, E, k, I, fused):
     moe = lib()
@@ -125,11 +131,11 @@ def test_backward_empty_experts_get_zero_weight_grads():
     assert not dgu[empty].any() and not ddn[empty].any()
 
 
-def _sampled_forward_check(cfg_name, n_tokens=192):
+def _sampled_forward_check(cfg_name, n_tokens=192, fused="rows"):
     moe = lib()
     cfg = synth.CONFIGS[cfg_name]
     inp = synth.make_inputs(cfg)
-    _, y, st = _forward(moe, inp)
+    _, y, st = _forward(moe, inp, fused=fused)
     r = oracle.route(inp.x, inp.w_router, inp.bias, cfg.k)
     same, tol = compare_ids(npi(st.ids), r)
     assert tol <= max(4, cfg.T // 2000)   # every one of them checked to be a near tie
@@ -145,8 +151,9 @@ def _sampled_forward_check(cfg_name, n_tokens=192):
     return st
 
 
-def test_qwen3_moe_forward_sampled():
-    _sampled_forward_check("qwen3_moe")
+@pytest.mark.parametrize("fused", ["rows", "cpasync"])
+def test_qwen3_moe_forward_sampled(fused):
+    _sampled_forward_check("qwen3_moe", fused=fused)
 
 
 def test_skewed_routing_forward_sampled():

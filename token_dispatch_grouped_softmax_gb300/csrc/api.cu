@@ -16,6 +16,8 @@ std::mutex g_mu;
 DeviceInfo g_dev[kMaxDevices];
 bool g_dev_ready[kMaxDevices] = {false};
 uint64_t g_wait_limit_ns = 2000000000ull;
+int g_test_stall_producer = 0;
+int g_gather_mode = 0;
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
@@ -37,6 +39,8 @@ int current_device(DeviceInfo* out) {
   }
   *out = g_dev[dev];
   out->wait_limit_ns = g_wait_limit_ns;
+  out->test_stall_producer = g_test_stall_producer;
+  out->gather_mode = g_gather_mode;
   return MOE_OK;
 }
 
@@ -100,6 +104,17 @@ const char* moe_error_string(int status) {
 
 int moe_set_wait_limit_ns(uint64_t ns) {
   moe::g_wait_limit_ns = ns ? ns : 2000000000ull;
+  return MOE_OK;
+}
+
+int moe_set_gather_mode(int mode) {
+  if (mode != 0 && mode != 1) return MOE_ERR_INVALID_ARG;
+  moe::g_gather_mode = mode;
+  return MOE_OK;
+}
+
+int moe_test_stall_gemm_producer(int on) {
+  moe::g_test_stall_producer = on ? 1 : 0;
   return MOE_OK;
 }
 

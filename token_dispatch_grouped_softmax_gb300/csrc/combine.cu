@@ -4,9 +4,9 @@
 // Parallelism": the experts' outputs summed with the gate weights;
 // "InternVL3.5 接入 pure FSDP2 后端开发实践" §8.3: unpermute):
 //   y[t] = sum_{j<k} w[t,j] * y_perm[row_map[t*k+j]]  (+ y_shared[t])
-// One warp per token; each lane owns 16-byte (8 x bf16) column chunks and
-// accumulates in fp32 in increasing j, so the result does not depend on the
-// launch shape (a gather, not a scatter-add: deterministic).
+// One warp per (token, 1024-column slice); each lane owns 16-byte (8 x bf16)
+// column chunks and accumulates in fp32 in increasing j, so the result does
+// not depend on the launch shape (a gather, not a scatter-add: deterministic).
 //
 // Backward (the gradient of the same expression, experts held fixed):
 //   combine_bwd   dy_perm[row] = dY[src_row[row]]: an exact copy (the rows
@@ -29,6 +29,11 @@ namespace {
 
 constexpr int kWarpsPerBlock = 8;
 
+// Rows are split into slices of kSliceChunks 16-byte chunks (1024 bf16), one
+// warp per (token, slice), so that a launch has enough warps in flight to
+// keep HBM busy even when T is small.
+constexpr int kSliceChunks = 128;
+
 __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict__ y_perm,
                                                       const int32_t* __restrict__ row_map,
                                                       const float* __restrict__ w,
@@ -36,7 +41,12 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict
                                                       int T, int H, int k,
                                                       uint16_t* __restrict__ y) {
   const int lane = threadIdx.x & 31;
-  const int t = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
+  const int nch = H / 8;
+  const int slices = (nch + kSliceChunks - 1) / kSliceChunks;
+  const int gw = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
+  const int t = gw / slices;
+  const int c_begin = (gw - t * slices) * kSliceChunks;
+  const int c_end = min(nch, c_begin + kSliceChunks);
   if (t >= T) return;
   int my_row = 0;
   float my_w = 0.f;
@@ -44,8 +54,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict
     my_row = row_map[(int64_t)t * k + lane];
     my_w = w[(int64_t)t * k + lane];
   }
-  const int nch = H / 8;
-  for (int c = lane; c < nch; c += 32) {
+  for (int c = c_begin + lane; c < c_end; c += 32) {
     float acc[8];
 #pragma unroll
     for (int q = 0; q < 8; ++q) acc[q] = 0.f;
@@ -126,7 +135,12 @@ __global__ void __launch_bounds__(256) gather_dx_kernel(const uint16_t* __restri
                                                         int H, int E, int k,
                                                         uint16_t* __restrict__ dx) {
   const int lane = threadIdx.x & 31;
-  const int t = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
+  const int nch = H / 8;
+  const int slices = (nch + kSliceChunks - 1) / kSliceChunks;
+  const int gw = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
+  const int t = gw / slices;
+  const int c_begin = (gw - t * slices) * kSliceChunks;
+  const int c_end = min(nch, c_begin + kSliceChunks);
   if (t >= T) return;
   int my_row = 0, my_id = 0;
   float my_dz = 0.f;
@@ -137,8 +151,7 @@ __global__ void __launch_bounds__(256) gather_dx_kernel(const uint16_t* __restri
       my_dz = d_logits[(int64_t)t * E + my_id];
     }
   }
-  const int nch = H / 8;
-  for (int c = lane; c < nch; c += 32) {
+  for (int c = c_begin + lane; c < c_end; c += 32) {
     float acc[8];
 #pragma unroll
     for (int q = 0; q < 8; ++q) acc[q] = 0.f;
@@ -216,7 +229,8 @@ cudaError_t launch_combine(const uint16_t* y_perm, const int32_t* row_map, const
                            const uint16_t* y_shared, int64_t T, int64_t H, int64_t k, uint16_t* y,
                            cudaStream_t stream) {
   if (T == 0) return cudaSuccess;
-  combine_kernel<<<(unsigned)((T + kWarpsPerBlock - 1) / kWarpsPerBlock), 256, 0, stream>>>(
+  const int64_t warps = T * ((H / 8 + kSliceChunks - 1) / kSliceChunks);
+  combine_kernel<<<(unsigned)((warps + kWarpsPerBlock - 1) / kWarpsPerBlock), 256, 0, stream>>>(
       y_perm, row_map, w, y_shared, (int)T, (int)H, (int)k, y);
   return cudaGetLastError();
 }
@@ -242,7 +256,8 @@ cudaError_t launch_gather_dx(const uint16_t* dx_perm, const int32_t* row_map, co
     dim3 g((unsigned)((E + 31) / 32), (unsigned)((H + 31) / 32));
     transpose_f32_kernel<<<g, dim3(32, 8), 0, stream>>>(w_router, (int)H, (int)E, wr_t);
   }
-  gather_dx_kernel<<<(unsigned)((T + kWarpsPerBlock - 1) / kWarpsPerBlock), 256, 0, stream>>>(
+  const int64_t warps = T * ((H / 8 + kSliceChunks - 1) / kSliceChunks);
+  gather_dx_kernel<<<(unsigned)((warps + kWarpsPerBlock - 1) / kWarpsPerBlock), 256, 0, stream>>>(
       dx_perm, row_map, d_logits, ids, wr_t, (int)T, (int)H, (int)E, (int)k, dx);
   return cudaGetLastError();
 }

@@ -16,8 +16,8 @@
 //   WGRAD_DOWN    d_down_e  = h_e^T . dy_perm_e
 //   WGRAD_GATEUP  d_gu_e    = x[src_rows of e]^T . dgu_e
 //
-// One persistent, warp-specialised kernel template serves all six (grid =
-// the SM count, 192 threads, one CTA per SM):
+// One persistent, warp-specialised kernel template serves all of them (grid
+// = the SM count, one CTA per SM):
 //   warp 0      TMA producer: per 64-wide K block one A tile (128 rows) and
 //               one B tile (256 columns) into a 4-stage shared-memory ring,
 //               128-byte swizzled.  Gathered A rows (the permute fused into
@@ -27,10 +27,14 @@
 //               and, from one lane, issues tcgen05.mma (M=128, N=256, K=16,
 //               bf16 x bf16 -> fp32); tcgen05.commit frees ring stages and
 //               hands finished accumulators to the epilogue.
-//   warps 2..5  epilogue: tcgen05.ld of the accumulator (one TMEM lane = one
-//               output row per thread), fused SwiGLU / SwiGLU-backward in
-//               fp32, bf16 stores.  Double-buffered accumulators let the
-//               epilogue of tile i overlap the main loop of tile i+1.
+//   warps 2..    epilogue, one warpgroup (two splitting the columns for the
+//               SwiGLU backward): tcgen05.ld of the accumulator (one TMEM
+//               lane = one output row per thread), fused SwiGLU /
+//               SwiGLU-backward in fp32, vector stores.  Double-buffered
+//               accumulators let the epilogue of tile i overlap the main
+//               loop of tile i+1.
+//   4 more      (gate_up only) cp.async row gather of the A operand, the
+//               permute fused into the load.
 //
 // The tile list is derived on the device from expert_offsets (no host read
 // back): forward and dgrad GEMMs are grouped along M (each expert's rows form
@@ -58,7 +62,8 @@ constexpr int STAGES = 4;
 constexpr int A_BYTES = BM * BK * 2;               // 16 KB
 constexpr int B_BYTES = BN * BK * 2;               // 32 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;     // 48 KB
-constexpr int kThreads = 192;
+constexpr int kGatherThreads = 128;      // cp.async row-gather warps (FWD_GATEUP only)
+constexpr int kGatherDepth = 2;          // stages a gather thread keeps in flight before arriving
 constexpr uint32_t TMEM_COLS = 512;
 constexpr int MN_CHUNK_BYTES = 64 * 128;           // one 64-wide MN chunk x 64 K rows
 
@@ -72,6 +77,14 @@ struct Traits {
                                 MODE == WGRAD_GATEUP || MODE == ROUTER);
   static constexpr bool kKGrouped = (MODE == WGRAD_DOWN || MODE == WGRAD_GATEUP);
   static constexpr bool kRouter = (MODE == ROUTER);
+  // Epilogue warps: one warpgroup, or two splitting the columns where the
+  // epilogue itself is heavy (the SwiGLU backward of DGRAD_DOWN).
+  static constexpr int kEpiWarps = (MODE == DGRAD_DOWN) ? 8 : 4;
+  static constexpr int kHalves = kEpiWarps / 4;
+  // FWD_GATEUP has four more warps that gather token rows with cp.async
+  static constexpr int kGatherWarps = (MODE == FWD_GATEUP) ? 4 : 0;
+  // warp 0 TMA producer, warp 1 MMA issuer, then the epilogue and gather warps
+  static constexpr int kThreads = 32 * (2 + kEpiWarps + kGatherWarps);
 };
 
 struct GemmParams {   // 64-byte aligned through its CUtensorMap members
@@ -79,12 +92,15 @@ struct GemmParams {   // 64-byte aligned through its CUtensorMap members
   CUtensorMap tmB;
   const int32_t* offsets;   // [E+1] expert row offsets, or nullptr: one group of `rows`
   const int32_t* gidx;      // gather indices (src_row), or nullptr: identity
+  const uint16_t* a_ptr;    // A base pointer for the cp.async row gather (row stride K)
+  int a_cpasync;            // FWD_GATEUP with gidx: 1 = cp.async row gather, 0 = TMA tile::gather4
   const float* aux;         // fp32 gu_pre [R, 2I] read by DGRAD_DOWN
   const float* wrow;        // gate weight of each permuted row [R] (nullable)
   uint16_t* out;
   float* out_gu;            // FWD_GATEUP: fp32 pre-activations g | u [R, 2I] (nullable)
   uint16_t* out_hw;         // FWD_GATEUP: bf16(w_row * h) [R, I] (nullable, needs wrow)
-  float* out_part;          // DGRAD_DOWN: per (row, n tile) partial of <dY . Wd^T, h> [R, nt]
+  float* out_part;          // DGRAD_DOWN: per (row, n tile, column half) partial of
+                            // <dY . Wd^T, h> [R, 2 nt]
                             // ROUTER: fp32 partial logits [parts, rows, n_out]
   uint32_t* status;
   uint64_t wait_limit_ns;
@@ -97,6 +113,7 @@ struct GemmParams {   // 64-byte aligned through its CUtensorMap members
   int nt;                   // n tiles
   int mt_w;                 // m tiles per expert (K-grouped modes)
   int64_t ldo;              // leading dimension of out
+  int stall_producer;       // test hook: the producer issues no loads (a wait that runs out)
 };
 
 // UMMA shared-memory descriptor, 128-byte swizzle, sm_100-family version bits.
@@ -179,12 +196,13 @@ __device__ __forceinline__ Tile decode_tile(const GemmParams& p, const int* pref
 }
 
 template <int MODE>
-__device__ __forceinline__ void store_zero_tile(const GemmParams& p, const Tile& t, int r) {
+__device__ __forceinline__ void store_zero_tile(const GemmParams& p, const Tile& t, int r, int half,
+                                                int halves) {
   const int m = t.mt * BM + r;
   if (m >= p.m_w) return;
   uint16_t* orow = p.out + ((int64_t)t.e * p.m_w + m) * p.ldo + (int64_t)t.nt * BN;
   const uint4 z = make_uint4(0, 0, 0, 0);
-  for (int c = 0; c < BN; c += 8)
+  for (int c = half * (BN / halves); c < (half + 1) * (BN / halves); c += 8)
     if (t.nt * BN + c < p.n_out) *reinterpret_cast<uint4*>(orow + c) = z;
 }
 
@@ -210,7 +228,8 @@ __device__ __forceinline__ void load32_f32(const float* src, float* v) {
 }
 
 template <int MODE>
-__global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_constant__ GemmParams p) {
+__global__ void __launch_bounds__(Traits<MODE>::kThreads, 1)
+    grouped_gemm_kernel(const __grid_constant__ GemmParams p) {
   using Tr = Traits<MODE>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -233,12 +252,12 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(full_bar(s), 1);
+      mbar_init(full_bar(s), 1 + (p.a_cpasync ? kGatherThreads : 0));
       mbar_init(empty_bar(s), 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(accf_bar(b), 1);
-      mbar_init(acce_bar(b), 128);
+      mbar_init(acce_bar(b), 32 * Tr::kEpiWarps);
     }
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
@@ -292,11 +311,11 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
     uint32_t issued_mask = 0;       // stages that ever received a load
     uint32_t last_parity = 0;       // bit s: parity of the last load into stage s
     bool ok = true;
-    for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x) {
+    for (int tile = blockIdx.x; tile < total_tiles && ok && !p.stall_producer; tile += gridDim.x) {
       const Tile t = decode_tile<MODE>(p, prefix, tile);
       if (t.kblocks == 0) continue;
       int gi[4] = {0, 0, 0, 0};
-      if (MODE == FWD_GATEUP && p.gidx) {   // this lane gathers tile rows 4*lane .. 4*lane+3
+      if (MODE == FWD_GATEUP && p.gidx && !p.a_cpasync) {   // this lane gathers rows 4*lane .. +3
 #pragma unroll
         for (int q = 0; q < 4; ++q) gi[q] = p.gidx[t.row0 + min(4 * lane + q, t.rows - 1)];
       }
@@ -309,14 +328,17 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
         const uint32_t sA = ring_u32 + stage * STAGE_BYTES;
         const uint32_t sB = sA + A_BYTES;
         const uint32_t fb = full_bar(stage);
-        if (lane == 0) mbar_arrive_expect_tx(fb, STAGE_BYTES);
+        if (lane == 0) mbar_arrive_expect_tx(fb, p.a_cpasync ? B_BYTES : STAGE_BYTES);
         __syncwarp();
         const int k0 = kb * BK;
         if (MODE == FWD_GATEUP) {
-          if (p.gidx)                                      // permute fused into the load
+          if (p.a_cpasync) {
+            // A rows come from the gather warps
+          } else if (p.gidx) {                             // permute fused into the load (TMA)
             tma_gather4(sA + 4 * lane * 128, &p.tmA, k0, gi[0], gi[1], gi[2], gi[3], fb);
-          else if (lane == 0)                              // rows already in permuted order
+          } else if (lane == 0) {                          // rows already in permuted order
             tma_load_2d(sA, &p.tmA, k0, t.row0, fb);
+          }
           if (lane == 0) {
             const int brow = t.e * p.K + k0;               // gate_up rows of expert e
             const int n0 = t.nt * 128;
@@ -471,16 +493,20 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
       while (!mbar_try_wait(drain_bar, 0) && globaltimer_ns() - t0 < p.wait_limit_ns) {
       }
     }
-  } else {
+  } else if (warp < 2 + Tr::kEpiWarps) {
     // ---------------------------------------------------------- epilogue
+    // Each warp reads the TMEM lane quarter its rank allows (warp % 4); with
+    // two warpgroups each takes one half of the tile's columns.
     const int quarter = warp & 3;            // TMEM lanes 32*quarter .. +31
+    const int half = (warp - 2) >> 2;        // column part of this warpgroup
+    constexpr int kH = Tr::kHalves;
     const int r = quarter * 32 + lane;       // accumulator row of this thread
     int buf = 0;
     uint32_t acc_phase = 0;
     for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
       const Tile t = decode_tile<MODE>(p, prefix, tile);
       if (t.kblocks == 0) {
-        if (Tr::kKGrouped) store_zero_tile<MODE>(p, t, r);
+        if (Tr::kKGrouped) store_zero_tile<MODE>(p, t, r, half, kH);
         continue;
       }
       bool w = true;
@@ -495,7 +521,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
         const int64_t row = t.row0 + r;
         const int n0 = t.nt * 128;
 #pragma unroll 1
-        for (int c0 = 0; c0 < 128; c0 += 32) {
+        for (int c0 = half * (128 / kH); c0 < (half + 1) * (128 / kH); c0 += 32) {
           if (n0 + c0 >= p.n_out) break;                 // warp-uniform
           float u[32];
           tmem_ld32(taddr + c0, v);                      // gate columns
@@ -521,14 +547,16 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
         float* orow = p.out_part + ((int64_t)t.e * p.rows + t.row0 + r) * p.ldo;
         const int n0 = t.nt * BN;
 #pragma unroll 1
-        for (int c0 = 0; c0 < BN; c0 += 32) {
+        for (int c0 = half * (BN / kH); c0 < (half + 1) * (BN / kH); c0 += 32) {
           if (n0 + c0 >= p.n_out) break;
           tmem_ld32(taddr + c0, v);
           if (row_ok) {
             if (n0 + c0 + 32 <= p.n_out && (p.ldo & 3) == 0) {
               store32_f32(orow + n0 + c0, v);
             } else {
-              for (int q = 0; q < 32 && n0 + c0 + q < p.n_out; ++q) orow[n0 + c0 + q] = v[q];
+#pragma unroll
+              for (int q = 0; q < 32; ++q)
+                if (n0 + c0 + q < p.n_out) orow[n0 + c0 + q] = v[q];
             }
           }
         }
@@ -537,7 +565,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
         const int64_t row = t.row0 + r;
         const int n0 = t.nt * BN;
 #pragma unroll 1
-        for (int c0 = 0; c0 < BN; c0 += 32) {
+        for (int c0 = half * (BN / kH); c0 < (half + 1) * (BN / kH); c0 += 32) {
           if (n0 + c0 >= p.n_out) break;
           tmem_ld32(taddr + c0, v);
           if (row_ok) store32(p.out + row * p.ldo + n0 + c0, v);
@@ -548,7 +576,7 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
         const int n0 = t.nt * BN;
         float dot = 0.f;                                 // <dY . Wd^T, h> over this tile's columns
 #pragma unroll 1
-        for (int c0 = 0; c0 < BN; c0 += 32) {
+        for (int c0 = half * (BN / kH); c0 < (half + 1) * (BN / kH); c0 += 32) {
           if (n0 + c0 >= p.n_out) break;
           tmem_ld32(taddr + c0, v);                      // dY . Wd^T (fp32)
           if (row_ok) {
@@ -570,14 +598,14 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
             store32(p.out + row * 2 * p.I + p.I + n0 + c0, u);
           }
         }
-        if (row_ok && p.out_part) p.out_part[row * p.nt + t.nt] = dot;
+        if (row_ok && p.out_part) p.out_part[row * 2 * p.nt + 2 * t.nt + half] = dot;
       } else {  // WGRAD_*: output rows m = mt*BM + r of expert e's weight-gradient block
         const int m = t.mt * BM + r;
         const bool row_ok = m < p.m_w;
         uint16_t* orow = p.out + ((int64_t)t.e * p.m_w + m) * p.ldo;
         const int n0 = t.nt * BN;
 #pragma unroll 1
-        for (int c0 = 0; c0 < BN; c0 += 32) {
+        for (int c0 = half * (BN / kH); c0 < (half + 1) * (BN / kH); c0 += 32) {
           if (n0 + c0 >= p.n_out) break;
           tmem_ld32(taddr + c0, v);
           if (row_ok) store32(orow + n0 + c0, v);
@@ -587,6 +615,53 @@ __global__ void __launch_bounds__(kThreads, 1) grouped_gemm_kernel(const __grid_
       mbar_arrive(acce_bar(buf));
       buf ^= 1;
       if (buf == 0) acc_phase ^= 1u;
+    }
+  } else if (Tr::kGatherWarps > 0 && p.a_cpasync) {
+    // ------------------------------------------- cp.async row gather of A
+    // Thread g owns tile row g: per 64-wide K block it copies the row's 128
+    // bytes of x[src_row[row0 + g]] into the stage, 16 bytes at a time, to
+    // the 128-byte-swizzled place the tensor core expects (16-byte chunk c of
+    // row g at chunk c ^ (g % 8)).  It keeps kGatherDepth stages in flight;
+    // once a stage's copies completed it fences them to the async proxy and
+    // arrives on that stage's full barrier.
+    const int g = threadIdx.x - 32 * (2 + Tr::kEpiWarps);
+    int stage = 0, oldest = 0, pend = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; tile < total_tiles && ok && !p.stall_producer; tile += gridDim.x) {
+      const Tile t = decode_tile<MODE>(p, prefix, tile);
+      if (t.kblocks == 0) continue;
+      const uint16_t* xrow = p.a_ptr + (int64_t)p.gidx[t.row0 + min(g, t.rows - 1)] * p.K;
+      const uint32_t sw = (uint32_t)(g & 7);
+      for (int kb = 0; kb < t.kblocks; ++kb) {
+        bool w = true;
+        if (lane == 0)
+          w = mbar_wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, p.wait_limit_ns, p.status, 5);
+        ok = __shfl_sync(0xffffffffu, w ? 1 : 0, 0) != 0;
+        if (!ok) break;
+        const uint32_t dst = ring_u32 + stage * STAGE_BYTES + g * 128;
+        const uint16_t* src = xrow + kb * BK;
+#pragma unroll
+        for (uint32_t c = 0; c < 8; ++c) cp_async_16(dst + ((c ^ sw) << 4), src + c * 8);
+        cp_async_commit();
+        if (++pend > kGatherDepth) {
+          cp_async_wait_group<kGatherDepth>();
+          fence_proxy_async_smem();
+          mbar_arrive(full_bar(oldest));
+          oldest = (oldest + 1 == STAGES) ? 0 : oldest + 1;
+          --pend;
+        }
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+    cp_async_wait_group<0>();
+    fence_proxy_async_smem();
+    for (; pend > 0 && ok; --pend) {
+      mbar_arrive(full_bar(oldest));
+      oldest = (oldest + 1 == STAGES) ? 0 : oldest + 1;
     }
   }
 
@@ -616,7 +691,7 @@ cudaError_t run_gemm(const GemmParams& p, int64_t tiles_upper_bound, const Devic
   }
   int64_t grid = tiles_upper_bound < dev.num_sms ? tiles_upper_bound : dev.num_sms;
   if (grid < 1) grid = 1;
-  grouped_gemm_kernel<MODE><<<(unsigned)grid, kThreads, smem, stream>>>(p);
+  grouped_gemm_kernel<MODE><<<(unsigned)grid, Traits<MODE>::kThreads, smem, stream>>>(p);
   return cudaGetLastError();
 }
 
@@ -634,6 +709,8 @@ void fill_common(GemmParams& p, const int32_t* offsets, int64_t R, int64_t E, in
                  const DeviceInfo& dev) {
   p.offsets = offsets;
   p.gidx = nullptr;
+  p.a_ptr = nullptr;
+  p.a_cpasync = 0;
   p.aux = nullptr;
   p.wrow = nullptr;
   p.out = nullptr;
@@ -642,6 +719,7 @@ void fill_common(GemmParams& p, const int32_t* offsets, int64_t R, int64_t E, in
   p.out_part = nullptr;
   p.status = dev.status;
   p.wait_limit_ns = dev.wait_limit_ns;
+  p.stall_producer = dev.test_stall_producer;
   p.rows = (int)R;
   p.E = (int)E;
   p.I = (int)I;
@@ -664,10 +742,13 @@ int launch_gemm_gate_up(const uint16_t* x, const int32_t* src_row, const int32_t
   if (R == 0) return 0;
   GemmParams p;
   fill_common(p, offsets, R, E, I, dev);
-  // gathered rows: one-row boxes for tile::gather4; rows in order: 128-row tiles
+  // gathered rows: one-row boxes for tile::gather4 (unused by the cp.async
+  // gather); rows in order: 128-row tiles
   const bool ok_a = src_row ? make_map(&p.tmA, x, T, H, 64, 1) : make_map(&p.tmA, x, R, H, 64, 128);
   if (!ok_a || !make_map(&p.tmB, gate_up, E * H, 2 * I, 64, 64)) return -1;
   p.gidx = src_row;
+  p.a_ptr = x;
+  p.a_cpasync = (src_row && dev.gather_mode == 0) ? 1 : 0;
   p.out = h;
   p.wrow = w_perm;
   p.out_gu = gu_pre;
@@ -724,7 +805,7 @@ int launch_gemm_down(const uint16_t* h, const int32_t* offsets, const uint16_t* 
   return run_gemm<FWD_DOWN>(p, mgrouped_tile_bound(R, E, p.nt), dev, stream) == cudaSuccess ? 0 : 1;
 }
 
-int down_bwd_parts(int64_t I) { return (int)((I + BN - 1) / BN); }
+int down_bwd_parts(int64_t I) { return 2 * (int)((I + BN - 1) / BN); }   // two column halves per tile
 
 int launch_gemm_down_bwd(const uint16_t* dy_perm, const uint16_t* h_w, const float* gu_pre,
                          const float* w_perm, const int32_t* offsets, const uint16_t* down, int64_t R,

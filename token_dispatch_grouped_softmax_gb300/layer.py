@@ -42,11 +42,11 @@ def moe_forward(x, w_router, gate_up, down, k, bias=None, sh_gate_up=None, sh_do
                 save_for_backward=False, fused_gather=False):
     """y [T, H] bf16 and the ForwardState.
 
-    fused_gather: the grouped gate_up GEMM gathers the token rows itself (TMA
-    tile::gather4, the permute fused into the operand load); False (default)
-    materialises the permuted rows first (moe_permute_rows) and streams them
-    with 128-row TMA tiles, which measures ~2.6x faster on GB300 because four
-    rows per gather instruction cannot keep the tensor cores fed."""
+    fused_gather: the grouped gate_up GEMM gathers the token rows itself (the
+    permute fused into the operand load, by cp.async copies or TMA
+    tile::gather4, see set_gather_mode); False (default) materialises the
+    permuted rows first (moe_permute_rows) and streams them with 128-row TMA
+    tiles, which measures ~2.5x faster for the GEMM on GB300."""
     T, H = x.shape
     E = w_router.shape[1]
     I = down.shape[0] // E
