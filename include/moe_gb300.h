@@ -72,13 +72,6 @@ int moe_sync_status(void* stream, uint32_t* detail);
  * default.  Not thread-safe against concurrent launches. */
 int moe_set_wait_limit_ns(uint64_t ns);
 
-/* How the grouped gate_up GEMM gathers token rows when it is given src_row
- * (the permute fused into the A-operand load): 0 (default) = 16-byte
- * cp.async copies by four dedicated warps into the swizzled stage; 1 = TMA
- * tile::gather4 (four rows per instruction).  Both give identical results.
- * Applies to launches after the call; not thread-safe against them. */
-int moe_set_gather_mode(int mode);
-
 /* Test hook of the failure-detection path: while on (1), the grouped GEMMs
  * launched afterwards issue no operand loads, so their MMA warp's bounded
  * wait runs out; the kernel then records MOE_ERR_TIMEOUT, stops its other

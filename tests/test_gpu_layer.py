@@ -1,9 +1,10 @@
 """GPU parity of the grouped GEMMs and the whole layer, forward and backward,
 against the fp64 oracle (through the C ABI).
 
-Small cases are compared element by element; they span several 128-row and
-256-column tiles, ragged expert tails, empty experts, and partial column
-tiles.  The named workloads (Qwen3-MoE shape, skewed routing, the training
+Small cases are compared element by element; they span several 128- and
+256-row tiles (the latter once experts average 512 rows), 256-column tiles,
+ragged expert tails of one and two 128-row halves, empty experts, and partial
+column tiles.  The named workloads (Qwen3-MoE shape, skewed routing, the training
 step, DeepSeek-V3 shape) run at full size in the launch configuration the
 benchmark times and are compared on seeded token / expert samples the oracle
 computes one by one; their integer outputs are compared in full.
@@ -25,7 +26,8 @@ SMALL = [
     (512, 256, 16, 4, 192),     # I = 192: a partial gate/up column tile
     (300, 384, 6, 3, 320),      # H = 384: a partial 256-column output tile
     (50, 128, 64, 1, 64),       # mostly empty experts
-    (1100, 256, 4, 2, 128),     # experts with several 128-row tiles
+    (1100, 256, 4, 2, 128),     # >= 512 rows per expert: 256-row tiles, one-half tails
+    (1400, 384, 4, 2, 192),     # 256-row tiles with two-half tails, partial column tiles
 ]
 
 
@@ -35,24 +37,20 @@ def _inputs(T, H, E, k, I, seed, **kw):
 
 
 def _forward(moe, inp, save=False, fused="rows"):
-    """fused: "cpasync" / "tma" gather the token rows inside the gate_up GEMM
-    (cp.async copies or TMA tile::gather4); "rows" materialises them first."""
+    """fused: "tma" gathers the token rows inside the gate_up GEMM (TMA
+    tile::gather4); "rows" materialises them first."""
     x, wr = bf(inp.x), f32(inp.w_router)
     gu, dn = bf(inp.gate_up), bf(inp.down)
     bias = f32(inp.bias) if inp.bias is not None else None
     sgu = bf(inp.sh_gate_up) if inp.sh_gate_up is not None else None
     sdn = bf(inp.sh_down) if inp.sh_down is not None else None
-    moe.set_gather_mode("tma" if fused == "tma" else "cpasync")
-    try:
-        y, st = moe.moe_forward(x, wr, gu, dn, inp.cfg.k, bias, sgu, sdn, save_for_backward=save,
-                                fused_gather=fused != "rows")
-        moe.sync_status()
-    finally:
-        moe.set_gather_mode("cpasync")
+    y, st = moe.moe_forward(x, wr, gu, dn, inp.cfg.k, bias, sgu, sdn, save_for_backward=save,
+                            fused_gather=fused != "rows")
+    moe.sync_status()
     return (x, wr, gu, dn), y, st
 
 
-@pytest.mark.parametrize("fused", ["cpasync", "tma", "rows"])
+@pytest.mark.parametrize("fused", ["tma", "rows"])
 @pytest.mark.parametrize("T,H,E,k,I", SMALL)
 def test_forward_elementwise(T, H, E, k, I, fused):
     moe = lib()
@@ -96,7 +94,7 @@ def test_shared_expert_layer():
     assert_close("y", f64(y), ref["y"])
 
 
-@pytest.mark.parametrize("fused", ["cpasync", "tma", "rows"])
+@pytest.mark.parametrize("fused", ["tma", "rows"])
 @pytest.mark.parametrize("T,H,E,k,I", SMALL)
 def test_backward_elementwise(T, H, E, k, I, fused):
     moe = lib()
@@ -151,7 +149,7 @@ def _sampled_forward_check(cfg_name, n_tokens=192, fused="rows"):
     return st
 
 
-@pytest.mark.parametrize("fused", ["rows", "cpasync"])
+@pytest.mark.parametrize("fused", ["rows", "tma"])
 def test_qwen3_moe_forward_sampled(fused):
     _sampled_forward_check("qwen3_moe", fused=fused)
 
@@ -190,3 +188,26 @@ def test_training_step_backward_sampled():
             rgu, rdn = oracle.backward_expert(e, inp.x, inp.gate_up, inp.down, r["ids"], r["w"], inp.dy)
             assert_close("d_gate_up[%d]" % e, f64(dgu[e * H:(e + 1) * H]), rgu)
             assert_close("d_down[%d]" % e, f64(ddn[e * I:(e + 1) * I]), rdn)
+
+
+def torch_equal(a, b):
+    import torch
+    return bool(torch.equal(a.view(torch.uint8) if a.dtype == torch.bfloat16 else a,
+                            b.view(torch.uint8) if b.dtype == torch.bfloat16 else b))
+
+
+def test_pipelined_forward_matches_forward():
+    """PipelinedForward (copies overlapped with the layer on two streams) gives
+    the same outputs as moe_forward, batch by batch."""
+    import torch
+    moe = lib()
+    cfg, inp = _inputs(256, 256, 8, 2, 128, seed=77)
+    wr, gu, dn = f32(inp.w_router), bf(inp.gate_up), bf(inp.down)
+    xs = [torch.from_numpy(synth.normal_bf16(s, synth.TID_X, (256, 256), 1.0).view(np.int16))
+          .view(torch.bfloat16).pin_memory() for s in (1, 2, 3)]
+    ys = [torch.empty((256, 256), dtype=torch.bfloat16).pin_memory() for _ in xs]
+    moe.PipelinedForward(wr, gu, dn, cfg.k).run(xs, ys)
+    moe.sync_status()
+    for xh, yh in zip(xs, ys):
+        y, _ = moe.moe_forward(xh.cuda(), wr, gu, dn, cfg.k)
+        assert torch_equal(y.cpu(), yh)

@@ -17,7 +17,6 @@ DeviceInfo g_dev[kMaxDevices];
 bool g_dev_ready[kMaxDevices] = {false};
 uint64_t g_wait_limit_ns = 2000000000ull;
 int g_test_stall_producer = 0;
-int g_gather_mode = 0;
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
@@ -40,7 +39,6 @@ int current_device(DeviceInfo* out) {
   *out = g_dev[dev];
   out->wait_limit_ns = g_wait_limit_ns;
   out->test_stall_producer = g_test_stall_producer;
-  out->gather_mode = g_gather_mode;
   return MOE_OK;
 }
 
@@ -104,12 +102,6 @@ const char* moe_error_string(int status) {
 
 int moe_set_wait_limit_ns(uint64_t ns) {
   moe::g_wait_limit_ns = ns ? ns : 2000000000ull;
-  return MOE_OK;
-}
-
-int moe_set_gather_mode(int mode) {
-  if (mode != 0 && mode != 1) return MOE_ERR_INVALID_ARG;
-  moe::g_gather_mode = mode;
   return MOE_OK;
 }
 

@@ -13,37 +13,45 @@
 //                 (= <dY, y_perm[r]>) as per-tile partials, h recomputed in
 //                 fp32 from the saved fp32 pre-activations
 //   DGRAD_GATEUP  dx_perm[r]= dgu[r] . Wgu_e^T
-//   WGRAD_DOWN    d_down_e  = h_e^T . dy_perm_e
+//   WGRAD_DOWN    d_down_e  = (w h)_e^T . dy_perm_e
 //   WGRAD_GATEUP  d_gu_e    = x[src_rows of e]^T . dgu_e
+//   ROUTER        split-K partial router logits x . [W0; W1; W2] (see route.cu)
 //
 // One persistent, warp-specialised kernel template serves all of them (grid
-// = the SM count, one CTA per SM):
-//   warp 0      TMA producer: per 64-wide K block one A tile (128 rows) and
-//               one B tile (256 columns) into a 4-stage shared-memory ring,
-//               128-byte swizzled.  Gathered A rows (the permute fused into
-//               the load) use cp.async.bulk.tensor ... tile::gather4, four
-//               token rows per instruction spread over the warp's lanes.
-//   warp 1      allocates 512 TMEM columns (two 128 x 256 fp32 accumulators)
-//               and, from one lane, issues tcgen05.mma (M=128, N=256, K=16,
-//               bf16 x bf16 -> fp32); tcgen05.commit frees ring stages and
-//               hands finished accumulators to the epilogue.
-//   warps 2..    epilogue, one warpgroup (two splitting the columns for the
-//               SwiGLU backward): tcgen05.ld of the accumulator (one TMEM
-//               lane = one output row per thread), fused SwiGLU /
-//               SwiGLU-backward in fp32, vector stores.  Double-buffered
-//               accumulators let the epilogue of tile i overlap the main
-//               loop of tile i+1.
-//   4 more      (gate_up only) cp.async row gather of the A operand, the
-//               permute fused into the load.
+// = the SM count, one CTA per SM).  A tile is 256 output columns by one or
+// two 128-row halves (a per-mode choice, kH); the halves share each B tile:
+// per 64-wide K block the CTA loads A (kH x 16 KB) and B (32 KB) and issues
+// kH tcgen05.mma of M=128 x N=256.  Two halves need 7.6 KB of operands in
+// shared memory per MFLOP instead of 11.4 KB, so the 192 KB ring (3 stages
+// of 64 KB, or 4 of 48 KB with one half) hides more load latency.  Their two
+// 128 x 256 fp32 accumulators fill the 512 TMEM columns, so the epilogue
+// frees them as soon as it has read them into registers (packed to bf16),
+// and stores after that while the next tile's MMAs run.  Modes whose
+// epilogue cannot hold a tile row in registers (fp32 pre-activations saved
+// for backward; the SwiGLU backward) use one half and double-buffered
+// accumulators instead.  A tile whose rows end within its first half (the
+// ragged tail of an expert) loads and multiplies only that half.
+//   warp 0      TMA producer: A halves and B tiles into the ring, 128-byte
+//               swizzled.  Gathered A rows (the permute fused into the load)
+//               use cp.async.bulk.tensor ... tile::gather4, four token rows
+//               per instruction.
+//   warp 1      allocates the 512 TMEM columns and, from one lane, issues
+//               tcgen05.mma (M=128, N=256, K=16, bf16 x bf16 -> fp32);
+//               tcgen05.commit frees ring stages and hands finished
+//               accumulators to the epilogue.
+//   warps 2..9  epilogue: tcgen05.ld (one TMEM lane = one output row per
+//               thread), fused SwiGLU / SwiGLU backward / gate weight in
+//               fp32, vector stores.  With two halves warpgroup g drains half
+//               g; with one half warpgroup g takes column half g.
 //
 // The tile list is derived on the device from expert_offsets (no host read
 // back): forward and dgrad GEMMs are grouped along M (each expert's rows form
-// ceil(M_e/128) row tiles, empty experts none); wgrad GEMMs are grouped along
+// ceil(M_e/BM) row tiles, empty experts none); wgrad GEMMs are grouped along
 // K (every expert owns a fixed grid of output tiles; its K extent is M_e,
 // and an empty expert's tiles are written as zeros).  Within a wgrad tile,
 // K rows past the expert's last row are zeroed in shared memory before the
 // MMA so no other expert's rows leak in.  The K order inside a tile is fixed
-// and there is no split-K: results are deterministic.
+// and there is no split-K with atomics: results are deterministic.
 //
 // Every spin wait is bounded (globaltimer); on expiry the kernel records
 // MOE_ERR_TIMEOUT in the status word, lets the other roles stop, waits
@@ -55,36 +63,46 @@ namespace moe {
 
 namespace {
 
-constexpr int BM = 128;
+constexpr int BMH = 128;                           // rows of one half (one MMA)
 constexpr int BN = 256;
 constexpr int BK = 64;
-constexpr int STAGES = 4;
-constexpr int A_BYTES = BM * BK * 2;               // 16 KB
+constexpr int A_HALF_BYTES = BMH * BK * 2;         // 16 KB
 constexpr int B_BYTES = BN * BK * 2;               // 32 KB
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;     // 48 KB
-constexpr int kGatherThreads = 128;      // cp.async row-gather warps (FWD_GATEUP only)
-constexpr int kGatherDepth = 2;          // stages a gather thread keeps in flight before arriving
+constexpr int RING_BYTES = 192 * 1024;             // 3 x 64 KB or 4 x 48 KB
+constexpr int kEpiWarps = 8;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr int MN_CHUNK_BYTES = 64 * 128;           // one 64-wide MN chunk x 64 K rows
 
 enum Mode { FWD_GATEUP = 0, FWD_DOWN = 1, DGRAD_DOWN = 2, DGRAD_GATEUP = 3, WGRAD_DOWN = 4,
             WGRAD_GATEUP = 5, ROUTER = 6 };
 
-template <int MODE>
+// KH: 128-row halves per tile (1 or 2)
+template <int MODE, int KH>
 struct Traits {
+  static constexpr bool kGateUp = (MODE == FWD_GATEUP);
   static constexpr bool kAMN = (MODE == WGRAD_DOWN || MODE == WGRAD_GATEUP);
-  static constexpr bool kBMN = (MODE == FWD_GATEUP || MODE == FWD_DOWN || MODE == WGRAD_DOWN ||
+  static constexpr bool kBMN = (kGateUp || MODE == FWD_DOWN || MODE == WGRAD_DOWN ||
                                 MODE == WGRAD_GATEUP || MODE == ROUTER);
   static constexpr bool kKGrouped = (MODE == WGRAD_DOWN || MODE == WGRAD_GATEUP);
   static constexpr bool kRouter = (MODE == ROUTER);
-  // Epilogue warps: one warpgroup, or two splitting the columns where the
-  // epilogue itself is heavy (the SwiGLU backward of DGRAD_DOWN).
-  static constexpr int kEpiWarps = (MODE == DGRAD_DOWN) ? 8 : 4;
-  static constexpr int kHalves = kEpiWarps / 4;
-  // FWD_GATEUP has four more warps that gather token rows with cp.async
-  static constexpr int kGatherWarps = (MODE == FWD_GATEUP) ? 4 : 0;
-  // warp 0 TMA producer, warp 1 MMA issuer, then the epilogue and gather warps
-  static constexpr int kThreads = 32 * (2 + kEpiWarps + kGatherWarps);
+  // One half for the epilogues with per-element math (SwiGLU, its backward),
+  // which then overlap with the next tile's MMAs through two accumulators,
+  // and for the router (few, narrow tiles: its K is split instead); two for
+  // the wgrad GEMMs; either for the plain bf16-store GEMMs (the host picks).
+  static_assert(KH == 1 || KH == 2, "one or two halves");
+  static_assert(KH == 1 || (MODE != FWD_GATEUP && MODE != DGRAD_DOWN && MODE != ROUTER),
+                "per-element epilogues use one half");
+  static_assert(KH == 2 || (MODE != WGRAD_DOWN && MODE != WGRAD_GATEUP), "wgrad uses two halves");
+  static constexpr int kH = KH;
+  static constexpr int kBM = kH * BMH;
+  static constexpr int kAccBufs = 2 / kH;
+  static constexpr int kABytes = kH * A_HALF_BYTES;
+  static constexpr int kStageBytes = kABytes + B_BYTES;
+  static constexpr int kStages = RING_BYTES / kStageBytes;
+  // read the accumulators into registers (bf16), free them, then store
+  static constexpr bool kEarlyRelease = (kH == 2);
+  // warp 0 TMA producer, warp 1 MMA issuer, then the epilogue warps
+  static constexpr int kThreads = 32 * (2 + kEpiWarps);
 };
 
 struct GemmParams {   // 64-byte aligned through its CUtensorMap members
@@ -92,26 +110,23 @@ struct GemmParams {   // 64-byte aligned through its CUtensorMap members
   CUtensorMap tmB;
   const int32_t* offsets;   // [E+1] expert row offsets, or nullptr: one group of `rows`
   const int32_t* gidx;      // gather indices (src_row), or nullptr: identity
-  const uint16_t* a_ptr;    // A base pointer for the cp.async row gather (row stride K)
-  int a_cpasync;            // FWD_GATEUP with gidx: 1 = cp.async row gather, 0 = TMA tile::gather4
   const float* aux;         // fp32 gu_pre [R, 2I] read by DGRAD_DOWN
   const float* wrow;        // gate weight of each permuted row [R] (nullable)
   uint16_t* out;
   float* out_gu;            // FWD_GATEUP: fp32 pre-activations g | u [R, 2I] (nullable)
   uint16_t* out_hw;         // FWD_GATEUP: bf16(w_row * h) [R, I] (nullable, needs wrow)
-  float* out_part;          // DGRAD_DOWN: per (row, n tile, column half) partial of
-                            // <dY . Wd^T, h> [R, 2 nt]
-                            // ROUTER: fp32 partial logits [parts, rows, n_out]
+  float* out_part;          // DGRAD_DOWN: per (row, 128-column block) partial of <dY . Wd^T, h>
+                            // [R, 2 nt]; ROUTER: fp32 partial logits [parts, rows, n_out]
   uint32_t* status;
   uint64_t wait_limit_ns;
   int rows;                 // permuted rows R
   int E;
-  int K;                    // contraction length (M-grouped modes)
+  int K;                    // contraction length (M-grouped modes; per part for ROUTER)
   int I;
   int n_out;                // valid output columns
   int m_w;                  // output rows per expert (K-grouped modes)
   int nt;                   // n tiles
-  int mt_w;                 // m tiles per expert (K-grouped modes)
+  int mt_w;                 // m tiles per expert (K-grouped modes; per part for ROUTER)
   int64_t ldo;              // leading dimension of out
   int stall_producer;       // test hook: the producer issues no loads (a wait that runs out)
 };
@@ -127,16 +142,16 @@ __device__ __forceinline__ uint64_t umma_desc(uint32_t saddr, uint32_t lbo, uint
   return d;
 }
 
-template <int MODE>
+template <int MODE, int KH>
 __device__ __forceinline__ uint32_t make_idesc() {
-  using Tr = Traits<MODE>;
+  using Tr = Traits<MODE, KH>;
   return (1u << 4)                       // D: fp32
          | (1u << 7)                     // A: bf16
          | (1u << 10)                    // B: bf16
          | ((Tr::kAMN ? 1u : 0u) << 15)  // A major: 0 = K, 1 = MN
          | ((Tr::kBMN ? 1u : 0u) << 16)  // B major
          | ((uint32_t)(BN >> 3) << 17)   // N
-         | ((uint32_t)(BM >> 4) << 24);  // M
+         | ((uint32_t)(BMH >> 4) << 24); // M (one half)
 }
 
 struct Tile {
@@ -144,6 +159,7 @@ struct Tile {
   int row0;       // M-grouped: first permuted row; K-grouped: first K row of the expert
   int rows;       // M-grouped: valid rows in the tile; K-grouped: K extent of the expert
   int kblocks;
+  int halves;     // 128-row halves that carry valid output rows
 };
 
 __device__ __forceinline__ void group_range(const GemmParams& p, int e, int& start, int& count) {
@@ -156,19 +172,21 @@ __device__ __forceinline__ void group_range(const GemmParams& p, int e, int& sta
   }
 }
 
-template <int MODE>
+template <int MODE, int KH>
 __device__ __forceinline__ Tile decode_tile(const GemmParams& p, const int* prefix, int tile) {
+  using Tr = Traits<MODE, KH>;
   Tile t;
-  if (Traits<MODE>::kRouter) {   // e = K part; rows of x in order; K range [e*K, (e+1)*K)
+  if (Tr::kRouter) {   // e = K part; rows of x in order; K range [e*K, (e+1)*K)
     const int per = p.mt_w * p.nt;
     t.e = tile / per;
     const int local = tile - t.e * per;
     t.mt = local / p.nt;
     t.nt = local - t.mt * p.nt;
-    t.row0 = t.mt * BM;
-    t.rows = min(BM, p.rows - t.row0);
+    t.row0 = t.mt * Tr::kBM;
+    t.rows = min(Tr::kBM, p.rows - t.row0);
     t.kblocks = p.K / BK;
-  } else if (Traits<MODE>::kKGrouped) {
+    t.halves = t.rows > BMH ? 2 : 1;
+  } else if (Tr::kKGrouped) {
     const int per = p.mt_w * p.nt;
     t.e = tile / per;
     const int local = tile - t.e * per;
@@ -176,6 +194,7 @@ __device__ __forceinline__ Tile decode_tile(const GemmParams& p, const int* pref
     t.nt = local - t.mt * p.nt;
     group_range(p, t.e, t.row0, t.rows);
     t.kblocks = (t.rows + BK - 1) / BK;
+    t.halves = (Tr::kH == 2 && p.m_w - t.mt * Tr::kBM > BMH) ? 2 : 1;
   } else {
     int lo = 0, hi = p.E - 1;    // largest e with prefix[e] <= tile
     while (lo < hi) {
@@ -188,21 +207,20 @@ __device__ __forceinline__ Tile decode_tile(const GemmParams& p, const int* pref
     t.nt = local - t.mt * p.nt;
     int start, count;
     group_range(p, t.e, start, count);
-    t.row0 = start + t.mt * BM;
-    t.rows = min(BM, count - t.mt * BM);
+    t.row0 = start + t.mt * Tr::kBM;
+    t.rows = min(Tr::kBM, count - t.mt * Tr::kBM);
     t.kblocks = p.K / BK;
+    t.halves = (Tr::kH == 2 && t.rows > BMH) ? 2 : 1;
   }
   return t;
 }
 
-template <int MODE>
-__device__ __forceinline__ void store_zero_tile(const GemmParams& p, const Tile& t, int r, int half,
-                                                int halves) {
-  const int m = t.mt * BM + r;
+// Zero row m of an empty expert's weight-gradient tile (K-grouped modes).
+__device__ __forceinline__ void store_zero_rows(const GemmParams& p, const Tile& t, int m) {
   if (m >= p.m_w) return;
   uint16_t* orow = p.out + ((int64_t)t.e * p.m_w + m) * p.ldo + (int64_t)t.nt * BN;
   const uint4 z = make_uint4(0, 0, 0, 0);
-  for (int c = half * (BN / halves); c < (half + 1) * (BN / halves); c += 8)
+  for (int c = 0; c < BN; c += 8)
     if (t.nt * BN + c < p.n_out) *reinterpret_cast<uint4*>(orow + c) = z;
 }
 
@@ -210,6 +228,13 @@ __device__ __forceinline__ void store32(uint16_t* dst, const float* v) {
   uint4* d = reinterpret_cast<uint4*>(dst);
 #pragma unroll
   for (int q = 0; q < 4; ++q) d[q] = pack8(v + 8 * q);
+}
+
+// 32 bf16 already packed in pairs
+__device__ __forceinline__ void store32_packed(uint16_t* dst, const uint32_t* pk) {
+  uint4* d = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) d[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
 }
 
 __device__ __forceinline__ void store32_f32(float* dst, const float* v) {
@@ -227,16 +252,19 @@ __device__ __forceinline__ void load32_f32(const float* src, float* v) {
   }
 }
 
-template <int MODE>
-__global__ void __launch_bounds__(Traits<MODE>::kThreads, 1)
+__device__ __forceinline__ float swiglu(float g, float u) { return g / (1.0f + expf(-g)) * u; }
+
+template <int MODE, int KH>
+__global__ void __launch_bounds__(Traits<MODE, KH>::kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ GemmParams p) {
-  using Tr = Traits<MODE>;
+  using Tr = Traits<MODE, KH>;
+  constexpr int STAGES = Tr::kStages;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* ring = smem;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
-  // bars: full[STAGES], empty[STAGES], acc_full[2], acc_empty[2], drain
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + RING_BYTES);
+  // bars: full[STAGES], empty[STAGES], acc_full[2], acc_empty[2], drain (at most 13 of 16)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 16);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* prefix = reinterpret_cast<int*>(tmem_slot + 2);   // [E+1]
 
@@ -252,12 +280,12 @@ __global__ void __launch_bounds__(Traits<MODE>::kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(full_bar(s), 1 + (p.a_cpasync ? kGatherThreads : 0));
+      mbar_init(full_bar(s), 1);
       mbar_init(empty_bar(s), 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(accf_bar(b), 1);
-      mbar_init(acce_bar(b), 32 * Tr::kEpiWarps);
+      mbar_init(acce_bar(b), 32 * kEpiWarps);
     }
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
@@ -271,7 +299,9 @@ __global__ void __launch_bounds__(Traits<MODE>::kThreads, 1)
     tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
     tmem_relinquish();
   }
-  // Tile prefix over experts (M-grouped modes): prefix[e] = sum_{e'<e} ceil(M_e'/BM) * nt
+  // Tile prefix over experts (M-grouped modes): prefix[e] = sum_{e'<e} ceil(M_e'/BM) * nt.
+  // Tiles go out in expert order, so the row tiles of one expert run at about
+  // the same time and read its weights from L2 after the first of them.
   int total_tiles;
   if (Tr::kKGrouped || Tr::kRouter) {
     total_tiles = p.E * p.mt_w * p.nt;
@@ -284,7 +314,7 @@ __global__ void __launch_bounds__(Traits<MODE>::kThreads, 1)
         if (e < p.E) {
           int start, count;
           group_range(p, e, start, count);
-          v = ((count + BM - 1) / BM) * p.nt;
+          v = ((count + Tr::kBM - 1) / Tr::kBM) * p.nt;
         }
         int incl = v;
 #pragma unroll
@@ -306,38 +336,46 @@ __global__ void __launch_bounds__(Traits<MODE>::kThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------ TMA producer
+    // Gathered token rows are re-read by every expert a token was routed to,
+    // spread over the whole launch while the weights stream through L2: keep
+    // them resident.
+    const uint64_t keep_x = l2_policy_evict_last();
     int stage = 0;
     uint32_t phase = 0;
     uint32_t issued_mask = 0;       // stages that ever received a load
     uint32_t last_parity = 0;       // bit s: parity of the last load into stage s
     bool ok = true;
     for (int tile = blockIdx.x; tile < total_tiles && ok && !p.stall_producer; tile += gridDim.x) {
-      const Tile t = decode_tile<MODE>(p, prefix, tile);
+      const Tile t = decode_tile<MODE, KH>(p, prefix, tile);
       if (t.kblocks == 0) continue;
-      int gi[4] = {0, 0, 0, 0};
-      if (MODE == FWD_GATEUP && p.gidx && !p.a_cpasync) {   // this lane gathers rows 4*lane .. +3
+      int gi[Tr::kH][4];
+      if (Tr::kGateUp && p.gidx) {   // lane's rows: 4*lane .. +3 of each half
 #pragma unroll
-        for (int q = 0; q < 4; ++q) gi[q] = p.gidx[t.row0 + min(4 * lane + q, t.rows - 1)];
+        for (int h = 0; h < Tr::kH; ++h)
+#pragma unroll
+          for (int q = 0; q < 4; ++q) gi[h][q] = p.gidx[t.row0 + min(h * BMH + 4 * lane + q, t.rows - 1)];
       }
+      const uint32_t a_bytes = (uint32_t)(t.halves * A_HALF_BYTES);
       for (int kb = 0; kb < t.kblocks; ++kb) {
         bool w = true;
         if (lane == 0)
           w = mbar_wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, p.wait_limit_ns, p.status, 1);
         ok = __shfl_sync(0xffffffffu, w ? 1 : 0, 0) != 0;
         if (!ok) break;
-        const uint32_t sA = ring_u32 + stage * STAGE_BYTES;
-        const uint32_t sB = sA + A_BYTES;
+        const uint32_t sA = ring_u32 + stage * Tr::kStageBytes;
+        const uint32_t sB = sA + Tr::kABytes;
         const uint32_t fb = full_bar(stage);
-        if (lane == 0) mbar_arrive_expect_tx(fb, p.a_cpasync ? B_BYTES : STAGE_BYTES);
+        if (lane == 0) mbar_arrive_expect_tx(fb, a_bytes + (uint32_t)B_BYTES);
         __syncwarp();
         const int k0 = kb * BK;
-        if (MODE == FWD_GATEUP) {
-          if (p.a_cpasync) {
-            // A rows come from the gather warps
-          } else if (p.gidx) {                             // permute fused into the load (TMA)
-            tma_gather4(sA + 4 * lane * 128, &p.tmA, k0, gi[0], gi[1], gi[2], gi[3], fb);
+        if (Tr::kGateUp) {
+          if (p.gidx) {                                    // permute fused into the load (TMA)
+            for (int h = 0; h < t.halves; ++h)
+              tma_gather4_hint(sA + h * A_HALF_BYTES + 4 * lane * 128, &p.tmA, k0, gi[h][0], gi[h][1],
+                               gi[h][2], gi[h][3], fb, keep_x);
           } else if (lane == 0) {                          // rows already in permuted order
-            tma_load_2d(sA, &p.tmA, k0, t.row0, fb);
+            for (int h = 0; h < t.halves; ++h)
+              tma_load_2d(sA + h * A_HALF_BYTES, &p.tmA, k0, t.row0 + h * BMH, fb);
           }
           if (lane == 0) {
             const int brow = t.e * p.K + k0;               // gate_up rows of expert e
@@ -350,14 +388,16 @@ __global__ void __launch_bounds__(Traits<MODE>::kThreads, 1)
         } else if (MODE == ROUTER) {
           if (lane == 0) {
             const int kg = t.e * p.K + k0;                 // row of the stacked [W0; W1; W2]
-            tma_load_2d(sA, &p.tmA, kg % p.I, t.row0, fb); // x repeats along the stacked K
+            for (int h = 0; h < t.halves; ++h)             // x repeats along the stacked K
+              tma_load_2d(sA + h * A_HALF_BYTES, &p.tmA, kg % p.I, t.row0 + h * BMH, fb);
             const int n0 = t.nt * BN;
 #pragma unroll
             for (int c = 0; c < 4; ++c) tma_load_2d(sB + c * MN_CHUNK_BYTES, &p.tmB, n0 + 64 * c, kg, fb);
           }
         } else if (MODE == FWD_DOWN) {
           if (lane == 0) {
-            tma_load_2d(sA, &p.tmA, k0, t.row0, fb);
+            for (int h = 0; h < t.halves; ++h)
+              tma_load_2d(sA + h * A_HALF_BYTES, &p.tmA, k0, t.row0 + h * BMH, fb);
             const int brow = t.e * p.K + k0;               // down rows of expert e
             const int n0 = t.nt * BN;
 #pragma unroll
@@ -365,39 +405,38 @@ __global__ void __launch_bounds__(Traits<MODE>::kThreads, 1)
           }
         } else if (MODE == DGRAD_DOWN || MODE == DGRAD_GATEUP) {
           if (lane == 0) {
-            tma_load_2d(sA, &p.tmA, k0, t.row0, fb);
-            // B^T rows: expert e's block of n_rows_per_expert rows, K-major
+            for (int h = 0; h < t.halves; ++h)
+              tma_load_2d(sA + h * A_HALF_BYTES, &p.tmA, k0, t.row0 + h * BMH, fb);
+            // B^T rows: expert e's block of rows_per_e rows, K-major
             const int rows_per_e = (MODE == DGRAD_DOWN) ? p.I : p.n_out;
             tma_load_2d(sB, &p.tmB, k0, t.e * rows_per_e + t.nt * BN, fb);
           }
-        } else if (MODE == WGRAD_DOWN) {
-          if (lane == 0) {
-            const int krow = t.row0 + k0;
-            const int m0 = t.mt * BM;
-            tma_load_2d(sA + 0 * MN_CHUNK_BYTES, &p.tmA, m0, krow, fb);
-            tma_load_2d(sA + 1 * MN_CHUNK_BYTES, &p.tmA, m0 + 64, krow, fb);
-            const int n0 = t.nt * BN;
+        } else {  // WGRAD_*: A = rows of the expert (K = tokens), MN-major chunks of 64 m
+          const int krow = t.row0 + k0;
+          const int m0 = t.mt * Tr::kBM;
+          if (MODE == WGRAD_GATEUP && p.gidx) {            // gathered through src_row
+            // lane: MN chunk c = lane >> 3, K rows 8*(lane & 7) .. +7 (two gather4)
+            const int c = lane >> 3;
+            if (c < 2 * t.halves) {
 #pragma unroll
-            for (int c = 0; c < 4; ++c) tma_load_2d(sB + c * MN_CHUNK_BYTES, &p.tmB, n0 + 64 * c, krow, fb);
-          }
-        } else {  // WGRAD_GATEUP: A = x rows of the expert (K = tokens), MN-major
-          if (p.gidx) {                       // gathered through src_row
-            const int c = lane >> 4;          // MN chunk 0/1
-            const int g = lane & 15;          // k rows 4g .. 4g+3
-            int r4[4];
+              for (int q2 = 0; q2 < 2; ++q2) {
+                const int kr0 = 8 * (lane & 7) + 4 * q2;
+                int r4[4];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) r4[q] = p.gidx[t.row0 + min(k0 + 4 * g + q, t.rows - 1)];
-            tma_gather4(sA + c * MN_CHUNK_BYTES + 4 * g * 128, &p.tmA, t.mt * BM + 64 * c, r4[0], r4[1],
-                        r4[2], r4[3], fb);
-          } else if (lane == 0) {             // rows already in permuted order
-            tma_load_2d(sA + 0 * MN_CHUNK_BYTES, &p.tmA, t.mt * BM, t.row0 + k0, fb);
-            tma_load_2d(sA + 1 * MN_CHUNK_BYTES, &p.tmA, t.mt * BM + 64, t.row0 + k0, fb);
+                for (int q = 0; q < 4; ++q) r4[q] = p.gidx[t.row0 + min(k0 + kr0 + q, t.rows - 1)];
+                tma_gather4_hint(sA + c * MN_CHUNK_BYTES + kr0 * 128, &p.tmA, m0 + 64 * c, r4[0], r4[1],
+                                 r4[2], r4[3], fb, keep_x);
+              }
+            }
+          } else if (lane == 0) {                          // rows already in permuted order
+            for (int c = 0; c < 2 * t.halves; ++c)
+              tma_load_2d(sA + c * MN_CHUNK_BYTES, &p.tmA, m0 + 64 * c, krow, fb);
           }
           if (lane == 0) {
             const int n0 = t.nt * BN;
 #pragma unroll
-            for (int cc = 0; cc < 4; ++cc)
-              tma_load_2d(sB + cc * MN_CHUNK_BYTES, &p.tmB, n0 + 64 * cc, t.row0 + k0, fb);
+            for (int c = 0; c < 4; ++c)
+              tma_load_2d(sB + c * MN_CHUNK_BYTES, &p.tmB, n0 + 64 * c, krow, fb);
           }
         }
         issued_mask |= 1u << stage;
@@ -420,36 +459,36 @@ __global__ void __launch_bounds__(Traits<MODE>::kThreads, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------- MMA issuer
-    const uint32_t idesc = make_idesc<MODE>();
+    const uint32_t idesc = make_idesc<MODE, KH>();
     int stage = 0;
     uint32_t phase = 0;
-    int buf = 0;
+    int acc = 0;                 // accumulator buffer (always 0 with two halves)
     uint32_t acc_phase = 0;
     bool ok = true;
     bool issued_any = false;
     for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x) {
-      const Tile t = decode_tile<MODE>(p, prefix, tile);
+      const Tile t = decode_tile<MODE, KH>(p, prefix, tile);
       if (t.kblocks == 0) continue;
       bool w = true;
-      if (lane == 0)
-        w = mbar_wait_bounded(acce_bar(buf), acc_phase ^ 1u, abort_flag, p.wait_limit_ns, p.status, 2);
+      if (lane == 0)    // the epilogue has drained this accumulator buffer
+        w = mbar_wait_bounded(acce_bar(acc), acc_phase ^ 1u, abort_flag, p.wait_limit_ns, p.status, 2);
       ok = __shfl_sync(0xffffffffu, w ? 1 : 0, 0) != 0;
       if (!ok) break;
       tc_fence_after();
-      const uint32_t d_tmem = tmem_base + (uint32_t)(buf * BN);
       for (int kb = 0; kb < t.kblocks; ++kb) {
         if (lane == 0)
           w = mbar_wait_bounded(full_bar(stage), phase, abort_flag, p.wait_limit_ns, p.status, 3);
         ok = __shfl_sync(0xffffffffu, w ? 1 : 0, 0) != 0;
         if (!ok) break;
-        const uint32_t sA = ring_u32 + stage * STAGE_BYTES;
-        const uint32_t sB = sA + A_BYTES;
+        const uint32_t sA = ring_u32 + stage * Tr::kStageBytes;
+        const uint32_t sB = sA + Tr::kABytes;
         if (Tr::kKGrouped) {
           const int kvalid = t.rows - kb * BK;
-          if (kvalid < BK) {   // zero the K rows past the expert's last row (A: 2 chunks, B: 4)
-            uint8_t* gA = ring + stage * STAGE_BYTES;
+          if (kvalid < BK) {   // zero the K rows past the expert's last row (A then B chunks)
+            constexpr int kChunks = (Tr::kABytes + B_BYTES) / MN_CHUNK_BYTES;
+            uint8_t* gA = ring + stage * Tr::kStageBytes;
             const int nrow = BK - kvalid;
-            for (int q = lane; q < nrow * 8 * 6; q += 32) {
+            for (int q = lane; q < nrow * 8 * kChunks; q += 32) {
               const int chunk = q / (nrow * 8);
               const int rem = q - chunk * nrow * 8;
               const int row = kvalid + rem / 8;
@@ -465,11 +504,15 @@ __global__ void __launch_bounds__(Traits<MODE>::kThreads, 1)
         if (lane == 0) {
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk) {
-            const uint64_t ad = Tr::kAMN ? umma_desc(sA + kk * 2048, MN_CHUNK_BYTES, 1024)
-                                         : umma_desc(sA + kk * 32, 16, 1024);
             const uint64_t bd = Tr::kBMN ? umma_desc(sB + kk * 2048, MN_CHUNK_BYTES, 1024)
                                          : umma_desc(sB + kk * 32, 16, 1024);
-            tc_mma_bf16(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+            for (int h = 0; h < t.halves; ++h) {
+              const uint32_t aBase = sA + h * A_HALF_BYTES;
+              const uint64_t ad = Tr::kAMN ? umma_desc(aBase + kk * 2048, MN_CHUNK_BYTES, 1024)
+                                           : umma_desc(aBase + kk * 32, 16, 1024);
+              tc_mma_bf16(tmem_base + (uint32_t)((acc + h) * BN), ad, bd, idesc,
+                          (kb | kk) != 0 ? 1u : 0u);
+            }
           }
           tc_commit(empty_bar(stage));
         }
@@ -481,10 +524,12 @@ __global__ void __launch_bounds__(Traits<MODE>::kThreads, 1)
         }
       }
       if (!ok) break;
-      if (lane == 0) tc_commit(accf_bar(buf));
+      if (lane == 0) tc_commit(accf_bar(acc));
       __syncwarp();
-      buf ^= 1;
-      if (buf == 0) acc_phase ^= 1u;
+      if (++acc == Tr::kAccBufs) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
     }
     if (!ok && issued_any && lane == 0) {
       // stopped early: make sure every MMA issued has finished before TMEM is freed
@@ -493,35 +538,79 @@ __global__ void __launch_bounds__(Traits<MODE>::kThreads, 1)
       while (!mbar_try_wait(drain_bar, 0) && globaltimer_ns() - t0 < p.wait_limit_ns) {
       }
     }
-  } else if (warp < 2 + Tr::kEpiWarps) {
+  } else {
     // ---------------------------------------------------------- epilogue
-    // Each warp reads the TMEM lane quarter its rank allows (warp % 4); with
-    // two warpgroups each takes one half of the tile's columns.
-    const int quarter = warp & 3;            // TMEM lanes 32*quarter .. +31
-    const int half = (warp - 2) >> 2;        // column part of this warpgroup
-    constexpr int kH = Tr::kHalves;
-    const int r = quarter * 32 + lane;       // accumulator row of this thread
-    int buf = 0;
+    // Each warp reads the TMEM lane quarter its rank allows (warp % 4).  With
+    // two halves warpgroup wg drains half wg (all 256 columns); with one,
+    // warpgroup wg takes columns [128 wg, 128 wg + 128) of the single half.
+    const int quarter = warp & 3;                     // TMEM lanes 32*quarter .. +31
+    const int wg = (warp - 2) >> 2;
+    const int half = Tr::kH == 2 ? wg : 0;
+    const int r = half * BMH + quarter * 32 + lane;   // tile row of this thread
+    int acc = 0;
     uint32_t acc_phase = 0;
     for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
-      const Tile t = decode_tile<MODE>(p, prefix, tile);
+      const Tile t = decode_tile<MODE, KH>(p, prefix, tile);
       if (t.kblocks == 0) {
-        if (Tr::kKGrouped) store_zero_tile<MODE>(p, t, r, half, kH);
+        if (Tr::kKGrouped) store_zero_rows(p, t, t.mt * Tr::kBM + r);
         continue;
       }
       bool w = true;
       if (lane == 0)
-        w = mbar_wait_bounded(accf_bar(buf), acc_phase, abort_flag, p.wait_limit_ns, p.status, 4);
+        w = mbar_wait_bounded(accf_bar(acc), acc_phase, abort_flag, p.wait_limit_ns, p.status, 4);
       if (__shfl_sync(0xffffffffu, w ? 1 : 0, 0) == 0) break;
       tc_fence_after();
-      const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)(buf * BN);
+      const bool active = half < t.halves;     // warp-uniform
+      const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)((acc + half) * BN);
+      const uint32_t done = acce_bar(acc);
+      if (++acc == Tr::kAccBufs) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
       float v[32];
-      if (MODE == FWD_GATEUP) {
+      if (Tr::kEarlyRelease) {
+        // read the whole row into registers as bf16 (16 columns at a time:
+        // the packed row already takes 128 registers), free the accumulator,
+        // then store while the next tile's MMAs run
+        uint32_t pk[BN / 2];
+        if (active) {
+#pragma unroll
+          for (int c = 0; c < 16; ++c) {
+            tmem_ld16(taddr + 16 * c, v);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) pk[8 * c + q] = pack_bf16x2(v[2 * q], v[2 * q + 1]);
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(done);
+        if (active) {
+          uint16_t* orow;
+          bool row_ok;
+          const int n0 = t.nt * BN;
+          if (Tr::kKGrouped) {   // rows m = mt*BM + r of expert e's weight-gradient block
+            const int m = t.mt * Tr::kBM + r;
+            row_ok = m < p.m_w;
+            orow = p.out + ((int64_t)t.e * p.m_w + m) * p.ldo;
+          } else {
+            row_ok = r < t.rows;
+            orow = p.out + (int64_t)(t.row0 + r) * p.ldo;
+          }
+          if (row_ok) {
+#pragma unroll
+            for (int c = 0; c < BN / 32; ++c)
+              if (n0 + 32 * c < p.n_out) store32_packed(orow + n0 + 32 * c, pk + 16 * c);
+          }
+        }
+        continue;
+      }
+      if (!active) {
+        // this half carries no rows of the tile: nothing to read or store
+      } else if (MODE == FWD_GATEUP) {
         const bool row_ok = r < t.rows;
         const int64_t row = t.row0 + r;
         const int n0 = t.nt * 128;
 #pragma unroll 1
-        for (int c0 = half * (128 / kH); c0 < (half + 1) * (128 / kH); c0 += 32) {
+        for (int c0 = 64 * wg; c0 < 64 * wg + 64; c0 += 32) {
           if (n0 + c0 >= p.n_out) break;                 // warp-uniform
           float u[32];
           tmem_ld32(taddr + c0, v);                      // gate columns
@@ -532,7 +621,7 @@ __global__ void __launch_bounds__(Traits<MODE>::kThreads, 1)
               store32_f32(p.out_gu + row * 2 * p.I + p.I + n0 + c0, u);
             }
 #pragma unroll
-            for (int q = 0; q < 32; ++q) v[q] = v[q] / (1.0f + expf(-v[q])) * u[q];
+            for (int q = 0; q < 32; ++q) v[q] = swiglu(v[q], u[q]);
             store32(p.out + row * p.ldo + n0 + c0, v);
             if (p.out_hw) {
               const float wr = p.wrow[row];
@@ -547,7 +636,7 @@ __global__ void __launch_bounds__(Traits<MODE>::kThreads, 1)
         float* orow = p.out_part + ((int64_t)t.e * p.rows + t.row0 + r) * p.ldo;
         const int n0 = t.nt * BN;
 #pragma unroll 1
-        for (int c0 = half * (BN / kH); c0 < (half + 1) * (BN / kH); c0 += 32) {
+        for (int c0 = 128 * wg; c0 < 128 * wg + 128; c0 += 32) {
           if (n0 + c0 >= p.n_out) break;
           tmem_ld32(taddr + c0, v);
           if (row_ok) {
@@ -560,12 +649,12 @@ __global__ void __launch_bounds__(Traits<MODE>::kThreads, 1)
             }
           }
         }
-      } else if (MODE == FWD_DOWN || MODE == DGRAD_GATEUP) {
+      } else if (MODE == FWD_DOWN || MODE == DGRAD_GATEUP) {   // one half: column half wg
         const bool row_ok = r < t.rows;
         const int64_t row = t.row0 + r;
         const int n0 = t.nt * BN;
 #pragma unroll 1
-        for (int c0 = half * (BN / kH); c0 < (half + 1) * (BN / kH); c0 += 32) {
+        for (int c0 = 128 * wg; c0 < 128 * wg + 128; c0 += 32) {
           if (n0 + c0 >= p.n_out) break;
           tmem_ld32(taddr + c0, v);
           if (row_ok) store32(p.out + row * p.ldo + n0 + c0, v);
@@ -574,9 +663,9 @@ __global__ void __launch_bounds__(Traits<MODE>::kThreads, 1)
         const bool row_ok = r < t.rows;
         const int64_t row = t.row0 + r;
         const int n0 = t.nt * BN;
-        float dot = 0.f;                                 // <dY . Wd^T, h> over this tile's columns
+        float dot = 0.f;                                 // <dY . Wd^T, h> over this thread's columns
 #pragma unroll 1
-        for (int c0 = half * (BN / kH); c0 < (half + 1) * (BN / kH); c0 += 32) {
+        for (int c0 = 128 * wg; c0 < 128 * wg + 128; c0 += 32) {
           if (n0 + c0 >= p.n_out) break;
           tmem_ld32(taddr + c0, v);                      // dY . Wd^T (fp32)
           if (row_ok) {
@@ -598,70 +687,10 @@ __global__ void __launch_bounds__(Traits<MODE>::kThreads, 1)
             store32(p.out + row * 2 * p.I + p.I + n0 + c0, u);
           }
         }
-        if (row_ok && p.out_part) p.out_part[row * 2 * p.nt + 2 * t.nt + half] = dot;
-      } else {  // WGRAD_*: output rows m = mt*BM + r of expert e's weight-gradient block
-        const int m = t.mt * BM + r;
-        const bool row_ok = m < p.m_w;
-        uint16_t* orow = p.out + ((int64_t)t.e * p.m_w + m) * p.ldo;
-        const int n0 = t.nt * BN;
-#pragma unroll 1
-        for (int c0 = half * (BN / kH); c0 < (half + 1) * (BN / kH); c0 += 32) {
-          if (n0 + c0 >= p.n_out) break;
-          tmem_ld32(taddr + c0, v);
-          if (row_ok) store32(orow + n0 + c0, v);
-        }
+        if (row_ok && p.out_part) p.out_part[row * 2 * p.nt + 2 * t.nt + wg] = dot;
       }
       tc_fence_before();
-      mbar_arrive(acce_bar(buf));
-      buf ^= 1;
-      if (buf == 0) acc_phase ^= 1u;
-    }
-  } else if (Tr::kGatherWarps > 0 && p.a_cpasync) {
-    // ------------------------------------------- cp.async row gather of A
-    // Thread g owns tile row g: per 64-wide K block it copies the row's 128
-    // bytes of x[src_row[row0 + g]] into the stage, 16 bytes at a time, to
-    // the 128-byte-swizzled place the tensor core expects (16-byte chunk c of
-    // row g at chunk c ^ (g % 8)).  It keeps kGatherDepth stages in flight;
-    // once a stage's copies completed it fences them to the async proxy and
-    // arrives on that stage's full barrier.
-    const int g = threadIdx.x - 32 * (2 + Tr::kEpiWarps);
-    int stage = 0, oldest = 0, pend = 0;
-    uint32_t phase = 0;
-    bool ok = true;
-    for (int tile = blockIdx.x; tile < total_tiles && ok && !p.stall_producer; tile += gridDim.x) {
-      const Tile t = decode_tile<MODE>(p, prefix, tile);
-      if (t.kblocks == 0) continue;
-      const uint16_t* xrow = p.a_ptr + (int64_t)p.gidx[t.row0 + min(g, t.rows - 1)] * p.K;
-      const uint32_t sw = (uint32_t)(g & 7);
-      for (int kb = 0; kb < t.kblocks; ++kb) {
-        bool w = true;
-        if (lane == 0)
-          w = mbar_wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, p.wait_limit_ns, p.status, 5);
-        ok = __shfl_sync(0xffffffffu, w ? 1 : 0, 0) != 0;
-        if (!ok) break;
-        const uint32_t dst = ring_u32 + stage * STAGE_BYTES + g * 128;
-        const uint16_t* src = xrow + kb * BK;
-#pragma unroll
-        for (uint32_t c = 0; c < 8; ++c) cp_async_16(dst + ((c ^ sw) << 4), src + c * 8);
-        cp_async_commit();
-        if (++pend > kGatherDepth) {
-          cp_async_wait_group<kGatherDepth>();
-          fence_proxy_async_smem();
-          mbar_arrive(full_bar(oldest));
-          oldest = (oldest + 1 == STAGES) ? 0 : oldest + 1;
-          --pend;
-        }
-        if (++stage == STAGES) {
-          stage = 0;
-          phase ^= 1u;
-        }
-      }
-    }
-    cp_async_wait_group<0>();
-    fence_proxy_async_smem();
-    for (; pend > 0 && ok; --pend) {
-      mbar_arrive(full_bar(oldest));
-      oldest = (oldest + 1 == STAGES) ? 0 : oldest + 1;
+      mbar_arrive(done);
     }
   }
 
@@ -673,17 +702,15 @@ __global__ void __launch_bounds__(Traits<MODE>::kThreads, 1)
   }
 }
 
-size_t gemm_smem_bytes(int E) {
-  return 1024 + (size_t)STAGES * STAGE_BYTES + 8 * (2 * STAGES + 5) + 16 + 4 * (size_t)(E + 1) + 64;
-}
+size_t gemm_smem_bytes(int E) { return 1024 + (size_t)RING_BYTES + 8 * 16 + 16 + 4 * (size_t)(E + 1) + 64; }
 
-template <int MODE>
+template <int MODE, int KH>
 cudaError_t run_gemm(const GemmParams& p, int64_t tiles_upper_bound, const DeviceInfo& dev,
                      cudaStream_t stream) {
   const size_t smem = gemm_smem_bytes(p.E);
   static int configured[kMaxDevices] = {0};
   if (!configured[dev.ordinal]) {
-    cudaError_t err = cudaFuncSetAttribute(grouped_gemm_kernel<MODE>,
+    cudaError_t err = cudaFuncSetAttribute(grouped_gemm_kernel<MODE, KH>,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            (int)gemm_smem_bytes(kMaxExperts));
     if (err != cudaSuccess) return err;
@@ -691,7 +718,7 @@ cudaError_t run_gemm(const GemmParams& p, int64_t tiles_upper_bound, const Devic
   }
   int64_t grid = tiles_upper_bound < dev.num_sms ? tiles_upper_bound : dev.num_sms;
   if (grid < 1) grid = 1;
-  grouped_gemm_kernel<MODE><<<(unsigned)grid, Traits<MODE>::kThreads, smem, stream>>>(p);
+  grouped_gemm_kernel<MODE, KH><<<(unsigned)grid, Traits<MODE, KH>::kThreads, smem, stream>>>(p);
   return cudaGetLastError();
 }
 
@@ -709,8 +736,6 @@ void fill_common(GemmParams& p, const int32_t* offsets, int64_t R, int64_t E, in
                  const DeviceInfo& dev) {
   p.offsets = offsets;
   p.gidx = nullptr;
-  p.a_ptr = nullptr;
-  p.a_cpasync = 0;
   p.aux = nullptr;
   p.wrow = nullptr;
   p.out = nullptr;
@@ -731,40 +756,32 @@ void fill_common(GemmParams& p, const int32_t* offsets, int64_t R, int64_t E, in
   p.ldo = 0;
 }
 
-int64_t mgrouped_tile_bound(int64_t R, int64_t E, int nt) { return ((R + BM - 1) / BM + E) * nt; }
+template <int MODE, int KH>
+int64_t mgrouped_tile_bound(int64_t R, int64_t E, int nt) {
+  constexpr int bm = Traits<MODE, KH>::kBM;
+  return ((R + bm - 1) / bm + E) * nt;
+}
+
+// The M-grouped GEMMs with a plain bf16 epilogue take 256-row tiles once
+// experts average 512 rows or more, else 128-row tiles: with few row tiles
+// per expert, tiles of one and two halves mixed in a static round-robin
+// leave some SMs with twice the work of others (measured on the Qwen3-MoE
+// shape: 256 rows per expert favour 128-row tiles, 512 favour 256-row).
+template <int MODE>
+cudaError_t run_bf16_mgrouped(const GemmParams& p, int64_t R, int64_t E, const DeviceInfo& dev,
+                              cudaStream_t stream) {
+  if (R >= 512 * E) return run_gemm<MODE, 2>(p, mgrouped_tile_bound<MODE, 2>(R, E, p.nt), dev, stream);
+  return run_gemm<MODE, 1>(p, mgrouped_tile_bound<MODE, 1>(R, E, p.nt), dev, stream);
+}
 
 }  // namespace
 
-int launch_gemm_gate_up(const uint16_t* x, const int32_t* src_row, const int32_t* offsets,
-                        const uint16_t* gate_up, int64_t T, int64_t R, int64_t H, int64_t E,
-                        int64_t I, uint16_t* h, const float* w_perm, float* gu_pre, uint16_t* h_w,
-                        const DeviceInfo& dev, cudaStream_t stream) {
-  if (R == 0) return 0;
-  GemmParams p;
-  fill_common(p, offsets, R, E, I, dev);
-  // gathered rows: one-row boxes for tile::gather4 (unused by the cp.async
-  // gather); rows in order: 128-row tiles
-  const bool ok_a = src_row ? make_map(&p.tmA, x, T, H, 64, 1) : make_map(&p.tmA, x, R, H, 64, 128);
-  if (!ok_a || !make_map(&p.tmB, gate_up, E * H, 2 * I, 64, 64)) return -1;
-  p.gidx = src_row;
-  p.a_ptr = x;
-  p.a_cpasync = (src_row && dev.gather_mode == 0) ? 1 : 0;
-  p.out = h;
-  p.wrow = w_perm;
-  p.out_gu = gu_pre;
-  p.out_hw = h_w;
-  p.K = (int)H;
-  p.n_out = (int)I;
-  p.nt = (int)((I + 127) / 128);
-  p.ldo = I;
-  return run_gemm<FWD_GATEUP>(p, mgrouped_tile_bound(R, E, p.nt), dev, stream) == cudaSuccess ? 0 : 1;
-}
-
 // K split of the router GEMM: the smallest divisor of its 64-wide K blocks
-// giving at least 228 tiles (1.5 waves on the 152 SMs of a GB300); fixed by
-// the shape alone so that workspace sizes do not depend on the device.
+// giving at least 228 tiles (1.5 per SM of a GB300); fixed by the shape
+// alone so that workspace sizes do not depend on the device.
 int router_parts(int64_t T, int64_t H, int64_t E) {
-  const int64_t tiles = ((T + BM - 1) / BM) * ((E + BN - 1) / BN);
+  constexpr int bm = Traits<ROUTER, 1>::kBM;
+  const int64_t tiles = ((T + bm - 1) / bm) * ((E + BN - 1) / BN);
   const int64_t kb = 3 * H / BK;          // 64-wide K blocks of the stacked split weight
   int parts = 1;
   for (int cand = 1; cand <= 48; ++cand) {
@@ -780,14 +797,37 @@ int launch_router_logits(const uint16_t* x, const uint16_t* w_split, int64_t T, 
   if (T == 0) return 0;
   GemmParams p;
   fill_common(p, nullptr, T, parts, H, dev);
-  if (!make_map(&p.tmA, x, T, H, 64, 128) || !make_map(&p.tmB, w_split, 3 * H, E, 64, 64)) return -1;
+  if (!make_map(&p.tmA, x, T, H, 64, BMH) || !make_map(&p.tmB, w_split, 3 * H, E, 64, 64)) return -1;
   p.out_part = part_out;
   p.K = (int)(3 * H / parts);   // K extent of one part
   p.n_out = (int)E;
-  p.mt_w = (int)((T + BM - 1) / BM);
+  p.mt_w = (int)((T + BMH - 1) / BMH);
   p.nt = (int)((E + BN - 1) / BN);
   p.ldo = E;
-  return run_gemm<ROUTER>(p, (int64_t)parts * p.mt_w * p.nt, dev, stream) == cudaSuccess ? 0 : 1;
+  return run_gemm<ROUTER, 1>(p, (int64_t)parts * p.mt_w * p.nt, dev, stream) == cudaSuccess ? 0 : 1;
+}
+
+int launch_gemm_gate_up(const uint16_t* x, const int32_t* src_row, const int32_t* offsets,
+                        const uint16_t* gate_up, int64_t T, int64_t R, int64_t H, int64_t E,
+                        int64_t I, uint16_t* h, const float* w_perm, float* gu_pre, uint16_t* h_w,
+                        const DeviceInfo& dev, cudaStream_t stream) {
+  if (R == 0) return 0;
+  GemmParams p;
+  fill_common(p, offsets, R, E, I, dev);
+  // gathered rows: one-row boxes for tile::gather4; rows in order: 128-row
+  // boxes, one per half
+  const bool ok_a = src_row ? make_map(&p.tmA, x, T, H, 64, 1) : make_map(&p.tmA, x, R, H, 64, BMH);
+  if (!ok_a || !make_map(&p.tmB, gate_up, E * H, 2 * I, 64, 64)) return -1;
+  p.gidx = src_row;
+  p.out = h;
+  p.wrow = w_perm;
+  p.out_gu = gu_pre;
+  p.out_hw = h_w;
+  p.K = (int)H;
+  p.n_out = (int)I;
+  p.nt = (int)((I + 127) / 128);
+  p.ldo = I;
+  return run_gemm<FWD_GATEUP, 1>(p, mgrouped_tile_bound<FWD_GATEUP, 1>(R, E, p.nt), dev, stream) == cudaSuccess ? 0 : 1;
 }
 
 int launch_gemm_down(const uint16_t* h, const int32_t* offsets, const uint16_t* down, int64_t R,
@@ -796,16 +836,16 @@ int launch_gemm_down(const uint16_t* h, const int32_t* offsets, const uint16_t* 
   if (R == 0) return 0;
   GemmParams p;
   fill_common(p, offsets, R, E, I, dev);
-  if (!make_map(&p.tmA, h, R, I, 64, 128) || !make_map(&p.tmB, down, E * I, H, 64, 64)) return -1;
+  if (!make_map(&p.tmA, h, R, I, 64, BMH) || !make_map(&p.tmB, down, E * I, H, 64, 64)) return -1;
   p.out = y_perm;
   p.K = (int)I;
   p.n_out = (int)H;
   p.nt = (int)((H + BN - 1) / BN);
   p.ldo = H;
-  return run_gemm<FWD_DOWN>(p, mgrouped_tile_bound(R, E, p.nt), dev, stream) == cudaSuccess ? 0 : 1;
+  return run_bf16_mgrouped<FWD_DOWN>(p, R, E, dev, stream) == cudaSuccess ? 0 : 1;
 }
 
-int down_bwd_parts(int64_t I) { return 2 * (int)((I + BN - 1) / BN); }   // two column halves per tile
+int down_bwd_parts(int64_t I) { return 2 * (int)((I + BN - 1) / BN); }   // one per 128 columns
 
 int launch_gemm_down_bwd(const uint16_t* dy_perm, const uint16_t* h_w, const float* gu_pre,
                          const float* w_perm, const int32_t* offsets, const uint16_t* down, int64_t R,
@@ -814,7 +854,7 @@ int launch_gemm_down_bwd(const uint16_t* dy_perm, const uint16_t* h_w, const flo
   if (R > 0) {  // dgu = SwiGLU'(w * (dy_perm . Wd_e^T), gu_pre)
     GemmParams p;
     fill_common(p, offsets, R, E, I, dev);
-    if (!make_map(&p.tmA, dy_perm, R, H, 64, 128) || !make_map(&p.tmB, down, E * I, H, 64, 256))
+    if (!make_map(&p.tmA, dy_perm, R, H, 64, BMH) || !make_map(&p.tmB, down, E * I, H, 64, 256))
       return -1;
     p.aux = gu_pre;
     p.wrow = w_perm;
@@ -824,7 +864,7 @@ int launch_gemm_down_bwd(const uint16_t* dy_perm, const uint16_t* h_w, const flo
     p.n_out = (int)I;
     p.nt = (int)((I + BN - 1) / BN);
     p.ldo = 2 * I;
-    if (run_gemm<DGRAD_DOWN>(p, mgrouped_tile_bound(R, E, p.nt), dev, stream) != cudaSuccess) return 1;
+    if (run_gemm<DGRAD_DOWN, 1>(p, mgrouped_tile_bound<DGRAD_DOWN, 1>(R, E, p.nt), dev, stream) != cudaSuccess) return 1;
   }
   {  // d_down_e = (w h)_e^T . dy_perm_e
     GemmParams p;
@@ -835,10 +875,10 @@ int launch_gemm_down_bwd(const uint16_t* dy_perm, const uint16_t* h_w, const flo
     p.out = d_down;
     p.m_w = (int)I;
     p.n_out = (int)H;
-    p.mt_w = (int)((I + BM - 1) / BM);
+    p.mt_w = (int)((I + 2 * BMH - 1) / (2 * BMH));
     p.nt = (int)((H + BN - 1) / BN);
     p.ldo = H;
-    if (run_gemm<WGRAD_DOWN>(p, E * p.mt_w * p.nt, dev, stream) != cudaSuccess) return 1;
+    if (run_gemm<WGRAD_DOWN, 2>(p, E * p.mt_w * p.nt, dev, stream) != cudaSuccess) return 1;
   }
   return 0;
 }
@@ -850,14 +890,14 @@ int launch_gemm_gate_up_bwd(const uint16_t* dgu, const uint16_t* x, const int32_
   if (R > 0) {  // dx_perm = dgu . Wgu_e^T
     GemmParams p;
     fill_common(p, offsets, R, E, I, dev);
-    if (!make_map(&p.tmA, dgu, R, 2 * I, 64, 128) || !make_map(&p.tmB, gate_up, E * H, 2 * I, 64, 256))
+    if (!make_map(&p.tmA, dgu, R, 2 * I, 64, BMH) || !make_map(&p.tmB, gate_up, E * H, 2 * I, 64, 256))
       return -1;
     p.out = dx_perm;
     p.K = (int)(2 * I);
     p.n_out = (int)H;
     p.nt = (int)((H + BN - 1) / BN);
     p.ldo = H;
-    if (run_gemm<DGRAD_GATEUP>(p, mgrouped_tile_bound(R, E, p.nt), dev, stream) != cudaSuccess) return 1;
+    if (run_bf16_mgrouped<DGRAD_GATEUP>(p, R, E, dev, stream) != cudaSuccess) return 1;
   }
   {  // d_gate_up_e = x[rows of e]^T . dgu_e
     GemmParams p;
@@ -870,10 +910,10 @@ int launch_gemm_gate_up_bwd(const uint16_t* dgu, const uint16_t* x, const int32_
     p.out = d_gate_up;
     p.m_w = (int)H;
     p.n_out = (int)(2 * I);
-    p.mt_w = (int)((H + BM - 1) / BM);
+    p.mt_w = (int)((H + 2 * BMH - 1) / (2 * BMH));
     p.nt = (int)((2 * I + BN - 1) / BN);
     p.ldo = 2 * I;
-    if (run_gemm<WGRAD_GATEUP>(p, E * p.mt_w * p.nt, dev, stream) != cudaSuccess) return 1;
+    if (run_gemm<WGRAD_GATEUP, 2>(p, E * p.mt_w * p.nt, dev, stream) != cudaSuccess) return 1;
   }
   return 0;
 }

@@ -20,7 +20,6 @@ struct DeviceInfo {
   uint32_t* status;        // device address of the status word
   uint64_t wait_limit_ns;  // bound of every device-side spin wait
   int test_stall_producer; // test hook of the bounded-wait path (grouped GEMMs)
-  int gather_mode;         // gathered gate_up A rows: 0 = cp.async, 1 = TMA tile::gather4
 };
 
 // Device information of the current device (status word address, SM count).

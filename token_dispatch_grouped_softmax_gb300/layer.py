@@ -43,10 +43,10 @@ def moe_forward(x, w_router, gate_up, down, k, bias=None, sh_gate_up=None, sh_do
     """y [T, H] bf16 and the ForwardState.
 
     fused_gather: the grouped gate_up GEMM gathers the token rows itself (the
-    permute fused into the operand load, by cp.async copies or TMA
-    tile::gather4, see set_gather_mode); False (default) materialises the
-    permuted rows first (moe_permute_rows) and streams them with 128-row TMA
-    tiles, which measures ~2.5x faster for the GEMM on GB300."""
+    permute fused into the operand load by TMA tile::gather4); False
+    (default) materialises the permuted rows first (moe_permute_rows) and
+    streams them with 128-row TMA tiles, which measures ~2.5x faster for the
+    GEMM on GB300."""
     T, H = x.shape
     E = w_router.shape[1]
     I = down.shape[0] // E
@@ -130,3 +130,61 @@ class MoELayer(torch.nn.Module):
 
     def forward(self, x, bias=None):
         return MoELayerFunction.apply(x, self.w_router, self.gate_up, self.down, self.k, bias)
+
+
+class PipelinedForward:
+    """The forward over a stream of host batches, with copies overlapped.
+
+    Batch i's layer runs on the compute stream while batch i+1's tokens are
+    copied host -> device and batch i-1's output device -> host on a copy
+    stream (double-buffered device tensors, events between the streams).
+    Host tensors must be pinned for the copies to be asynchronous.
+    """
+
+    def __init__(self, w_router, gate_up, down, k, bias=None, sh_gate_up=None, sh_down=None,
+                 fused_gather=False):
+        self.args = (w_router, gate_up, down, k, bias, sh_gate_up, sh_down)
+        self.fused_gather = fused_gather
+        self.copy_stream = torch.cuda.Stream()
+        self.x_dev = [None, None]
+        self.ev_loaded = [torch.cuda.Event(), torch.cuda.Event()]
+        self.ev_done = [torch.cuda.Event(), torch.cuda.Event()]
+        self.ev_stored = [torch.cuda.Event(), torch.cuda.Event()]
+
+    def run(self, x_host_batches, y_host_batches):
+        """y_host_batches[i] <- layer(x_host_batches[i]); returns when all are stored."""
+        w_router, gate_up, down, k, bias, sh_gu, sh_dn = self.args
+        compute = torch.cuda.current_stream()
+        n = len(x_host_batches)
+        for b in range(2):
+            self.ev_done[b].record(compute)     # both buffers free at the start
+            self.ev_stored[b].record(compute)
+
+        def load(i):
+            b = i % 2
+            xh = x_host_batches[i]
+            if self.x_dev[b] is None or self.x_dev[b].shape != xh.shape:
+                self.x_dev[b] = torch.empty(xh.shape, dtype=xh.dtype, device=w_router.device)
+            with torch.cuda.stream(self.copy_stream):
+                self.copy_stream.wait_event(self.ev_done[b])     # the layer no longer reads it
+                self.x_dev[b].copy_(xh, non_blocking=True)
+                self.ev_loaded[b].record(self.copy_stream)
+
+        if n:
+            load(0)
+        for i in range(n):
+            b = i % 2
+            if i + 1 < n:
+                load(i + 1)
+            compute.wait_event(self.ev_loaded[b])
+            compute.wait_event(self.ev_stored[b])                # batch i-2's output was copied out
+            y, _ = moe_forward(self.x_dev[b], w_router, gate_up, down, k, bias, sh_gu, sh_dn,
+                               fused_gather=self.fused_gather)
+            self.ev_done[b].record(compute)
+            with torch.cuda.stream(self.copy_stream):
+                self.copy_stream.wait_event(self.ev_done[b])
+                y_host_batches[i].copy_(y, non_blocking=True)
+                y.record_stream(self.copy_stream)
+                self.ev_stored[b].record(self.copy_stream)
+        self.copy_stream.synchronize()
+        compute.synchronize()

@@ -53,11 +53,6 @@ def set_wait_limit_ns(ns: int):
     call("moe_set_wait_limit_ns", int(ns))
 
 
-def set_gather_mode(mode: str):
-    """'cpasync' (default) or 'tma': how the gate_up GEMM gathers token rows."""
-    call("moe_set_gather_mode", {"cpasync": 0, "tma": 1}[mode])
-
-
 # ----------------------------------------------------------------- forward
 
 def route(x, w_router, k, bias=None, return_logits=False):
