@@ -224,35 +224,145 @@ __device__ __forceinline__ void store_zero_rows(const GemmParams& p, const Tile&
     if (t.nt * BN + c < p.n_out) *reinterpret_cast<uint4*>(orow + c) = z;
 }
 
-__device__ __forceinline__ void store32(uint16_t* dst, const float* v) {
-  uint4* d = reinterpret_cast<uint4*>(dst);
-#pragma unroll
-  for (int q = 0; q < 4; ++q) d[q] = pack8(v + 8 * q);
-}
-
-// 32 bf16 already packed in pairs
-__device__ __forceinline__ void store32_packed(uint16_t* dst, const uint32_t* pk) {
-  uint4* d = reinterpret_cast<uint4*>(dst);
-#pragma unroll
-  for (int q = 0; q < 4; ++q) d[q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
-}
-
 __device__ __forceinline__ void store32_f32(float* dst, const float* v) {
   float4* d = reinterpret_cast<float4*>(dst);
 #pragma unroll
   for (int q = 0; q < 8; ++q) d[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
 }
 
-__device__ __forceinline__ void load32_f32(const float* src, float* v) {
+__device__ __forceinline__ void load16_f32(const float* src, float* v) {
   const float4* s = reinterpret_cast<const float4*>(src);
 #pragma unroll
-  for (int q = 0; q < 8; ++q) {
+  for (int q = 0; q < 4; ++q) {
     const float4 a = __ldg(s + q);
     v[4 * q] = a.x; v[4 * q + 1] = a.y; v[4 * q + 2] = a.z; v[4 * q + 3] = a.w;
   }
 }
 
 __device__ __forceinline__ float swiglu(float g, float u) { return g / (1.0f + expf(-g)) * u; }
+
+// Transposes 16-byte chunks within each 8-lane group of the warp (three
+// xor-butterfly stages of shuffles): on entry lane i holds chunks 0..7 of its
+// own row in c[4j .. 4j+3]; on return it holds chunk (i % 8) of the group's
+// row j there.
+__device__ __forceinline__ void transpose_chunks8(uint32_t* c, int lane) {
+#pragma unroll
+  for (int b = 1; b < 8; b <<= 1) {
+    const bool hi = (lane & b) != 0;
+#pragma unroll
+    for (int pos = 0; pos < 8; ++pos) {
+      if (pos & b) continue;
+#pragma unroll
+      for (int w = 0; w < 4; ++w) {
+        const uint32_t send = hi ? c[4 * pos + w] : c[4 * (pos | b) + w];
+        const uint32_t recv = __shfl_xor_sync(0xffffffffu, send, b);
+        if (hi) c[4 * pos + w] = recv;
+        else c[4 * (pos | b) + w] = recv;
+      }
+    }
+  }
+}
+
+// Stores a block of 32 rows x 128 bytes held one row per lane (c: that row's
+// 128 bytes).  After the transpose every store instruction writes four whole
+// 128-byte rows, where one row per lane would touch 32 lines per instruction
+// and write each 32-byte sector in two halves.  base: the block's first byte
+// in the warp's row 0; ld: row pitch in bytes; rows whose bit is clear in
+// row_mask are skipped.  Warp-wide.
+__device__ __forceinline__ void store_block128(uint8_t* base, int64_t ld, uint32_t* c, int lane,
+                                               uint32_t row_mask) {
+  transpose_chunks8(c, lane);
+  const int g = lane >> 3, i = lane & 7;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const int row = 8 * g + j;
+    if ((row_mask >> row) & 1u)
+      *reinterpret_cast<uint4*>(base + row * ld + 16 * i) =
+          make_uint4(c[4 * j], c[4 * j + 1], c[4 * j + 2], c[4 * j + 3]);
+  }
+}
+
+// The copies of one K block of a tile: A (KH halves or MN chunks) and B into
+// the stage at sA / sB, completing on the barrier fb.  Warp-wide: gathered
+// loads spread over the lanes, the others are issued by lane 0.
+template <int MODE, int KH>
+__device__ __forceinline__ void stage_loads(const GemmParams& p, const Tile& t, int kb, uint32_t sA,
+                                            uint32_t sB, uint32_t fb, int lane, const int (&gi)[KH][4],
+                                            uint64_t keep_x) {
+  using Tr = Traits<MODE, KH>;
+  const int k0 = kb * BK;
+  if (Tr::kGateUp) {
+    if (p.gidx) {                                    // permute fused into the load (TMA)
+      for (int h = 0; h < t.halves; ++h)
+        tma_gather4_hint(sA + h * A_HALF_BYTES + 4 * lane * 128, &p.tmA, k0, gi[h][0], gi[h][1],
+                         gi[h][2], gi[h][3], fb, keep_x);
+    } else if (lane == 0) {                          // rows already in permuted order
+      for (int h = 0; h < t.halves; ++h)
+        tma_load_2d(sA + h * A_HALF_BYTES, &p.tmA, k0, t.row0 + h * BMH, fb);
+    }
+    if (lane == 0) {
+      const int brow = t.e * p.K + k0;               // gate_up rows of expert e
+      const int n0 = t.nt * 128;
+      tma_load_2d(sB + 0 * MN_CHUNK_BYTES, &p.tmB, n0, brow, fb);
+      tma_load_2d(sB + 1 * MN_CHUNK_BYTES, &p.tmB, n0 + 64, brow, fb);
+      tma_load_2d(sB + 2 * MN_CHUNK_BYTES, &p.tmB, p.I + n0, brow, fb);
+      tma_load_2d(sB + 3 * MN_CHUNK_BYTES, &p.tmB, p.I + n0 + 64, brow, fb);
+    }
+  } else if (MODE == ROUTER) {
+    if (lane == 0) {
+      const int kg = t.e * p.K + k0;                 // row of the stacked [W0; W1; W2]
+      for (int h = 0; h < t.halves; ++h)             // x repeats along the stacked K
+        tma_load_2d(sA + h * A_HALF_BYTES, &p.tmA, kg % p.I, t.row0 + h * BMH, fb);
+      const int n0 = t.nt * BN;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tma_load_2d(sB + c * MN_CHUNK_BYTES, &p.tmB, n0 + 64 * c, kg, fb);
+    }
+  } else if (MODE == FWD_DOWN) {
+    if (lane == 0) {
+      for (int h = 0; h < t.halves; ++h)
+        tma_load_2d(sA + h * A_HALF_BYTES, &p.tmA, k0, t.row0 + h * BMH, fb);
+      const int brow = t.e * p.K + k0;               // down rows of expert e
+      const int n0 = t.nt * BN;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tma_load_2d(sB + c * MN_CHUNK_BYTES, &p.tmB, n0 + 64 * c, brow, fb);
+    }
+  } else if (MODE == DGRAD_DOWN || MODE == DGRAD_GATEUP) {
+    if (lane == 0) {
+      for (int h = 0; h < t.halves; ++h)
+        tma_load_2d(sA + h * A_HALF_BYTES, &p.tmA, k0, t.row0 + h * BMH, fb);
+      // B^T rows: expert e's block of rows_per_e rows, K-major
+      const int rows_per_e = (MODE == DGRAD_DOWN) ? p.I : p.n_out;
+      tma_load_2d(sB, &p.tmB, k0, t.e * rows_per_e + t.nt * BN, fb);
+    }
+  } else {  // WGRAD_*: A = rows of the expert (K = tokens), MN-major chunks of 64 m
+    const int krow = t.row0 + k0;
+    const int m0 = t.mt * Tr::kBM;
+    if (MODE == WGRAD_GATEUP && p.gidx) {            // gathered through src_row
+      // lane: MN chunk c = lane >> 3, K rows 8*(lane & 7) .. +7 (two gather4)
+      const int c = lane >> 3;
+      if (c < 2 * t.halves) {
+#pragma unroll
+        for (int q2 = 0; q2 < 2; ++q2) {
+          const int kr0 = 8 * (lane & 7) + 4 * q2;
+          int r4[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) r4[q] = p.gidx[t.row0 + min(k0 + kr0 + q, t.rows - 1)];
+          tma_gather4_hint(sA + c * MN_CHUNK_BYTES + kr0 * 128, &p.tmA, m0 + 64 * c, r4[0], r4[1],
+                           r4[2], r4[3], fb, keep_x);
+        }
+      }
+    } else if (lane == 0) {                          // rows already in permuted order
+      for (int c = 0; c < 2 * t.halves; ++c)
+        tma_load_2d(sA + c * MN_CHUNK_BYTES, &p.tmA, m0 + 64 * c, krow, fb);
+    }
+    if (lane == 0) {
+      const int n0 = t.nt * BN;
+#pragma unroll
+      for (int c = 0; c < 4; ++c)
+        tma_load_2d(sB + c * MN_CHUNK_BYTES, &p.tmB, n0 + 64 * c, krow, fb);
+    }
+  }
+}
 
 template <int MODE, int KH>
 __global__ void __launch_bounds__(Traits<MODE, KH>::kThreads, 1)
@@ -367,78 +477,7 @@ __global__ void __launch_bounds__(Traits<MODE, KH>::kThreads, 1)
         const uint32_t fb = full_bar(stage);
         if (lane == 0) mbar_arrive_expect_tx(fb, a_bytes + (uint32_t)B_BYTES);
         __syncwarp();
-        const int k0 = kb * BK;
-        if (Tr::kGateUp) {
-          if (p.gidx) {                                    // permute fused into the load (TMA)
-            for (int h = 0; h < t.halves; ++h)
-              tma_gather4_hint(sA + h * A_HALF_BYTES + 4 * lane * 128, &p.tmA, k0, gi[h][0], gi[h][1],
-                               gi[h][2], gi[h][3], fb, keep_x);
-          } else if (lane == 0) {                          // rows already in permuted order
-            for (int h = 0; h < t.halves; ++h)
-              tma_load_2d(sA + h * A_HALF_BYTES, &p.tmA, k0, t.row0 + h * BMH, fb);
-          }
-          if (lane == 0) {
-            const int brow = t.e * p.K + k0;               // gate_up rows of expert e
-            const int n0 = t.nt * 128;
-            tma_load_2d(sB + 0 * MN_CHUNK_BYTES, &p.tmB, n0, brow, fb);
-            tma_load_2d(sB + 1 * MN_CHUNK_BYTES, &p.tmB, n0 + 64, brow, fb);
-            tma_load_2d(sB + 2 * MN_CHUNK_BYTES, &p.tmB, p.I + n0, brow, fb);
-            tma_load_2d(sB + 3 * MN_CHUNK_BYTES, &p.tmB, p.I + n0 + 64, brow, fb);
-          }
-        } else if (MODE == ROUTER) {
-          if (lane == 0) {
-            const int kg = t.e * p.K + k0;                 // row of the stacked [W0; W1; W2]
-            for (int h = 0; h < t.halves; ++h)             // x repeats along the stacked K
-              tma_load_2d(sA + h * A_HALF_BYTES, &p.tmA, kg % p.I, t.row0 + h * BMH, fb);
-            const int n0 = t.nt * BN;
-#pragma unroll
-            for (int c = 0; c < 4; ++c) tma_load_2d(sB + c * MN_CHUNK_BYTES, &p.tmB, n0 + 64 * c, kg, fb);
-          }
-        } else if (MODE == FWD_DOWN) {
-          if (lane == 0) {
-            for (int h = 0; h < t.halves; ++h)
-              tma_load_2d(sA + h * A_HALF_BYTES, &p.tmA, k0, t.row0 + h * BMH, fb);
-            const int brow = t.e * p.K + k0;               // down rows of expert e
-            const int n0 = t.nt * BN;
-#pragma unroll
-            for (int c = 0; c < 4; ++c) tma_load_2d(sB + c * MN_CHUNK_BYTES, &p.tmB, n0 + 64 * c, brow, fb);
-          }
-        } else if (MODE == DGRAD_DOWN || MODE == DGRAD_GATEUP) {
-          if (lane == 0) {
-            for (int h = 0; h < t.halves; ++h)
-              tma_load_2d(sA + h * A_HALF_BYTES, &p.tmA, k0, t.row0 + h * BMH, fb);
-            // B^T rows: expert e's block of rows_per_e rows, K-major
-            const int rows_per_e = (MODE == DGRAD_DOWN) ? p.I : p.n_out;
-            tma_load_2d(sB, &p.tmB, k0, t.e * rows_per_e + t.nt * BN, fb);
-          }
-        } else {  // WGRAD_*: A = rows of the expert (K = tokens), MN-major chunks of 64 m
-          const int krow = t.row0 + k0;
-          const int m0 = t.mt * Tr::kBM;
-          if (MODE == WGRAD_GATEUP && p.gidx) {            // gathered through src_row
-            // lane: MN chunk c = lane >> 3, K rows 8*(lane & 7) .. +7 (two gather4)
-            const int c = lane >> 3;
-            if (c < 2 * t.halves) {
-#pragma unroll
-              for (int q2 = 0; q2 < 2; ++q2) {
-                const int kr0 = 8 * (lane & 7) + 4 * q2;
-                int r4[4];
-#pragma unroll
-                for (int q = 0; q < 4; ++q) r4[q] = p.gidx[t.row0 + min(k0 + kr0 + q, t.rows - 1)];
-                tma_gather4_hint(sA + c * MN_CHUNK_BYTES + kr0 * 128, &p.tmA, m0 + 64 * c, r4[0], r4[1],
-                                 r4[2], r4[3], fb, keep_x);
-              }
-            }
-          } else if (lane == 0) {                          // rows already in permuted order
-            for (int c = 0; c < 2 * t.halves; ++c)
-              tma_load_2d(sA + c * MN_CHUNK_BYTES, &p.tmA, m0 + 64 * c, krow, fb);
-          }
-          if (lane == 0) {
-            const int n0 = t.nt * BN;
-#pragma unroll
-            for (int c = 0; c < 4; ++c)
-              tma_load_2d(sB + c * MN_CHUNK_BYTES, &p.tmB, n0 + 64 * c, krow, fb);
-          }
-        }
+        stage_loads<MODE, KH>(p, t, kb, sA, sB, fb, lane, gi, keep_x);
         issued_mask |= 1u << stage;
         last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
         if (++stage == STAGES) {
@@ -567,6 +606,9 @@ __global__ void __launch_bounds__(Traits<MODE, KH>::kThreads, 1)
         acc = 0;
         acc_phase ^= 1u;
       }
+      // Rows of this warp: 32 consecutive tile rows starting at wrow (one
+      // per lane); stores go through store_block128 (whole 128-byte rows).
+      const int wrow = half * BMH + quarter * 32;
       float v[32];
       if (Tr::kEarlyRelease) {
         // read the whole row into registers as bf16 (16 columns at a time:
@@ -584,56 +626,66 @@ __global__ void __launch_bounds__(Traits<MODE, KH>::kThreads, 1)
         tc_fence_before();
         mbar_arrive(done);
         if (active) {
-          uint16_t* orow;
-          bool row_ok;
+          uint8_t* base;
+          uint32_t row_mask;
           const int n0 = t.nt * BN;
           if (Tr::kKGrouped) {   // rows m = mt*BM + r of expert e's weight-gradient block
-            const int m = t.mt * Tr::kBM + r;
-            row_ok = m < p.m_w;
-            orow = p.out + ((int64_t)t.e * p.m_w + m) * p.ldo;
+            const int m0 = t.mt * Tr::kBM + wrow;
+            row_mask = __ballot_sync(0xffffffffu, m0 + lane < p.m_w);
+            base = reinterpret_cast<uint8_t*>(p.out + ((int64_t)t.e * p.m_w + m0) * p.ldo + n0);
           } else {
-            row_ok = r < t.rows;
-            orow = p.out + (int64_t)(t.row0 + r) * p.ldo;
+            row_mask = __ballot_sync(0xffffffffu, wrow + lane < t.rows);
+            base = reinterpret_cast<uint8_t*>(p.out + (int64_t)(t.row0 + wrow) * p.ldo + n0);
           }
-          if (row_ok) {
 #pragma unroll
-            for (int c = 0; c < BN / 32; ++c)
-              if (n0 + 32 * c < p.n_out) store32_packed(orow + n0 + 32 * c, pk + 16 * c);
-          }
+          for (int blk = 0; blk < BN / 64; ++blk)
+            if (n0 + 64 * blk < p.n_out)
+              store_block128(base + 128 * blk, p.ldo * 2, pk + 32 * blk, lane, row_mask);
         }
         continue;
       }
       if (!active) {
         // this half carries no rows of the tile: nothing to read or store
       } else if (MODE == FWD_GATEUP) {
-        const bool row_ok = r < t.rows;
-        const int64_t row = t.row0 + r;
-        const int n0 = t.nt * 128;
-#pragma unroll 1
-        for (int c0 = 64 * wg; c0 < 64 * wg + 64; c0 += 32) {
-          if (n0 + c0 >= p.n_out) break;                 // warp-uniform
-          float u[32];
-          tmem_ld32(taddr + c0, v);                      // gate columns
-          tmem_ld32(taddr + 128 + c0, u);                // up columns
-          if (row_ok) {
-            if (p.out_gu) {
-              store32_f32(p.out_gu + row * 2 * p.I + n0 + c0, v);
-              store32_f32(p.out_gu + row * 2 * p.I + p.I + n0 + c0, u);
+        // warpgroup wg: h columns [64 wg, 64 wg + 64) of the tile (gate and
+        // up accumulator columns c and 128 + c)
+        const uint32_t row_mask = __ballot_sync(0xffffffffu, wrow + lane < t.rows);
+        const int64_t row0 = t.row0 + wrow;
+        const int n0 = t.nt * 128 + 64 * wg;               // first h column
+        if (n0 < p.n_out) {
+          const bool row_ok = wrow + lane < t.rows;
+          const float wr = (p.out_hw && row_ok) ? p.wrow[row0 + lane] : 0.f;
+          uint32_t hk[32], hw[32];
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            float u[32];
+            tmem_ld32(taddr + 64 * wg + 32 * c, v);        // gate columns
+            tmem_ld32(taddr + 128 + 64 * wg + 32 * c, u);  // up columns
+            if (p.out_gu) {                                // fp32 pre-activations, 128-byte blocks
+              float* g0 = p.out_gu + row0 * 2 * p.I + n0 + 32 * c;
+              uint32_t bits[32];
+#pragma unroll
+              for (int q = 0; q < 32; ++q) bits[q] = __float_as_uint(v[q]);
+              store_block128(reinterpret_cast<uint8_t*>(g0), 8 * p.I, bits, lane, row_mask);
+#pragma unroll
+              for (int q = 0; q < 32; ++q) bits[q] = __float_as_uint(u[q]);
+              store_block128(reinterpret_cast<uint8_t*>(g0 + p.I), 8 * p.I, bits, lane, row_mask);
             }
 #pragma unroll
-            for (int q = 0; q < 32; ++q) v[q] = swiglu(v[q], u[q]);
-            store32(p.out + row * p.ldo + n0 + c0, v);
-            if (p.out_hw) {
-              const float wr = p.wrow[row];
-#pragma unroll
-              for (int q = 0; q < 32; ++q) v[q] *= wr;
-              store32(p.out_hw + row * p.ldo + n0 + c0, v);
+            for (int q = 0; q < 16; ++q) {
+              const float h0 = swiglu(v[2 * q], u[2 * q]), h1 = swiglu(v[2 * q + 1], u[2 * q + 1]);
+              hk[16 * c + q] = pack_bf16x2(h0, h1);
+              hw[16 * c + q] = pack_bf16x2(h0 * wr, h1 * wr);
             }
           }
+          store_block128(reinterpret_cast<uint8_t*>(p.out + row0 * p.ldo + n0), p.ldo * 2, hk, lane, row_mask);
+          if (p.out_hw)
+            store_block128(reinterpret_cast<uint8_t*>(p.out_hw + row0 * p.ldo + n0), p.ldo * 2, hw, lane,
+                           row_mask);
         }
       } else if (MODE == ROUTER) {
-        const bool row_ok = r < t.rows;
-        float* orow = p.out_part + ((int64_t)t.e * p.rows + t.row0 + r) * p.ldo;
+        const bool row_ok = wrow + lane < t.rows;
+        float* orow = p.out_part + ((int64_t)t.e * p.rows + t.row0 + wrow + lane) * p.ldo;
         const int n0 = t.nt * BN;
 #pragma unroll 1
         for (int c0 = 128 * wg; c0 < 128 * wg + 128; c0 += 32) {
@@ -650,42 +702,64 @@ __global__ void __launch_bounds__(Traits<MODE, KH>::kThreads, 1)
           }
         }
       } else if (MODE == FWD_DOWN || MODE == DGRAD_GATEUP) {   // one half: column half wg
-        const bool row_ok = r < t.rows;
-        const int64_t row = t.row0 + r;
-        const int n0 = t.nt * BN;
+        const uint32_t row_mask = __ballot_sync(0xffffffffu, wrow + lane < t.rows);
+        const int n0 = t.nt * BN + 128 * wg;
+        uint8_t* base = reinterpret_cast<uint8_t*>(p.out + (int64_t)(t.row0 + wrow) * p.ldo + n0);
 #pragma unroll 1
-        for (int c0 = 128 * wg; c0 < 128 * wg + 128; c0 += 32) {
-          if (n0 + c0 >= p.n_out) break;
-          tmem_ld32(taddr + c0, v);
-          if (row_ok) store32(p.out + row * p.ldo + n0 + c0, v);
+        for (int blk = 0; blk < 2; ++blk) {
+          if (n0 + 64 * blk >= p.n_out) break;
+          uint32_t pk[32];
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+            tmem_ld32(taddr + 128 * wg + 64 * blk + 32 * c, v);
+#pragma unroll
+            for (int q = 0; q < 16; ++q) pk[16 * c + q] = pack_bf16x2(v[2 * q], v[2 * q + 1]);
+          }
+          store_block128(base + 128 * blk, p.ldo * 2, pk, lane, row_mask);
         }
       } else if (MODE == DGRAD_DOWN) {
-        const bool row_ok = r < t.rows;
-        const int64_t row = t.row0 + r;
-        const int n0 = t.nt * BN;
+        const bool row_ok = wrow + lane < t.rows;
+        const uint32_t row_mask = __ballot_sync(0xffffffffu, row_ok);
+        const int64_t row = t.row0 + wrow + lane;
+        const int64_t row0 = t.row0 + wrow;
+        const int n0 = t.nt * BN + 128 * wg;
+        const float wr = row_ok ? p.wrow[row] : 0.f;     // dh = w * (dY . Wd^T)
         float dot = 0.f;                                 // <dY . Wd^T, h> over this thread's columns
 #pragma unroll 1
-        for (int c0 = 128 * wg; c0 < 128 * wg + 128; c0 += 32) {
-          if (n0 + c0 >= p.n_out) break;
-          tmem_ld32(taddr + c0, v);                      // dY . Wd^T (fp32)
-          if (row_ok) {
-            float g[32], u[32];
-            load32_f32(p.aux + row * 2 * p.I + n0 + c0, g);
-            load32_f32(p.aux + row * 2 * p.I + p.I + n0 + c0, u);
-            const float wr = p.wrow[row];                // dh = w * (dY . Wd^T)
+        for (int blk = 0; blk < 2; ++blk) {
+          if (n0 + 64 * blk >= p.n_out) break;
+          uint32_t dg[32], du[32];
 #pragma unroll
-            for (int q = 0; q < 32; ++q) {
+          for (int c = 0; c < 4; ++c) {                    // 16 columns at a time
+            const int col = n0 + 64 * blk + 16 * c;
+            tmem_ld16(taddr + 128 * wg + 64 * blk + 16 * c, v);   // dY . Wd^T (fp32)
+            float g[16], u[16];
+            if (row_ok) {
+              load16_f32(p.aux + row * 2 * p.I + col, g);
+              load16_f32(p.aux + row * 2 * p.I + p.I + col, u);
+            } else {
+#pragma unroll
+              for (int q = 0; q < 16; ++q) g[q] = u[q] = 0.f;
+            }
+#pragma unroll
+            for (int q = 0; q < 16; ++q) {
               const float s = 1.0f / (1.0f + expf(-g[q]));
               dot = fmaf(v[q], g[q] * s * u[q], dot);    // h = silu(g) * u from the fp32 pre-activations
               const float dh = wr * v[q];
-              const float dg = dh * u[q] * s * (1.0f + g[q] * (1.0f - s));
-              const float du = dh * g[q] * s;
-              g[q] = dg;
-              u[q] = du;
+              const float dgq = dh * u[q] * s * (1.0f + g[q] * (1.0f - s));
+              const float duq = dh * g[q] * s;
+              g[q] = dgq;
+              u[q] = duq;
             }
-            store32(p.out + row * 2 * p.I + n0 + c0, g);
-            store32(p.out + row * 2 * p.I + p.I + n0 + c0, u);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+              dg[8 * c + q] = pack_bf16x2(g[2 * q], g[2 * q + 1]);
+              du[8 * c + q] = pack_bf16x2(u[2 * q], u[2 * q + 1]);
+            }
           }
+          uint8_t* gbase = reinterpret_cast<uint8_t*>(p.out + row0 * 2 * p.I + n0 + 64 * blk);
+          store_block128(gbase, 4 * p.I, dg, lane, row_mask);
+          store_block128(gbase + 2 * p.I, 4 * p.I, du, lane, row_mask);
         }
         if (row_ok && p.out_part) p.out_part[row * 2 * p.nt + 2 * t.nt + wg] = dot;
       }
