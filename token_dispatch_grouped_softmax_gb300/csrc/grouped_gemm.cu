@@ -230,27 +230,19 @@ __device__ __forceinline__ void store32_f32(float* dst, const float* v) {
   for (int q = 0; q < 8; ++q) d[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
 }
 
-__device__ __forceinline__ void load16_f32(const float* src, float* v) {
-  const float4* s = reinterpret_cast<const float4*>(src);
-#pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    const float4 a = __ldg(s + q);
-    v[4 * q] = a.x; v[4 * q + 1] = a.y; v[4 * q + 2] = a.z; v[4 * q + 3] = a.w;
-  }
-}
-
 __device__ __forceinline__ float swiglu(float g, float u) { return g / (1.0f + expf(-g)) * u; }
 
-// Transposes 16-byte chunks within each 8-lane group of the warp (three
-// xor-butterfly stages of shuffles): on entry lane i holds chunks 0..7 of its
-// own row in c[4j .. 4j+3]; on return it holds chunk (i % 8) of the group's
-// row j there.
-__device__ __forceinline__ void transpose_chunks8(uint32_t* c, int lane) {
+// Transposes 16-byte chunks within each N-lane group of the warp (log2 N
+// xor-butterfly stages of shuffles): on entry lane i holds chunks 0..N-1 of
+// its own row in c[4j .. 4j+3]; on return it holds chunk (i % N) of the
+// group's row j there.  The transpose is its own inverse.
+template <int N>
+__device__ __forceinline__ void transpose_chunks(uint32_t* c, int lane) {
 #pragma unroll
-  for (int b = 1; b < 8; b <<= 1) {
+  for (int b = 1; b < N; b <<= 1) {
     const bool hi = (lane & b) != 0;
 #pragma unroll
-    for (int pos = 0; pos < 8; ++pos) {
+    for (int pos = 0; pos < N; ++pos) {
       if (pos & b) continue;
 #pragma unroll
       for (int w = 0; w < 4; ++w) {
@@ -263,23 +255,45 @@ __device__ __forceinline__ void transpose_chunks8(uint32_t* c, int lane) {
   }
 }
 
-// Stores a block of 32 rows x 128 bytes held one row per lane (c: that row's
-// 128 bytes).  After the transpose every store instruction writes four whole
-// 128-byte rows, where one row per lane would touch 32 lines per instruction
-// and write each 32-byte sector in two halves.  base: the block's first byte
-// in the warp's row 0; ld: row pitch in bytes; rows whose bit is clear in
-// row_mask are skipped.  Warp-wide.
-__device__ __forceinline__ void store_block128(uint8_t* base, int64_t ld, uint32_t* c, int lane,
-                                               uint32_t row_mask) {
-  transpose_chunks8(c, lane);
-  const int g = lane >> 3, i = lane & 7;
+// Stores a block of 32 rows x 16N bytes (N = 8: 128, N = 4: 64) held one
+// row per lane (c: that row's bytes).  After the transpose every store
+// instruction writes 32/N whole row segments, where one row per lane would
+// touch 32 lines per instruction and write each 32-byte sector in two halves.
+// base: the block's first byte in the warp's row 0; ld: row pitch in bytes;
+// rows whose bit is clear in row_mask are skipped.  Warp-wide.
+template <int N>
+__device__ __forceinline__ void store_block(uint8_t* base, int64_t ld, uint32_t* c, int lane,
+                                            uint32_t row_mask) {
+  transpose_chunks<N>(c, lane);
+  const int g = lane / N, i = lane % N;
 #pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    const int row = 8 * g + j;
+  for (int j = 0; j < N; ++j) {
+    const int row = N * g + j;
     if ((row_mask >> row) & 1u)
       *reinterpret_cast<uint4*>(base + row * ld + 16 * i) =
           make_uint4(c[4 * j], c[4 * j + 1], c[4 * j + 2], c[4 * j + 3]);
   }
+}
+
+__device__ __forceinline__ void store_block128(uint8_t* base, int64_t ld, uint32_t* c, int lane,
+                                               uint32_t row_mask) {
+  store_block<8>(base, ld, c, lane, row_mask);
+}
+
+// The inverse of store_block<8>: reads 32 rows x 128 bytes with four whole
+// rows per load instruction, then transposes so that lane l holds row l's
+// 128 bytes in c.  Rows whose bit is clear in row_mask read as zeros.
+__device__ __forceinline__ void load_block128(const uint8_t* base, int64_t ld, uint32_t* c, int lane,
+                                              uint32_t row_mask) {
+  const int g = lane >> 3, i = lane & 7;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const int row = 8 * g + j;
+    uint4 q = make_uint4(0, 0, 0, 0);
+    if ((row_mask >> row) & 1u) q = __ldg(reinterpret_cast<const uint4*>(base + row * ld + 16 * i));
+    c[4 * j] = q.x; c[4 * j + 1] = q.y; c[4 * j + 2] = q.z; c[4 * j + 3] = q.w;
+  }
+  transpose_chunks<8>(c, lane);
 }
 
 // The copies of one K block of a tile: A (KH halves or MN chunks) and B into
@@ -655,33 +669,36 @@ __global__ void __launch_bounds__(Traits<MODE, KH>::kThreads, 1)
         if (n0 < p.n_out) {
           const bool row_ok = wrow + lane < t.rows;
           const float wr = (p.out_hw && row_ok) ? p.wrow[row0 + lane] : 0.f;
-          uint32_t hk[32], hw[32];
+#pragma unroll 1
+          for (int c = 0; c < 2; ++c) {                    // 32 h columns at a time
+            const int col = n0 + 32 * c;
+            uint32_t bits[32];
+            if (p.out_gu) {                                // fp32 pre-activations g | u, 128-byte blocks
 #pragma unroll
-          for (int c = 0; c < 2; ++c) {
+              for (int gu = 0; gu < 2; ++gu) {
+                tmem_ld32(taddr + 128 * gu + 64 * wg + 32 * c, v);
+#pragma unroll
+                for (int q = 0; q < 32; ++q) bits[q] = __float_as_uint(v[q]);
+                store_block128(reinterpret_cast<uint8_t*>(p.out_gu + row0 * 2 * p.I + gu * p.I + col), 8 * p.I,
+                               bits, lane, row_mask);
+              }
+            }
             float u[32];
             tmem_ld32(taddr + 64 * wg + 32 * c, v);        // gate columns
             tmem_ld32(taddr + 128 + 64 * wg + 32 * c, u);  // up columns
-            if (p.out_gu) {                                // fp32 pre-activations, 128-byte blocks
-              float* g0 = p.out_gu + row0 * 2 * p.I + n0 + 32 * c;
-              uint32_t bits[32];
-#pragma unroll
-              for (int q = 0; q < 32; ++q) bits[q] = __float_as_uint(v[q]);
-              store_block128(reinterpret_cast<uint8_t*>(g0), 8 * p.I, bits, lane, row_mask);
-#pragma unroll
-              for (int q = 0; q < 32; ++q) bits[q] = __float_as_uint(u[q]);
-              store_block128(reinterpret_cast<uint8_t*>(g0 + p.I), 8 * p.I, bits, lane, row_mask);
-            }
+            // bits[0..15]: h, bits[16..31]: w * h (bf16 pairs)
 #pragma unroll
             for (int q = 0; q < 16; ++q) {
               const float h0 = swiglu(v[2 * q], u[2 * q]), h1 = swiglu(v[2 * q + 1], u[2 * q + 1]);
-              hk[16 * c + q] = pack_bf16x2(h0, h1);
-              hw[16 * c + q] = pack_bf16x2(h0 * wr, h1 * wr);
+              bits[q] = pack_bf16x2(h0, h1);
+              bits[16 + q] = pack_bf16x2(h0 * wr, h1 * wr);
             }
-          }
-          store_block128(reinterpret_cast<uint8_t*>(p.out + row0 * p.ldo + n0), p.ldo * 2, hk, lane, row_mask);
-          if (p.out_hw)
-            store_block128(reinterpret_cast<uint8_t*>(p.out_hw + row0 * p.ldo + n0), p.ldo * 2, hw, lane,
+            store_block<4>(reinterpret_cast<uint8_t*>(p.out + row0 * p.ldo + col), p.ldo * 2, bits, lane,
                            row_mask);
+            if (p.out_hw)   // warp-uniform
+              store_block<4>(reinterpret_cast<uint8_t*>(p.out_hw + row0 * p.ldo + col), p.ldo * 2, bits + 16,
+                             lane, row_mask);
+          }
         }
       } else if (MODE == ROUTER) {
         const bool row_ok = wrow + lane < t.rows;
@@ -725,41 +742,34 @@ __global__ void __launch_bounds__(Traits<MODE, KH>::kThreads, 1)
         const int n0 = t.nt * BN + 128 * wg;
         const float wr = row_ok ? p.wrow[row] : 0.f;     // dh = w * (dY . Wd^T)
         float dot = 0.f;                                 // <dY . Wd^T, h> over this thread's columns
+        const uint8_t* aux0 = reinterpret_cast<const uint8_t*>(p.aux + row0 * 2 * p.I);
+        uint8_t* out0 = reinterpret_cast<uint8_t*>(p.out + row0 * 2 * p.I);
 #pragma unroll 1
-        for (int blk = 0; blk < 2; ++blk) {
-          if (n0 + 64 * blk >= p.n_out) break;
-          uint32_t dg[32], du[32];
+        for (int c = 0; c < 4; ++c) {                    // 32 columns at a time
+          const int col = n0 + 32 * c;
+          if (col >= p.n_out) break;
+          tmem_ld32(taddr + 128 * wg + 32 * c, v);       // dY . Wd^T (fp32)
+          uint32_t gb[32], ub[32];                       // the row's fp32 pre-activations g | u
+          load_block128(aux0 + 4 * col, 8 * p.I, gb, lane, row_mask);
+          load_block128(aux0 + 4 * (p.I + col), 8 * p.I, ub, lane, row_mask);
+          uint32_t dg[16], du[16];
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {                    // 16 columns at a time
-            const int col = n0 + 64 * blk + 16 * c;
-            tmem_ld16(taddr + 128 * wg + 64 * blk + 16 * c, v);   // dY . Wd^T (fp32)
-            float g[16], u[16];
-            if (row_ok) {
-              load16_f32(p.aux + row * 2 * p.I + col, g);
-              load16_f32(p.aux + row * 2 * p.I + p.I + col, u);
-            } else {
+          for (int q = 0; q < 32; q += 2) {
+            float o[2][2];
 #pragma unroll
-              for (int q = 0; q < 16; ++q) g[q] = u[q] = 0.f;
+            for (int e2 = 0; e2 < 2; ++e2) {
+              const float g = __uint_as_float(gb[q + e2]), u = __uint_as_float(ub[q + e2]);
+              const float s = 1.0f / (1.0f + expf(-g));
+              dot = fmaf(v[q + e2], g * s * u, dot);     // h = silu(g) * u from the fp32 pre-activations
+              const float dh = wr * v[q + e2];
+              o[0][e2] = dh * u * s * (1.0f + g * (1.0f - s));
+              o[1][e2] = dh * g * s;
             }
-#pragma unroll
-            for (int q = 0; q < 16; ++q) {
-              const float s = 1.0f / (1.0f + expf(-g[q]));
-              dot = fmaf(v[q], g[q] * s * u[q], dot);    // h = silu(g) * u from the fp32 pre-activations
-              const float dh = wr * v[q];
-              const float dgq = dh * u[q] * s * (1.0f + g[q] * (1.0f - s));
-              const float duq = dh * g[q] * s;
-              g[q] = dgq;
-              u[q] = duq;
-            }
-#pragma unroll
-            for (int q = 0; q < 8; ++q) {
-              dg[8 * c + q] = pack_bf16x2(g[2 * q], g[2 * q + 1]);
-              du[8 * c + q] = pack_bf16x2(u[2 * q], u[2 * q + 1]);
-            }
+            dg[q / 2] = pack_bf16x2(o[0][0], o[0][1]);
+            du[q / 2] = pack_bf16x2(o[1][0], o[1][1]);
           }
-          uint8_t* gbase = reinterpret_cast<uint8_t*>(p.out + row0 * 2 * p.I + n0 + 64 * blk);
-          store_block128(gbase, 4 * p.I, dg, lane, row_mask);
-          store_block128(gbase + 2 * p.I, 4 * p.I, du, lane, row_mask);
+          store_block<4>(out0 + 2 * col, 4 * p.I, dg, lane, row_mask);
+          store_block<4>(out0 + 2 * (p.I + col), 4 * p.I, du, lane, row_mask);
         }
         if (row_ok && p.out_part) p.out_part[row * 2 * p.nt + 2 * t.nt + wg] = dot;
       }
