@@ -279,18 +279,39 @@ def run_native(args):
     barrier(dist)
     torch.cuda.synchronize()
     t0 = time.time()
+    # (1) eager launches with an event between kernels: the per-kernel times
     for i in range(K):
         flush.zero_()
         step(evs[i])
     torch.cuda.synchronize()
     barrier(dist)
+    moe.sync_status()
+    eager_ms = [evs[i][0].elapsed_time(evs[i][-1]) for i in range(K)]
+    per_kernel = {n: sum(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(K)) / K
+                  for j, n in enumerate(names)}
+    eager_s = max_over_ranks(dist, sum(eager_ms) / 1e3, device)
+    # (2) the same forward as one CUDA graph per step (ForwardGraph): the value
+    graph = moe.ForwardGraph(T, d["w_router"], d["gate_up"], d["down"], k, d["bias"], d["sh_gate_up"],
+                             d["sh_down"], fused_gather=fused)
+    graph.x.copy_(d["x"])
+    for _ in range(max(args.warmup, 3)):
+        graph.replay()
+    torch.cuda.synchronize()
+    barrier(dist)
+    gevs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
+    for i in range(K):
+        flush.zero_()
+        gevs[i][0].record(stream)
+        graph.replay()
+        gevs[i][1].record(stream)
+    torch.cuda.synchronize()
+    barrier(dist)
     t1 = time.time()
     clk = clocks.stop(t0, t1)
     moe.sync_status()
-
-    step_ms = [evs[i][0].elapsed_time(evs[i][-1]) for i in range(K)]
-    per_kernel = {n: sum(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(K)) / K
-                  for j, n in enumerate(names)}
+    y_graph_ok = bool(torch.equal(graph.y.view(torch.int16), step().view(torch.int16)))
+    del graph
+    step_ms = [gevs[i][0].elapsed_time(gevs[i][1]) for i in range(K)]
     total_s = sum(step_ms) / 1e3
     total_s = max_over_ranks(dist, total_s, device)
     value = ws * T * K / total_s
@@ -338,6 +359,11 @@ def run_native(args):
                    "parallelism": "replicas" if ws > 1 else "single",
                    "gather": args.gather},
         "roofline": roofline,
+        "timing": "value and ms_per_step: the forward replayed as one CUDA graph per step "
+                  "(ForwardGraph), CUDA events around each replay; kernels_us and eager: the same "
+                  "kernels launched one by one with an event between kernels",
+        "eager": {"value": round(ws * T * K / eager_s, 1), "ms_per_step": round(1e3 * eager_s / K, 4)},
+        "graph_output_matches_eager": y_graph_ok,
         "kernels_us": {n: round(v * 1e3, 2) for n, v in per_kernel.items()},
         "gemm": {"tflops": round(gemm_flops / (gemm_ms * 1e-3) / 1e12, 1),
                  "frac_of_peak": round(gemm_flops / (gemm_ms * 1e-3) / 1e12 / peak_tf, 4),
@@ -370,7 +396,7 @@ def e2e(moe, d, cfg, torch, stream, dist, device, ws, K, fused):
     layer on two streams).  Every step's input upload and output download is
     inside the timed region."""
     T, H = cfg.T, cfg.H
-    runner = moe.PipelinedForward(d["w_router"], d["gate_up"], d["down"], cfg.k, d["bias"], d["sh_gate_up"],
+    runner = moe.PipelinedForward(T, d["w_router"], d["gate_up"], d["down"], cfg.k, d["bias"], d["sh_gate_up"],
                                   d["sh_down"], fused_gather=fused)
     xs = [d["x_host"]] * K
     ys = [torch.empty((T, H), dtype=torch.bfloat16).pin_memory() for _ in range(2)]
@@ -387,7 +413,7 @@ def e2e(moe, d, cfg, torch, stream, dist, device, ws, K, fused):
             "d2h_bytes_per_step": T * H * 2, "steps": K,
             "note": "weights resident; every step copies x host->device (pinned) and y device->host "
                     "(pinned); host wall clock around K steps with both streams synchronised; copies "
-                    "of neighbouring steps overlap the layer (PipelinedForward)"}
+                    "of neighbouring steps overlap the layer (PipelinedForward: ForwardGraph replays)"}
 
 
 def fwd_bwd(moe, torch, stream, dist, device, ws, flush, pk, fused, K=30, W=3):

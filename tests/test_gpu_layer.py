@@ -206,8 +206,26 @@ def test_pipelined_forward_matches_forward():
     xs = [torch.from_numpy(synth.normal_bf16(s, synth.TID_X, (256, 256), 1.0).view(np.int16))
           .view(torch.bfloat16).pin_memory() for s in (1, 2, 3)]
     ys = [torch.empty((256, 256), dtype=torch.bfloat16).pin_memory() for _ in xs]
-    moe.PipelinedForward(wr, gu, dn, cfg.k).run(xs, ys)
+    moe.PipelinedForward(256, wr, gu, dn, cfg.k).run(xs, ys)
     moe.sync_status()
     for xh, yh in zip(xs, ys):
         y, _ = moe.moe_forward(xh.cuda(), wr, gu, dn, cfg.k)
         assert torch_equal(y.cpu(), yh)
+
+
+def test_forward_graph_replays_match_forward():
+    """ForwardGraph: one capture, replayed on new tokens (new routing each
+    time), gives moe_forward's outputs bit for bit, the shared expert too."""
+    import torch
+    moe = lib()
+    cfg, inp = _inputs(300, 256, 8, 2, 128, seed=91, I_shared=64)
+    wr, gu, dn = f32(inp.w_router), bf(inp.gate_up), bf(inp.down)
+    sgu, sdn = bf(inp.sh_gate_up), bf(inp.sh_down)
+    g = moe.ForwardGraph(300, wr, gu, dn, cfg.k, None, sgu, sdn)
+    for s in (5, 6, 7):
+        x = torch.from_numpy(synth.normal_bf16(s, synth.TID_X, (300, 256), 1.0).view(np.int16)) \
+            .view(torch.bfloat16).cuda()
+        y_graph = g(x).clone()
+        y_eager, _ = moe.moe_forward(x, wr, gu, dn, cfg.k, None, sgu, sdn)
+        moe.sync_status()
+        assert torch_equal(y_graph, y_eager)

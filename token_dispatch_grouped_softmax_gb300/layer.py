@@ -132,28 +132,72 @@ class MoELayer(torch.nn.Module):
         return MoELayerFunction.apply(x, self.w_router, self.gate_up, self.down, self.k, bias)
 
 
+class ForwardGraph:
+    """The layer forward captured once as a CUDA graph, for a fixed token
+    count and fixed weights (inference).
+
+    Write a batch's tokens into ``x`` (or pass them to ``__call__``); a replay
+    runs route, permute, both grouped GEMMs and the combine as one graph
+    launch, with no per-kernel launch gaps, and writes ``y``, which the next
+    replay overwrites.  Every step of the path stays on the device (expert
+    offsets included), so one capture serves any routing.  The graph keeps
+    its intermediates in its own memory pool.
+    """
+
+    def __init__(self, T, w_router, gate_up, down, k, bias=None, sh_gate_up=None, sh_down=None,
+                 fused_gather=False):
+        H = w_router.shape[0]
+        self.args = (w_router, gate_up, down, k, bias, sh_gate_up, sh_down)
+        self.fused_gather = fused_gather
+        self.x = torch.zeros((T, H), dtype=torch.bfloat16, device=w_router.device)
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):          # one-time library set-up happens outside the capture
+            for _ in range(2):
+                self._forward()
+        torch.cuda.current_stream().wait_stream(side)
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph):
+            self.y = self._forward()
+
+    def _forward(self):
+        w_router, gate_up, down, k, bias, sh_gu, sh_dn = self.args
+        y, _ = moe_forward(self.x, w_router, gate_up, down, k, bias, sh_gu, sh_dn,
+                           fused_gather=self.fused_gather)
+        return y
+
+    def replay(self):
+        """Runs the layer on the current contents of ``x``; returns ``y``."""
+        self.graph.replay()
+        return self.y
+
+    def __call__(self, x):
+        self.x.copy_(x)
+        return self.replay()
+
+
 class PipelinedForward:
     """The forward over a stream of host batches, with copies overlapped.
 
     Batch i's layer runs on the compute stream while batch i+1's tokens are
     copied host -> device and batch i-1's output device -> host on a copy
-    stream (double-buffered device tensors, events between the streams).
-    Host tensors must be pinned for the copies to be asynchronous.
+    stream (events between the streams).  The layer runs as one of two
+    ForwardGraph replays, one per input buffer.  Host tensors must be pinned
+    for the copies to be asynchronous; every batch has the token count the
+    graphs were captured for.
     """
 
-    def __init__(self, w_router, gate_up, down, k, bias=None, sh_gate_up=None, sh_down=None,
+    def __init__(self, T, w_router, gate_up, down, k, bias=None, sh_gate_up=None, sh_down=None,
                  fused_gather=False):
-        self.args = (w_router, gate_up, down, k, bias, sh_gate_up, sh_down)
-        self.fused_gather = fused_gather
+        self.graphs = [ForwardGraph(T, w_router, gate_up, down, k, bias, sh_gate_up, sh_down,
+                                    fused_gather) for _ in range(2)]
         self.copy_stream = torch.cuda.Stream()
-        self.x_dev = [None, None]
         self.ev_loaded = [torch.cuda.Event(), torch.cuda.Event()]
         self.ev_done = [torch.cuda.Event(), torch.cuda.Event()]
         self.ev_stored = [torch.cuda.Event(), torch.cuda.Event()]
 
     def run(self, x_host_batches, y_host_batches):
         """y_host_batches[i] <- layer(x_host_batches[i]); returns when all are stored."""
-        w_router, gate_up, down, k, bias, sh_gu, sh_dn = self.args
         compute = torch.cuda.current_stream()
         n = len(x_host_batches)
         for b in range(2):
@@ -162,12 +206,9 @@ class PipelinedForward:
 
         def load(i):
             b = i % 2
-            xh = x_host_batches[i]
-            if self.x_dev[b] is None or self.x_dev[b].shape != xh.shape:
-                self.x_dev[b] = torch.empty(xh.shape, dtype=xh.dtype, device=w_router.device)
             with torch.cuda.stream(self.copy_stream):
                 self.copy_stream.wait_event(self.ev_done[b])     # the layer no longer reads it
-                self.x_dev[b].copy_(xh, non_blocking=True)
+                self.graphs[b].x.copy_(x_host_batches[i], non_blocking=True)
                 self.ev_loaded[b].record(self.copy_stream)
 
         if n:
@@ -178,13 +219,11 @@ class PipelinedForward:
                 load(i + 1)
             compute.wait_event(self.ev_loaded[b])
             compute.wait_event(self.ev_stored[b])                # batch i-2's output was copied out
-            y, _ = moe_forward(self.x_dev[b], w_router, gate_up, down, k, bias, sh_gu, sh_dn,
-                               fused_gather=self.fused_gather)
+            y = self.graphs[b].replay()
             self.ev_done[b].record(compute)
             with torch.cuda.stream(self.copy_stream):
                 self.copy_stream.wait_event(self.ev_done[b])
                 y_host_batches[i].copy_(y, non_blocking=True)
-                y.record_stream(self.copy_stream)
                 self.ev_stored[b].record(self.copy_stream)
         self.copy_stream.synchronize()
         compute.synchronize()
