@@ -72,6 +72,14 @@ int moe_sync_status(void* stream, uint32_t* detail);
  * default.  Not thread-safe against concurrent launches. */
 int moe_set_wait_limit_ns(uint64_t ns);
 
+/* Where the forward and dgrad grouped GEMMs run: 0 (default) on single CTAs
+ * (128- or 256-row tiles), 1 on CTA pairs (clusters of two CTAs issuing 2-SM
+ * tcgen05 MMAs on 256-row tiles, 128-row tails as M = 128 pair MMAs; each
+ * CTA holds half of every operand tile).  Results are bit-identical either
+ * way; on GB300 at the Qwen3-MoE shapes the two measure within 3%.  Applies
+ * to launches after the call; not thread-safe against them. */
+int moe_set_gemm_pairs(int on);
+
 /* Test hook of the failure-detection path: while on (1), the grouped GEMMs
  * launched afterwards issue no operand loads, so their MMA warp's bounded
  * wait runs out; the kernel then records MOE_ERR_TIMEOUT, stops its other
@@ -214,7 +222,7 @@ int moe_unpermute_combine_bwd(const uint16_t* dy, const int32_t* src_row, int64_
                               int64_t k, uint16_t* dy_perm, void* stream);
 
 /* Number of partial sums per permuted row that moe_grouped_gemm_down_bwd
- * writes into dw_part (two per 256-column tile of I). */
+ * writes into dw_part (one per 64 columns of I: I / 64). */
 int moe_grouped_gemm_down_bwd_parts(int64_t I, int64_t* nparts);
 
 /* Backward of the down GEMM and of the SwiGLU, per expert e:

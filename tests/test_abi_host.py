@@ -120,7 +120,7 @@ def test_gemm_validation(lib):
     assert b1(FAKE, FAKE, FAKE, None, FAKE, FAKE, 128, 128, 8, 64, FAKE, FAKE, FAKE, None) == INVALID
     assert b1(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 128, 128, 8, 64, FAKE, FAKE, None, None) == INVALID
     n = ctypes.c_int64(0)
-    assert lib.moe_grouped_gemm_down_bwd_parts(768, ctypes.byref(n)) == 0 and n.value == 6
+    assert lib.moe_grouped_gemm_down_bwd_parts(768, ctypes.byref(n)) == 0 and n.value == 12
     b2 = lib.moe_grouped_gemm_gate_up_bwd
     assert b2(FAKE, FAKE, FAKE, FAKE, FAKE, 64, 128, 128, 8, 64, FAKE, None, None) == INVALID
 

@@ -229,3 +229,26 @@ def test_forward_graph_replays_match_forward():
         y_eager, _ = moe.moe_forward(x, wr, gu, dn, cfg.k, None, sgu, sdn)
         moe.sync_status()
         assert torch_equal(y_graph, y_eager)
+
+
+@pytest.mark.parametrize("fused", ["rows", "tma"])
+@pytest.mark.parametrize("T,H,E,k,I", SMALL + [(4096, 256, 16, 2, 192)])
+def test_cta_pairs_bit_identical(T, H, E, k, I, fused):
+    """The grouped GEMMs on CTA pairs (2-SM MMAs, 256-row tiles, M = 128 pair
+    MMAs for tails of up to 128 rows) give the single-CTA results bit for bit:
+    forward with saved activations and the whole backward."""
+    import torch
+    moe = lib()
+    cfg, inp = _inputs(T, H, E, k, I, seed=5 * T + I)
+    outs = []
+    for pairs in (False, True):
+        moe.set_gemm_pairs(pairs)
+        try:
+            (x, wr, gu, dn), y, st = _forward(moe, inp, save=True, fused=fused)
+            g = moe.moe_backward(bf(inp.dy), st, wr, gu, dn)
+            moe.sync_status()
+        finally:
+            moe.set_gemm_pairs(False)
+        outs.append([y, st.h, st.gu_pre, st.h_w, st.y_perm] + [g[n] for n in sorted(g)])
+    for a, b in zip(*outs):
+        assert torch_equal(a, b)

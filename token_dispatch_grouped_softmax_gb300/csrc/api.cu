@@ -17,6 +17,7 @@ DeviceInfo g_dev[kMaxDevices];
 bool g_dev_ready[kMaxDevices] = {false};
 uint64_t g_wait_limit_ns = 2000000000ull;
 int g_test_stall_producer = 0;
+int g_gemm_pairs = 0;
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
@@ -39,6 +40,7 @@ int current_device(DeviceInfo* out) {
   *out = g_dev[dev];
   out->wait_limit_ns = g_wait_limit_ns;
   out->test_stall_producer = g_test_stall_producer;
+  out->gemm_pairs = g_gemm_pairs;
   return MOE_OK;
 }
 
@@ -102,6 +104,11 @@ const char* moe_error_string(int status) {
 
 int moe_set_wait_limit_ns(uint64_t ns) {
   moe::g_wait_limit_ns = ns ? ns : 2000000000ull;
+  return MOE_OK;
+}
+
+int moe_set_gemm_pairs(int on) {
+  moe::g_gemm_pairs = on ? 1 : 0;
   return MOE_OK;
 }
 

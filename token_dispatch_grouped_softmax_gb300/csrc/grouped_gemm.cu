@@ -76,8 +76,9 @@ constexpr int MN_CHUNK_BYTES = 64 * 128;           // one 64-wide MN chunk x 64 
 enum Mode { FWD_GATEUP = 0, FWD_DOWN = 1, DGRAD_DOWN = 2, DGRAD_GATEUP = 3, WGRAD_DOWN = 4,
             WGRAD_GATEUP = 5, ROUTER = 6 };
 
-// KH: 128-row halves per tile (1 or 2)
-template <int MODE, int KH>
+// KH: 128-row halves per CTA (1 or 2); CG: CTAs per tile (1, or 2: a CTA
+// pair issuing 2-SM MMAs, one 128-row half per CTA)
+template <int MODE, int KH, int CG>
 struct Traits {
   static constexpr bool kGateUp = (MODE == FWD_GATEUP);
   static constexpr bool kAMN = (MODE == WGRAD_DOWN || MODE == WGRAD_GATEUP);
@@ -85,20 +86,29 @@ struct Traits {
                                 MODE == WGRAD_GATEUP || MODE == ROUTER);
   static constexpr bool kKGrouped = (MODE == WGRAD_DOWN || MODE == WGRAD_GATEUP);
   static constexpr bool kRouter = (MODE == ROUTER);
-  // One half for the epilogues with per-element math (SwiGLU, its backward),
-  // which then overlap with the next tile's MMAs through two accumulators,
-  // and for the router (few, narrow tiles: its K is split instead); two for
-  // the wgrad GEMMs; either for the plain bf16-store GEMMs (the host picks).
+  // One half per CTA for the epilogues with per-element math (SwiGLU, its
+  // backward), which then overlap with the next tile's MMAs through two
+  // accumulators, and for the router (few, narrow tiles: its K is split
+  // instead); either for the plain bf16-store GEMMs.  A CTA pair holds one
+  // half per CTA and half of each B tile, so a 256 x 256 tile moves 32 KB per
+  // CTA per K block and keeps two accumulators.  (The weight-gradient GEMMs
+  // zero a tile's K rows past its expert in shared memory once the copies
+  // have landed, which the second CTA of a pair cannot see: they run on
+  // single CTAs.)
   static_assert(KH == 1 || KH == 2, "one or two halves");
+  static_assert(CG == 1 || CG == 2, "one CTA or a pair");
   static_assert(KH == 1 || (MODE != FWD_GATEUP && MODE != DGRAD_DOWN && MODE != ROUTER),
                 "per-element epilogues use one half");
-  static_assert(KH == 2 || (MODE != WGRAD_DOWN && MODE != WGRAD_GATEUP), "wgrad uses two halves");
+  static_assert(CG == 1 || (KH == 1 && MODE != ROUTER && MODE != WGRAD_DOWN && MODE != WGRAD_GATEUP),
+                "a pair holds one half per CTA; the router and wgrad run on single CTAs");
+  static_assert(KH == 2 || (MODE != WGRAD_DOWN && MODE != WGRAD_GATEUP), "wgrad uses 256-row tiles");
   static constexpr int kH = KH;
-  static constexpr int kBM = kH * BMH;
+  static constexpr int kBM = kH * BMH * CG;          // rows of a tile
   static constexpr int kAccBufs = 2 / kH;
-  static constexpr int kABytes = kH * A_HALF_BYTES;
-  static constexpr int kStageBytes = kABytes + B_BYTES;
-  static constexpr int kStages = RING_BYTES / kStageBytes;
+  static constexpr int kABytes = kH * A_HALF_BYTES;  // per CTA
+  static constexpr int kBBytes = B_BYTES / CG;       // per CTA: a pair splits the N columns
+  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kStages = RING_BYTES / kStageBytes;   // 4, 3, or 6 for a pair
   // read the accumulators into registers (bf16), free them, then store
   static constexpr bool kEarlyRelease = (kH == 2);
   // warp 0 TMA producer, warp 1 MMA issuer, then the epilogue warps
@@ -115,8 +125,8 @@ struct GemmParams {   // 64-byte aligned through its CUtensorMap members
   uint16_t* out;
   float* out_gu;            // FWD_GATEUP: fp32 pre-activations g | u [R, 2I] (nullable)
   uint16_t* out_hw;         // FWD_GATEUP: bf16(w_row * h) [R, I] (nullable, needs wrow)
-  float* out_part;          // DGRAD_DOWN: per (row, 128-column block) partial of <dY . Wd^T, h>
-                            // [R, 2 nt]; ROUTER: fp32 partial logits [parts, rows, n_out]
+  float* out_part;          // DGRAD_DOWN: per (row, 64-column block of I) partial of
+                            // <dY . Wd^T, h> [R, I/64]; ROUTER: fp32 partial logits [parts, rows, n_out]
   uint32_t* status;
   uint64_t wait_limit_ns;
   int rows;                 // permuted rows R
@@ -142,16 +152,16 @@ __device__ __forceinline__ uint64_t umma_desc(uint32_t saddr, uint32_t lbo, uint
   return d;
 }
 
-template <int MODE, int KH>
-__device__ __forceinline__ uint32_t make_idesc() {
-  using Tr = Traits<MODE, KH>;
+template <int MODE, int KH, int CG>
+__device__ __forceinline__ uint32_t make_idesc(int m = BMH * CG) {
+  using Tr = Traits<MODE, KH, CG>;
   return (1u << 4)                       // D: fp32
          | (1u << 7)                     // A: bf16
          | (1u << 10)                    // B: bf16
          | ((Tr::kAMN ? 1u : 0u) << 15)  // A major: 0 = K, 1 = MN
          | ((Tr::kBMN ? 1u : 0u) << 16)  // B major
          | ((uint32_t)(BN >> 3) << 17)   // N
-         | ((uint32_t)(BMH >> 4) << 24); // M (one half)
+         | ((uint32_t)(m >> 4) << 24);   // M: one half, or 256 (128 for a half tile) over a pair
 }
 
 struct Tile {
@@ -160,6 +170,7 @@ struct Tile {
   int rows;       // M-grouped: valid rows in the tile; K-grouped: K extent of the expert
   int kblocks;
   int halves;     // 128-row halves that carry valid output rows
+  int half;       // a pair's tile of at most 128 rows: one M = 128 pair MMA, 64 rows per CTA
 };
 
 __device__ __forceinline__ void group_range(const GemmParams& p, int e, int& start, int& count) {
@@ -172,10 +183,11 @@ __device__ __forceinline__ void group_range(const GemmParams& p, int e, int& sta
   }
 }
 
-template <int MODE, int KH>
+template <int MODE, int KH, int CG>
 __device__ __forceinline__ Tile decode_tile(const GemmParams& p, const int* prefix, int tile) {
-  using Tr = Traits<MODE, KH>;
+  using Tr = Traits<MODE, KH, CG>;
   Tile t;
+  t.half = 0;
   if (Tr::kRouter) {   // e = K part; rows of x in order; K range [e*K, (e+1)*K)
     const int per = p.mt_w * p.nt;
     t.e = tile / per;
@@ -194,7 +206,7 @@ __device__ __forceinline__ Tile decode_tile(const GemmParams& p, const int* pref
     t.nt = local - t.mt * p.nt;
     group_range(p, t.e, t.row0, t.rows);
     t.kblocks = (t.rows + BK - 1) / BK;
-    t.halves = (Tr::kH == 2 && p.m_w - t.mt * Tr::kBM > BMH) ? 2 : 1;
+    t.halves = (Tr::kBM == 2 * BMH && p.m_w - t.mt * Tr::kBM > BMH) ? 2 : 1;
   } else {
     int lo = 0, hi = p.E - 1;    // largest e with prefix[e] <= tile
     while (lo < hi) {
@@ -210,17 +222,20 @@ __device__ __forceinline__ Tile decode_tile(const GemmParams& p, const int* pref
     t.row0 = start + t.mt * Tr::kBM;
     t.rows = min(Tr::kBM, count - t.mt * Tr::kBM);
     t.kblocks = p.K / BK;
-    t.halves = (Tr::kH == 2 && t.rows > BMH) ? 2 : 1;
+    t.halves = (Tr::kBM == 2 * BMH && t.rows > BMH) ? 2 : 1;
+    t.half = (CG == 2 && t.rows <= BMH) ? 1 : 0;
   }
   return t;
 }
 
-// Zero row m of an empty expert's weight-gradient tile (K-grouped modes).
-__device__ __forceinline__ void store_zero_rows(const GemmParams& p, const Tile& t, int m) {
+// Zero columns [c_lo, c_hi) of row m of an empty expert's weight-gradient
+// tile (K-grouped modes).
+__device__ __forceinline__ void store_zero_rows(const GemmParams& p, const Tile& t, int m, int c_lo,
+                                               int c_hi) {
   if (m >= p.m_w) return;
   uint16_t* orow = p.out + ((int64_t)t.e * p.m_w + m) * p.ldo + (int64_t)t.nt * BN;
   const uint4 z = make_uint4(0, 0, 0, 0);
-  for (int c = 0; c < BN; c += 8)
+  for (int c = c_lo; c < c_hi; c += 8)
     if (t.nt * BN + c < p.n_out) *reinterpret_cast<uint4*>(orow + c) = z;
 }
 
@@ -297,30 +312,53 @@ __device__ __forceinline__ void load_block128(const uint8_t* base, int64_t ld, u
 }
 
 // The copies of one K block of a tile: A (KH halves or MN chunks) and B into
-// the stage at sA / sB, completing on the barrier fb.  Warp-wide: gathered
-// loads spread over the lanes, the others are issued by lane 0.
-template <int MODE, int KH>
+// the stage at sA / sB, completing on the barrier fb.  In a CTA pair, CTA
+// `crank` copies its own 128 rows of A and its half of the B columns (chunks
+// 2 crank, 2 crank + 1 of the tile's four 64-wide chunks) into its own
+// stage; the bytes of both count on rank 0's barrier.
+// Warp-wide: gathered loads spread over the lanes, the others are issued by
+// lane 0.
+template <int MODE, int KH, int CG>
 __device__ __forceinline__ void stage_loads(const GemmParams& p, const Tile& t, int kb, uint32_t sA,
-                                            uint32_t sB, uint32_t fb, int lane, const int (&gi)[KH][4],
-                                            uint64_t keep_x) {
-  using Tr = Traits<MODE, KH>;
+                                            uint32_t sB, uint32_t fb, int lane, int crank,
+                                            const int (&gi)[KH][4], uint64_t keep_x) {
+  using Tr = Traits<MODE, KH, CG>;
+  // a pair's copies count on rank 0's barrier (fb is its shared::cluster address)
+  auto tma_load_2d = [&](uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
+    if (CG == 2) tma_load_2d_pair(dst, map, x, y, bar);
+    else ::moe::tma_load_2d(dst, map, x, y, bar);
+  };
+  auto tma_gather4_hint = [&](uint32_t dst, const CUtensorMap* map, int x, int r0, int r1, int r2, int r3,
+                              uint32_t bar, uint64_t pol) {
+    if (CG == 2) tma_gather4_pair_hint(dst, map, x, r0, r1, r2, r3, bar, pol);
+    else ::moe::tma_gather4_hint(dst, map, x, r0, r1, r2, r3, bar, pol);
+  };
   const int k0 = kb * BK;
+  const int ah = CG == 2 ? 1 : t.halves;             // A halves this CTA loads
+  // M-grouped: its first A row (a pair's half tile: 64 rows per CTA, of which
+  // the 128-row box brings the first 64 into use)
+  const int arow0 = t.row0 + crank * (t.half ? BMH / 2 : BMH);
+  const int c0 = CG == 2 ? 2 * crank : 0;            // its first B chunk of the tile
+  const int nc = CG == 2 ? 2 : 4;
   if (Tr::kGateUp) {
     if (p.gidx) {                                    // permute fused into the load (TMA)
-      for (int h = 0; h < t.halves; ++h)
+      for (int h = 0; h < ah; ++h)
         tma_gather4_hint(sA + h * A_HALF_BYTES + 4 * lane * 128, &p.tmA, k0, gi[h][0], gi[h][1],
                          gi[h][2], gi[h][3], fb, keep_x);
     } else if (lane == 0) {                          // rows already in permuted order
-      for (int h = 0; h < t.halves; ++h)
-        tma_load_2d(sA + h * A_HALF_BYTES, &p.tmA, k0, t.row0 + h * BMH, fb);
+      for (int h = 0; h < ah; ++h)
+        tma_load_2d(sA + h * A_HALF_BYTES, &p.tmA, k0, arow0 + h * BMH, fb);
     }
     if (lane == 0) {
       const int brow = t.e * p.K + k0;               // gate_up rows of expert e
-      const int n0 = t.nt * 128;
-      tma_load_2d(sB + 0 * MN_CHUNK_BYTES, &p.tmB, n0, brow, fb);
-      tma_load_2d(sB + 1 * MN_CHUNK_BYTES, &p.tmB, n0 + 64, brow, fb);
-      tma_load_2d(sB + 2 * MN_CHUNK_BYTES, &p.tmB, p.I + n0, brow, fb);
-      tma_load_2d(sB + 3 * MN_CHUNK_BYTES, &p.tmB, p.I + n0 + 64, brow, fb);
+      const int n0 = t.nt * 128;                     // chunks: gate n0, n0+64; up I+n0, I+n0+64
+      for (int c = 0; c < nc; ++c) {
+        // a pair's half tile folds each CTA's 256 columns into two TMEM lane
+        // halves of 128: CTA r takes gate and up chunk r, so that a row's
+        // gate and up columns share a TMEM lane
+        const int cc = (CG == 2 && t.half) ? (c == 0 ? crank : 2 + crank) : c0 + c;
+        tma_load_2d(sB + c * MN_CHUNK_BYTES, &p.tmB, (cc >> 1) * p.I + n0 + 64 * (cc & 1), brow, fb);
+      }
     }
   } else if (MODE == ROUTER) {
     if (lane == 0) {
@@ -333,28 +371,30 @@ __device__ __forceinline__ void stage_loads(const GemmParams& p, const Tile& t, 
     }
   } else if (MODE == FWD_DOWN) {
     if (lane == 0) {
-      for (int h = 0; h < t.halves; ++h)
-        tma_load_2d(sA + h * A_HALF_BYTES, &p.tmA, k0, t.row0 + h * BMH, fb);
+      for (int h = 0; h < ah; ++h)
+        tma_load_2d(sA + h * A_HALF_BYTES, &p.tmA, k0, arow0 + h * BMH, fb);
       const int brow = t.e * p.K + k0;               // down rows of expert e
       const int n0 = t.nt * BN;
-#pragma unroll
-      for (int c = 0; c < 4; ++c) tma_load_2d(sB + c * MN_CHUNK_BYTES, &p.tmB, n0 + 64 * c, brow, fb);
+      for (int c = 0; c < nc; ++c)
+        tma_load_2d(sB + c * MN_CHUNK_BYTES, &p.tmB, n0 + 64 * (c0 + c), brow, fb);
     }
   } else if (MODE == DGRAD_DOWN || MODE == DGRAD_GATEUP) {
     if (lane == 0) {
-      for (int h = 0; h < t.halves; ++h)
-        tma_load_2d(sA + h * A_HALF_BYTES, &p.tmA, k0, t.row0 + h * BMH, fb);
-      // B^T rows: expert e's block of rows_per_e rows, K-major
+      for (int h = 0; h < ah; ++h)
+        tma_load_2d(sA + h * A_HALF_BYTES, &p.tmA, k0, arow0 + h * BMH, fb);
+      // B^T rows: expert e's block of rows_per_e rows, K-major (one box of
+      // BN / CG rows)
       const int rows_per_e = (MODE == DGRAD_DOWN) ? p.I : p.n_out;
-      tma_load_2d(sB, &p.tmB, k0, t.e * rows_per_e + t.nt * BN, fb);
+      tma_load_2d(sB, &p.tmB, k0, t.e * rows_per_e + t.nt * BN + crank * (BN / 2), fb);
     }
   } else {  // WGRAD_*: A = rows of the expert (K = tokens), MN-major chunks of 64 m
     const int krow = t.row0 + k0;
-    const int m0 = t.mt * Tr::kBM;
+    const int m0 = t.mt * Tr::kBM + crank * BMH;
+    const int ac = CG == 2 ? 2 : 2 * t.halves;      // A chunks this CTA loads
     if (MODE == WGRAD_GATEUP && p.gidx) {            // gathered through src_row
       // lane: MN chunk c = lane >> 3, K rows 8*(lane & 7) .. +7 (two gather4)
       const int c = lane >> 3;
-      if (c < 2 * t.halves) {
+      if (c < ac) {
 #pragma unroll
         for (int q2 = 0; q2 < 2; ++q2) {
           const int kr0 = 8 * (lane & 7) + 4 * q2;
@@ -366,34 +406,57 @@ __device__ __forceinline__ void stage_loads(const GemmParams& p, const Tile& t, 
         }
       }
     } else if (lane == 0) {                          // rows already in permuted order
-      for (int c = 0; c < 2 * t.halves; ++c)
+      for (int c = 0; c < ac; ++c)
         tma_load_2d(sA + c * MN_CHUNK_BYTES, &p.tmA, m0 + 64 * c, krow, fb);
     }
     if (lane == 0) {
       const int n0 = t.nt * BN;
-#pragma unroll
-      for (int c = 0; c < 4; ++c)
-        tma_load_2d(sB + c * MN_CHUNK_BYTES, &p.tmB, n0 + 64 * c, krow, fb);
+      for (int c = 0; c < nc; ++c)
+        tma_load_2d(sB + c * MN_CHUNK_BYTES, &p.tmB, n0 + 64 * (c0 + c), krow, fb);
     }
   }
 }
 
-template <int MODE, int KH>
-__global__ void __launch_bounds__(Traits<MODE, KH>::kThreads, 1)
+// Zeroes the K rows [kvalid, 64) of every 64 x 128-byte chunk of a stage (a
+// weight-gradient tile's last K block may run past its expert's rows).
+// Warp-wide; makes the writes visible to the tensor cores.
+template <int STAGE_BYTES>
+__device__ __forceinline__ void zero_k_tail(uint8_t* stage, int kvalid, int lane) {
+  constexpr int kChunks = STAGE_BYTES / MN_CHUNK_BYTES;
+  const int nrow = BK - kvalid;
+  for (int q = lane; q < nrow * 8 * kChunks; q += 32) {
+    const int chunk = q / (nrow * 8);
+    const int rem = q - chunk * nrow * 8;
+    const int row = kvalid + rem / 8;
+    const int u = rem & 7;
+    *reinterpret_cast<uint4*>(stage + chunk * MN_CHUNK_BYTES + row * 128 + u * 16) = make_uint4(0, 0, 0, 0);
+  }
+  fence_proxy_async_smem();
+  __syncwarp();
+}
+
+template <int MODE, int KH, int CG>
+__global__ void __launch_bounds__(Traits<MODE, KH, CG>::kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ GemmParams p) {
-  using Tr = Traits<MODE, KH>;
+  using Tr = Traits<MODE, KH, CG>;
   constexpr int STAGES = Tr::kStages;
+  constexpr bool kPair = (CG == 2);
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* ring = smem;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + RING_BYTES);
-  // bars: full[STAGES], empty[STAGES], acc_full[2], acc_empty[2], drain (at most 13 of 16)
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 16);
+  // bars: full[STAGES], empty[STAGES], acc_full[2], acc_empty[2], drain (at most 17 of 24)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 24);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   int* prefix = reinterpret_cast<int*>(tmem_slot + 2);   // [E+1]
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  // In a CTA pair: rank 0 issues the MMAs for both; each CTA loads its own
+  // operand halves into its own ring and drains its own 128 TMEM lanes.
+  const int crank = kPair ? (int)cluster_ctarank() : 0;
+  const int tile0 = kPair ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+  const int tile_step = kPair ? (int)(gridDim.x >> 1) : (int)gridDim.x;
   const uint32_t ring_u32 = smem_u32(ring);
   const uint32_t bar_u32 = smem_u32(bars);
   auto full_bar = [&](int s) { return bar_u32 + 8u * s; };
@@ -404,12 +467,14 @@ __global__ void __launch_bounds__(Traits<MODE, KH>::kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
+      // in a pair only rank 0's full barriers are used: its producer arrives
+      // and expects the bytes of both CTAs
       mbar_init(full_bar(s), 1);
       mbar_init(empty_bar(s), 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(accf_bar(b), 1);
-      mbar_init(acce_bar(b), 32 * kEpiWarps);
+      mbar_init(acce_bar(b), kEpiWarps * CG);   // one arrive per epilogue warp (of both CTAs)
     }
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
@@ -420,8 +485,13 @@ __global__ void __launch_bounds__(Traits<MODE, KH>::kThreads, 1)
     tma_prefetch_desc(&p.tmB);
   }
   if (warp == 1) {
-    tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
-    tmem_relinquish();
+    if (kPair) {
+      tmem_alloc_pair(smem_u32(tmem_slot), TMEM_COLS);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(smem_u32(tmem_slot), TMEM_COLS);
+      tmem_relinquish();
+    }
   }
   // Tile prefix over experts (M-grouped modes): prefix[e] = sum_{e'<e} ceil(M_e'/BM) * nt.
   // Tiles go out in expert order, so the row tiles of one expert run at about
@@ -454,6 +524,7 @@ __global__ void __launch_bounds__(Traits<MODE, KH>::kThreads, 1)
   }
   tc_fence_before();
   __syncthreads();
+  if (kPair) cluster_sync_all();   // both CTAs' barriers exist before either signals the other
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   if (!Tr::kKGrouped && !Tr::kRouter) total_tiles = prefix[p.E];
@@ -469,29 +540,31 @@ __global__ void __launch_bounds__(Traits<MODE, KH>::kThreads, 1)
     uint32_t issued_mask = 0;       // stages that ever received a load
     uint32_t last_parity = 0;       // bit s: parity of the last load into stage s
     bool ok = true;
-    for (int tile = blockIdx.x; tile < total_tiles && ok && !p.stall_producer; tile += gridDim.x) {
-      const Tile t = decode_tile<MODE, KH>(p, prefix, tile);
+    for (int tile = tile0; tile < total_tiles && ok && !p.stall_producer; tile += tile_step) {
+      const Tile t = decode_tile<MODE, KH, CG>(p, prefix, tile);
       if (t.kblocks == 0) continue;
       int gi[Tr::kH][4];
-      if (Tr::kGateUp && p.gidx) {   // lane's rows: 4*lane .. +3 of each half
+      if (Tr::kGateUp && p.gidx) {   // lane's rows: 4*lane .. +3 of each of this CTA's halves
 #pragma unroll
         for (int h = 0; h < Tr::kH; ++h)
 #pragma unroll
-          for (int q = 0; q < 4; ++q) gi[h][q] = p.gidx[t.row0 + min(h * BMH + 4 * lane + q, t.rows - 1)];
+          for (int q = 0; q < 4; ++q)
+            gi[h][q] = p.gidx[t.row0 + min(crank * (t.half ? BMH / 2 : BMH) + h * BMH + 4 * lane + q, t.rows - 1)];
       }
-      const uint32_t a_bytes = (uint32_t)(t.halves * A_HALF_BYTES);
+      const uint32_t a_bytes = (uint32_t)((kPair ? 1 : t.halves) * A_HALF_BYTES);
       for (int kb = 0; kb < t.kblocks; ++kb) {
         bool w = true;
         if (lane == 0)
-          w = mbar_wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, p.wait_limit_ns, p.status, 1);
+          w = mbar_wait_bounded<kPair>(empty_bar(stage), phase ^ 1u, abort_flag, p.wait_limit_ns, p.status, 1);
         ok = __shfl_sync(0xffffffffu, w ? 1 : 0, 0) != 0;
         if (!ok) break;
         const uint32_t sA = ring_u32 + stage * Tr::kStageBytes;
         const uint32_t sB = sA + Tr::kABytes;
-        const uint32_t fb = full_bar(stage);
-        if (lane == 0) mbar_arrive_expect_tx(fb, a_bytes + (uint32_t)B_BYTES);
+        const uint32_t fb = (kPair && crank != 0) ? mapa_shared(full_bar(stage), 0) : full_bar(stage);
+        if (lane == 0 && crank == 0)
+          mbar_arrive_expect_tx(fb, (uint32_t)CG * (a_bytes + (uint32_t)Tr::kBBytes));
         __syncwarp();
-        stage_loads<MODE, KH>(p, t, kb, sA, sB, fb, lane, gi, keep_x);
+        stage_loads<MODE, KH, CG>(p, t, kb, sA, sB, fb, lane, crank, gi, keep_x);
         issued_mask |= 1u << stage;
         last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
         if (++stage == STAGES) {
@@ -500,8 +573,9 @@ __global__ void __launch_bounds__(Traits<MODE, KH>::kThreads, 1)
         }
       }
     }
-    if (!ok && lane == 0) {
-      // stopped early: wait (bounded) for the copies still in flight
+    if (!ok && lane == 0 && crank == 0) {
+      // stopped early: wait (bounded) for the copies still in flight (in a
+      // pair rank 0's barriers count both CTAs' copies)
       for (int s = 0; s < STAGES; ++s)
         if (issued_mask & (1u << s)) {
           const uint64_t t0 = globaltimer_ns();
@@ -510,64 +584,59 @@ __global__ void __launch_bounds__(Traits<MODE, KH>::kThreads, 1)
           }
         }
     }
+  } else if (warp == 1 && crank != 0) {
+    // the second CTA of a pair issues no MMAs: rank 0 issues them for both
   } else if (warp == 1) {
     // ------------------------------------------------------- MMA issuer
-    const uint32_t idesc = make_idesc<MODE, KH>();
+    const uint32_t idesc = make_idesc<MODE, KH, CG>();
+    const uint32_t idesc_half = make_idesc<MODE, KH, CG>(BMH);   // a pair's half tile
     int stage = 0;
     uint32_t phase = 0;
     int acc = 0;                 // accumulator buffer (always 0 with two halves)
     uint32_t acc_phase = 0;
     bool ok = true;
     bool issued_any = false;
-    for (int tile = blockIdx.x; tile < total_tiles && ok; tile += gridDim.x) {
-      const Tile t = decode_tile<MODE, KH>(p, prefix, tile);
+    for (int tile = tile0; tile < total_tiles && ok; tile += tile_step) {
+      const Tile t = decode_tile<MODE, KH, CG>(p, prefix, tile);
       if (t.kblocks == 0) continue;
       bool w = true;
-      if (lane == 0)    // the epilogue has drained this accumulator buffer
-        w = mbar_wait_bounded(acce_bar(acc), acc_phase ^ 1u, abort_flag, p.wait_limit_ns, p.status, 2);
+      if (lane == 0)    // the epilogue (of both CTAs) has drained this accumulator buffer
+        w = mbar_wait_bounded<kPair>(acce_bar(acc), acc_phase ^ 1u, abort_flag, p.wait_limit_ns, p.status, 2);
       ok = __shfl_sync(0xffffffffu, w ? 1 : 0, 0) != 0;
       if (!ok) break;
       tc_fence_after();
       for (int kb = 0; kb < t.kblocks; ++kb) {
         if (lane == 0)
-          w = mbar_wait_bounded(full_bar(stage), phase, abort_flag, p.wait_limit_ns, p.status, 3);
+          w = mbar_wait_bounded<kPair>(full_bar(stage), phase, abort_flag, p.wait_limit_ns, p.status, 3);
         ok = __shfl_sync(0xffffffffu, w ? 1 : 0, 0) != 0;
         if (!ok) break;
         const uint32_t sA = ring_u32 + stage * Tr::kStageBytes;
         const uint32_t sB = sA + Tr::kABytes;
-        if (Tr::kKGrouped) {
-          const int kvalid = t.rows - kb * BK;
-          if (kvalid < BK) {   // zero the K rows past the expert's last row (A then B chunks)
-            constexpr int kChunks = (Tr::kABytes + B_BYTES) / MN_CHUNK_BYTES;
-            uint8_t* gA = ring + stage * Tr::kStageBytes;
-            const int nrow = BK - kvalid;
-            for (int q = lane; q < nrow * 8 * kChunks; q += 32) {
-              const int chunk = q / (nrow * 8);
-              const int rem = q - chunk * nrow * 8;
-              const int row = kvalid + rem / 8;
-              const int u = rem & 7;
-              *reinterpret_cast<uint4*>(gA + chunk * MN_CHUNK_BYTES + row * 128 + u * 16) =
-                  make_uint4(0, 0, 0, 0);
-            }
-            fence_proxy_async_smem();
-            __syncwarp();
-          }
-        }
+        if (Tr::kKGrouped && t.rows - kb * BK < BK)   // K rows past the expert's last row
+          zero_k_tail<Tr::kStageBytes>(ring + stage * Tr::kStageBytes, t.rows - kb * BK, lane);
         tc_fence_after();
         if (lane == 0) {
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk) {
             const uint64_t bd = Tr::kBMN ? umma_desc(sB + kk * 2048, MN_CHUNK_BYTES, 1024)
                                          : umma_desc(sB + kk * 32, 16, 1024);
-            for (int h = 0; h < t.halves; ++h) {
-              const uint32_t aBase = sA + h * A_HALF_BYTES;
-              const uint64_t ad = Tr::kAMN ? umma_desc(aBase + kk * 2048, MN_CHUNK_BYTES, 1024)
-                                           : umma_desc(aBase + kk * 32, 16, 1024);
-              tc_mma_bf16(tmem_base + (uint32_t)((acc + h) * BN), ad, bd, idesc,
-                          (kb | kk) != 0 ? 1u : 0u);
+            if (kPair) {   // one M = 256 MMA over both CTAs' halves
+              const uint64_t ad = Tr::kAMN ? umma_desc(sA + kk * 2048, MN_CHUNK_BYTES, 1024)
+                                           : umma_desc(sA + kk * 32, 16, 1024);
+              tc_mma_bf16_pair(tmem_base + (uint32_t)(acc * BN), ad, bd, t.half ? idesc_half : idesc,
+                               (kb | kk) != 0 ? 1u : 0u);
+            } else {
+              for (int h = 0; h < t.halves; ++h) {
+                const uint32_t aBase = sA + h * A_HALF_BYTES;
+                const uint64_t ad = Tr::kAMN ? umma_desc(aBase + kk * 2048, MN_CHUNK_BYTES, 1024)
+                                             : umma_desc(aBase + kk * 32, 16, 1024);
+                tc_mma_bf16(tmem_base + (uint32_t)((acc + h) * BN), ad, bd, idesc,
+                            (kb | kk) != 0 ? 1u : 0u);
+              }
             }
           }
-          tc_commit(empty_bar(stage));
+          if (kPair) tc_commit_pair(empty_bar(stage), 3);   // frees the stage in both CTAs
+          else tc_commit(empty_bar(stage));
         }
         issued_any = true;
         __syncwarp();
@@ -577,7 +646,10 @@ __global__ void __launch_bounds__(Traits<MODE, KH>::kThreads, 1)
         }
       }
       if (!ok) break;
-      if (lane == 0) tc_commit(accf_bar(acc));
+      if (lane == 0) {
+        if (kPair) tc_commit_pair(accf_bar(acc), 3);
+        else tc_commit(accf_bar(acc));
+      }
       __syncwarp();
       if (++acc == Tr::kAccBufs) {
         acc = 0;
@@ -586,7 +658,8 @@ __global__ void __launch_bounds__(Traits<MODE, KH>::kThreads, 1)
     }
     if (!ok && issued_any && lane == 0) {
       // stopped early: make sure every MMA issued has finished before TMEM is freed
-      tc_commit(drain_bar);
+      if (kPair) tc_commit_pair(drain_bar, 1);
+      else tc_commit(drain_bar);
       const uint64_t t0 = globaltimer_ns();
       while (!mbar_try_wait(drain_bar, 0) && globaltimer_ns() - t0 < p.wait_limit_ns) {
       }
@@ -595,22 +668,36 @@ __global__ void __launch_bounds__(Traits<MODE, KH>::kThreads, 1)
     // ---------------------------------------------------------- epilogue
     // Each warp reads the TMEM lane quarter its rank allows (warp % 4).  With
     // two halves warpgroup wg drains half wg (all 256 columns); with one,
-    // warpgroup wg takes columns [128 wg, 128 wg + 128) of the single half.
+    // warpgroup wg takes columns [128 wg, 128 wg + 128) of the single half
+    // (in a pair: of this CTA's 128 rows of the 256-row tile).
     const int quarter = warp & 3;                     // TMEM lanes 32*quarter .. +31
     const int wg = (warp - 2) >> 2;
     const int half = Tr::kH == 2 ? wg : 0;
-    const int r = half * BMH + quarter * 32 + lane;   // tile row of this thread
+    const int rbase = crank * BMH;                    // this CTA's first row of the tile
+    const int r = rbase + half * BMH + quarter * 32 + lane;   // tile row of this thread
+    // a warp's arrive that frees an accumulator buffer (rank 0's barrier in a pair)
+    auto release = [&](uint32_t bar) {
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        if (kPair && crank != 0) mbar_arrive_cluster(mapa_shared(bar, 0));
+        else mbar_arrive(bar);
+      }
+    };
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
-      const Tile t = decode_tile<MODE, KH>(p, prefix, tile);
+    for (int tile = tile0; tile < total_tiles; tile += tile_step) {
+      const Tile t = decode_tile<MODE, KH, CG>(p, prefix, tile);
       if (t.kblocks == 0) {
-        if (Tr::kKGrouped) store_zero_rows(p, t, t.mt * Tr::kBM + r);
+        if (Tr::kKGrouped) {   // an empty expert: zero its weight-gradient tile
+          if (Tr::kH == 2) store_zero_rows(p, t, t.mt * Tr::kBM + r, 0, BN);
+          else store_zero_rows(p, t, t.mt * Tr::kBM + r, 128 * wg, 128 * wg + 128);
+        }
         continue;
       }
       bool w = true;
       if (lane == 0)
-        w = mbar_wait_bounded(accf_bar(acc), acc_phase, abort_flag, p.wait_limit_ns, p.status, 4);
+        w = mbar_wait_bounded<kPair>(accf_bar(acc), acc_phase, abort_flag, p.wait_limit_ns, p.status, 4);
       if (__shfl_sync(0xffffffffu, w ? 1 : 0, 0) == 0) break;
       tc_fence_after();
       const bool active = half < t.halves;     // warp-uniform
@@ -621,8 +708,13 @@ __global__ void __launch_bounds__(Traits<MODE, KH>::kThreads, 1)
         acc_phase ^= 1u;
       }
       // Rows of this warp: 32 consecutive tile rows starting at wrow (one
-      // per lane); stores go through store_block128 (whole 128-byte rows).
-      const int wrow = half * BMH + quarter * 32;
+      // per lane); stores go through store_block (whole row segments).  A
+      // pair's half tile folds each CTA's 64 rows x 256 columns into TMEM
+      // lanes: lane L holds row 64 r + L % 64, columns 128 (L / 64) .. +127
+      // in TMEM columns 0..127 (nh = L / 64 for this warp).
+      const bool ht = kPair && t.half;   // warp-uniform
+      const int nh = quarter >> 1;
+      const int wrow = ht ? crank * (BMH / 2) + 32 * (quarter & 1) : rbase + half * BMH + quarter * 32;
       float v[32];
       if (Tr::kEarlyRelease) {
         // read the whole row into registers as bf16 (16 columns at a time:
@@ -637,8 +729,7 @@ __global__ void __launch_bounds__(Traits<MODE, KH>::kThreads, 1)
             for (int q = 0; q < 8; ++q) pk[8 * c + q] = pack_bf16x2(v[2 * q], v[2 * q + 1]);
           }
         }
-        tc_fence_before();
-        mbar_arrive(done);
+        release(done);
         if (active) {
           uint8_t* base;
           uint32_t row_mask;
@@ -662,21 +753,25 @@ __global__ void __launch_bounds__(Traits<MODE, KH>::kThreads, 1)
         // this half carries no rows of the tile: nothing to read or store
       } else if (MODE == FWD_GATEUP) {
         // warpgroup wg: h columns [64 wg, 64 wg + 64) of the tile (gate and
-        // up accumulator columns c and 128 + c)
+        // up accumulator columns c and 128 + c); in a pair's half tile h
+        // columns 64 nh + [32 wg, 32 wg + 32) (gate at TMEM column c, up at
+        // 64 + c)
         const uint32_t row_mask = __ballot_sync(0xffffffffu, wrow + lane < t.rows);
         const int64_t row0 = t.row0 + wrow;
-        const int n0 = t.nt * 128 + 64 * wg;               // first h column
-        if (n0 < p.n_out) {
+        {
           const bool row_ok = wrow + lane < t.rows;
           const float wr = (p.out_hw && row_ok) ? p.wrow[row0 + lane] : 0.f;
 #pragma unroll 1
-          for (int c = 0; c < 2; ++c) {                    // 32 h columns at a time
-            const int col = n0 + 32 * c;
+          for (int c = 0; c < (ht ? 1 : 2); ++c) {         // 32 h columns at a time
+            const int gcol = ht ? 32 * wg : 64 * wg + 32 * c;            // TMEM column of the gate values
+            const int ucol = ht ? 64 + 32 * wg : 128 + 64 * wg + 32 * c;  // ... of the up values
+            const int col = t.nt * 128 + (ht ? 64 * nh + 32 * wg : 64 * wg + 32 * c);   // h column
+            if (col >= p.n_out) break;                     // warp-uniform
             uint32_t bits[32];
             if (p.out_gu) {                                // fp32 pre-activations g | u, 128-byte blocks
 #pragma unroll
               for (int gu = 0; gu < 2; ++gu) {
-                tmem_ld32(taddr + 128 * gu + 64 * wg + 32 * c, v);
+                tmem_ld32(taddr + (gu ? ucol : gcol), v);
 #pragma unroll
                 for (int q = 0; q < 32; ++q) bits[q] = __float_as_uint(v[q]);
                 store_block128(reinterpret_cast<uint8_t*>(p.out_gu + row0 * 2 * p.I + gu * p.I + col), 8 * p.I,
@@ -684,8 +779,8 @@ __global__ void __launch_bounds__(Traits<MODE, KH>::kThreads, 1)
               }
             }
             float u[32];
-            tmem_ld32(taddr + 64 * wg + 32 * c, v);        // gate columns
-            tmem_ld32(taddr + 128 + 64 * wg + 32 * c, u);  // up columns
+            tmem_ld32(taddr + gcol, v);                    // gate columns
+            tmem_ld32(taddr + ucol, u);                    // up columns
             // bits[0..15]: h, bits[16..31]: w * h (bf16 pairs)
 #pragma unroll
             for (int q = 0; q < 16; ++q) {
@@ -718,17 +813,27 @@ __global__ void __launch_bounds__(Traits<MODE, KH>::kThreads, 1)
             }
           }
         }
-      } else if (MODE == FWD_DOWN || MODE == DGRAD_GATEUP) {   // one half: column half wg
-        const uint32_t row_mask = __ballot_sync(0xffffffffu, wrow + lane < t.rows);
-        const int n0 = t.nt * BN + 128 * wg;
-        uint8_t* base = reinterpret_cast<uint8_t*>(p.out + (int64_t)(t.row0 + wrow) * p.ldo + n0);
+      } else if (MODE == FWD_DOWN || MODE == DGRAD_GATEUP || Tr::kKGrouped) {   // one half: column half wg
+        // (a pair's half tile: columns 128 nh + [64 wg, 64 wg + 64), one block)
+        const int n0 = t.nt * BN + (ht ? 128 * nh + 64 * wg : 128 * wg);
+        const int tc0 = ht ? 64 * wg : 128 * wg;         // TMEM column of the first block
+        uint32_t row_mask;
+        uint8_t* base;
+        if (Tr::kKGrouped) {   // rows m = mt*BM + r of expert e's weight-gradient block
+          const int m0 = t.mt * Tr::kBM + wrow;
+          row_mask = __ballot_sync(0xffffffffu, m0 + lane < p.m_w);
+          base = reinterpret_cast<uint8_t*>(p.out + ((int64_t)t.e * p.m_w + m0) * p.ldo + n0);
+        } else {
+          row_mask = __ballot_sync(0xffffffffu, wrow + lane < t.rows);
+          base = reinterpret_cast<uint8_t*>(p.out + (int64_t)(t.row0 + wrow) * p.ldo + n0);
+        }
 #pragma unroll 1
-        for (int blk = 0; blk < 2; ++blk) {
+        for (int blk = 0; blk < (ht ? 1 : 2); ++blk) {
           if (n0 + 64 * blk >= p.n_out) break;
           uint32_t pk[32];
 #pragma unroll
           for (int c = 0; c < 2; ++c) {
-            tmem_ld32(taddr + 128 * wg + 64 * blk + 32 * c, v);
+            tmem_ld32(taddr + tc0 + 64 * blk + 32 * c, v);
 #pragma unroll
             for (int q = 0; q < 16; ++q) pk[16 * c + q] = pack_bf16x2(v[2 * q], v[2 * q + 1]);
           }
@@ -739,16 +844,20 @@ __global__ void __launch_bounds__(Traits<MODE, KH>::kThreads, 1)
         const uint32_t row_mask = __ballot_sync(0xffffffffu, row_ok);
         const int64_t row = t.row0 + wrow + lane;
         const int64_t row0 = t.row0 + wrow;
-        const int n0 = t.nt * BN + 128 * wg;
+        // columns as in the bf16 path: 128 wg + [0, 128), or in a pair's half
+        // tile 128 nh + 64 wg + [0, 64)
+        const int n0 = t.nt * BN + (ht ? 128 * nh + 64 * wg : 128 * wg);
+        const int tc0 = ht ? 64 * wg : 128 * wg;
+        const int nparts = (p.n_out + 63) / 64;          // one dw partial per 64 columns
         const float wr = row_ok ? p.wrow[row] : 0.f;     // dh = w * (dY . Wd^T)
-        float dot = 0.f;                                 // <dY . Wd^T, h> over this thread's columns
+        float dot = 0.f;                                 // <dY . Wd^T, h> over a 64-column block
         const uint8_t* aux0 = reinterpret_cast<const uint8_t*>(p.aux + row0 * 2 * p.I);
         uint8_t* out0 = reinterpret_cast<uint8_t*>(p.out + row0 * 2 * p.I);
 #pragma unroll 1
-        for (int c = 0; c < 4; ++c) {                    // 32 columns at a time
+        for (int c = 0; c < (ht ? 2 : 4); ++c) {         // 32 columns at a time
           const int col = n0 + 32 * c;
-          if (col >= p.n_out) break;
-          tmem_ld32(taddr + 128 * wg + 32 * c, v);       // dY . Wd^T (fp32)
+          if (col >= p.n_out) break;                     // blocks of 64 are whole (I % 64 == 0)
+          tmem_ld32(taddr + tc0 + 32 * c, v);            // dY . Wd^T (fp32)
           uint32_t gb[32], ub[32];                       // the row's fp32 pre-activations g | u
           load_block128(aux0 + 4 * col, 8 * p.I, gb, lane, row_mask);
           load_block128(aux0 + 4 * (p.I + col), 8 * p.I, ub, lane, row_mask);
@@ -770,40 +879,72 @@ __global__ void __launch_bounds__(Traits<MODE, KH>::kThreads, 1)
           }
           store_block<4>(out0 + 2 * col, 4 * p.I, dg, lane, row_mask);
           store_block<4>(out0 + 2 * (p.I + col), 4 * p.I, du, lane, row_mask);
+          if (c & 1) {                                   // a 64-column block is done
+            if (row_ok && p.out_part) p.out_part[row * nparts + col / 64] = dot;
+            dot = 0.f;
+          }
         }
-        if (row_ok && p.out_part) p.out_part[row * 2 * p.nt + 2 * t.nt + wg] = dot;
       }
-      tc_fence_before();
-      mbar_arrive(done);
+      release(done);
     }
   }
 
   tc_fence_before();
   __syncthreads();
+  if (kPair) cluster_sync_all();   // neither CTA frees TMEM or leaves while the other may signal it
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, TMEM_COLS);
+    if (kPair) tmem_dealloc_pair(tmem_base, TMEM_COLS);
+    else tmem_dealloc(tmem_base, TMEM_COLS);
   }
 }
 
-size_t gemm_smem_bytes(int E) { return 1024 + (size_t)RING_BYTES + 8 * 16 + 16 + 4 * (size_t)(E + 1) + 64; }
+size_t gemm_smem_bytes(int E) { return 1024 + (size_t)RING_BYTES + 8 * 24 + 16 + 4 * (size_t)(E + 1) + 64; }
 
-template <int MODE, int KH>
+// Persistent launch: one CTA per SM, or one pair per two SMs (a cluster of
+// two CTAs; as many clusters as fit at once, capped by the tile count).
+template <int MODE, int KH, int CG>
 cudaError_t run_gemm(const GemmParams& p, int64_t tiles_upper_bound, const DeviceInfo& dev,
                      cudaStream_t stream) {
   const size_t smem = gemm_smem_bytes(p.E);
   static int configured[kMaxDevices] = {0};
+  static int max_pairs[kMaxDevices] = {0};
   if (!configured[dev.ordinal]) {
-    cudaError_t err = cudaFuncSetAttribute(grouped_gemm_kernel<MODE, KH>,
+    cudaError_t err = cudaFuncSetAttribute(grouped_gemm_kernel<MODE, KH, CG>,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            (int)gemm_smem_bytes(kMaxExperts));
     if (err != cudaSuccess) return err;
     configured[dev.ordinal] = 1;
   }
-  int64_t grid = tiles_upper_bound < dev.num_sms ? tiles_upper_bound : dev.num_sms;
-  if (grid < 1) grid = 1;
-  grouped_gemm_kernel<MODE, KH><<<(unsigned)grid, Traits<MODE, KH>::kThreads, smem, stream>>>(p);
-  return cudaGetLastError();
+  if (CG == 1) {
+    int64_t grid = tiles_upper_bound < dev.num_sms ? tiles_upper_bound : dev.num_sms;
+    if (grid < 1) grid = 1;
+    grouped_gemm_kernel<MODE, KH, CG><<<(unsigned)grid, Traits<MODE, KH, CG>::kThreads, smem, stream>>>(p);
+    return cudaGetLastError();
+  }
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(Traits<MODE, KH, CG>::kThreads);
+  cfg.dynamicSmemBytes = gemm_smem_bytes(kMaxExperts);
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (!max_pairs[dev.ordinal]) {
+    cfg.gridDim = dim3((unsigned)dev.num_sms);
+    int n = 0;
+    cudaError_t err = cudaOccupancyMaxActiveClusters(&n, grouped_gemm_kernel<MODE, KH, CG>, &cfg);
+    if (err != cudaSuccess) return err;
+    max_pairs[dev.ordinal] = n > 0 ? n : 1;
+  }
+  int64_t pairs = tiles_upper_bound < max_pairs[dev.ordinal] ? tiles_upper_bound : max_pairs[dev.ordinal];
+  if (pairs < 1) pairs = 1;
+  cfg.gridDim = dim3((unsigned)(2 * pairs));
+  cfg.dynamicSmemBytes = smem;
+  return cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<MODE, KH, CG>, p);
 }
 
 // 2-D bf16 tensor map over a row-major [rows, cols] matrix, 128-byte swizzle.
@@ -840,23 +981,29 @@ void fill_common(GemmParams& p, const int32_t* offsets, int64_t R, int64_t E, in
   p.ldo = 0;
 }
 
-template <int MODE, int KH>
+template <int MODE, int KH, int CG>
 int64_t mgrouped_tile_bound(int64_t R, int64_t E, int nt) {
-  constexpr int bm = Traits<MODE, KH>::kBM;
+  constexpr int bm = Traits<MODE, KH, CG>::kBM;
   return ((R + bm - 1) / bm + E) * nt;
 }
 
-// The M-grouped GEMMs with a plain bf16 epilogue take 256-row tiles once
-// experts average 512 rows or more, else 128-row tiles: with few row tiles
-// per expert, tiles of one and two halves mixed in a static round-robin
-// leave some SMs with twice the work of others (measured on the Qwen3-MoE
-// shape: 256 rows per expert favour 128-row tiles, 512 favour 256-row).
+// CTA pairs (2-SM MMAs, 256-row tiles with 128-row tails) for the M-grouped
+// GEMMs when selected (moe_set_gemm_pairs).
+bool use_pair(const DeviceInfo& dev) { return dev.gemm_pairs != 0; }
+
+// Single-CTA M-grouped GEMMs with a plain bf16 epilogue take 256-row tiles
+// once experts average 512 rows or more, else 128-row tiles: with few row
+// tiles per expert, tiles of one and two halves mixed in a static
+// round-robin leave some SMs with twice the work of others (measured on the
+// Qwen3-MoE shape: 256 rows per expert favour 128-row tiles, 512 favour
+// 256-row).
 template <int MODE>
 cudaError_t run_bf16_mgrouped(const GemmParams& p, int64_t R, int64_t E, const DeviceInfo& dev,
                               cudaStream_t stream) {
-  if (R >= 512 * E) return run_gemm<MODE, 2>(p, mgrouped_tile_bound<MODE, 2>(R, E, p.nt), dev, stream);
-  return run_gemm<MODE, 1>(p, mgrouped_tile_bound<MODE, 1>(R, E, p.nt), dev, stream);
+  if (R >= 512 * E) return run_gemm<MODE, 2, 1>(p, mgrouped_tile_bound<MODE, 2, 1>(R, E, p.nt), dev, stream);
+  return run_gemm<MODE, 1, 1>(p, mgrouped_tile_bound<MODE, 1, 1>(R, E, p.nt), dev, stream);
 }
+
 
 }  // namespace
 
@@ -864,7 +1011,7 @@ cudaError_t run_bf16_mgrouped(const GemmParams& p, int64_t R, int64_t E, const D
 // giving at least 228 tiles (1.5 per SM of a GB300); fixed by the shape
 // alone so that workspace sizes do not depend on the device.
 int router_parts(int64_t T, int64_t H, int64_t E) {
-  constexpr int bm = Traits<ROUTER, 1>::kBM;
+  constexpr int bm = Traits<ROUTER, 1, 1>::kBM;
   const int64_t tiles = ((T + bm - 1) / bm) * ((E + BN - 1) / BN);
   const int64_t kb = 3 * H / BK;          // 64-wide K blocks of the stacked split weight
   int parts = 1;
@@ -888,7 +1035,7 @@ int launch_router_logits(const uint16_t* x, const uint16_t* w_split, int64_t T, 
   p.mt_w = (int)((T + BMH - 1) / BMH);
   p.nt = (int)((E + BN - 1) / BN);
   p.ldo = E;
-  return run_gemm<ROUTER, 1>(p, (int64_t)parts * p.mt_w * p.nt, dev, stream) == cudaSuccess ? 0 : 1;
+  return run_gemm<ROUTER, 1, 1>(p, (int64_t)parts * p.mt_w * p.nt, dev, stream) == cudaSuccess ? 0 : 1;
 }
 
 int launch_gemm_gate_up(const uint16_t* x, const int32_t* src_row, const int32_t* offsets,
@@ -911,7 +1058,10 @@ int launch_gemm_gate_up(const uint16_t* x, const int32_t* src_row, const int32_t
   p.n_out = (int)I;
   p.nt = (int)((I + 127) / 128);
   p.ldo = I;
-  return run_gemm<FWD_GATEUP, 1>(p, mgrouped_tile_bound<FWD_GATEUP, 1>(R, E, p.nt), dev, stream) == cudaSuccess ? 0 : 1;
+  const cudaError_t err =
+      use_pair(dev) ? run_gemm<FWD_GATEUP, 1, 2>(p, mgrouped_tile_bound<FWD_GATEUP, 1, 2>(R, E, p.nt), dev, stream)
+                     : run_gemm<FWD_GATEUP, 1, 1>(p, mgrouped_tile_bound<FWD_GATEUP, 1, 1>(R, E, p.nt), dev, stream);
+  return err == cudaSuccess ? 0 : 1;
 }
 
 int launch_gemm_down(const uint16_t* h, const int32_t* offsets, const uint16_t* down, int64_t R,
@@ -926,10 +1076,13 @@ int launch_gemm_down(const uint16_t* h, const int32_t* offsets, const uint16_t* 
   p.n_out = (int)H;
   p.nt = (int)((H + BN - 1) / BN);
   p.ldo = H;
-  return run_bf16_mgrouped<FWD_DOWN>(p, R, E, dev, stream) == cudaSuccess ? 0 : 1;
+  const cudaError_t err =
+      use_pair(dev) ? run_gemm<FWD_DOWN, 1, 2>(p, mgrouped_tile_bound<FWD_DOWN, 1, 2>(R, E, p.nt), dev, stream)
+                     : run_bf16_mgrouped<FWD_DOWN>(p, R, E, dev, stream);
+  return err == cudaSuccess ? 0 : 1;
 }
 
-int down_bwd_parts(int64_t I) { return 2 * (int)((I + BN - 1) / BN); }   // one per 128 columns
+int down_bwd_parts(int64_t I) { return (int)((I + 63) / 64); }   // one per 64 columns of I
 
 int launch_gemm_down_bwd(const uint16_t* dy_perm, const uint16_t* h_w, const float* gu_pre,
                          const float* w_perm, const int32_t* offsets, const uint16_t* down, int64_t R,
@@ -938,7 +1091,8 @@ int launch_gemm_down_bwd(const uint16_t* dy_perm, const uint16_t* h_w, const flo
   if (R > 0) {  // dgu = SwiGLU'(w * (dy_perm . Wd_e^T), gu_pre)
     GemmParams p;
     fill_common(p, offsets, R, E, I, dev);
-    if (!make_map(&p.tmA, dy_perm, R, H, 64, BMH) || !make_map(&p.tmB, down, E * I, H, 64, 256))
+    const bool pair = use_pair(dev);   // a pair's CTA loads 128 of the tile's 256 B rows
+    if (!make_map(&p.tmA, dy_perm, R, H, 64, BMH) || !make_map(&p.tmB, down, E * I, H, 64, pair ? 128 : 256))
       return -1;
     p.aux = gu_pre;
     p.wrow = w_perm;
@@ -948,7 +1102,10 @@ int launch_gemm_down_bwd(const uint16_t* dy_perm, const uint16_t* h_w, const flo
     p.n_out = (int)I;
     p.nt = (int)((I + BN - 1) / BN);
     p.ldo = 2 * I;
-    if (run_gemm<DGRAD_DOWN, 1>(p, mgrouped_tile_bound<DGRAD_DOWN, 1>(R, E, p.nt), dev, stream) != cudaSuccess) return 1;
+    const cudaError_t err =
+        pair ? run_gemm<DGRAD_DOWN, 1, 2>(p, mgrouped_tile_bound<DGRAD_DOWN, 1, 2>(R, E, p.nt), dev, stream)
+             : run_gemm<DGRAD_DOWN, 1, 1>(p, mgrouped_tile_bound<DGRAD_DOWN, 1, 1>(R, E, p.nt), dev, stream);
+    if (err != cudaSuccess) return 1;
   }
   {  // d_down_e = (w h)_e^T . dy_perm_e
     GemmParams p;
@@ -962,7 +1119,7 @@ int launch_gemm_down_bwd(const uint16_t* dy_perm, const uint16_t* h_w, const flo
     p.mt_w = (int)((I + 2 * BMH - 1) / (2 * BMH));
     p.nt = (int)((H + BN - 1) / BN);
     p.ldo = H;
-    if (run_gemm<WGRAD_DOWN, 2>(p, E * p.mt_w * p.nt, dev, stream) != cudaSuccess) return 1;
+    if (run_gemm<WGRAD_DOWN, 2, 1>(p, E * p.mt_w * p.nt, dev, stream) != cudaSuccess) return 1;
   }
   return 0;
 }
@@ -974,14 +1131,19 @@ int launch_gemm_gate_up_bwd(const uint16_t* dgu, const uint16_t* x, const int32_
   if (R > 0) {  // dx_perm = dgu . Wgu_e^T
     GemmParams p;
     fill_common(p, offsets, R, E, I, dev);
-    if (!make_map(&p.tmA, dgu, R, 2 * I, 64, BMH) || !make_map(&p.tmB, gate_up, E * H, 2 * I, 64, 256))
+    const bool pair = use_pair(dev);
+    if (!make_map(&p.tmA, dgu, R, 2 * I, 64, BMH) ||
+        !make_map(&p.tmB, gate_up, E * H, 2 * I, 64, pair ? 128 : 256))
       return -1;
     p.out = dx_perm;
     p.K = (int)(2 * I);
     p.n_out = (int)H;
     p.nt = (int)((H + BN - 1) / BN);
     p.ldo = H;
-    if (run_bf16_mgrouped<DGRAD_GATEUP>(p, R, E, dev, stream) != cudaSuccess) return 1;
+    const cudaError_t err =
+        pair ? run_gemm<DGRAD_GATEUP, 1, 2>(p, mgrouped_tile_bound<DGRAD_GATEUP, 1, 2>(R, E, p.nt), dev, stream)
+             : run_bf16_mgrouped<DGRAD_GATEUP>(p, R, E, dev, stream);
+    if (err != cudaSuccess) return 1;
   }
   {  // d_gate_up_e = x[rows of e]^T . dgu_e
     GemmParams p;
@@ -997,7 +1159,7 @@ int launch_gemm_gate_up_bwd(const uint16_t* dgu, const uint16_t* x, const int32_
     p.mt_w = (int)((H + 2 * BMH - 1) / (2 * BMH));
     p.nt = (int)((2 * I + BN - 1) / BN);
     p.ldo = 2 * I;
-    if (run_gemm<WGRAD_GATEUP, 2>(p, E * p.mt_w * p.nt, dev, stream) != cudaSuccess) return 1;
+    if (run_gemm<WGRAD_GATEUP, 2, 1>(p, E * p.mt_w * p.nt, dev, stream) != cudaSuccess) return 1;
   }
   return 0;
 }

@@ -53,6 +53,12 @@ def set_wait_limit_ns(ns: int):
     call("moe_set_wait_limit_ns", int(ns))
 
 
+def set_gemm_pairs(on: bool):
+    """Forward and dgrad grouped GEMMs on CTA pairs (2-SM MMAs) or single CTAs
+    (default); the results are bit-identical."""
+    call("moe_set_gemm_pairs", 1 if on else 0)
+
+
 # ----------------------------------------------------------------- forward
 
 def route(x, w_router, k, bias=None, return_logits=False):
