@@ -67,8 +67,7 @@ constexpr int BMH = 128;                           // rows of one half (one MMA)
 constexpr int BN = 256;
 constexpr int BK = 64;
 constexpr int A_HALF_BYTES = BMH * BK * 2;         // 16 KB
-constexpr int B_BYTES = BN * BK * 2;               // 32 KB
-constexpr int RING_BYTES = 192 * 1024;             // 3 x 64 KB or 4 x 48 KB
+constexpr int RING_BYTES = 192 * 1024;             // 3 x 64, 4 x 48 or 6 x 32 KB stages
 constexpr int kEpiWarps = 8;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr int MN_CHUNK_BYTES = 64 * 128;           // one 64-wide MN chunk x 64 K rows
@@ -105,8 +104,11 @@ struct Traits {
   static constexpr int kH = KH;
   static constexpr int kBM = kH * BMH * CG;          // rows of a tile
   static constexpr int kAccBufs = 2 / kH;
+  // N of a tile: 256, or 128 for the router (E is often 128; split K gives
+  // it its parallelism)
+  static constexpr int kBN = (MODE == ROUTER) ? 128 : BN;
   static constexpr int kABytes = kH * A_HALF_BYTES;  // per CTA
-  static constexpr int kBBytes = B_BYTES / CG;       // per CTA: a pair splits the N columns
+  static constexpr int kBBytes = kBN * BK * 2 / CG;  // per CTA: a pair splits the N columns
   static constexpr int kStageBytes = kABytes + kBBytes;
   static constexpr int kStages = RING_BYTES / kStageBytes;   // 4, 3, or 6 for a pair
   // read the accumulators into registers (bf16), free them, then store
@@ -160,7 +162,7 @@ __device__ __forceinline__ uint32_t make_idesc(int m = BMH * CG) {
          | (1u << 10)                    // B: bf16
          | ((Tr::kAMN ? 1u : 0u) << 15)  // A major: 0 = K, 1 = MN
          | ((Tr::kBMN ? 1u : 0u) << 16)  // B major
-         | ((uint32_t)(BN >> 3) << 17)   // N
+         | ((uint32_t)(Tr::kBN >> 3) << 17)   // N
          | ((uint32_t)(m >> 4) << 24);   // M: one half, or 256 (128 for a half tile) over a pair
 }
 
@@ -237,12 +239,6 @@ __device__ __forceinline__ void store_zero_rows(const GemmParams& p, const Tile&
   const uint4 z = make_uint4(0, 0, 0, 0);
   for (int c = c_lo; c < c_hi; c += 8)
     if (t.nt * BN + c < p.n_out) *reinterpret_cast<uint4*>(orow + c) = z;
-}
-
-__device__ __forceinline__ void store32_f32(float* dst, const float* v) {
-  float4* d = reinterpret_cast<float4*>(dst);
-#pragma unroll
-  for (int q = 0; q < 8; ++q) d[q] = make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
 }
 
 __device__ __forceinline__ float swiglu(float g, float u) { return g / (1.0f + expf(-g)) * u; }
@@ -365,9 +361,9 @@ __device__ __forceinline__ void stage_loads(const GemmParams& p, const Tile& t, 
       const int kg = t.e * p.K + k0;                 // row of the stacked [W0; W1; W2]
       for (int h = 0; h < t.halves; ++h)             // x repeats along the stacked K
         tma_load_2d(sA + h * A_HALF_BYTES, &p.tmA, kg % p.I, t.row0 + h * BMH, fb);
-      const int n0 = t.nt * BN;
+      const int n0 = t.nt * Tr::kBN;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) tma_load_2d(sB + c * MN_CHUNK_BYTES, &p.tmB, n0 + 64 * c, kg, fb);
+      for (int c = 0; c < Tr::kBN / 64; ++c) tma_load_2d(sB + c * MN_CHUNK_BYTES, &p.tmB, n0 + 64 * c, kg, fb);
     }
   } else if (MODE == FWD_DOWN) {
     if (lane == 0) {
@@ -795,22 +791,25 @@ __global__ void __launch_bounds__(Traits<MODE, KH, CG>::kThreads, 1)
                              lane, row_mask);
           }
         }
-      } else if (MODE == ROUTER) {
+      } else if (MODE == ROUTER) {   // fp32 partial logits; warpgroup wg: columns [64 wg, 64 wg + 64)
         const bool row_ok = wrow + lane < t.rows;
-        float* orow = p.out_part + ((int64_t)t.e * p.rows + t.row0 + wrow + lane) * p.ldo;
-        const int n0 = t.nt * BN;
+        const uint32_t row_mask = __ballot_sync(0xffffffffu, row_ok);
+        float* orow0 = p.out_part + ((int64_t)t.e * p.rows + t.row0 + wrow) * p.ldo;
+        const int n0 = t.nt * Tr::kBN;
 #pragma unroll 1
-        for (int c0 = 128 * wg; c0 < 128 * wg + 128; c0 += 32) {
-          if (n0 + c0 >= p.n_out) break;
+        for (int c0 = (Tr::kBN / 2) * wg; c0 < (Tr::kBN / 2) * (wg + 1); c0 += 32) {
+          if (n0 + c0 >= p.n_out) break;                 // warp-uniform
           tmem_ld32(taddr + c0, v);
-          if (row_ok) {
-            if (n0 + c0 + 32 <= p.n_out && (p.ldo & 3) == 0) {
-              store32_f32(orow + n0 + c0, v);
-            } else {
+          if (n0 + c0 + 32 <= p.n_out && (p.ldo & 3) == 0) {   // whole 128-byte row segments
+            uint32_t bits[32];
 #pragma unroll
-              for (int q = 0; q < 32; ++q)
-                if (n0 + c0 + q < p.n_out) orow[n0 + c0 + q] = v[q];
-            }
+            for (int q = 0; q < 32; ++q) bits[q] = __float_as_uint(v[q]);
+            store_block128(reinterpret_cast<uint8_t*>(orow0 + n0 + c0), p.ldo * 4, bits, lane, row_mask);
+          } else if (row_ok) {
+            float* orow = orow0 + (int64_t)lane * p.ldo;
+#pragma unroll
+            for (int q = 0; q < 32; ++q)
+              if (n0 + c0 + q < p.n_out) orow[n0 + c0 + q] = v[q];
           }
         }
       } else if (MODE == FWD_DOWN || MODE == DGRAD_GATEUP || Tr::kKGrouped) {   // one half: column half wg
@@ -1011,8 +1010,8 @@ cudaError_t run_bf16_mgrouped(const GemmParams& p, int64_t R, int64_t E, const D
 // giving at least 228 tiles (1.5 per SM of a GB300); fixed by the shape
 // alone so that workspace sizes do not depend on the device.
 int router_parts(int64_t T, int64_t H, int64_t E) {
-  constexpr int bm = Traits<ROUTER, 1, 1>::kBM;
-  const int64_t tiles = ((T + bm - 1) / bm) * ((E + BN - 1) / BN);
+  constexpr int bm = Traits<ROUTER, 1, 1>::kBM, bn = Traits<ROUTER, 1, 1>::kBN;
+  const int64_t tiles = ((T + bm - 1) / bm) * ((E + bn - 1) / bn);
   const int64_t kb = 3 * H / BK;          // 64-wide K blocks of the stacked split weight
   int parts = 1;
   for (int cand = 1; cand <= 48; ++cand) {
@@ -1033,7 +1032,7 @@ int launch_router_logits(const uint16_t* x, const uint16_t* w_split, int64_t T, 
   p.K = (int)(3 * H / parts);   // K extent of one part
   p.n_out = (int)E;
   p.mt_w = (int)((T + BMH - 1) / BMH);
-  p.nt = (int)((E + BN - 1) / BN);
+  p.nt = (int)((E + Traits<ROUTER, 1, 1>::kBN - 1) / Traits<ROUTER, 1, 1>::kBN);
   p.ldo = E;
   return run_gemm<ROUTER, 1, 1>(p, (int64_t)parts * p.mt_w * p.nt, dev, stream) == cudaSuccess ? 0 : 1;
 }

@@ -5,10 +5,11 @@
 //
 // Deterministic three-pass counting sort, no order-dependent atomics:
 //   1. permute_hist_kernel   block b counts the ids of its chunk of
-//                            kChunk assignments -> hist[b][e]
+//                            CHUNK assignments -> hist[b][e]
 //   2. permute_scan_kernel   one block: counts[e] = sum_b hist[b][e];
 //                            offsets = exclusive scan; hist[b][e] becomes
-//                            offsets[e] + sum_{b'<b} hist[b'][e]
+//                            offsets[e] + sum_{b'<b} hist[b'][e] (each
+//                            expert's blocks split over G threads)
 //   3. permute_scatter_kernel block b ranks its chunk stably: warp w owns a
 //                            contiguous slice, warp bases come from a scan of
 //                            per-warp counts, and inside a warp step the
@@ -26,11 +27,15 @@ namespace moe {
 
 namespace {
 
-constexpr int kChunk = 2048;     // assignments per block
+// Assignments per block: 256 (one 32-wide step per warp) fill the GPU at a
+// few thousand tokens; moe_permute_noalloc keeps 2048, which its fixed
+// scratch limit is stated in.
+constexpr int kChunk = 256;
+constexpr int kChunkNoAlloc = 2048;
 constexpr int kPermThreads = 256;
 constexpr int kPermWarps = kPermThreads / 32;
-constexpr int kPerWarp = kChunk / kPermWarps;   // 256 = 8 steps of 32
 
+template <int CHUNK>
 __global__ void __launch_bounds__(kPermThreads) permute_hist_kernel(const int32_t* __restrict__ ids,
                                                                     int64_t R, int E,
                                                                     int32_t* __restrict__ hist,
@@ -38,8 +43,8 @@ __global__ void __launch_bounds__(kPermThreads) permute_hist_kernel(const int32_
   extern __shared__ int32_t sh[];  // [E]
   for (int e = threadIdx.x; e < E; e += blockDim.x) sh[e] = 0;
   __syncthreads();
-  const int64_t base = (int64_t)blockIdx.x * kChunk;
-  for (int q = threadIdx.x; q < kChunk; q += blockDim.x) {
+  const int64_t base = (int64_t)blockIdx.x * CHUNK;
+  for (int q = threadIdx.x; q < CHUNK; q += blockDim.x) {
     const int64_t i = base + q;
     if (i < R) {
       const int e = ids[i];
@@ -54,16 +59,40 @@ __global__ void __launch_bounds__(kPermThreads) permute_hist_kernel(const int32_
   for (int e = threadIdx.x; e < E; e += blockDim.x) hist[(int64_t)blockIdx.x * E + e] = sh[e];
 }
 
+// One block of 1024 threads.  Each expert's block histograms are split into
+// G = 1024 / E contiguous ranges of blocks, one thread per (range, expert):
+// range sums, then per expert the total and the exclusive scan over
+// experts, then each thread rewrites its range with running bases.
 __global__ void __launch_bounds__(1024) permute_scan_kernel(int32_t* __restrict__ hist, int nblocks,
                                                             int E, int32_t* __restrict__ counts,
                                                             int32_t* __restrict__ offsets) {
+  __shared__ int32_t part[1024];     // [G][E] range sums, then exclusive range prefixes
   __shared__ int32_t warp_tot[32];
-  const int e = threadIdx.x;
+  __shared__ int32_t ex[1024];       // offsets[e]
+  const int tid = threadIdx.x;
+  const int G = 1024 / E;            // E <= 1024
+  const int g = tid / E, e = tid - (tid / E) * E;
+  const bool act = g < G;
+  const int per = (nblocks + G - 1) / G;
+  const int b0 = min(nblocks, g * per), b1 = min(nblocks, b0 + per);
+  if (act) {
+    int32_t sum = 0;
+#pragma unroll 8
+    for (int b = b0; b < b1; ++b) sum += hist[(int64_t)b * E + e];
+    part[g * E + e] = sum;
+  }
+  __syncthreads();
+  // per expert (thread tid = e < E): the total, and the ranges' exclusive prefixes
   int32_t c = 0;
-  if (e < E)
-    for (int b = 0; b < nblocks; ++b) c += hist[(int64_t)b * E + e];
+  if (tid < E) {
+    for (int gg = 0; gg < G; ++gg) {
+      const int32_t v = part[gg * E + tid];
+      part[gg * E + tid] = c;
+      c += v;
+    }
+  }
   // exclusive scan of c over e (block of 1024 threads = 32 warps)
-  const int lane = e & 31, wid = e >> 5;
+  const int lane = tid & 31, wid = tid >> 5;
   int32_t incl = c;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
@@ -83,27 +112,39 @@ __global__ void __launch_bounds__(1024) permute_scan_kernel(int32_t* __restrict_
     warp_tot[lane] = s - v;   // exclusive prefix of warp totals
   }
   __syncthreads();
-  const int32_t excl = incl - c + warp_tot[wid];
-  if (e < E) {
-    counts[e] = c;
-    offsets[e] = excl;
-    if (e == E - 1) offsets[E] = excl + c;
-    int32_t run = excl;
-    for (int b = 0; b < nblocks; ++b) {
-      const int32_t h = hist[(int64_t)b * E + e];
-      hist[(int64_t)b * E + e] = run;
-      run += h;
+  if (tid < E) {
+    const int32_t excl = incl - c + warp_tot[wid];
+    counts[tid] = c;
+    offsets[tid] = excl;
+    if (tid == E - 1) offsets[E] = excl + c;
+    ex[tid] = excl;
+  }
+  __syncthreads();
+  if (act) {
+    // eight reads in flight before the writes (the array is read and written)
+    int32_t run = ex[e] + part[g * E + e];
+    for (int b = b0; b < b1; b += 8) {
+      int32_t h[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) h[q] = (b + q < b1) ? hist[(int64_t)(b + q) * E + e] : 0;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        if (b + q < b1) hist[(int64_t)(b + q) * E + e] = run;
+        run += h[q];
+      }
     }
   }
 }
 
+template <int CHUNK>
 __global__ void __launch_bounds__(kPermThreads) permute_scatter_kernel(
     const int32_t* __restrict__ ids, const float* __restrict__ w, int64_t R, int k, int E,
     const int32_t* __restrict__ base_be, int32_t* __restrict__ row_map, int32_t* __restrict__ src_row,
     float* __restrict__ w_perm) {
+  constexpr int kPerWarp = CHUNK / kPermWarps;  // assignments per warp, in steps of 32
   extern __shared__ int32_t sh[];              // [kPermWarps][E] counts, then bases
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-  const int64_t chunk0 = (int64_t)blockIdx.x * kChunk;
+  const int64_t chunk0 = (int64_t)blockIdx.x * CHUNK;
   const int64_t slice0 = chunk0 + (int64_t)wid * kPerWarp;
   for (int q = threadIdx.x; q < kPermWarps * E; q += blockDim.x) sh[q] = 0;
   __syncthreads();
@@ -160,24 +201,36 @@ __global__ void permute_rows_kernel(const uint16_t* __restrict__ x, const int32_
 
 }  // namespace
 
-size_t permute_workspace_bytes(int64_t R, int64_t E) {
-  const int64_t nb = (R + kChunk - 1) / kChunk;
+size_t permute_workspace_bytes(int64_t R, int64_t E, bool noalloc) {
+  const int64_t chunk = noalloc ? kChunkNoAlloc : kChunk;
+  const int64_t nb = (R + chunk - 1) / chunk;
   return (size_t)((nb > 0 ? nb : 1) * E * sizeof(int32_t));
+}
+
+template <int CHUNK>
+void enqueue_permute(const int32_t* ids, const float* w, int64_t R, int64_t k, int64_t E, int32_t* counts,
+                     int32_t* offsets, int32_t* row_map, int32_t* src_row, float* w_perm, int32_t* hist,
+                     uint32_t* status, cudaStream_t stream) {
+  const int nb = (int)((R + CHUNK - 1) / CHUNK);
+  if (nb > 0)
+    permute_hist_kernel<CHUNK><<<nb, kPermThreads, E * sizeof(int32_t), stream>>>(ids, R, (int)E, hist,
+                                                                                   status);
+  permute_scan_kernel<<<1, 1024, 0, stream>>>(hist, nb, (int)E, counts, offsets);
+  if (nb > 0)
+    permute_scatter_kernel<CHUNK><<<nb, kPermThreads, kPermWarps * E * sizeof(int32_t), stream>>>(
+        ids, w, R, (int)k, (int)E, hist, row_map, src_row, w_perm);
 }
 
 cudaError_t launch_permute(const int32_t* ids, const float* w, int64_t T, int64_t k, int64_t E,
                            int32_t* counts, int32_t* offsets, int32_t* row_map, int32_t* src_row,
-                           float* w_perm, void* ws, uint32_t* status, cudaStream_t stream) {
-  const int64_t R = T * k;
-  const int nb = (int)((R + kChunk - 1) / kChunk);
+                           float* w_perm, void* ws, uint32_t* status, cudaStream_t stream, bool noalloc) {
   int32_t* hist = static_cast<int32_t*>(ws);
-  if (nb > 0)
-    permute_hist_kernel<<<nb, kPermThreads, E * sizeof(int32_t), stream>>>(ids, R, (int)E, hist,
-                                                                           status);
-  permute_scan_kernel<<<1, 1024, 0, stream>>>(hist, nb, (int)E, counts, offsets);
-  if (nb > 0)
-    permute_scatter_kernel<<<nb, kPermThreads, kPermWarps * E * sizeof(int32_t), stream>>>(
-        ids, w, R, (int)k, (int)E, hist, row_map, src_row, w_perm);
+  if (noalloc)
+    enqueue_permute<kChunkNoAlloc>(ids, w, T * k, k, E, counts, offsets, row_map, src_row, w_perm, hist,
+                                   status, stream);
+  else
+    enqueue_permute<kChunk>(ids, w, T * k, k, E, counts, offsets, row_map, src_row, w_perm, hist, status,
+                            stream);
   return cudaGetLastError();
 }
 
@@ -217,7 +270,7 @@ extern "C" int moe_permute_noalloc(const int32_t* ids, const float* w, int64_t T
   if (!counts || !offsets || (T > 0 && (!ids || !row_map || !src_row))) return MOE_ERR_INVALID_ARG;
   if ((w == nullptr) != (w_perm == nullptr)) return MOE_ERR_INVALID_ARG;
   if (E > moe::kMaxExperts) return MOE_ERR_UNSUPPORTED;
-  if (moe::permute_workspace_bytes(T * k, E) > sizeof(moe::g_permute_scratch))
+  if (moe::permute_workspace_bytes(T * k, E, true) > sizeof(moe::g_permute_scratch))
     return MOE_ERR_SCRATCH_LIMIT;
   moe::DeviceInfo dev;
   int rc = moe::device_info(&dev);
@@ -238,7 +291,7 @@ extern "C" int moe_permute_noalloc(const int32_t* ids, const float* w, int64_t T
   // Every call fully overwrites the histogram entries it reads (the count
   // pass writes all nblocks x E of them first), so nothing has to be cleared.
   return moe::launch_permute(ids, w, T, k, E, counts, offsets, row_map, src_row, w_perm, scratch,
-                             dev.status, static_cast<cudaStream_t>(stream)) == cudaSuccess
+                             dev.status, static_cast<cudaStream_t>(stream), true) == cudaSuccess
              ? MOE_OK
              : MOE_ERR_CUDA;
 }
