@@ -377,7 +377,10 @@ def run_native(args):
     }
 
     if not args.no_e2e:
-        out["e2e"] = e2e(moe, d, cfg, torch, stream, dist, device, ws, min(K, 100), fused)
+        e_pipe = e2e(moe, d, cfg, torch, stream, dist, device, ws, min(K, 100), fused, "PipelinedForward")
+        e_over = e2e(moe, d, cfg, torch, stream, dist, device, ws, min(K, 100), fused, "OverlappedForward")
+        out["e2e"] = e_over
+        out["e2e_pipelined"] = {k_: e_pipe[k_] for k_ in ("value", "api")}
     if not args.no_fwd_bwd:
         del d
         torch.cuda.empty_cache()
@@ -390,14 +393,15 @@ def run_native(args):
         dist.destroy_process_group()
 
 
-def e2e(moe, d, cfg, torch, stream, dist, device, ws, K, fused):
+def e2e(moe, d, cfg, torch, stream, dist, device, ws, K, fused, runner_cls="OverlappedForward"):
     """Tokens from pinned host memory -> layer -> output back to pinned host memory,
-    through the public PipelinedForward (copies of neighbouring steps overlap the
-    layer on two streams).  Every step's input upload and output download is
-    inside the timed region."""
+    through a public pipelined forward (PipelinedForward: copies of neighbouring
+    steps overlap the layer; OverlappedForward: also the route/permute of step
+    i+1 overlaps the expert GEMMs of step i).  Every step's input upload and
+    output download is inside the timed region."""
     T, H = cfg.T, cfg.H
-    runner = moe.PipelinedForward(T, d["w_router"], d["gate_up"], d["down"], cfg.k, d["bias"], d["sh_gate_up"],
-                                  d["sh_down"], fused_gather=fused)
+    runner = getattr(moe, runner_cls)(T, d["w_router"], d["gate_up"], d["down"], cfg.k, d["bias"],
+                                      d["sh_gate_up"], d["sh_down"], fused_gather=fused)
     xs = [d["x_host"]] * K
     ys = [torch.empty((T, H), dtype=torch.bfloat16).pin_memory() for _ in range(2)]
     ys = [ys[i % 2] for i in range(K)]
@@ -409,11 +413,11 @@ def e2e(moe, d, cfg, torch, stream, dist, device, ws, K, fused):
     dt = time.perf_counter() - t0
     barrier(dist)
     s = max_over_ranks(dist, dt, device)
+    del runner
     return {"value": round(ws * T * K / s, 1), "unit": "tokens/s", "h2d_bytes_per_step": T * H * 2,
-            "d2h_bytes_per_step": T * H * 2, "steps": K,
+            "d2h_bytes_per_step": T * H * 2, "steps": K, "api": runner_cls,
             "note": "weights resident; every step copies x host->device (pinned) and y device->host "
-                    "(pinned); host wall clock around K steps with both streams synchronised; copies "
-                    "of neighbouring steps overlap the layer (PipelinedForward: ForwardGraph replays)"}
+                    "(pinned); host wall clock around K steps with all streams synchronised"}
 
 
 def fwd_bwd(moe, torch, stream, dist, device, ws, flush, pk, fused, K=30, W=3):

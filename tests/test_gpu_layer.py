@@ -252,3 +252,24 @@ def test_cta_pairs_bit_identical(T, H, E, k, I, fused):
         outs.append([y, st.h, st.gu_pre, st.h_w, st.y_perm] + [g[n] for n in sorted(g)])
     for a, b in zip(*outs):
         assert torch_equal(a, b)
+
+
+def test_overlapped_forward_matches_forward():
+    """OverlappedForward (route/permute of batch i+1 overlapping the expert
+    GEMMs of batch i, on two streams) gives moe_forward's outputs bit for
+    bit, with and without a shared expert."""
+    import torch
+    moe = lib()
+    for I_s in (0, 64):
+        cfg, inp = _inputs(300, 256, 8, 2, 128, seed=93, I_shared=I_s)
+        wr, gu, dn = f32(inp.w_router), bf(inp.gate_up), bf(inp.down)
+        sgu = bf(inp.sh_gate_up) if I_s else None
+        sdn = bf(inp.sh_down) if I_s else None
+        xs = [torch.from_numpy(synth.normal_bf16(s, synth.TID_X, (300, 256), 1.0).view(np.int16))
+              .view(torch.bfloat16).pin_memory() for s in (11, 12, 13, 14, 15)]
+        ys = [torch.empty((300, 256), dtype=torch.bfloat16).pin_memory() for _ in xs]
+        moe.OverlappedForward(300, wr, gu, dn, cfg.k, None, sgu, sdn).run(xs, ys)
+        moe.sync_status()
+        for xh, yh in zip(xs, ys):
+            y, _ = moe.moe_forward(xh.cuda(), wr, gu, dn, cfg.k, None, sgu, sdn)
+            assert torch_equal(y.cpu(), yh)

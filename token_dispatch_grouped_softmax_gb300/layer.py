@@ -227,3 +227,108 @@ class PipelinedForward:
                 self.ev_stored[b].record(self.copy_stream)
         self.copy_stream.synchronize()
         compute.synchronize()
+
+
+class OverlappedForward:
+    """The forward over a stream of host batches as a two-stage pipeline, so
+    that the token-side steps of one batch overlap the expert GEMMs of the
+    previous one (the single-GPU part of the Domino-style overlap: ByteDance
+    "FSDPTurbo" domino dispatcher; "InternVL3.5 pure FSDP2 训练性能优化实践").
+
+    Stage F (route -> permute -> row gather) and stage G (grouped gate_up
+    GEMM -> grouped down GEMM -> combine, plus the shared expert) are each
+    captured as a CUDA graph per buffer set, two sets, and run on their own
+    streams: F of batch i+1 runs while G of batch i runs.  Tokens are not
+    split within a batch, so every expert's weights are still read once per
+    batch.  A copy stream uploads each batch and downloads its output.
+    Outputs equal moe_forward's bit for bit.  Host tensors must be pinned;
+    every batch has the token count given here.
+    """
+
+    def __init__(self, T, w_router, gate_up, down, k, bias=None, sh_gate_up=None, sh_down=None,
+                 fused_gather=False):
+        H, E = w_router.shape
+        I = down.shape[0] // E
+        self.stream_f = torch.cuda.Stream()
+        self.stream_g = torch.cuda.Stream()
+        self.copy_stream = torch.cuda.Stream()
+        self.sets = []
+        for _ in range(2):
+            st = {"x": torch.zeros((T, H), dtype=torch.bfloat16, device=w_router.device)}
+
+            def front(st=st):
+                ids, w = ops.route(st["x"], w_router, k, bias)
+                counts, offsets, row_map, src_row = ops.permute(ids, E)
+                x_perm = None if fused_gather else ops.permute_rows(st["x"], src_row)
+                st.update(w=w, offsets=offsets, row_map=row_map, src_row=src_row, x_perm=x_perm)
+
+            def back(st=st):
+                if fused_gather:
+                    h, _, _ = ops.grouped_gemm_gate_up_swiglu(st["x"], st["src_row"], st["offsets"], gate_up, I)
+                else:
+                    h, _, _ = ops.grouped_gemm_gate_up_swiglu(st["x_perm"], None, st["offsets"], gate_up, I)
+                y_perm = ops.grouped_gemm_down(h, st["offsets"], down, H)
+                y_sh = None
+                if sh_gate_up is not None:
+                    I_s = sh_down.shape[0]
+                    hs, _, _ = ops.grouped_gemm_gate_up_swiglu(st["x"], None, None, sh_gate_up, I_s)
+                    y_sh = ops.grouped_gemm_down(hs, None, sh_down, H)
+                st["y"] = ops.unpermute_combine(y_perm, st["row_map"], st["w"], y_sh)
+
+            side = torch.cuda.Stream()
+            side.wait_stream(torch.cuda.current_stream())
+            with torch.cuda.stream(side):      # one-time library set-up outside the captures
+                for _ in range(2):
+                    front()
+                    back()
+            torch.cuda.current_stream().wait_stream(side)
+            st["gf"], st["gg"] = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+            with torch.cuda.graph(st["gf"]):
+                front()
+            with torch.cuda.graph(st["gg"]):
+                back()
+            st.update(ev_loaded=torch.cuda.Event(), ev_f=torch.cuda.Event(), ev_g=torch.cuda.Event(),
+                      ev_stored=torch.cuda.Event())
+            self.sets.append(st)
+
+    def run(self, x_host_batches, y_host_batches):
+        """y_host_batches[i] <- layer(x_host_batches[i]); returns when all are stored."""
+        cur = torch.cuda.current_stream()
+        for st in self.sets:                    # every buffer free at the start
+            for ev in ("ev_f", "ev_g", "ev_stored"):
+                st[ev].record(cur)
+        for s in (self.stream_f, self.stream_g, self.copy_stream):
+            s.wait_stream(cur)
+        n = len(x_host_batches)
+
+        def load(i):
+            st = self.sets[i % 2]
+            with torch.cuda.stream(self.copy_stream):
+                self.copy_stream.wait_event(st["ev_f"])          # F of batch i-2 has read x
+                st["x"].copy_(x_host_batches[i], non_blocking=True)
+                st["ev_loaded"].record(self.copy_stream)
+
+        if n:
+            load(0)
+        for i in range(n):
+            st = self.sets[i % 2]
+            if i + 1 < n:
+                load(i + 1)
+            with torch.cuda.stream(self.stream_f):
+                self.stream_f.wait_event(st["ev_loaded"])
+                self.stream_f.wait_event(st["ev_g"])             # G of batch i-2 no longer reads this set
+                st["gf"].replay()
+                st["ev_f"].record(self.stream_f)
+            with torch.cuda.stream(self.stream_g):
+                self.stream_g.wait_event(st["ev_f"])
+                self.stream_g.wait_event(st["ev_stored"])        # batch i-2's output was copied out
+                st["gg"].replay()
+                st["ev_g"].record(self.stream_g)
+            with torch.cuda.stream(self.copy_stream):
+                self.copy_stream.wait_event(st["ev_g"])
+                y_host_batches[i].copy_(st["y"], non_blocking=True)
+                st["ev_stored"].record(self.copy_stream)
+        self.copy_stream.synchronize()
+        cur.wait_stream(self.stream_f)
+        cur.wait_stream(self.stream_g)
+        cur.synchronize()
