@@ -467,7 +467,7 @@ def cpu_baseline(cfg, target_s=15.0, max_tokens=None):
     import synth
 
     inp = synth.make_inputs(cfg)
-    cores = os.cpu_count() or 1
+    cores = oracle.threads()   # OpenMP threads of the oracle's loops
 
     def run(n):
         x = np.ascontiguousarray(inp.x[:n])
@@ -522,7 +522,7 @@ def run_reference(args):
            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
            "config": {"workload": cfg.name, "T": cfg.T, "H": cfg.H, "E": cfg.E, "k": cfg.k, "I": cfg.I,
                       "I_shared": cfg.I_shared, "seed": cfg.seed},
-           "cpu_baseline": {"value": round(value, 2), "unit": "tokens/s", "cores": os.cpu_count() or 1,
+           "cpu_baseline": {"value": round(value, 2), "unit": "tokens/s", "cores": oracle.threads(),
                             "kind": "oracle",
                             "sample": "first %d of %d tokens per step (fp64 oracle, route + experts + combine)"
                                       % (n, cfg.T)},

@@ -69,8 +69,15 @@ def _load():
         lib.oracle_permute_rows.restype = None
         lib.oracle_unpermute_combine.argtypes = [_I, _I, _I, _P, _P, _P, _P, _P]
         lib.oracle_unpermute_combine.restype = None
+        lib.oracle_threads.argtypes = []
+        lib.oracle_threads.restype = ctypes.c_int
         _lib = lib
     return _lib
+
+
+def threads():
+    """OpenMP threads the oracle's parallel loops run on."""
+    return int(_load().oracle_threads())
 
 
 def _ptr(a):

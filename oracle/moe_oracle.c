@@ -21,9 +21,13 @@
  *             gradient of each token sums to zero
  */
 #include <math.h>
+#include <omp.h>
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
+
+/* Threads the parallel loops below run on (OpenMP's current maximum). */
+int oracle_threads(void) { return omp_get_max_threads(); }
 
 static inline double bf16_bits_to_f64(uint16_t b) {
   uint32_t u = (uint32_t)b << 16;
