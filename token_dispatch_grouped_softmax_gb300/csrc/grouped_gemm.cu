@@ -414,19 +414,18 @@ __device__ __forceinline__ void stage_loads(const GemmParams& p, const Tile& t, 
 }
 
 // Zeroes the K rows [kvalid, 64) of every 64 x 128-byte chunk of a stage (a
-// weight-gradient tile's last K block may run past its expert's rows).
-// Warp-wide; makes the writes visible to the tensor cores.
+// weight-gradient tile's last K block may run past its expert's rows).  Lane
+// l writes 16-byte unit l % 8 of rows kvalid + l / 8, +4, ... of each chunk:
+// no divisions on the MMA issuer's path.  Warp-wide; makes the writes
+// visible to the tensor cores.
 template <int STAGE_BYTES>
 __device__ __forceinline__ void zero_k_tail(uint8_t* stage, int kvalid, int lane) {
   constexpr int kChunks = STAGE_BYTES / MN_CHUNK_BYTES;
-  const int nrow = BK - kvalid;
-  for (int q = lane; q < nrow * 8 * kChunks; q += 32) {
-    const int chunk = q / (nrow * 8);
-    const int rem = q - chunk * nrow * 8;
-    const int row = kvalid + rem / 8;
-    const int u = rem & 7;
-    *reinterpret_cast<uint4*>(stage + chunk * MN_CHUNK_BYTES + row * 128 + u * 16) = make_uint4(0, 0, 0, 0);
-  }
+  uint8_t* unit = stage + (lane & 7) * 16;
+#pragma unroll
+  for (int chunk = 0; chunk < kChunks; ++chunk)
+    for (int row = kvalid + (lane >> 3); row < BK; row += 4)
+      *reinterpret_cast<uint4*>(unit + chunk * MN_CHUNK_BYTES + row * 128) = make_uint4(0, 0, 0, 0);
   fence_proxy_async_smem();
   __syncwarp();
 }
