@@ -40,6 +40,12 @@ METRIC = "MoE layer tokens/s (fwd; fwd+bwd) and grouped-GEMM % of GB300 bf16 pea
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
+def route_launches(H, E):
+    """Kernels of one moe_route call: the bf16 split of W_r, then the fused
+    cluster router (16 <= E <= 256, E % 16 == 0) or the router GEMM and top-k."""
+    return 2 if (H % 64 == 0 and E % 16 == 0 and 16 <= E <= 256) else 3
+
+
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -265,7 +271,9 @@ def run_native(args):
         mark()
         return y
 
-    launches_per_step = 2 + 3 + (0 if fused else 1) + 1 + 1 + (2 if I_s else 0) + 1
+    # route (weight split + fused router, or split + router GEMM + top-k),
+    # permute (3), row gather, gate_up, down, shared expert (2), combine
+    launches_per_step = route_launches(H, cfg.E) + 3 + (0 if fused else 1) + 1 + 1 + (2 if I_s else 0) + 1
     for _ in range(max(args.warmup, 3)):
         step()
     moe.sync_status()
@@ -453,7 +461,7 @@ def fwd_bwd(moe, torch, stream, dist, device, ws, flush, pk, fused, K=30, W=3):
     return {"workload": cfg.name, "T": cfg.T, "value": round(ws * cfg.T * K / s, 1), "unit": "tokens/s",
             "ms_per_step": round(1e3 * s / K, 4), "gemm_flops_per_step": flops,
             "layer_tflops": round(flops * K / s / 1e12, 1), "steps": K,
-            "launches_per_step": 8 + (0 if fused else 1) + 1 + 1 + 2 + 2 + 2}
+            "launches_per_step": route_launches(cfg.H, cfg.E) + 6 + (0 if fused else 1) + 1 + 1 + 2 + 2 + 2}
 
 
 # -------------------------------------------------------------- CPU oracle

@@ -90,9 +90,10 @@ int moe_test_stall_gemm_producer(int on);
 /* ------------------------------------------------------------------ route */
 
 /* Bytes of workspace moe_route needs.  With E % 8 == 0 and H % 64 == 0 the
- * logits run on the tensor cores: the workspace holds the exact three-term
- * bf16 split of W_r (3*H*E*2 bytes) and fp32 partial logits of a split-K
- * GEMM (parts*T*E*4 bytes); otherwise it holds the fp32 logits (T*E*4). */
+ * logits run on the tensor cores and the workspace holds the exact
+ * three-term bf16 split of W_r (3*H*E*2 bytes); when E is not also a
+ * multiple of 16 in [16, 256] it adds the fp32 partial logits of a split-K
+ * GEMM (parts*T*E*4 bytes).  Other shapes: the fp32 logits (T*E*4). */
 int moe_route_workspace_size(int64_t T, int64_t H, int64_t E, size_t* bytes);
 
 /* Router (MindSpeed page §8.2: gate -> FP32 softmax -> top-k -> renormalise).

@@ -74,10 +74,13 @@ def test_route_validation(lib):
     assert lib.moe_route(FAKE, FAKE, None, 4, 64, 8, 2, FAKE, FAKE, None, None, 0, None) == WORKSPACE
     n = S(0)
     assert lib.moe_route_workspace_size(4096, 2048, 128, ctypes.byref(n)) == 0
-    # tensor-core router: split weight (3*H*E bf16) + split-K fp32 partials
-    assert n.value >= 3 * 2048 * 128 * 2 + 4096 * 128 * 4
+    # fused tensor-core router (E % 16 == 0, E <= 256): the split weight (3*H*E bf16) only
+    assert n.value >= 3 * 2048 * 128 * 2
     assert lib.moe_route(FAKE, FAKE, None, 4096, 2048, 128, 8, FAKE, FAKE, None, FAKE, n.value - 1,
                          None) == WORKSPACE
+    # split-K tensor-core router (other E % 8 == 0): split weight + fp32 partials
+    assert lib.moe_route_workspace_size(4096, 2048, 200, ctypes.byref(n)) == 0
+    assert n.value >= 3 * 2048 * 200 * 2 + 4096 * 200 * 4
     assert lib.moe_route_workspace_size(4, 64, 7, ctypes.byref(n)) == 0 and n.value >= 4 * 7 * 4
     # T == 0 is a valid no-op
     assert lib.moe_route(None, None, None, 0, 64, 4, 2, None, None, None, None, 0, None) == 0

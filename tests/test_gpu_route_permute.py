@@ -11,8 +11,14 @@ pytestmark = pytest.mark.gpu
 
 
 @pytest.mark.parametrize("T,H,E,k", [(64, 128, 8, 2), (1, 64, 4, 1), (333, 256, 16, 4), (1000, 512, 128, 8),
-                                     (97, 128, 200, 8), (50, 64, 32, 32), (40, 96, 1024, 6)])
+                                     (97, 128, 200, 8), (50, 64, 32, 32), (40, 96, 1024, 6),
+                                     (129, 128, 48, 6), (257, 192, 240, 3), (300, 7168, 256, 8),
+                                     (4100, 2048, 128, 8)])
 def test_route_matches_oracle(T, H, E, k):
+    """Shapes of the three router paths: the fused cluster kernel (16 <= E <=
+    256, E % 16 == 0; clusters of 3, 6 and 8 CTAs, a partial 64-expert
+    chunk, ragged 128-token tiles), the split-K tensor-core GEMM with a
+    separate top-k (E % 8 == 0 otherwise) and the CUDA-core GEMM."""
     moe = lib()
     cfg = synth.MoEConfig("r", T=T, H=H, E=E, k=k, I=64, seed=T + E)
     inp = synth.make_inputs(cfg, weights=False)
@@ -92,8 +98,14 @@ def test_permute_rejects_out_of_range_id_on_device():
 
 
 @pytest.mark.parametrize("T,H,k,shared", [(64, 128, 2, False), (300, 256, 8, True), (1, 64, 1, False),
-                                          (1000, 2048, 8, False)])
+                                          (1000, 2048, 8, False), (37, 136, 32, True), (3, 8, 4, True),
+                                          (2000, 2056, 3, False), (5000, 2048, 8, False),
+                                          (300, 7168, 8, True)])
 def test_combine_matches_oracle(T, H, k, shared):
+    """Shapes of the shared-memory gather: k = 32 with the shared expert's row
+    (33 rows a stage), one 8-column chunk, a slice that is the whole odd-width
+    row, many units per CTA (the stage ring wraps), and 896-column slices of
+    7168-wide rows."""
     moe = lib()
     R = T * k
     yp_bits = synth.normal_bf16(5, 50, (R, H), 1.0)

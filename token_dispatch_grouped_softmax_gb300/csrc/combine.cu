@@ -54,7 +54,12 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict
     my_row = row_map[(int64_t)t * k + lane];
     my_w = w[(int64_t)t * k + lane];
   }
-  for (int c = c_begin + lane; c < c_end; c += 32) {
+  // The chunk loop stays warp-uniform (lanes past the slice only predicate
+  // their loads and stores) because every lane takes part in the shuffles
+  // that hand out the k rows and weights.
+  for (int base = c_begin; base < c_end; base += 32) {
+    const int c = base + lane;
+    const bool act = c < c_end;
     float acc[8];
 #pragma unroll
     for (int q = 0; q < 8; ++q) acc[q] = 0.f;
@@ -62,12 +67,15 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict
     for (int j = 0; j < k; ++j) {
       const int row = __shfl_sync(0xffffffffu, my_row, j);
       const float wj = __shfl_sync(0xffffffffu, my_w, j);
-      const uint4 v = __ldg(reinterpret_cast<const uint4*>(y_perm + (int64_t)row * H) + c);
-      float f[8];
-      unpack8(v, f);
+      if (act) {
+        const uint4 v = __ldg(reinterpret_cast<const uint4*>(y_perm + (int64_t)row * H) + c);
+        float f[8];
+        unpack8(v, f);
 #pragma unroll
-      for (int q = 0; q < 8; ++q) acc[q] = fmaf(wj, f[q], acc[q]);
+        for (int q = 0; q < 8; ++q) acc[q] = fmaf(wj, f[q], acc[q]);
+      }
     }
+    if (!act) continue;
     if (y_shared) {
       const uint4 v = __ldg(reinterpret_cast<const uint4*>(y_shared + (int64_t)t * H) + c);
       float f[8];
@@ -151,31 +159,37 @@ __global__ void __launch_bounds__(256) gather_dx_kernel(const uint16_t* __restri
       my_dz = d_logits[(int64_t)t * E + my_id];
     }
   }
-  for (int c = c_begin + lane; c < c_end; c += 32) {
+  for (int base = c_begin; base < c_end; base += 32) {   // warp-uniform, as in combine_kernel
+    const int c = base + lane;
+    const bool act = c < c_end;
     float acc[8];
 #pragma unroll
     for (int q = 0; q < 8; ++q) acc[q] = 0.f;
 #pragma unroll 8
     for (int j = 0; j < k; ++j) {
       const int row = __shfl_sync(0xffffffffu, my_row, j);
-      float f[8];
-      unpack8(__ldg(reinterpret_cast<const uint4*>(dx_perm + (int64_t)row * H) + c), f);
+      if (act) {
+        float f[8];
+        unpack8(__ldg(reinterpret_cast<const uint4*>(dx_perm + (int64_t)row * H) + c), f);
 #pragma unroll
-      for (int q = 0; q < 8; ++q) acc[q] += f[q];
+        for (int q = 0; q < 8; ++q) acc[q] += f[q];
+      }
     }
     if (d_logits) {
       for (int j = 0; j < k; ++j) {
         const int e = __shfl_sync(0xffffffffu, my_id, j);
         const float dz = __shfl_sync(0xffffffffu, my_dz, j);
-        const float4* wr = reinterpret_cast<const float4*>(wr_t + (int64_t)e * H) + 2 * c;
-        const float4 a = __ldg(wr), b = __ldg(wr + 1);
-        acc[0] = fmaf(dz, a.x, acc[0]); acc[1] = fmaf(dz, a.y, acc[1]);
-        acc[2] = fmaf(dz, a.z, acc[2]); acc[3] = fmaf(dz, a.w, acc[3]);
-        acc[4] = fmaf(dz, b.x, acc[4]); acc[5] = fmaf(dz, b.y, acc[5]);
-        acc[6] = fmaf(dz, b.z, acc[6]); acc[7] = fmaf(dz, b.w, acc[7]);
+        if (act) {
+          const float4* wr = reinterpret_cast<const float4*>(wr_t + (int64_t)e * H) + 2 * c;
+          const float4 a = __ldg(wr), b = __ldg(wr + 1);
+          acc[0] = fmaf(dz, a.x, acc[0]); acc[1] = fmaf(dz, a.y, acc[1]);
+          acc[2] = fmaf(dz, a.z, acc[2]); acc[3] = fmaf(dz, a.w, acc[3]);
+          acc[4] = fmaf(dz, b.x, acc[4]); acc[5] = fmaf(dz, b.y, acc[5]);
+          acc[6] = fmaf(dz, b.z, acc[6]); acc[7] = fmaf(dz, b.w, acc[7]);
+        }
       }
     }
-    reinterpret_cast<uint4*>(dx + (int64_t)t * H)[c] = pack8(acc);
+    if (act) reinterpret_cast<uint4*>(dx + (int64_t)t * H)[c] = pack8(acc);
   }
 }
 

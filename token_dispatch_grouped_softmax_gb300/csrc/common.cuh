@@ -130,7 +130,8 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t par
 template <bool CLUSTER = false>
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
                                                   volatile int* abort, uint64_t limit_ns,
-                                                  uint32_t* status, uint32_t site) {
+                                                  uint32_t* status, uint32_t site,
+                                                  uint32_t kernel = kKernGemm) {
   auto try_wait = [&]() { return CLUSTER ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity); };
   if (try_wait()) return true;
   const uint64_t t0 = globaltimer_ns();
@@ -140,7 +141,7 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
       if (*abort) return false;
       if (globaltimer_ns() - t0 > limit_ns) {
         *abort = 1;
-        report_status(status, kStatusTimeout, kKernGemm, site);
+        report_status(status, kStatusTimeout, kernel, site);
         return false;
       }
     }
@@ -165,6 +166,31 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
   uint32_t r;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
   return r;
+}
+
+// Number of CTAs in this CTA's cluster.
+__device__ __forceinline__ uint32_t cluster_nctas() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+  return r;
+}
+
+// fp32 load from a shared::cluster address (possibly another CTA's memory).
+// No memory clobber: a run of them issues back to back; order them against
+// the cluster barrier that publishes the data (an asm with a memory clobber).
+__device__ __forceinline__ float ld_shared_cluster_f32(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr));
+  return v;
+}
+
+// The same, four consecutive floats (a 16-byte aligned address).
+__device__ __forceinline__ float4 ld_shared_cluster_f32x4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(addr));
+  return v;
 }
 
 // Arrive (release at cluster scope) on an mbarrier given by its
@@ -287,6 +313,17 @@ __device__ __forceinline__ void tmem_relinquish_pair() {
 __device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
   asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
                : "memory");
+}
+
+// UMMA shared-memory descriptor, 128-byte swizzle, sm_100-family version bits.
+__device__ __forceinline__ uint64_t umma_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+  d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;
+  return d;
 }
 
 // D[tmem] (+)= A[smem] * B[smem], bf16 inputs, fp32 accumulator.

@@ -143,17 +143,6 @@ struct GemmParams {   // 64-byte aligned through its CUtensorMap members
   int stall_producer;       // test hook: the producer issues no loads (a wait that runs out)
 };
 
-// UMMA shared-memory descriptor, 128-byte swizzle, sm_100-family version bits.
-__device__ __forceinline__ uint64_t umma_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
-  uint64_t d = 0;
-  d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
-  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
-  d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
-  d |= (uint64_t)1 << 46;
-  d |= (uint64_t)2 << 61;
-  return d;
-}
-
 template <int MODE, int KH, int CG>
 __device__ __forceinline__ uint32_t make_idesc(int m = BMH * CG) {
   using Tr = Traits<MODE, KH, CG>;

@@ -13,6 +13,10 @@
 // with x repeated along K, split into `parts` K ranges (one CTA tile each)
 // whose fp32 partials the top-k kernel adds in a fixed order.
 //
+// With 16 <= E <= 256 and E % 16 == 0 one fused kernel also picks the top
+// k: a cluster of CTAs per 128-token tile splits K and sums its fp32
+// partials over distributed shared memory (fused_router_kernel below).
+//
 // Other shapes use route_logits_kernel: a register-tiled fp32 GEMM on the
 // CUDA cores (32 tokens x 64 experts per 256-thread block).
 //
@@ -118,11 +122,6 @@ __global__ void __launch_bounds__(256) route_logits_kernel(const uint16_t* __res
   }
 }
 
-// (value, index) with larger value first, lower index first on equal values
-__device__ __forceinline__ bool better(float v1, int i1, float v2, int i2) {
-  return v1 > v2 || (v1 == v2 && i1 < i2);
-}
-
 // W_r [H, E] fp32 -> [3, H, E] bf16 with W_r = W0 + W1 + W2 exactly.
 __global__ void split_router_weight_kernel(const float* __restrict__ wr, int64_t n,
                                            uint16_t* __restrict__ out) {
@@ -140,6 +139,85 @@ __global__ void split_router_weight_kernel(const float* __restrict__ wr, int64_t
   }
 }
 
+// Order-preserving 64-bit key of (logit v, expert e): larger v gives a
+// larger key, and on equal v the lower expert index does (the float's bits
+// are mapped to an unsigned order, the index is stored complemented).
+__device__ __forceinline__ uint64_t topk_key(float v, int e) {
+  uint32_t u = __float_as_uint(v);
+  u = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+  return ((uint64_t)u << 32) | (uint64_t)(0xFFFFFFFFu - (uint32_t)e);
+}
+__device__ __forceinline__ float topk_key_value(uint64_t key) {
+  uint32_t u = (uint32_t)(key >> 32);
+  u = (u & 0x80000000u) ? (u & 0x7FFFFFFFu) : ~u;
+  return __uint_as_float(u);
+}
+__device__ __forceinline__ int topk_key_index(uint64_t key) { return (int)(0xFFFFFFFFu - (uint32_t)key); }
+
+// Expert held in v[i] by lane `lane`: l + 32 i, or with QUAD 128 (i / 4) +
+// 4 l + i % 4 (four consecutive experts per lane, read as one vector).
+template <bool QUAD>
+__device__ __forceinline__ int topk_expert(int lane, int i) {
+  return QUAD ? 128 * (i / 4) + 4 * lane + (i % 4) : lane + 32 * i;
+}
+
+// Top k of one token's logits, warp-wide: lane l holds z[topk_expert(l, i)]
+// in v[i] (the partial sums, before the bias).  Adds the bias, writes the logits
+// when asked, and writes the ids and renormalised weights.  Each lane sorts
+// its NV keys; round j takes the warp maximum of the lanes' leading keys
+// (warp reductions) and the lane that held it drops it.  The keys
+// are distinct (they carry the index), so the order is the (value desc,
+// index asc) order; w_j = exp(z_j - z_0) / sum_j exp(z_j - z_0), summed in
+// increasing j.
+template <int NV, bool QUAD = false>
+__device__ __forceinline__ void topk_row(float (&v)[NV], int64_t t, int E, int k, int lane,
+                                         const float* __restrict__ bias, int32_t* __restrict__ ids,
+                                         float* __restrict__ w, float* __restrict__ logits_out) {
+  uint64_t key[NV];
+#pragma unroll
+  for (int i = 0; i < NV; ++i) {
+    const int e = topk_expert<QUAD>(lane, i);
+    key[i] = 0;   // below every logit's key
+    if (e < E) {
+      if (bias) v[i] += bias[e];
+      if (logits_out) logits_out[t * E + e] = v[i];
+      key[i] = topk_key(v[i], e);
+    }
+  }
+#pragma unroll
+  for (int a = 0; a < NV - 1; ++a)     // descending, by adjacent compare-exchanges
+#pragma unroll
+    for (int b = NV - 1; b > a; --b)
+      if (key[b] > key[b - 1]) {
+        const uint64_t tmp = key[b];
+        key[b] = key[b - 1];
+        key[b - 1] = tmp;
+      }
+  uint64_t mine = 0;   // lane j < k: the j-th chosen key
+  for (int j = 0; j < k; ++j) {
+    // warp maximum of the leading keys: of the value bits, then of the
+    // index bits among the lanes holding that value (two warp reductions)
+    const uint32_t hi = (uint32_t)(key[0] >> 32), lo = (uint32_t)key[0];
+    const uint32_t mhi = __reduce_max_sync(0xffffffffu, hi);
+    const uint32_t mlo = __reduce_max_sync(0xffffffffu, hi == mhi ? lo : 0u);
+    const uint64_t m = ((uint64_t)mhi << 32) | mlo;
+    if (key[0] == m) {   // this lane held it
+#pragma unroll
+      for (int i = 0; i < NV - 1; ++i) key[i] = key[i + 1];
+      key[NV - 1] = 0;
+    }
+    if (lane == j) mine = m;
+  }
+  const float zmax = topk_key_value(__shfl_sync(0xffffffffu, mine, 0));
+  const float ez = lane < k ? expf(topk_key_value(mine) - zmax) : 0.f;
+  float esum = 0.f;
+  for (int j = 0; j < k; ++j) esum += __shfl_sync(0xffffffffu, ez, j);
+  if (lane < k) {
+    ids[t * k + lane] = topk_key_index(mine);
+    w[t * k + lane] = ez / esum;
+  }
+}
+
 // One warp per token.  z[e] = sum_p part[p][t][e] (+ bias[e]), p in
 // increasing order; NV = logits per lane (E <= 32 * NV).
 template <int NV>
@@ -151,7 +229,6 @@ __global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict
   const int lane = threadIdx.x & 31;
   const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
   if (t >= T) return;
-  const float NEG = -INFINITY;
   float v[NV];
   // partials added in increasing part order; the NV loads of one part are
   // independent, and the part loop is unrolled so the loads overlap
@@ -169,53 +246,338 @@ __global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict
       if (e < E) v[i] += __ldg(pq + e);
     }
   }
-#pragma unroll
-  for (int i = 0; i < NV; ++i) {
-    const int e = lane + 32 * i;
-    if (e < E) {
-      if (bias) v[i] += bias[e];
-      if (logits_out) logits_out[(int64_t)t * E + e] = v[i];
-    } else {
-      v[i] = NEG;
+  topk_row<NV>(v, t, E, k, lane, bias, ids, w, logits_out);
+}
+
+// ---------------------------------------------------------------------------
+// Fused router (E % 16 == 0, 16 <= E <= 256, H % 64 == 0).  One cluster of P
+// CTAs per 128-token tile splits K into P equal ranges.  CTA c accumulates
+// its range in TMEM (tcgen05.mma, M = 128, N = E, bf16 x bf16 -> fp32; warp
+// 0 loads x and W tiles by TMA, warp 1 issues the MMAs), warps 2..5 copy the
+// fp32 partial tile into shared memory (over the emptied operand ring), and
+// after a cluster barrier each CTA sums, for its share of the tile's rows,
+// the P partials over distributed shared memory in increasing CTA rank and
+// picks the top k of each row.  No partial logits reach HBM.
+//   E <= 128: a stage holds one 64-wide K block of x and of all three terms
+//             W0, W1, W2 (x loaded once for the three); K = H is split.
+//   E > 128:  a stage holds one K block of the stacked K = 3H of [W0; W1; W2]
+//             and the x block it multiplies.
+// Waits are bounded (MOE_ERR_TIMEOUT in the status word).
+// Threads per CTA: warps 0..5 take the roles above; then every warp picks
+// the top k of rows of the tile, one row at a time.  With E <= 128 a CTA has
+// 32 warps, so a cluster of 4 has one warp per row of its 128-token tile;
+// with E > 128 (more registers per lane) 12.
+template <int NV>
+__host__ __device__ constexpr int fr_threads() { return NV <= 4 ? 1024 : 384; }
+constexpr int kFrStages = 3;
+constexpr int kFrMaxCluster = 8;
+constexpr int kFrABytes = 128 * 64 * 2;     // 128 tokens x 64 K
+constexpr int kFrChunkBytes = 64 * 64 * 2;  // 64 K x 64 experts
+
+struct FusedRouterParams {
+  CUtensorMap tmA;   // x [T, H] bf16, boxes of 64 K x 128 tokens, 128-byte swizzle
+  CUtensorMap tmB;   // [W0; W1; W2] [3H, E] bf16, boxes of 64 experts x 64 K
+  const float* bias;
+  int32_t* ids;
+  float* w;
+  float* logits;
+  uint32_t* status;
+  uint64_t wait_limit_ns;
+  int T, H, E, k;
+  int kblocks;       // 64-wide K blocks per CTA
+  int nchunks;       // 64-expert chunks of a B tile: ceil(E / 64)
+  int terms;         // W terms per stage: 3 (K = H split), or 1 (K = 3H split)
+  uint32_t tmem_cols;
+};
+
+__host__ __device__ inline int fr_stage_bytes(int nchunks, int terms) {
+  return kFrABytes + terms * nchunks * kFrChunkBytes;
+}
+
+template <int NV>
+__global__ void __launch_bounds__(fr_threads<NV>(), 1) fused_router_kernel(const __grid_constant__ FusedRouterParams p) {
+  constexpr int kWarps = fr_threads<NV>() / 32;
+  extern __shared__ uint8_t fr_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(fr_raw) + 1023) & ~uintptr_t(1023));
+  const int stage_bytes = fr_stage_bytes(p.nchunks, p.terms);
+  uint8_t* ring = smem;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kFrStages * stage_bytes);   // full[3], empty[3], accf, drain
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kFrStages + 2);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  // the partial tile [128][E + 4] (16-byte aligned rows) over the ring, once
+  // the MMAs are done
+  float* part = reinterpret_cast<float*>(smem);
+  const int ldp = p.E + 4;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int P = (int)cluster_nctas();
+  const int crank = (int)cluster_ctarank();
+  const int row0 = (blockIdx.x / P) * 128;
+  const uint32_t bar0 = smem_u32(bars);
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (kFrStages + s); };
+  const uint32_t accf_bar = bar0 + 8u * (2 * kFrStages);
+  const uint32_t drain_bar = bar0 + 8u * (2 * kFrStages + 1);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kFrStages; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
     }
+    mbar_init(accf_bar, 1);
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
   }
-  float zmax = 0.f, esum = 0.f;
-  int my_id = 0;
-  float my_e = 0.f;
-  uint32_t taken = 0;               // bit i: expert lane + 32 i already chosen
-  for (int j = 0; j < k; ++j) {
-    float bv = NEG;
-    int bi = 0x7fffffff;
-#pragma unroll
-    for (int i = 0; i < NV; ++i) {
-      const int e = lane + 32 * i;
-      if (e < E && !((taken >> i) & 1u) && better(v[i], e, bv, bi)) {
-        bv = v[i];
-        bi = e;
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&p.tmA);
+    tma_prefetch_desc(&p.tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), p.tmem_cols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const int kb0 = crank * p.kblocks;   // first K block of this CTA (of H, or of the stacked 3H)
+
+  if (warp == 0) {
+    // ------------------------------------------------------ TMA producer
+    int stage = 0;
+    uint32_t phase = 0;
+    uint32_t issued = 0, last_par = 0;
+    bool ok = true;
+    for (int kb = 0; kb < p.kblocks; ++kb) {
+      bool w = true;
+      if (lane == 0)
+        w = mbar_wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, p.wait_limit_ns, p.status, 1, kKernRoute);
+      ok = __shfl_sync(0xffffffffu, w ? 1 : 0, 0) != 0;
+      if (!ok) break;
+      if (lane == 0) {
+        const uint32_t fb = full_bar(stage);
+        const uint32_t sA = smem_u32(ring + stage * stage_bytes);
+        const int kg = (kb0 + kb) * 64;   // K row: of H (three terms), or of the stacked 3H
+        mbar_arrive_expect_tx(fb, (uint32_t)stage_bytes);
+        tma_load_2d(sA, &p.tmA, kg % p.H, row0, fb);   // x repeats along the stacked K
+        for (int q = 0; q < p.terms; ++q)              // term q: rows q*H + kg of [W0; W1; W2]
+          for (int c = 0; c < p.nchunks; ++c)
+            tma_load_2d(sA + kFrABytes + (q * p.nchunks + c) * kFrChunkBytes, &p.tmB, 64 * c, q * p.H + kg, fb);
+      }
+      __syncwarp();
+      issued |= 1u << stage;
+      last_par = (last_par & ~(1u << stage)) | (phase << stage);
+      if (++stage == kFrStages) {
+        stage = 0;
+        phase ^= 1u;
       }
     }
+    if (!ok && lane == 0) {   // stopped early: wait (bounded) for the copies in flight
+      for (int s = 0; s < kFrStages; ++s)
+        if (issued & (1u << s)) {
+          const uint64_t t0 = globaltimer_ns();
+          while (!mbar_try_wait(full_bar(s), (last_par >> s) & 1u) && globaltimer_ns() - t0 < p.wait_limit_ns) {
+          }
+        }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------- MMA issuer
+    // D fp32, A bf16 K-major, B bf16 MN-major, N = E, M = 128
+    const uint32_t idesc = (1u << 4) | (1u << 7) | (1u << 10) | (1u << 16) | ((uint32_t)(p.E >> 3) << 17) |
+                           ((uint32_t)(128 >> 4) << 24);
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true, issued_any = false;
+    for (int kb = 0; kb < p.kblocks; ++kb) {
+      bool w = true;
+      if (lane == 0)
+        w = mbar_wait_bounded(full_bar(stage), phase, abort_flag, p.wait_limit_ns, p.status, 2, kKernRoute);
+      ok = __shfl_sync(0xffffffffu, w ? 1 : 0, 0) != 0;
+      if (!ok) break;
+      tc_fence_after();
+      if (lane == 0) {
+        const uint32_t sA = smem_u32(ring + stage * stage_bytes);
+        for (int q = 0; q < p.terms; ++q) {
+          const uint32_t sB = sA + kFrABytes + q * p.nchunks * kFrChunkBytes;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-      if (better(ov, oi, bv, bi)) {
-        bv = ov;
-        bi = oi;
+          for (int kk = 0; kk < 4; ++kk)
+            tc_mma_bf16(tmem_base, umma_desc(sA + kk * 32, 16, 1024),
+                        umma_desc(sB + kk * 2048, kFrChunkBytes, 1024), idesc, (kb | q | kk) != 0 ? 1u : 0u);
+        }
+        tc_commit(empty_bar(stage));
+      }
+      issued_any = true;
+      __syncwarp();
+      if (++stage == kFrStages) {
+        stage = 0;
+        phase ^= 1u;
       }
     }
-    if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
-    if (j == 0) zmax = bv;
-    const float ez = expf(bv - zmax);
-    esum += ez;
-    if (lane == j) {
-      my_id = bi;
-      my_e = ez;
+    if (lane == 0) {
+      if (ok) {
+        tc_commit(accf_bar);
+      } else if (issued_any) {   // make sure every MMA issued has finished before TMEM is freed
+        tc_commit(drain_bar);
+        const uint64_t t0 = globaltimer_ns();
+        while (!mbar_try_wait(drain_bar, 0) && globaltimer_ns() - t0 < p.wait_limit_ns) {
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp < 6) {
+    // ------------------------------------- partial tile: TMEM -> shared
+    bool w = true;
+    if (lane == 0) w = mbar_wait_bounded(accf_bar, 0, abort_flag, p.wait_limit_ns, p.status, 3, kKernRoute);
+    if (__shfl_sync(0xffffffffu, w ? 1 : 0, 0) != 0) {
+      tc_fence_after();
+      const int quarter = warp & 3;              // TMEM lanes 32 quarter .. +31
+      const int r = quarter * 32 + lane;         // tile row of this thread
+      float* prow = part + r * ldp;
+      for (int c0 = 0; c0 < p.E; c0 += 32) {   // E % 16 == 0: 4-column groups are whole
+        float v[32];
+        tmem_ld32(tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)c0, v);
+#pragma unroll
+        for (int q = 0; q < 32; q += 4)
+          if (c0 + q < p.E) *reinterpret_cast<float4*>(prow + c0 + q) = make_float4(v[q], v[q + 1], v[q + 2], v[q + 3]);
+      }
     }
   }
-  if (lane < k) {
-    ids[(int64_t)t * k + lane] = my_id;
-    w[(int64_t)t * k + lane] = my_e / esum;
+
+  // every CTA's partial tile is in its shared memory
+  __syncwarp();
+  tc_fence_before();
+  cluster_sync_all();
+  // ------------------------------------------------ reduce and pick top k
+  // rows crank, crank + P, ... of the tile, one warp per row
+  const uint32_t part_u32 = smem_u32(part);
+  for (int r = crank + P * warp; r < 128; r += P * kWarps) {
+    const int64_t t = row0 + r;
+    if (t >= p.T) break;
+    // all remote loads first (they overlap), four consecutive experts per
+    // lane and load; then the sums in increasing CTA rank
+    float4 xs[kFrMaxCluster][NV / 4];
+    const uint32_t row_addr = part_u32 + (uint32_t)(r * ldp) * 4u;
+#pragma unroll
+    for (int c = 0; c < kFrMaxCluster; ++c) {
+      if (c < P) {
+        const uint32_t base = mapa_shared(row_addr, (uint32_t)c);
+#pragma unroll
+        for (int q = 0; q < NV / 4; ++q) {
+          const int e = topk_expert<true>(lane, 4 * q);
+          xs[c][q] = e < p.E ? ld_shared_cluster_f32x4(base + 4u * (uint32_t)e) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+      }
+    }
+    float v[NV];
+#pragma unroll
+    for (int q = 0; q < NV / 4; ++q) {
+      float4 a = xs[0][q];
+#pragma unroll
+      for (int c = 1; c < kFrMaxCluster; ++c)
+        if (c < P) {
+          a.x += xs[c][q].x;
+          a.y += xs[c][q].y;
+          a.z += xs[c][q].z;
+          a.w += xs[c][q].w;
+        }
+      v[4 * q] = a.x;
+      v[4 * q + 1] = a.y;
+      v[4 * q + 2] = a.z;
+      v[4 * q + 3] = a.w;
+    }
+    topk_row<NV, true>(v, t, p.E, p.k, lane, p.bias, p.ids, p.w, p.logits);
   }
+  // no CTA leaves (or frees its TMEM) while another may still read its partials
+  __syncwarp();
+  cluster_sync_all();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, p.tmem_cols);
+  }
+}
+
+int fused_router_terms(int64_t E) { return E <= 128 ? 3 : 1; }
+
+// The cluster size: a divisor of the CTA's K blocks, at most 8 (the portable
+// cluster limit); with three terms per stage (one CTA per SM) the largest one
+// that keeps the grid within one wave of the SMs, else the largest.
+int fused_router_cluster(int64_t T, int64_t H, int64_t E, int num_sms) {
+  const int terms = fused_router_terms(E);
+  const int64_t kb = (terms == 3 ? 1 : 3) * H / 64;
+  const int64_t tiles = (T + 127) / 128;
+  for (int d = kFrMaxCluster; d > 1; --d)
+    if (kb % d == 0 && (terms == 1 || tiles * d <= num_sms)) return d;
+  return 1;
+}
+
+bool fused_router_ok(int64_t H, int64_t E) { return H % 64 == 0 && E % 16 == 0 && E >= 16 && E <= 256; }
+
+size_t fused_router_smem(int64_t E) {
+  return 1024 + (size_t)kFrStages * fr_stage_bytes((int)((E + 63) / 64), fused_router_terms(E)) +
+         8 * (2 * kFrStages + 2) + 16;
+}
+
+template <int NV>
+cudaError_t launch_fused_router_nv(const FusedRouterParams& p, int P, int64_t T, const DeviceInfo& dev,
+                                   cudaStream_t stream) {
+  static int configured[kMaxDevices] = {0};
+  if (!configured[dev.ordinal]) {
+    const cudaError_t err = cudaFuncSetAttribute(fused_router_kernel<NV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                 (int)std::max(fused_router_smem(128), fused_router_smem(256)));
+    if (err != cudaSuccess) return err;
+    configured[dev.ordinal] = 1;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)P;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3((unsigned)(((T + 127) / 128) * P));
+  cfg.blockDim = dim3(fr_threads<NV>());
+  cfg.dynamicSmemBytes = fused_router_smem(p.E);
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, fused_router_kernel<NV>, p);
+}
+
+cudaError_t launch_fused_router(const uint16_t* x, const uint16_t* w_split, const float* bias, int64_t T, int64_t H,
+                                int64_t E, int64_t k, int32_t* ids, float* w, float* logits, const DeviceInfo& dev,
+                                cudaStream_t stream) {
+  FusedRouterParams p;
+  const cuuint32_t estr[2] = {1, 1};
+  {
+    const cuuint64_t dims[2] = {(cuuint64_t)H, (cuuint64_t)T};
+    const cuuint64_t strides[1] = {(cuuint64_t)(H * 2)};
+    const cuuint32_t box[2] = {64, 128};
+    if (!encode_tensor_map_2d_bf16(&p.tmA, x, dims, strides, box, estr)) return cudaErrorInvalidValue;
+  }
+  {
+    const cuuint64_t dims[2] = {(cuuint64_t)E, (cuuint64_t)(3 * H)};
+    const cuuint64_t strides[1] = {(cuuint64_t)(E * 2)};
+    const cuuint32_t box[2] = {64, 64};
+    if (!encode_tensor_map_2d_bf16(&p.tmB, w_split, dims, strides, box, estr)) return cudaErrorInvalidValue;
+  }
+  const int P = fused_router_cluster(T, H, E, dev.num_sms);
+  p.bias = bias;
+  p.ids = ids;
+  p.w = w;
+  p.logits = logits;
+  p.status = dev.status;
+  p.wait_limit_ns = dev.wait_limit_ns;
+  p.T = (int)T;
+  p.H = (int)H;
+  p.E = (int)E;
+  p.k = (int)k;
+  p.terms = fused_router_terms(E);
+  p.kblocks = (int)((p.terms == 3 ? 1 : 3) * H / 64 / P);
+  p.nchunks = (int)((E + 63) / 64);
+  p.tmem_cols = E <= 32 ? 32u : E <= 64 ? 64u : E <= 128 ? 128u : 256u;
+  // NV: logits per lane, four consecutive experts per vector
+  if (E <= 128) return launch_fused_router_nv<4>(p, P, T, dev, stream);
+  return launch_fused_router_nv<8>(p, P, T, dev, stream);
 }
 
 template <int NV>
@@ -241,6 +603,7 @@ bool route_on_tensor_cores(int64_t H, int64_t E) { return E % 8 == 0 && H % 64 =
 
 size_t route_workspace_bytes(int64_t T, int64_t H, int64_t E) {
   auto align = [](size_t b) { return (b + 255) & ~size_t(255); };
+  if (fused_router_ok(H, E)) return align((size_t)(3 * H * E * 2));
   if (route_on_tensor_cores(H, E)) {
     const int parts = router_parts(T, H, E);
     return align((size_t)(3 * H * E * 2)) + align((size_t)(parts * T * E * 4));
@@ -254,7 +617,14 @@ cudaError_t launch_route(const uint16_t* x, const float* w_router, const float* 
   if (T == 0) return cudaSuccess;
   auto align = [](size_t b) { return (b + 255) & ~size_t(255); };
   uint8_t* wsb = static_cast<uint8_t*>(ws);
-  if (route_on_tensor_cores(H, E)) {
+  if (fused_router_ok(H, E)) {
+    uint16_t* w_split = reinterpret_cast<uint16_t*>(wsb);
+    const int64_t n = H * E;
+    split_router_weight_kernel<<<(unsigned)std::min<int64_t>((n + 255) / 256, 4096), 256, 0, stream>>>(
+        w_router, n, w_split);
+    const cudaError_t err = launch_fused_router(x, w_split, bias, T, H, E, k, ids, w, logits, dev, stream);
+    if (err != cudaSuccess) return err;
+  } else if (route_on_tensor_cores(H, E)) {
     const int parts = router_parts(T, H, E);
     uint16_t* w_split = reinterpret_cast<uint16_t*>(wsb);
     float* part = reinterpret_cast<float*>(wsb + align((size_t)(3 * H * E * 2)));
