@@ -115,7 +115,9 @@ int moe_route(const uint16_t* x, const float* w_router, const float* bias, int64
 
 /* ---------------------------------------------------------------- permute */
 
-/* Bytes of workspace moe_permute needs (per-block expert histograms). */
+/* Bytes of workspace moe_permute needs: per-block expert histograms, the
+ * expert totals and two grid-barrier counters (the workspace must be 16-byte
+ * aligned; nothing in it needs clearing). */
 int moe_permute_workspace_size(int64_t T, int64_t k, int64_t E, size_t* bytes);
 
 /* Group the R = T*k assignments by expert ("Awesome-ML-SYS-Tutorial" guide:
@@ -128,9 +130,13 @@ int moe_permute_workspace_size(int64_t T, int64_t k, int64_t E, size_t* bytes);
  *                                rows of one expert keep increasing i
  *   src_row  [R] int32 (out)     token of each permuted row (= i / k)
  *   w_perm   [R] fp32 (out) or NULL   w_perm[row_map[i]] = w[i]
- * Deterministic (no order-dependent atomics).  An id outside [0, E) sets
- * MOE_ERR_DEVICE in the status word; the outputs are then undefined.
- * Limits: E <= 1024, R < 2^31. */
+ * Deterministic (no order-dependent atomics).  When all of its blocks fit on
+ * the device at once (R up to about 300k assignments on a GB300) it is one
+ * cooperative launch whose two grid barriers are bounded waits
+ * (MOE_ERR_TIMEOUT in the status word if one runs out); otherwise three
+ * launches.  An id outside [0, E) sets MOE_ERR_DEVICE in the status word;
+ * the outputs are then undefined.  A misaligned workspace returns
+ * MOE_ERR_INVALID_ARG.  Limits: E <= 1024, R < 2^31. */
 int moe_permute(const int32_t* ids, const float* w, int64_t T, int64_t k, int64_t E, int32_t* counts,
                 int32_t* offsets, int32_t* row_map, int32_t* src_row, float* w_perm, void* workspace,
                 size_t workspace_bytes, void* stream);

@@ -97,6 +97,8 @@ def test_permute_validation(lib):
     assert pm(None, None, 100, 8, 128, FAKE, FAKE, FAKE, FAKE, None, FAKE, n.value, None) == INVALID
     # w and w_perm come together
     assert pm(FAKE, FAKE, 100, 8, 128, FAKE, FAKE, FAKE, FAKE, None, FAKE, n.value, None) == INVALID
+    # the workspace holds the grid-barrier counters: 16-byte aligned
+    assert pm(FAKE, None, 100, 8, 128, FAKE, FAKE, FAKE, FAKE, None, MISALIGNED, n.value, None) == INVALID
 
 
 def test_gemm_validation(lib):

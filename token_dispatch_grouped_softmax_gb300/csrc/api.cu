@@ -173,11 +173,12 @@ int moe_permute(const int32_t* ids, const float* w, int64_t T, int64_t k, int64_
   if ((w == nullptr) != (w_perm == nullptr)) return MOE_ERR_INVALID_ARG;
   if (E > moe::kMaxExperts) return MOE_ERR_UNSUPPORTED;
   if (!workspace || workspace_bytes < moe::permute_workspace_bytes(T * k, E)) return MOE_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return MOE_ERR_INVALID_ARG;
   moe::DeviceInfo dev;
   int rc = moe::current_device(&dev);
   if (rc != MOE_OK) return rc;
   return cuda_status(moe::launch_permute(ids, w, T, k, E, counts, offsets, row_map, src_row, w_perm,
-                                         workspace, dev.status, static_cast<cudaStream_t>(stream)));
+                                         workspace, dev, static_cast<cudaStream_t>(stream)));
 }
 
 int moe_permute_rows(const uint16_t* x, const int32_t* src_row, int64_t R, int64_t H,

@@ -40,7 +40,7 @@ cudaError_t launch_route(const uint16_t* x, const float* w_router, const float* 
 size_t permute_workspace_bytes(int64_t R, int64_t E, bool noalloc = false);
 cudaError_t launch_permute(const int32_t* ids, const float* w, int64_t T, int64_t k, int64_t E,
                            int32_t* counts, int32_t* offsets, int32_t* row_map, int32_t* src_row,
-                           float* w_perm, void* ws, uint32_t* status, cudaStream_t stream,
+                           float* w_perm, void* ws, const DeviceInfo& dev, cudaStream_t stream,
                            bool noalloc = false);
 cudaError_t launch_permute_rows(const uint16_t* x, const int32_t* src_row, int64_t R, int64_t H,
                                 uint16_t* x_perm, cudaStream_t stream);

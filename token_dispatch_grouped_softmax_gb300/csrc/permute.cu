@@ -189,6 +189,170 @@ __global__ void __launch_bounds__(kPermThreads) permute_scatter_kernel(
   }
 }
 
+// ------------------------------------------------------------------------
+// The same counting sort in one cooperative launch (every block resident at
+// once), its three passes separated by two grid barriers:
+//   1. block b counts its chunk per warp (kept in shared memory) and writes
+//      its block histogram hist[b][e];
+//   2. warp g of the grid scans expert column e = g, g + G, ...: hist[b][e]
+//      becomes sum_{b' < b} hist[b'][e], totals[e] the column sum;
+//   3. every block scans the totals over experts (offsets; block 0 writes
+//      counts and offsets), forms its warps' bases offsets[e] + hist[b][e] +
+//      the counts of its lower warps, and ranks its chunk stably.
+// Each barrier is an arrival counter (zeroed by the host before the launch)
+// that a block's thread 0 waits on with a bounded spin; a wait that runs out
+// records MOE_ERR_TIMEOUT and ends the block.
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ bool grid_barrier(uint32_t* count, uint32_t nblocks, uint64_t limit_ns,
+                                             uint32_t* status, uint32_t site, int* ok_sh) {
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    atomicAdd(count, 1u);
+    bool ok = true;
+    if (ld_acquire_gpu(count) < nblocks) {
+      const uint64_t t0 = globaltimer_ns();
+      while (ld_acquire_gpu(count) < nblocks) {
+        if (globaltimer_ns() - t0 > limit_ns) {
+          report_status(status, kStatusTimeout, kKernPermute, site);
+          ok = false;
+          break;
+        }
+      }
+    }
+    __threadfence();
+    *ok_sh = ok ? 1 : 0;
+  }
+  __syncthreads();
+  return *ok_sh != 0;
+}
+
+template <int CHUNK>
+__global__ void __launch_bounds__(kPermThreads) permute_fused_kernel(
+    const int32_t* __restrict__ ids, const float* __restrict__ w, int64_t R, int k, int E,
+    int32_t* __restrict__ hist, int32_t* __restrict__ totals, uint32_t* __restrict__ bar,
+    int32_t* __restrict__ counts, int32_t* __restrict__ offsets, int32_t* __restrict__ row_map,
+    int32_t* __restrict__ src_row, float* __restrict__ w_perm, uint32_t* status, uint64_t wait_limit_ns) {
+  constexpr int kPerWarp = CHUNK / kPermWarps;
+  extern __shared__ int32_t sh[];   // [kPermWarps][E] warp counts, then bases; [E] offsets; [32] scan
+  int32_t* off = sh + kPermWarps * E;
+  int32_t* wtot = off + E;
+  __shared__ int ok_sh;
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  const int nb = gridDim.x;
+  const int64_t slice0 = (int64_t)blockIdx.x * CHUNK + (int64_t)wid * kPerWarp;
+
+  // 1. per-warp counts and the block histogram
+  for (int q = threadIdx.x; q < kPermWarps * E; q += blockDim.x) sh[q] = 0;
+  __syncthreads();
+  for (int s = 0; s < kPerWarp; s += 32) {
+    const int64_t i = slice0 + s + lane;
+    if (i < R) {
+      const int e = ids[i];
+      if (e < 0 || e >= E) report_status(status, kStatusDevice, kKernPermute, 1);
+      else atomicAdd(&sh[wid * E + e], 1);   // counts only: the order of increments is irrelevant
+    }
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int32_t c = 0;
+    for (int w2 = 0; w2 < kPermWarps; ++w2) c += sh[w2 * E + e];
+    hist[(int64_t)blockIdx.x * E + e] = c;
+  }
+  if (!grid_barrier(bar, (uint32_t)nb, wait_limit_ns, status, 3, &ok_sh)) return;
+
+  // 2. column scans over the blocks, one warp per expert column
+  const int G = nb * kPermWarps;
+  for (int e = blockIdx.x * kPermWarps + wid; e < E; e += G) {
+    int32_t carry = 0;
+    for (int b0 = 0; b0 < nb; b0 += 32) {
+      const int b = b0 + lane;
+      const int32_t v = b < nb ? __ldcg(hist + (int64_t)b * E + e) : 0;
+      int32_t incl = v;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int32_t n = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += n;
+      }
+      if (b < nb) hist[(int64_t)b * E + e] = carry + incl - v;
+      carry += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) totals[e] = carry;
+  }
+  if (!grid_barrier(bar + 1, (uint32_t)nb, wait_limit_ns, status, 4, &ok_sh)) return;
+
+  // 3a. offsets: exclusive scan of the totals over experts (every block)
+  for (int e0 = 0; e0 < E; e0 += blockDim.x) {
+    const int e = e0 + threadIdx.x;
+    const int32_t v = e < E ? __ldcg(totals + e) : 0;
+    int32_t incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int32_t n = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += n;
+    }
+    if (lane == 31) wtot[wid] = incl;
+    __syncthreads();
+    if (wid == 0) {
+      const int32_t t = lane < kPermWarps ? wtot[lane] : 0;
+      int32_t s2 = t;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int32_t n = __shfl_up_sync(0xffffffffu, s2, o);
+        if (lane >= o) s2 += n;
+      }
+      if (lane < kPermWarps) wtot[lane] = s2 - t;           // exclusive prefix of the warp sums
+      if (lane == kPermWarps - 1) wtot[kPermWarps] = s2;    // this chunk's total
+    }
+    __syncthreads();
+    const int32_t base = e0 == 0 ? 0 : off[e0 - 1] + __ldcg(totals + e0 - 1);
+    if (e < E) off[e] = base + wtot[wid] + incl - v;
+    __syncthreads();
+  }
+  if (blockIdx.x == 0) {
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+      const int32_t c = __ldcg(totals + e);
+      counts[e] = c;
+      offsets[e] = off[e];
+      if (e == E - 1) offsets[E] = off[e] + c;
+    }
+  }
+  // 3b. warp bases: offsets[e] + the block's prefix + the counts of lower warps
+  for (int e = threadIdx.x; e < E; e += blockDim.x) {
+    int32_t run = off[e] + __ldcg(hist + (int64_t)blockIdx.x * E + e);
+    for (int w2 = 0; w2 < kPermWarps; ++w2) {
+      const int32_t c = sh[w2 * E + e];
+      sh[w2 * E + e] = run;
+      run += c;
+    }
+  }
+  __syncthreads();
+  // 3c. stable ranking inside each warp's slice (as permute_scatter_kernel)
+  int32_t* my = sh + wid * E;
+  for (int s = 0; s < kPerWarp; s += 32) {
+    const int64_t i = slice0 + s + lane;
+    const bool valid = i < R;
+    int e = valid ? ids[i] : -1;
+    if (e < 0 || e >= E) e = E + lane;
+    const uint32_t peers = __match_any_sync(0xffffffffu, e);
+    const uint32_t lower = peers & ((1u << lane) - 1u);
+    if (e < E) {
+      const int32_t row = my[e] + __popc(lower);
+      row_map[i] = row;
+      src_row[row] = (int32_t)(i / k);
+      if (w_perm) w_perm[row] = w[i];
+    }
+    __syncwarp();
+    if (e < E && (peers >> lane) == 1u) my[e] += __popc(peers);
+    __syncwarp();
+  }
+}
+
 __global__ void permute_rows_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ src_row,
                                     int64_t R, int H, uint16_t* __restrict__ x_perm) {
   const int64_t row = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
@@ -201,10 +365,29 @@ __global__ void permute_rows_kernel(const uint16_t* __restrict__ x, const int32_
 
 }  // namespace
 
+// Workspace: hist [nblocks][E]; with the one-launch path also totals [E]
+// and the two barrier counters (256-byte aligned after hist).
 size_t permute_workspace_bytes(int64_t R, int64_t E, bool noalloc) {
   const int64_t chunk = noalloc ? kChunkNoAlloc : kChunk;
   const int64_t nb = (R + chunk - 1) / chunk;
-  return (size_t)((nb > 0 ? nb : 1) * E * sizeof(int32_t));
+  const size_t hist = (size_t)((nb > 0 ? nb : 1) * E * sizeof(int32_t));
+  if (noalloc) return hist;
+  return ((hist + 255) & ~size_t(255)) + (((size_t)E * sizeof(int32_t) + 255) & ~size_t(255)) + 256;
+}
+
+// Blocks of permute_fused_kernel that can be resident at once on `dev`.
+int64_t permute_fused_capacity(const DeviceInfo& dev, int64_t E) {
+  static int per_sm[kMaxDevices][2] = {{0}};
+  const int slot = E <= 256 ? 0 : 1;   // shared memory grows with E; size the query for the larger E
+  if (!per_sm[dev.ordinal][slot]) {
+    const size_t smem = ((size_t)(kPermWarps + 1) * (slot ? kMaxExperts : 256) + 40) * sizeof(int32_t);
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, permute_fused_kernel<kChunk>, kPermThreads, smem) !=
+        cudaSuccess)
+      return 0;
+    per_sm[dev.ordinal][slot] = n > 0 ? n : -1;
+  }
+  return per_sm[dev.ordinal][slot] > 0 ? (int64_t)per_sm[dev.ordinal][slot] * dev.num_sms : 0;
 }
 
 template <int CHUNK>
@@ -223,8 +406,32 @@ void enqueue_permute(const int32_t* ids, const float* w, int64_t R, int64_t k, i
 
 cudaError_t launch_permute(const int32_t* ids, const float* w, int64_t T, int64_t k, int64_t E,
                            int32_t* counts, int32_t* offsets, int32_t* row_map, int32_t* src_row,
-                           float* w_perm, void* ws, uint32_t* status, cudaStream_t stream, bool noalloc) {
+                           float* w_perm, void* ws, const DeviceInfo& dev, cudaStream_t stream, bool noalloc) {
   int32_t* hist = static_cast<int32_t*>(ws);
+  const int64_t R = T * k;
+  const int64_t nb = (R + kChunk - 1) / kChunk;
+  if (!noalloc && nb > 0 && nb <= permute_fused_capacity(dev, E)) {
+    // one cooperative launch (every block resident), after zeroing its barrier counters
+    const size_t hist_bytes = ((size_t)(nb * E * sizeof(int32_t)) + 255) & ~size_t(255);
+    int32_t* totals = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(ws) + hist_bytes);
+    uint32_t* bar = reinterpret_cast<uint32_t*>(reinterpret_cast<uint8_t*>(totals) +
+                                                ((E * sizeof(int32_t) + 255) & ~size_t(255)));
+    cudaError_t err = cudaMemsetAsync(bar, 0, 2 * sizeof(uint32_t), stream);
+    if (err != cudaSuccess) return err;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.gridDim = dim3((unsigned)nb);
+    cfg.blockDim = dim3(kPermThreads);
+    cfg.dynamicSmemBytes = ((size_t)(kPermWarps + 1) * E + 40) * sizeof(int32_t);
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, permute_fused_kernel<kChunk>, ids, w, R, (int)k, (int)E, hist, totals, bar,
+                              counts, offsets, row_map, src_row, w_perm, dev.status, dev.wait_limit_ns);
+  }
+  uint32_t* status = dev.status;
   if (noalloc)
     enqueue_permute<kChunkNoAlloc>(ids, w, T * k, k, E, counts, offsets, row_map, src_row, w_perm, hist,
                                    status, stream);
@@ -291,7 +498,7 @@ extern "C" int moe_permute_noalloc(const int32_t* ids, const float* w, int64_t T
   // Every call fully overwrites the histogram entries it reads (the count
   // pass writes all nblocks x E of them first), so nothing has to be cleared.
   return moe::launch_permute(ids, w, T, k, E, counts, offsets, row_map, src_row, w_perm, scratch,
-                             dev.status, static_cast<cudaStream_t>(stream), true) == cudaSuccess
+                             dev, static_cast<cudaStream_t>(stream), true) == cudaSuccess
              ? MOE_OK
              : MOE_ERR_CUDA;
 }
