@@ -40,10 +40,20 @@ METRIC = "MoE layer tokens/s (fwd; fwd+bwd) and grouped-GEMM % of GB300 bf16 pea
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
+SPACER_CYCLES = 2_000_000   # about 1 ms of device spin ahead of each eager step
+
+
 def route_launches(H, E):
     """Kernels of one moe_route call: the bf16 split of W_r, then the fused
     cluster router (16 <= E <= 256, E % 16 == 0) or the router GEMM and top-k."""
     return 2 if (H % 64 == 0 and E % 16 == 0 and 16 <= E <= 256) else 3
+
+
+def permute_launches(R, torch, device):
+    """Kernels of one moe_permute call: one cooperative launch while its
+    256-assignment blocks fit on the device at once (8 per SM), else three."""
+    sms = torch.cuda.get_device_properties(device).multi_processor_count
+    return 1 if (R + 255) // 256 <= 8 * sms else 3
 
 
 def parse():
@@ -272,8 +282,10 @@ def run_native(args):
         return y
 
     # route (weight split + fused router, or split + router GEMM + top-k),
-    # permute (3), row gather, gate_up, down, shared expert (2), combine
-    launches_per_step = route_launches(H, cfg.E) + 3 + (0 if fused else 1) + 1 + 1 + (2 if I_s else 0) + 1
+    # permute (one cooperative kernel, or three), row gather, gate_up, down,
+    # shared expert (2), combine
+    launches_per_step = route_launches(H, cfg.E) + permute_launches(T * k, torch, device) + \
+        (0 if fused else 1) + 1 + 1 + (2 if I_s else 0) + 1
     for _ in range(max(args.warmup, 3)):
         step()
     moe.sync_status()
@@ -287,9 +299,13 @@ def run_native(args):
     barrier(dist)
     torch.cuda.synchronize()
     t0 = time.time()
-    # (1) eager launches with an event between kernels: the per-kernel times
+    # (1) eager launches with an event between kernels: the per-kernel times.
+    # A spin of about a millisecond on the device after the flush lets the
+    # host enqueue the whole step before the device reaches it, so the events
+    # bracket device time only (no host launch gaps between kernels).
     for i in range(K):
         flush.zero_()
+        torch.cuda._sleep(SPACER_CYCLES)
         step(evs[i])
     torch.cuda.synchronize()
     barrier(dist)
@@ -369,7 +385,8 @@ def run_native(args):
         "roofline": roofline,
         "timing": "value and ms_per_step: the forward replayed as one CUDA graph per step "
                   "(ForwardGraph), CUDA events around each replay; kernels_us and eager: the same "
-                  "kernels launched one by one with an event between kernels",
+                  "kernels launched one by one with an event between kernels, enqueued behind a "
+                  "device-side spin so that no host launch gap falls between the events",
         "eager": {"value": round(ws * T * K / eager_s, 1), "ms_per_step": round(1e3 * eager_s / K, 4)},
         "graph_output_matches_eager": y_graph_ok,
         "kernels_us": {n: round(v * 1e3, 2) for n, v in per_kernel.items()},
@@ -449,6 +466,7 @@ def fwd_bwd(moe, torch, stream, dist, device, ws, flush, pk, fused, K=30, W=3):
     barrier(dist)
     for i in range(K):
         flush.zero_()
+        torch.cuda._sleep(SPACER_CYCLES)   # the host enqueues ahead of the device (see the forward)
         evs[i][0].record(stream)
         step()
         evs[i][1].record(stream)
@@ -461,7 +479,8 @@ def fwd_bwd(moe, torch, stream, dist, device, ws, flush, pk, fused, K=30, W=3):
     return {"workload": cfg.name, "T": cfg.T, "value": round(ws * cfg.T * K / s, 1), "unit": "tokens/s",
             "ms_per_step": round(1e3 * s / K, 4), "gemm_flops_per_step": flops,
             "layer_tflops": round(flops * K / s / 1e12, 1), "steps": K,
-            "launches_per_step": route_launches(cfg.H, cfg.E) + 6 + (0 if fused else 1) + 1 + 1 + 2 + 2 + 2}
+            "launches_per_step": route_launches(cfg.H, cfg.E) + permute_launches(cfg.T * cfg.k, torch, device) + 3 +
+                                 (0 if fused else 1) + 1 + 1 + 2 + 2 + 2}
 
 
 # -------------------------------------------------------------- CPU oracle
