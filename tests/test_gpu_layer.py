@@ -257,10 +257,11 @@ def test_cta_pairs_bit_identical(T, H, E, k, I, fused):
 def test_overlapped_forward_matches_forward():
     """OverlappedForward (route/permute of batch i+1 overlapping the expert
     GEMMs of batch i, on two streams) gives moe_forward's outputs bit for
-    bit, with and without a shared expert."""
+    bit, with and without a shared expert and with the row gather fused into
+    the gate_up GEMM (both read x inside the expert stage)."""
     import torch
     moe = lib()
-    for I_s in (0, 64):
+    for I_s, fused in ((0, False), (64, False), (0, True)):
         cfg, inp = _inputs(300, 256, 8, 2, 128, seed=93, I_shared=I_s)
         wr, gu, dn = f32(inp.w_router), bf(inp.gate_up), bf(inp.down)
         sgu = bf(inp.sh_gate_up) if I_s else None
@@ -268,7 +269,7 @@ def test_overlapped_forward_matches_forward():
         xs = [torch.from_numpy(synth.normal_bf16(s, synth.TID_X, (300, 256), 1.0).view(np.int16))
               .view(torch.bfloat16).pin_memory() for s in (11, 12, 13, 14, 15)]
         ys = [torch.empty((300, 256), dtype=torch.bfloat16).pin_memory() for _ in xs]
-        moe.OverlappedForward(300, wr, gu, dn, cfg.k, None, sgu, sdn).run(xs, ys)
+        moe.OverlappedForward(300, wr, gu, dn, cfg.k, None, sgu, sdn, fused_gather=fused).run(xs, ys)
         moe.sync_status()
         for xh, yh in zip(xs, ys):
             y, _ = moe.moe_forward(xh.cuda(), wr, gu, dn, cfg.k, None, sgu, sdn)

@@ -252,6 +252,8 @@ class OverlappedForward:
         self.stream_f = torch.cuda.Stream()
         self.stream_g = torch.cuda.Stream()
         self.copy_stream = torch.cuda.Stream()
+        # stage G reads x itself for the shared expert and the fused row gather
+        self.g_reads_x = sh_gate_up is not None or fused_gather
         self.sets = []
         for _ in range(2):
             st = {"x": torch.zeros((T, H), dtype=torch.bfloat16, device=w_router.device)}
@@ -305,6 +307,8 @@ class OverlappedForward:
             st = self.sets[i % 2]
             with torch.cuda.stream(self.copy_stream):
                 self.copy_stream.wait_event(st["ev_f"])          # F of batch i-2 has read x
+                if self.g_reads_x:
+                    self.copy_stream.wait_event(st["ev_g"])      # and so has G of batch i-2
                 st["x"].copy_(x_host_batches[i], non_blocking=True)
                 st["ev_loaded"].record(self.copy_stream)
 
