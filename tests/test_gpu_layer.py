@@ -254,6 +254,27 @@ def test_cta_pairs_bit_identical(T, H, E, k, I, fused):
         assert torch_equal(a, b)
 
 
+@pytest.mark.parametrize("T,H,E,k,I", [(300, 384, 6, 3, 320), (1100, 256, 4, 2, 128)])
+def test_programmatic_launch_bit_identical(T, H, E, k, I):
+    """Kernels launched with and without programmatic dependent launch (each
+    kernel's set-up overlapping the previous kernel's tail) give the same
+    forward and backward bit for bit."""
+    moe = lib()
+    cfg, inp = _inputs(T, H, E, k, I, seed=7 * T + I)
+    outs = []
+    for pdl in (True, False):
+        moe.set_pdl(pdl)
+        try:
+            (x, wr, gu, dn), y, st = _forward(moe, inp, save=True)
+            g = moe.moe_backward(bf(inp.dy), st, wr, gu, dn, want_dw_router=True)
+            moe.sync_status()
+        finally:
+            moe.set_pdl(True)
+        outs.append([y, st.ids, st.row_map, st.h, st.gu_pre, st.y_perm] + [g[n] for n in sorted(g)])
+    for a, b in zip(*outs):
+        assert torch_equal(a, b)
+
+
 def test_overlapped_forward_matches_forward():
     """OverlappedForward (route/permute of batch i+1 overlapping the expert
     GEMMs of batch i, on two streams) gives moe_forward's outputs bit for

@@ -28,6 +28,7 @@ SIGNATURES = {
     "moe_set_wait_limit_ns": [ctypes.c_uint64],
     "moe_test_stall_gemm_producer": [INT],
     "moe_set_gemm_pairs": [INT],
+    "moe_set_pdl": [INT],
     "moe_route_workspace_size": [I64, I64, I64, ctypes.POINTER(SZ)],
     "moe_route": [P, P, P, I64, I64, I64, I64, P, P, P, P, SZ, P],
     "moe_permute_workspace_size": [I64, I64, I64, ctypes.POINTER(SZ)],

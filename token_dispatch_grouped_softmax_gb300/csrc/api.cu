@@ -10,6 +10,8 @@ namespace moe {
 
 __device__ uint32_t g_status_word;   // first device-side error (see common.cuh)
 
+std::atomic<int> g_pdl{1};           // programmatic dependent launch (moe_set_pdl)
+
 namespace {
 
 std::mutex g_mu;
@@ -109,6 +111,11 @@ int moe_set_wait_limit_ns(uint64_t ns) {
 
 int moe_set_gemm_pairs(int on) {
   moe::g_gemm_pairs = on ? 1 : 0;
+  return MOE_OK;
+}
+
+int moe_set_pdl(int on) {
+  moe::g_pdl.store(on ? 1 : 0);
   return MOE_OK;
 }
 

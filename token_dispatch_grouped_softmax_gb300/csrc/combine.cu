@@ -40,6 +40,8 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict
                                                       const uint16_t* __restrict__ y_shared,
                                                       int T, int H, int k,
                                                       uint16_t* __restrict__ y) {
+  pdl_wait();
+  pdl_trigger();
   const int lane = threadIdx.x & 31;
   const int nch = H / 8;
   const int slices = (nch + kSliceChunks - 1) / kSliceChunks;
@@ -94,6 +96,8 @@ __global__ void __launch_bounds__(256) route_bwd_kernel(const float* __restrict_
                                                         int E, int k,
                                                         float* __restrict__ d_logits,
                                                         float* __restrict__ dw) {
+  pdl_wait();
+  pdl_trigger();
   const int lane = threadIdx.x & 31;
   const int t = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
   if (t >= T) return;
@@ -122,6 +126,8 @@ __global__ void __launch_bounds__(256) route_bwd_kernel(const float* __restrict_
 
 __global__ void transpose_f32_kernel(const float* __restrict__ in, int rows, int cols,
                                      float* __restrict__ out) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ float tile[32][33];
   const int c0 = blockIdx.x * 32, r0 = blockIdx.y * 32;
   for (int q = threadIdx.y; q < 32; q += blockDim.y) {
@@ -142,6 +148,8 @@ __global__ void __launch_bounds__(256) gather_dx_kernel(const uint16_t* __restri
                                                         const float* __restrict__ wr_t, int T,
                                                         int H, int E, int k,
                                                         uint16_t* __restrict__ dx) {
+  pdl_wait();
+  pdl_trigger();
   const int lane = threadIdx.x & 31;
   const int nch = H / 8;
   const int slices = (nch + kSliceChunks - 1) / kSliceChunks;
@@ -199,6 +207,8 @@ __global__ void __launch_bounds__(256) route_bwd_weight_kernel(const uint16_t* _
                                                                const float* __restrict__ dl, int T,
                                                                int H, int E,
                                                                float* __restrict__ dwr) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ __align__(16) float xs[32][32];  // [t][h]
   __shared__ __align__(16) float ds[32][64];  // [t][e]
   const int tid = threadIdx.x, ty = tid / 16, tx = tid % 16;
@@ -244,18 +254,16 @@ cudaError_t launch_combine(const uint16_t* y_perm, const int32_t* row_map, const
                            cudaStream_t stream) {
   if (T == 0) return cudaSuccess;
   const int64_t warps = T * ((H / 8 + kSliceChunks - 1) / kSliceChunks);
-  combine_kernel<<<(unsigned)((warps + kWarpsPerBlock - 1) / kWarpsPerBlock), 256, 0, stream>>>(
-      y_perm, row_map, w, y_shared, (int)T, (int)H, (int)k, y);
-  return cudaGetLastError();
+  return launch_pdl(combine_kernel, dim3((unsigned)((warps + kWarpsPerBlock - 1) / kWarpsPerBlock)), dim3(256), 0,
+                    stream, 1, y_perm, row_map, w, y_shared, (int)T, (int)H, (int)k, y);
 }
 
 cudaError_t launch_route_bwd(const float* dw_part, int nparts, const int32_t* row_map, const float* w,
                              const int32_t* ids, int64_t T, int64_t E, int64_t k, float* d_logits,
                              float* dw, cudaStream_t stream) {
   if (T == 0) return cudaSuccess;
-  route_bwd_kernel<<<(unsigned)((T + kWarpsPerBlock - 1) / kWarpsPerBlock), 256, 0, stream>>>(
-      dw_part, nparts, row_map, w, ids, (int)T, (int)E, (int)k, d_logits, dw);
-  return cudaGetLastError();
+  return launch_pdl(route_bwd_kernel, dim3((unsigned)((T + kWarpsPerBlock - 1) / kWarpsPerBlock)), dim3(256), 0,
+                    stream, 1, dw_part, nparts, row_map, w, ids, (int)T, (int)E, (int)k, d_logits, dw);
 }
 
 size_t gather_dx_workspace_bytes(int64_t H, int64_t E) { return (size_t)(H * E * sizeof(float)); }
@@ -268,19 +276,20 @@ cudaError_t launch_gather_dx(const uint16_t* dx_perm, const int32_t* row_map, co
   if (d_logits) {
     wr_t = static_cast<float*>(ws);
     dim3 g((unsigned)((E + 31) / 32), (unsigned)((H + 31) / 32));
-    transpose_f32_kernel<<<g, dim3(32, 8), 0, stream>>>(w_router, (int)H, (int)E, wr_t);
+    const cudaError_t err = launch_pdl(transpose_f32_kernel, g, dim3(32, 8), 0, stream, 1, w_router, (int)H,
+                                       (int)E, wr_t);
+    if (err != cudaSuccess) return err;
   }
   const int64_t warps = T * ((H / 8 + kSliceChunks - 1) / kSliceChunks);
-  gather_dx_kernel<<<(unsigned)((warps + kWarpsPerBlock - 1) / kWarpsPerBlock), 256, 0, stream>>>(
-      dx_perm, row_map, d_logits, ids, wr_t, (int)T, (int)H, (int)E, (int)k, dx);
-  return cudaGetLastError();
+  return launch_pdl(gather_dx_kernel, dim3((unsigned)((warps + kWarpsPerBlock - 1) / kWarpsPerBlock)), dim3(256),
+                    0, stream, 1, dx_perm, row_map, d_logits, ids, wr_t, (int)T, (int)H, (int)E, (int)k, dx);
 }
 
 cudaError_t launch_route_bwd_weight(const uint16_t* x, const float* d_logits, int64_t T, int64_t H,
                                     int64_t E, float* d_w_router, cudaStream_t stream) {
   dim3 g((unsigned)((H + 31) / 32), (unsigned)((E + 63) / 64));
-  route_bwd_weight_kernel<<<g, 256, 0, stream>>>(x, d_logits, (int)T, (int)H, (int)E, d_w_router);
-  return cudaGetLastError();
+  return launch_pdl(route_bwd_weight_kernel, g, dim3(256), 0, stream, 1, x, d_logits, (int)T, (int)H, (int)E,
+                    d_w_router);
 }
 
 }  // namespace moe

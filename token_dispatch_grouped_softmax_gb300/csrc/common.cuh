@@ -67,6 +67,18 @@ __device__ __forceinline__ float warp_max(float v) {
   return v;
 }
 
+// ------------------------------------------- programmatic dependent launch
+// Every kernel here is launched with programmatic stream serialization, so
+// it may start while the kernel before it on the stream still runs.
+// pdl_wait() blocks until that kernel has completed and its memory is
+// visible (at once when the launch had no such predecessor); pdl_trigger()
+// lets the next kernel start launching.  Each kernel waits before its first
+// global-memory access other than its parameters, and triggers only after
+// waiting, so its pre-wait part (barrier set-up, TMEM allocation, descriptor
+// prefetch) overlaps only the kernel right before it.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // ----------------------------------------------------------------- timing
 __device__ __forceinline__ uint64_t globaltimer_ns() {
   uint64_t t;

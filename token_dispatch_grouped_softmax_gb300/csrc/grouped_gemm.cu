@@ -477,6 +477,8 @@ __global__ void __launch_bounds__(Traits<MODE, KH, CG>::kThreads, 1)
       tmem_relinquish();
     }
   }
+  pdl_wait();      // the set-up above overlaps the kernel before this one
+  pdl_trigger();
   // Tile prefix over experts (M-grouped modes): prefix[e] = sum_{e'<e} ceil(M_e'/BM) * nt.
   // Tiles go out in expert order, so the row tiles of one expert run at about
   // the same time and read its weights from L2 after the first of them.
@@ -906,15 +908,17 @@ cudaError_t run_gemm(const GemmParams& p, int64_t tiles_upper_bound, const Devic
   if (CG == 1) {
     int64_t grid = tiles_upper_bound < dev.num_sms ? tiles_upper_bound : dev.num_sms;
     if (grid < 1) grid = 1;
-    grouped_gemm_kernel<MODE, KH, CG><<<(unsigned)grid, Traits<MODE, KH, CG>::kThreads, smem, stream>>>(p);
-    return cudaGetLastError();
+    return launch_pdl(grouped_gemm_kernel<MODE, KH, CG>, dim3((unsigned)grid), dim3(Traits<MODE, KH, CG>::kThreads),
+                      smem, stream, 1, p);
   }
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.blockDim = dim3(Traits<MODE, KH, CG>::kThreads);
   cfg.dynamicSmemBytes = gemm_smem_bytes(kMaxExperts);
   cfg.stream = stream;
@@ -931,6 +935,7 @@ cudaError_t run_gemm(const GemmParams& p, int64_t tiles_upper_bound, const Devic
   if (pairs < 1) pairs = 1;
   cfg.gridDim = dim3((unsigned)(2 * pairs));
   cfg.dynamicSmemBytes = smem;
+  cfg.numAttrs = g_pdl.load(std::memory_order_relaxed) ? 2 : 1;   // the occupancy query used the cluster alone
   return cudaLaunchKernelEx(&cfg, grouped_gemm_kernel<MODE, KH, CG>, p);
 }
 

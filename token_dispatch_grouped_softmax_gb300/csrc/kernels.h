@@ -7,9 +7,45 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <atomic>
+#include <utility>
+
 #include "common.cuh"
 
 namespace moe {
+
+// Programmatic dependent launch on (1) or off (0), moe_set_pdl.
+extern std::atomic<int> g_pdl;
+
+// Launches `kernel` with programmatic stream serialization while g_pdl is on
+// (see pdl_wait in common.cuh) and, when cluster_x > 1, in clusters of
+// cluster_x CTAs.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       unsigned cluster_x, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[2];
+  unsigned n = 0;
+  if (g_pdl.load(std::memory_order_relaxed)) {
+    attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[n].val.programmaticStreamSerializationAllowed = 1;
+    ++n;
+  }
+  if (cluster_x > 1) {
+    attr[n].id = cudaLaunchAttributeClusterDimension;
+    attr[n].val.clusterDim.x = cluster_x;
+    attr[n].val.clusterDim.y = 1;
+    attr[n].val.clusterDim.z = 1;
+    ++n;
+  }
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = n;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 constexpr int kMaxDevices = 64;
 constexpr int kMaxExperts = 1024;

@@ -40,6 +40,8 @@ __global__ void __launch_bounds__(kPermThreads) permute_hist_kernel(const int32_
                                                                     int64_t R, int E,
                                                                     int32_t* __restrict__ hist,
                                                                     uint32_t* status) {
+  pdl_wait();
+  pdl_trigger();
   extern __shared__ int32_t sh[];  // [E]
   for (int e = threadIdx.x; e < E; e += blockDim.x) sh[e] = 0;
   __syncthreads();
@@ -66,6 +68,8 @@ __global__ void __launch_bounds__(kPermThreads) permute_hist_kernel(const int32_
 __global__ void __launch_bounds__(1024) permute_scan_kernel(int32_t* __restrict__ hist, int nblocks,
                                                             int E, int32_t* __restrict__ counts,
                                                             int32_t* __restrict__ offsets) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ int32_t part[1024];     // [G][E] range sums, then exclusive range prefixes
   __shared__ int32_t warp_tot[32];
   __shared__ int32_t ex[1024];       // offsets[e]
@@ -141,6 +145,8 @@ __global__ void __launch_bounds__(kPermThreads) permute_scatter_kernel(
     const int32_t* __restrict__ ids, const float* __restrict__ w, int64_t R, int k, int E,
     const int32_t* __restrict__ base_be, int32_t* __restrict__ row_map, int32_t* __restrict__ src_row,
     float* __restrict__ w_perm) {
+  pdl_wait();
+  pdl_trigger();
   constexpr int kPerWarp = CHUNK / kPermWarps;  // assignments per warp, in steps of 32
   extern __shared__ int32_t sh[];              // [kPermWarps][E] counts, then bases
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
@@ -238,6 +244,8 @@ __global__ void __launch_bounds__(kPermThreads) permute_fused_kernel(
     int32_t* __restrict__ hist, int32_t* __restrict__ totals, uint32_t* __restrict__ bar,
     int32_t* __restrict__ counts, int32_t* __restrict__ offsets, int32_t* __restrict__ row_map,
     int32_t* __restrict__ src_row, float* __restrict__ w_perm, uint32_t* status, uint64_t wait_limit_ns) {
+  pdl_wait();
+  pdl_trigger();
   constexpr int kPerWarp = CHUNK / kPermWarps;
   extern __shared__ int32_t sh[];   // [kPermWarps][E] warp counts, then bases; [E] offsets; [32] scan
   int32_t* off = sh + kPermWarps * E;
@@ -355,6 +363,8 @@ __global__ void __launch_bounds__(kPermThreads) permute_fused_kernel(
 
 __global__ void permute_rows_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ src_row,
                                     int64_t R, int H, uint16_t* __restrict__ x_perm) {
+  pdl_wait();
+  pdl_trigger();
   const int64_t row = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (row >= R) return;
@@ -391,17 +401,20 @@ int64_t permute_fused_capacity(const DeviceInfo& dev, int64_t E) {
 }
 
 template <int CHUNK>
-void enqueue_permute(const int32_t* ids, const float* w, int64_t R, int64_t k, int64_t E, int32_t* counts,
-                     int32_t* offsets, int32_t* row_map, int32_t* src_row, float* w_perm, int32_t* hist,
-                     uint32_t* status, cudaStream_t stream) {
+cudaError_t enqueue_permute(const int32_t* ids, const float* w, int64_t R, int64_t k, int64_t E,
+                            int32_t* counts, int32_t* offsets, int32_t* row_map, int32_t* src_row,
+                            float* w_perm, int32_t* hist, uint32_t* status, cudaStream_t stream) {
   const int nb = (int)((R + CHUNK - 1) / CHUNK);
+  cudaError_t err = cudaSuccess;
   if (nb > 0)
-    permute_hist_kernel<CHUNK><<<nb, kPermThreads, E * sizeof(int32_t), stream>>>(ids, R, (int)E, hist,
-                                                                                   status);
-  permute_scan_kernel<<<1, 1024, 0, stream>>>(hist, nb, (int)E, counts, offsets);
-  if (nb > 0)
-    permute_scatter_kernel<CHUNK><<<nb, kPermThreads, kPermWarps * E * sizeof(int32_t), stream>>>(
-        ids, w, R, (int)k, (int)E, hist, row_map, src_row, w_perm);
+    err = launch_pdl(permute_hist_kernel<CHUNK>, dim3(nb), dim3(kPermThreads), E * sizeof(int32_t), stream, 1, ids,
+                     R, (int)E, hist, status);
+  if (err == cudaSuccess)
+    err = launch_pdl(permute_scan_kernel, dim3(1), dim3(1024), 0, stream, 1, hist, nb, (int)E, counts, offsets);
+  if (err == cudaSuccess && nb > 0)
+    err = launch_pdl(permute_scatter_kernel<CHUNK>, dim3(nb), dim3(kPermThreads), kPermWarps * E * sizeof(int32_t),
+                     stream, 1, ids, w, R, (int)k, (int)E, (const int32_t*)hist, row_map, src_row, w_perm);
+  return err;
 }
 
 cudaError_t launch_permute(const int32_t* ids, const float* w, int64_t T, int64_t k, int64_t E,
@@ -433,19 +446,17 @@ cudaError_t launch_permute(const int32_t* ids, const float* w, int64_t T, int64_
   }
   uint32_t* status = dev.status;
   if (noalloc)
-    enqueue_permute<kChunkNoAlloc>(ids, w, T * k, k, E, counts, offsets, row_map, src_row, w_perm, hist,
-                                   status, stream);
-  else
-    enqueue_permute<kChunk>(ids, w, T * k, k, E, counts, offsets, row_map, src_row, w_perm, hist, status,
-                            stream);
-  return cudaGetLastError();
+    return enqueue_permute<kChunkNoAlloc>(ids, w, T * k, k, E, counts, offsets, row_map, src_row, w_perm, hist,
+                                          status, stream);
+  return enqueue_permute<kChunk>(ids, w, T * k, k, E, counts, offsets, row_map, src_row, w_perm, hist, status,
+                                 stream);
 }
 
 cudaError_t launch_permute_rows(const uint16_t* x, const int32_t* src_row, int64_t R, int64_t H,
                                 uint16_t* x_perm, cudaStream_t stream) {
   if (R == 0) return cudaSuccess;
-  permute_rows_kernel<<<(unsigned)((R + 7) / 8), 256, 0, stream>>>(x, src_row, R, (int)H, x_perm);
-  return cudaGetLastError();
+  return launch_pdl(permute_rows_kernel, dim3((unsigned)((R + 7) / 8)), dim3(256), 0, stream, 1, x, src_row, R,
+                    (int)H, x_perm);
 }
 
 }  // namespace moe

@@ -43,6 +43,8 @@ __global__ void __launch_bounds__(256) route_logits_kernel(const uint16_t* __res
                                                            const float* __restrict__ bias, int T,
                                                            int H, int E,
                                                            float* __restrict__ logits) {
+  pdl_wait();
+  pdl_trigger();
   __shared__ __align__(16) float xs[kRK][kRT];   // [k][token]
   __shared__ __align__(16) float ws[kRK][kRE];   // [k][expert]
   const int tid = threadIdx.x;
@@ -125,6 +127,8 @@ __global__ void __launch_bounds__(256) route_logits_kernel(const uint16_t* __res
 // W_r [H, E] fp32 -> [3, H, E] bf16 with W_r = W0 + W1 + W2 exactly.
 __global__ void split_router_weight_kernel(const float* __restrict__ wr, int64_t n,
                                            uint16_t* __restrict__ out) {
+  pdl_wait();
+  pdl_trigger();
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
        i += (int64_t)gridDim.x * blockDim.x) {
     const float w = wr[i];
@@ -226,6 +230,8 @@ __global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict
                                                          int k, int32_t* __restrict__ ids,
                                                          float* __restrict__ w,
                                                          float* __restrict__ logits_out) {
+  pdl_wait();
+  pdl_trigger();
   const int lane = threadIdx.x & 31;
   const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
   if (t >= T) return;
@@ -337,6 +343,8 @@ __global__ void __launch_bounds__(fr_threads<NV>(), 1) fused_router_kernel(const
     tmem_alloc(smem_u32(tmem_slot), p.tmem_cols);
     tmem_relinquish();
   }
+  pdl_wait();      // the set-up above overlaps the kernel before this one
+  pdl_trigger();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -529,17 +537,19 @@ cudaError_t launch_fused_router_nv(const FusedRouterParams& p, int P, int64_t T,
     configured[dev.ordinal] = 1;
   }
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = (unsigned)P;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.gridDim = dim3((unsigned)(((T + 127) / 128) * P));
   cfg.blockDim = dim3(fr_threads<NV>());
   cfg.dynamicSmemBytes = fused_router_smem(p.E);
   cfg.stream = stream;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = g_pdl.load(std::memory_order_relaxed) ? 2 : 1;
   return cudaLaunchKernelEx(&cfg, fused_router_kernel<NV>, p);
 }
 
@@ -583,8 +593,8 @@ cudaError_t launch_fused_router(const uint16_t* x, const uint16_t* w_split, cons
 template <int NV>
 void launch_topk(const float* part, int nparts, const float* bias, int64_t T, int64_t E, int64_t k,
                  int32_t* ids, float* w, float* logits_out, cudaStream_t stream) {
-  route_topk_kernel<NV><<<(unsigned)((T + 7) / 8), 256, 0, stream>>>(part, nparts, bias, (int)T, (int)E,
-                                                                     (int)k, ids, w, logits_out);
+  launch_pdl(route_topk_kernel<NV>, dim3((unsigned)((T + 7) / 8)), dim3(256), 0, stream, 1, part, nparts, bias,
+             (int)T, (int)E, (int)k, ids, w, logits_out);
 }
 
 void topk_dispatch(const float* part, int nparts, const float* bias, int64_t T, int64_t E, int64_t k,
@@ -620,23 +630,27 @@ cudaError_t launch_route(const uint16_t* x, const float* w_router, const float* 
   if (fused_router_ok(H, E)) {
     uint16_t* w_split = reinterpret_cast<uint16_t*>(wsb);
     const int64_t n = H * E;
-    split_router_weight_kernel<<<(unsigned)std::min<int64_t>((n + 255) / 256, 4096), 256, 0, stream>>>(
-        w_router, n, w_split);
-    const cudaError_t err = launch_fused_router(x, w_split, bias, T, H, E, k, ids, w, logits, dev, stream);
+    cudaError_t err = launch_pdl(split_router_weight_kernel, dim3((unsigned)std::min<int64_t>((n + 255) / 256, 4096)),
+                                 dim3(256), 0, stream, 1, w_router, n, w_split);
+    if (err == cudaSuccess) err = launch_fused_router(x, w_split, bias, T, H, E, k, ids, w, logits, dev, stream);
     if (err != cudaSuccess) return err;
   } else if (route_on_tensor_cores(H, E)) {
     const int parts = router_parts(T, H, E);
     uint16_t* w_split = reinterpret_cast<uint16_t*>(wsb);
     float* part = reinterpret_cast<float*>(wsb + align((size_t)(3 * H * E * 2)));
     const int64_t n = H * E;
-    split_router_weight_kernel<<<(unsigned)std::min<int64_t>((n + 255) / 256, 4096), 256, 0, stream>>>(
-        w_router, n, w_split);
+    const cudaError_t err = launch_pdl(split_router_weight_kernel,
+                                       dim3((unsigned)std::min<int64_t>((n + 255) / 256, 4096)), dim3(256), 0,
+                                       stream, 1, w_router, n, w_split);
+    if (err != cudaSuccess) return err;
     if (launch_router_logits(x, w_split, T, H, E, parts, part, dev, stream) != 0) return cudaErrorInvalidValue;
     topk_dispatch(part, parts, bias, T, E, k, ids, w, logits, stream);
   } else {
     float* lg = reinterpret_cast<float*>(wsb);
     dim3 g1((unsigned)((T + kRT - 1) / kRT), (unsigned)((E + kRE - 1) / kRE));
-    route_logits_kernel<<<g1, 256, 0, stream>>>(x, w_router, nullptr, (int)T, (int)H, (int)E, lg);
+    const cudaError_t err = launch_pdl(route_logits_kernel, g1, dim3(256), 0, stream, 1, x, w_router,
+                                       (const float*)nullptr, (int)T, (int)H, (int)E, lg);
+    if (err != cudaSuccess) return err;
     topk_dispatch(lg, 1, bias, T, E, k, ids, w, logits, stream);
   }
   return cudaGetLastError();

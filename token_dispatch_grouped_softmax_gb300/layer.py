@@ -285,10 +285,18 @@ class OverlappedForward:
                     back()
             torch.cuda.current_stream().wait_stream(side)
             st["gf"], st["gg"] = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
-            with torch.cuda.graph(st["gf"]):
-                front()
-            with torch.cuda.graph(st["gg"]):
-                back()
+            # The two stages run side by side: captured without programmatic
+            # dependent launch, whose early-resident kernels would take the
+            # SMs that the other stage fills at each GEMM's tail.
+            pdl = ops.pdl_enabled()
+            ops.set_pdl(False)
+            try:
+                with torch.cuda.graph(st["gf"]):
+                    front()
+                with torch.cuda.graph(st["gg"]):
+                    back()
+            finally:
+                ops.set_pdl(pdl)
             st.update(ev_loaded=torch.cuda.Event(), ev_f=torch.cuda.Event(), ev_g=torch.cuda.Event(),
                       ev_stored=torch.cuda.Event())
             self.sets.append(st)

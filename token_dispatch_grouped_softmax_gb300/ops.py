@@ -59,6 +59,22 @@ def set_gemm_pairs(on: bool):
     call("moe_set_gemm_pairs", 1 if on else 0)
 
 
+_pdl_on = [True]
+
+
+def set_pdl(on: bool):
+    """Programmatic dependent launch of every kernel (default on): a kernel's
+    set-up overlaps the tail of the one before it on the stream.  Off for
+    graphs whose kernels run beside another stream's (OverlappedForward)."""
+    call("moe_set_pdl", 1 if on else 0)
+    _pdl_on[0] = bool(on)
+
+
+def pdl_enabled() -> bool:
+    """The setting last made through set_pdl (the library starts with it on)."""
+    return _pdl_on[0]
+
+
 # ----------------------------------------------------------------- forward
 
 def route(x, w_router, k, bias=None, return_logits=False):
