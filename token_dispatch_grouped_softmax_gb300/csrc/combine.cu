@@ -58,34 +58,52 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict
   }
   // The chunk loop stays warp-uniform (lanes past the slice only predicate
   // their loads and stores) because every lane takes part in the shuffles
-  // that hand out the k rows and weights.
-  for (int base = c_begin; base < c_end; base += 32) {
-    const int c = base + lane;
-    const bool act = c < c_end;
-    float acc[8];
+  // that hand out the k rows and weights.  Each lane takes two chunks per
+  // pass (c and c + 32), so 2k independent 16-byte loads are in flight.
+  for (int base = c_begin; base < c_end; base += 64) {
+    const int c0 = base + lane, c1 = c0 + 32;
+    const bool act0 = c0 < c_end, act1 = c1 < c_end;
+    float acc0[8], acc1[8];
 #pragma unroll
-    for (int q = 0; q < 8; ++q) acc[q] = 0.f;
+    for (int q = 0; q < 8; ++q) {
+      acc0[q] = 0.f;
+      acc1[q] = 0.f;
+    }
 #pragma unroll 8
     for (int j = 0; j < k; ++j) {
       const int row = __shfl_sync(0xffffffffu, my_row, j);
       const float wj = __shfl_sync(0xffffffffu, my_w, j);
-      if (act) {
-        const uint4 v = __ldg(reinterpret_cast<const uint4*>(y_perm + (int64_t)row * H) + c);
-        float f[8];
-        unpack8(v, f);
-#pragma unroll
-        for (int q = 0; q < 8; ++q) acc[q] = fmaf(wj, f[q], acc[q]);
-      }
-    }
-    if (!act) continue;
-    if (y_shared) {
-      const uint4 v = __ldg(reinterpret_cast<const uint4*>(y_shared + (int64_t)t * H) + c);
+      const uint4* src = reinterpret_cast<const uint4*>(y_perm + (int64_t)row * H);
+      uint4 v0 = make_uint4(0, 0, 0, 0), v1 = make_uint4(0, 0, 0, 0);
+      if (act0) v0 = __ldg(src + c0);
+      if (act1) v1 = __ldg(src + c1);
       float f[8];
-      unpack8(v, f);
+      unpack8(v0, f);
 #pragma unroll
-      for (int q = 0; q < 8; ++q) acc[q] += f[q];
+      for (int q = 0; q < 8; ++q) acc0[q] = fmaf(wj, f[q], acc0[q]);
+      unpack8(v1, f);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) acc1[q] = fmaf(wj, f[q], acc1[q]);
     }
-    reinterpret_cast<uint4*>(y + (int64_t)t * H)[c] = pack8(acc);
+    uint4* dst = reinterpret_cast<uint4*>(y + (int64_t)t * H);
+    if (act0) {
+      if (y_shared) {
+        float f[8];
+        unpack8(__ldg(reinterpret_cast<const uint4*>(y_shared + (int64_t)t * H) + c0), f);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) acc0[q] += f[q];
+      }
+      dst[c0] = pack8(acc0);
+    }
+    if (act1) {
+      if (y_shared) {
+        float f[8];
+        unpack8(__ldg(reinterpret_cast<const uint4*>(y_shared + (int64_t)t * H) + c1), f);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) acc1[q] += f[q];
+      }
+      dst[c1] = pack8(acc1);
+    }
   }
 }
 

@@ -370,7 +370,16 @@ __global__ void permute_rows_kernel(const uint16_t* __restrict__ x, const int32_
   if (row >= R) return;
   const uint4* src = reinterpret_cast<const uint4*>(x + (int64_t)src_row[row] * H);
   uint4* dst = reinterpret_cast<uint4*>(x_perm + row * H);
-  for (int c = lane; c < H / 8; c += 32) dst[c] = src[c];
+  const int nch = H / 8;
+  for (int c0 = lane; c0 < nch; c0 += 128) {   // four 16-byte loads in flight per lane
+    uint4 v[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      if (c0 + 32 * q < nch) v[q] = __ldg(src + c0 + 32 * q);
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      if (c0 + 32 * q < nch) dst[c0 + 32 * q] = v[q];
+  }
 }
 
 }  // namespace
