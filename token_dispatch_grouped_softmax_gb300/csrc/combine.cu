@@ -185,37 +185,56 @@ __global__ void __launch_bounds__(256) gather_dx_kernel(const uint16_t* __restri
       my_dz = d_logits[(int64_t)t * E + my_id];
     }
   }
-  for (int base = c_begin; base < c_end; base += 32) {   // warp-uniform, as in combine_kernel
-    const int c = base + lane;
-    const bool act = c < c_end;
-    float acc[8];
+  // warp-uniform, two chunks per lane per pass, as in combine_kernel
+  for (int base = c_begin; base < c_end; base += 64) {
+    const int c0 = base + lane, c1 = c0 + 32;
+    const bool act0 = c0 < c_end, act1 = c1 < c_end;
+    float acc0[8], acc1[8];
 #pragma unroll
-    for (int q = 0; q < 8; ++q) acc[q] = 0.f;
+    for (int q = 0; q < 8; ++q) {
+      acc0[q] = 0.f;
+      acc1[q] = 0.f;
+    }
 #pragma unroll 8
     for (int j = 0; j < k; ++j) {
       const int row = __shfl_sync(0xffffffffu, my_row, j);
-      if (act) {
-        float f[8];
-        unpack8(__ldg(reinterpret_cast<const uint4*>(dx_perm + (int64_t)row * H) + c), f);
+      const uint4* src = reinterpret_cast<const uint4*>(dx_perm + (int64_t)row * H);
+      uint4 v0 = make_uint4(0, 0, 0, 0), v1 = make_uint4(0, 0, 0, 0);
+      if (act0) v0 = __ldg(src + c0);
+      if (act1) v1 = __ldg(src + c1);
+      float f[8];
+      unpack8(v0, f);
 #pragma unroll
-        for (int q = 0; q < 8; ++q) acc[q] += f[q];
-      }
+      for (int q = 0; q < 8; ++q) acc0[q] += f[q];
+      unpack8(v1, f);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) acc1[q] += f[q];
     }
     if (d_logits) {
+#pragma unroll 4
       for (int j = 0; j < k; ++j) {
         const int e = __shfl_sync(0xffffffffu, my_id, j);
         const float dz = __shfl_sync(0xffffffffu, my_dz, j);
-        if (act) {
-          const float4* wr = reinterpret_cast<const float4*>(wr_t + (int64_t)e * H) + 2 * c;
-          const float4 a = __ldg(wr), b = __ldg(wr + 1);
-          acc[0] = fmaf(dz, a.x, acc[0]); acc[1] = fmaf(dz, a.y, acc[1]);
-          acc[2] = fmaf(dz, a.z, acc[2]); acc[3] = fmaf(dz, a.w, acc[3]);
-          acc[4] = fmaf(dz, b.x, acc[4]); acc[5] = fmaf(dz, b.y, acc[5]);
-          acc[6] = fmaf(dz, b.z, acc[6]); acc[7] = fmaf(dz, b.w, acc[7]);
+        const float4* wr = reinterpret_cast<const float4*>(wr_t + (int64_t)e * H);
+        if (act0) {
+          const float4 a = __ldg(wr + 2 * c0), b = __ldg(wr + 2 * c0 + 1);
+          acc0[0] = fmaf(dz, a.x, acc0[0]); acc0[1] = fmaf(dz, a.y, acc0[1]);
+          acc0[2] = fmaf(dz, a.z, acc0[2]); acc0[3] = fmaf(dz, a.w, acc0[3]);
+          acc0[4] = fmaf(dz, b.x, acc0[4]); acc0[5] = fmaf(dz, b.y, acc0[5]);
+          acc0[6] = fmaf(dz, b.z, acc0[6]); acc0[7] = fmaf(dz, b.w, acc0[7]);
+        }
+        if (act1) {
+          const float4 a = __ldg(wr + 2 * c1), b = __ldg(wr + 2 * c1 + 1);
+          acc1[0] = fmaf(dz, a.x, acc1[0]); acc1[1] = fmaf(dz, a.y, acc1[1]);
+          acc1[2] = fmaf(dz, a.z, acc1[2]); acc1[3] = fmaf(dz, a.w, acc1[3]);
+          acc1[4] = fmaf(dz, b.x, acc1[4]); acc1[5] = fmaf(dz, b.y, acc1[5]);
+          acc1[6] = fmaf(dz, b.z, acc1[6]); acc1[7] = fmaf(dz, b.w, acc1[7]);
         }
       }
     }
-    if (act) reinterpret_cast<uint4*>(dx + (int64_t)t * H)[c] = pack8(acc);
+    uint4* dst = reinterpret_cast<uint4*>(dx + (int64_t)t * H);
+    if (act0) dst[c0] = pack8(acc0);
+    if (act1) dst[c1] = pack8(acc1);
   }
 }
 
