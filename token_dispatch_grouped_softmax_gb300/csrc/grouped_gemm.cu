@@ -896,14 +896,15 @@ template <int MODE, int KH, int CG>
 cudaError_t run_gemm(const GemmParams& p, int64_t tiles_upper_bound, const DeviceInfo& dev,
                      cudaStream_t stream) {
   const size_t smem = gemm_smem_bytes(p.E);
-  static int configured[kMaxDevices] = {0};
-  static int max_pairs[kMaxDevices] = {0};
-  if (!configured[dev.ordinal]) {
+  // per-device set-up, cached (a race between host threads only repeats it)
+  static std::atomic<int> configured[kMaxDevices] = {};
+  static std::atomic<int> max_pairs[kMaxDevices] = {};
+  if (!configured[dev.ordinal].load()) {
     cudaError_t err = cudaFuncSetAttribute(grouped_gemm_kernel<MODE, KH, CG>,
                                            cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            (int)gemm_smem_bytes(kMaxExperts));
     if (err != cudaSuccess) return err;
-    configured[dev.ordinal] = 1;
+    configured[dev.ordinal].store(1);
   }
   if (CG == 1) {
     int64_t grid = tiles_upper_bound < dev.num_sms ? tiles_upper_bound : dev.num_sms;
@@ -924,14 +925,15 @@ cudaError_t run_gemm(const GemmParams& p, int64_t tiles_upper_bound, const Devic
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (!max_pairs[dev.ordinal]) {
+  if (!max_pairs[dev.ordinal].load()) {
     cfg.gridDim = dim3((unsigned)dev.num_sms);
     int n = 0;
     cudaError_t err = cudaOccupancyMaxActiveClusters(&n, grouped_gemm_kernel<MODE, KH, CG>, &cfg);
     if (err != cudaSuccess) return err;
-    max_pairs[dev.ordinal] = n > 0 ? n : 1;
+    max_pairs[dev.ordinal].store(n > 0 ? n : 1);
   }
-  int64_t pairs = tiles_upper_bound < max_pairs[dev.ordinal] ? tiles_upper_bound : max_pairs[dev.ordinal];
+  const int64_t mp = max_pairs[dev.ordinal].load();
+  int64_t pairs = tiles_upper_bound < mp ? tiles_upper_bound : mp;
   if (pairs < 1) pairs = 1;
   cfg.gridDim = dim3((unsigned)(2 * pairs));
   cfg.dynamicSmemBytes = smem;

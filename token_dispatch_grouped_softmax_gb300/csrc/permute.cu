@@ -396,17 +396,18 @@ size_t permute_workspace_bytes(int64_t R, int64_t E, bool noalloc) {
 
 // Blocks of permute_fused_kernel that can be resident at once on `dev`.
 int64_t permute_fused_capacity(const DeviceInfo& dev, int64_t E) {
-  static int per_sm[kMaxDevices][2] = {{0}};
+  static std::atomic<int> per_sm[kMaxDevices][2] = {};   // cached per device (a race only repeats the query)
   const int slot = E <= 256 ? 0 : 1;   // shared memory grows with E; size the query for the larger E
-  if (!per_sm[dev.ordinal][slot]) {
+  if (!per_sm[dev.ordinal][slot].load()) {
     const size_t smem = ((size_t)(kPermWarps + 1) * (slot ? kMaxExperts : 256) + 40) * sizeof(int32_t);
     int n = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, permute_fused_kernel<kChunk>, kPermThreads, smem) !=
         cudaSuccess)
       return 0;
-    per_sm[dev.ordinal][slot] = n > 0 ? n : -1;
+    per_sm[dev.ordinal][slot].store(n > 0 ? n : -1);
   }
-  return per_sm[dev.ordinal][slot] > 0 ? (int64_t)per_sm[dev.ordinal][slot] * dev.num_sms : 0;
+  const int ps = per_sm[dev.ordinal][slot].load();
+  return ps > 0 ? (int64_t)ps * dev.num_sms : 0;
 }
 
 template <int CHUNK>

@@ -529,12 +529,12 @@ size_t fused_router_smem(int64_t E) {
 template <int NV>
 cudaError_t launch_fused_router_nv(const FusedRouterParams& p, int P, int64_t T, const DeviceInfo& dev,
                                    cudaStream_t stream) {
-  static int configured[kMaxDevices] = {0};
-  if (!configured[dev.ordinal]) {
+  static std::atomic<int> configured[kMaxDevices] = {};   // per device (a race only repeats the set-up)
+  if (!configured[dev.ordinal].load()) {
     const cudaError_t err = cudaFuncSetAttribute(fused_router_kernel<NV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                  (int)std::max(fused_router_smem(128), fused_router_smem(256)));
     if (err != cudaSuccess) return err;
-    configured[dev.ordinal] = 1;
+    configured[dev.ordinal].store(1);
   }
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[2];
