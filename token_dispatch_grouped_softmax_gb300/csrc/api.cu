@@ -194,7 +194,12 @@ int moe_permute_rows(const uint16_t* x, const int32_t* src_row, int64_t R, int64
   if (R > 0 && (!x || !src_row || !x_perm)) return MOE_ERR_INVALID_ARG;
   if (H % 8 != 0) return MOE_ERR_UNSUPPORTED;
   if (R > 0 && (!aligned16(x) || !aligned16(x_perm))) return MOE_ERR_INVALID_ARG;
-  return cuda_status(moe::launch_permute_rows(x, src_row, R, H, x_perm, static_cast<cudaStream_t>(stream)));
+  if (R == 0) return MOE_OK;
+  moe::DeviceInfo dev;
+  const int rc = moe::current_device(&dev);
+  if (rc != MOE_OK) return rc;
+  return cuda_status(moe::launch_permute_rows(x, src_row, R, H, x_perm, 0, dev.status,
+                                              static_cast<cudaStream_t>(stream)));
 }
 
 /* ----------------------------------------------------------- grouped GEMMs */
@@ -252,7 +257,10 @@ int moe_unpermute_combine(const uint16_t* y_perm, const int32_t* row_map, const 
   if (T == 0) return MOE_OK;
   if (!y_perm || !row_map || !w || !y) return MOE_ERR_INVALID_ARG;
   if (!aligned16(y_perm) || !aligned16(y) || (y_shared && !aligned16(y_shared))) return MOE_ERR_INVALID_ARG;
-  return cuda_status(moe::launch_combine(y_perm, row_map, w, y_shared, T, H, k, y,
+  moe::DeviceInfo dev;
+  const int rc = moe::current_device(&dev);
+  if (rc != MOE_OK) return rc;
+  return cuda_status(moe::launch_combine(y_perm, row_map, w, y_shared, T, H, k, y, dev.status,
                                          static_cast<cudaStream_t>(stream)));
 }
 
@@ -265,7 +273,10 @@ int moe_unpermute_combine_bwd(const uint16_t* dy, const int32_t* src_row, int64_
   if (T == 0) return MOE_OK;
   if (!dy || !src_row || !dy_perm) return MOE_ERR_INVALID_ARG;
   if (!aligned16(dy) || !aligned16(dy_perm)) return MOE_ERR_INVALID_ARG;
-  return cuda_status(moe::launch_permute_rows(dy, src_row, T * k, H, dy_perm,
+  moe::DeviceInfo dev;
+  const int rc = moe::current_device(&dev);
+  if (rc != MOE_OK) return rc;
+  return cuda_status(moe::launch_permute_rows(dy, src_row, T * k, H, dy_perm, T, dev.status,
                                               static_cast<cudaStream_t>(stream)));
 }
 
@@ -277,8 +288,11 @@ int moe_route_bwd(const float* dw_part, int64_t nparts, const int32_t* row_map, 
   if (k > 32 || nparts > 64) return MOE_ERR_UNSUPPORTED;
   if (T == 0) return MOE_OK;
   if (!dw_part || !row_map || !w || !ids || !d_logits) return MOE_ERR_INVALID_ARG;
+  moe::DeviceInfo dev;
+  const int rc = moe::current_device(&dev);
+  if (rc != MOE_OK) return rc;
   return cuda_status(moe::launch_route_bwd(dw_part, (int)nparts, row_map, w, ids, T, E, k, d_logits, dw,
-                                           static_cast<cudaStream_t>(stream)));
+                                           dev.status, static_cast<cudaStream_t>(stream)));
 }
 
 int moe_grouped_gemm_down_bwd_parts(int64_t I, int64_t* nparts) {
@@ -348,8 +362,11 @@ int moe_gather_dx(const uint16_t* dx_perm, const int32_t* row_map, const float* 
   if (d_logits && (!workspace || !aligned16(workspace) ||
                    workspace_bytes < moe::gather_dx_workspace_bytes(H, E)))
     return MOE_ERR_WORKSPACE;
+  moe::DeviceInfo dev;
+  const int rc = moe::current_device(&dev);
+  if (rc != MOE_OK) return rc;
   return cuda_status(moe::launch_gather_dx(dx_perm, row_map, d_logits, ids, w_router, T, H, E, k, dx,
-                                           workspace, static_cast<cudaStream_t>(stream)));
+                                           workspace, dev.status, static_cast<cudaStream_t>(stream)));
 }
 
 int moe_route_bwd_weight(const uint16_t* x, const float* d_logits, int64_t T, int64_t H, int64_t E,

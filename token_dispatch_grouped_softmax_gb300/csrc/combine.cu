@@ -39,7 +39,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict
                                                       const float* __restrict__ w,
                                                       const uint16_t* __restrict__ y_shared,
                                                       int T, int H, int k,
-                                                      uint16_t* __restrict__ y) {
+                                                      uint16_t* __restrict__ y, uint32_t* status) {
   pdl_wait();
   pdl_trigger();
   const int lane = threadIdx.x & 31;
@@ -55,6 +55,10 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict
   if (lane < k) {
     my_row = row_map[(int64_t)t * k + lane];
     my_w = w[(int64_t)t * k + lane];
+    if (my_row < 0 || (int64_t)my_row >= (int64_t)T * k) {   // not a permuted row: report, read row 0
+      report_status(status, kStatusDevice, kKernCombine, 1);
+      my_row = 0;
+    }
   }
   // The chunk loop stays warp-uniform (lanes past the slice only predicate
   // their loads and stores) because every lane takes part in the shuffles
@@ -113,7 +117,7 @@ __global__ void __launch_bounds__(256) route_bwd_kernel(const float* __restrict_
                                                         const int32_t* __restrict__ ids, int T,
                                                         int E, int k,
                                                         float* __restrict__ d_logits,
-                                                        float* __restrict__ dw) {
+                                                        float* __restrict__ dw, uint32_t* status) {
   pdl_wait();
   pdl_trigger();
   const int lane = threadIdx.x & 31;
@@ -124,7 +128,11 @@ __global__ void __launch_bounds__(256) route_bwd_kernel(const float* __restrict_
   if (lane < k) {
     my_w = w[(int64_t)t * k + lane];
     my_id = ids[(int64_t)t * k + lane];
-    const int64_t row = row_map[(int64_t)t * k + lane];
+    int64_t row = row_map[(int64_t)t * k + lane];
+    if (row < 0 || row >= (int64_t)T * k) {   // not a permuted row: report, read row 0
+      report_status(status, kStatusDevice, kKernCombine, 4);
+      row = 0;
+    }
     for (int n = 0; n < nparts; ++n) my_dw += dw_part[row * nparts + n];   // fixed order
     if (dw) dw[(int64_t)t * k + lane] = my_dw;
   }
@@ -165,7 +173,7 @@ __global__ void __launch_bounds__(256) gather_dx_kernel(const uint16_t* __restri
                                                         const int32_t* __restrict__ ids,
                                                         const float* __restrict__ wr_t, int T,
                                                         int H, int E, int k,
-                                                        uint16_t* __restrict__ dx) {
+                                                        uint16_t* __restrict__ dx, uint32_t* status) {
   pdl_wait();
   pdl_trigger();
   const int lane = threadIdx.x & 31;
@@ -180,8 +188,16 @@ __global__ void __launch_bounds__(256) gather_dx_kernel(const uint16_t* __restri
   float my_dz = 0.f;
   if (lane < k) {
     my_row = row_map[(int64_t)t * k + lane];
+    if (my_row < 0 || (int64_t)my_row >= (int64_t)T * k) {   // not a permuted row: report, read row 0
+      report_status(status, kStatusDevice, kKernCombine, 2);
+      my_row = 0;
+    }
     if (d_logits) {
       my_id = ids[(int64_t)t * k + lane];
+      if (my_id < 0 || my_id >= E) {   // not an expert id: report, use expert 0
+        report_status(status, kStatusDevice, kKernCombine, 3);
+        my_id = 0;
+      }
       my_dz = d_logits[(int64_t)t * E + my_id];
     }
   }
@@ -288,26 +304,27 @@ __global__ void __launch_bounds__(256) route_bwd_weight_kernel(const uint16_t* _
 
 cudaError_t launch_combine(const uint16_t* y_perm, const int32_t* row_map, const float* w,
                            const uint16_t* y_shared, int64_t T, int64_t H, int64_t k, uint16_t* y,
-                           cudaStream_t stream) {
+                           uint32_t* status, cudaStream_t stream) {
   if (T == 0) return cudaSuccess;
   const int64_t warps = T * ((H / 8 + kSliceChunks - 1) / kSliceChunks);
   return launch_pdl(combine_kernel, dim3((unsigned)((warps + kWarpsPerBlock - 1) / kWarpsPerBlock)), dim3(256), 0,
-                    stream, 1, y_perm, row_map, w, y_shared, (int)T, (int)H, (int)k, y);
+                    stream, 1, y_perm, row_map, w, y_shared, (int)T, (int)H, (int)k, y, status);
 }
 
 cudaError_t launch_route_bwd(const float* dw_part, int nparts, const int32_t* row_map, const float* w,
                              const int32_t* ids, int64_t T, int64_t E, int64_t k, float* d_logits,
-                             float* dw, cudaStream_t stream) {
+                             float* dw, uint32_t* status, cudaStream_t stream) {
   if (T == 0) return cudaSuccess;
   return launch_pdl(route_bwd_kernel, dim3((unsigned)((T + kWarpsPerBlock - 1) / kWarpsPerBlock)), dim3(256), 0,
-                    stream, 1, dw_part, nparts, row_map, w, ids, (int)T, (int)E, (int)k, d_logits, dw);
+                    stream, 1, dw_part, nparts, row_map, w, ids, (int)T, (int)E, (int)k, d_logits, dw, status);
 }
 
 size_t gather_dx_workspace_bytes(int64_t H, int64_t E) { return (size_t)(H * E * sizeof(float)); }
 
 cudaError_t launch_gather_dx(const uint16_t* dx_perm, const int32_t* row_map, const float* d_logits,
                              const int32_t* ids, const float* w_router, int64_t T, int64_t H,
-                             int64_t E, int64_t k, uint16_t* dx, void* ws, cudaStream_t stream) {
+                             int64_t E, int64_t k, uint16_t* dx, void* ws, uint32_t* status,
+                             cudaStream_t stream) {
   if (T == 0) return cudaSuccess;
   float* wr_t = nullptr;
   if (d_logits) {
@@ -319,7 +336,8 @@ cudaError_t launch_gather_dx(const uint16_t* dx_perm, const int32_t* row_map, co
   }
   const int64_t warps = T * ((H / 8 + kSliceChunks - 1) / kSliceChunks);
   return launch_pdl(gather_dx_kernel, dim3((unsigned)((warps + kWarpsPerBlock - 1) / kWarpsPerBlock)), dim3(256),
-                    0, stream, 1, dx_perm, row_map, d_logits, ids, wr_t, (int)T, (int)H, (int)E, (int)k, dx);
+                    0, stream, 1, dx_perm, row_map, d_logits, ids, wr_t, (int)T, (int)H, (int)E, (int)k, dx,
+                    status);
 }
 
 cudaError_t launch_route_bwd_weight(const uint16_t* x, const float* d_logits, int64_t T, int64_t H,

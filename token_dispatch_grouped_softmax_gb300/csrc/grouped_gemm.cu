@@ -432,7 +432,7 @@ __global__ void __launch_bounds__(Traits<MODE, KH, CG>::kThreads, 1)
   // bars: full[STAGES], empty[STAGES], acc_full[2], acc_empty[2], drain (at most 17 of 24)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 24);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  int* prefix = reinterpret_cast<int*>(tmem_slot + 2);   // [E+1]
+  int* prefix = reinterpret_cast<int*>(tmem_slot + 2);   // [E+1], then the offsets check flag
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -482,16 +482,37 @@ __global__ void __launch_bounds__(Traits<MODE, KH, CG>::kThreads, 1)
   // Tile prefix over experts (M-grouped modes): prefix[e] = sum_{e'<e} ceil(M_e'/BM) * nt.
   // Tiles go out in expert order, so the row tiles of one expert run at about
   // the same time and read its weights from L2 after the first of them.
+  // Expert offsets that are not an exclusive scan of counts ending at the row
+  // count (offsets[0] = 0, non-decreasing, offsets[E] = rows) are reported
+  // and the launch does no work: no tile may store past its output or run
+  // for an unbounded K.
   int total_tiles;
+  if (warp == 2) {
+    bool bad = false;
+    if (p.offsets && !Tr::kRouter) {
+      for (int e0 = 0; e0 <= p.E; e0 += 32) {
+        const int e = e0 + lane;
+        if (e <= p.E) {
+          const int v = p.offsets[e];
+          const int prev = e > 0 ? p.offsets[e - 1] : 0;
+          if (v < prev || v > p.rows || (e == 0 && v != 0) || (e == p.E && v != p.rows)) bad = true;
+        }
+      }
+      bad = __any_sync(0xffffffffu, bad);
+      if (bad && lane == 0) report_status(p.status, kStatusDevice, kKernGemm, 5);
+    }
+    if (lane == 0) prefix[p.E + 1] = bad ? 1 : 0;
+  }
   if (Tr::kKGrouped || Tr::kRouter) {
     total_tiles = p.E * p.mt_w * p.nt;
   } else {
     if (warp == 2) {
+      const bool bad = __shfl_sync(0xffffffffu, lane == 0 ? prefix[p.E + 1] : 0, 0) != 0;
       int carry = 0;
       for (int e0 = 0; e0 < p.E; e0 += 32) {
         const int e = e0 + lane;
         int v = 0;
-        if (e < p.E) {
+        if (e < p.E && !bad) {
           int start, count;
           group_range(p, e, start, count);
           v = ((count + Tr::kBM - 1) / Tr::kBM) * p.nt;
@@ -514,6 +535,7 @@ __global__ void __launch_bounds__(Traits<MODE, KH, CG>::kThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   if (!Tr::kKGrouped && !Tr::kRouter) total_tiles = prefix[p.E];
+  if (prefix[p.E + 1]) total_tiles = 0;   // invalid expert offsets (reported above)
 
   if (warp == 0) {
     // ------------------------------------------------------ TMA producer
@@ -888,7 +910,8 @@ __global__ void __launch_bounds__(Traits<MODE, KH, CG>::kThreads, 1)
   }
 }
 
-size_t gemm_smem_bytes(int E) { return 1024 + (size_t)RING_BYTES + 8 * 24 + 16 + 4 * (size_t)(E + 1) + 64; }
+// ring, 24 mbarriers, TMEM slot + abort flag, prefix[E + 1] + the offsets check flag, slack
+size_t gemm_smem_bytes(int E) { return 1024 + (size_t)RING_BYTES + 8 * 24 + 16 + 4 * (size_t)(E + 2) + 64; }
 
 // Persistent launch: one CTA per SM, or one pair per two SMs (a cluster of
 // two CTAs; as many clusters as fit at once, capped by the tile count).

@@ -78,19 +78,21 @@ cudaError_t launch_permute(const int32_t* ids, const float* w, int64_t T, int64_
                            int32_t* counts, int32_t* offsets, int32_t* row_map, int32_t* src_row,
                            float* w_perm, void* ws, const DeviceInfo& dev, cudaStream_t stream,
                            bool noalloc = false);
+// src_rows: rows of x, checked on the device (0: unchecked)
 cudaError_t launch_permute_rows(const uint16_t* x, const int32_t* src_row, int64_t R, int64_t H,
-                                uint16_t* x_perm, cudaStream_t stream);
+                                uint16_t* x_perm, int64_t src_rows, uint32_t* status, cudaStream_t stream);
 
 cudaError_t launch_combine(const uint16_t* y_perm, const int32_t* row_map, const float* w,
                            const uint16_t* y_shared, int64_t T, int64_t H, int64_t k, uint16_t* y,
-                           cudaStream_t stream);
+                           uint32_t* status, cudaStream_t stream);
 cudaError_t launch_route_bwd(const float* dw_part, int nparts, const int32_t* row_map, const float* w,
                              const int32_t* ids, int64_t T, int64_t E, int64_t k, float* d_logits,
-                             float* dw, cudaStream_t stream);
+                             float* dw, uint32_t* status, cudaStream_t stream);
 size_t gather_dx_workspace_bytes(int64_t H, int64_t E);
 cudaError_t launch_gather_dx(const uint16_t* dx_perm, const int32_t* row_map, const float* d_logits,
                              const int32_t* ids, const float* w_router, int64_t T, int64_t H,
-                             int64_t E, int64_t k, uint16_t* dx, void* ws, cudaStream_t stream);
+                             int64_t E, int64_t k, uint16_t* dx, void* ws, uint32_t* status,
+                             cudaStream_t stream);
 cudaError_t launch_route_bwd_weight(const uint16_t* x, const float* d_logits, int64_t T, int64_t H,
                                     int64_t E, float* d_w_router, cudaStream_t stream);
 

@@ -361,14 +361,22 @@ __global__ void __launch_bounds__(kPermThreads) permute_fused_kernel(
   }
 }
 
+// src_rows: rows of x (a source row outside [0, src_rows) is reported and
+// row 0 read instead), or 0: unchecked.
 __global__ void permute_rows_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ src_row,
-                                    int64_t R, int H, uint16_t* __restrict__ x_perm) {
+                                    int64_t R, int H, uint16_t* __restrict__ x_perm, int64_t src_rows,
+                                    uint32_t* status) {
   pdl_wait();
   pdl_trigger();
   const int64_t row = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (row >= R) return;
-  const uint4* src = reinterpret_cast<const uint4*>(x + (int64_t)src_row[row] * H);
+  int64_t s = src_row[row];
+  if (src_rows > 0 && (s < 0 || s >= src_rows)) {
+    if (lane == 0) report_status(status, kStatusDevice, kKernPermute, 3);
+    s = 0;
+  }
+  const uint4* src = reinterpret_cast<const uint4*>(x + s * H);
   uint4* dst = reinterpret_cast<uint4*>(x_perm + row * H);
   const int nch = H / 8;
   for (int c0 = lane; c0 < nch; c0 += 128) {   // four 16-byte loads in flight per lane
@@ -463,10 +471,10 @@ cudaError_t launch_permute(const int32_t* ids, const float* w, int64_t T, int64_
 }
 
 cudaError_t launch_permute_rows(const uint16_t* x, const int32_t* src_row, int64_t R, int64_t H,
-                                uint16_t* x_perm, cudaStream_t stream) {
+                                uint16_t* x_perm, int64_t src_rows, uint32_t* status, cudaStream_t stream) {
   if (R == 0) return cudaSuccess;
   return launch_pdl(permute_rows_kernel, dim3((unsigned)((R + 7) / 8)), dim3(256), 0, stream, 1, x, src_row, R,
-                    (int)H, x_perm);
+                    (int)H, x_perm, src_rows, status);
 }
 
 }  // namespace moe
