@@ -175,11 +175,16 @@ int moe_permute_noalloc(const int32_t* ids, const float* w, int64_t T, int64_t k
                         float* w_perm, void* stream);
 
 /* The materialised permute: x_perm[row] = x[src_row[row]] for R rows of H
- * bf16 (the grouped GEMMs gather rows themselves and do not need it). */
+ * bf16 (the grouped GEMMs gather rows themselves and do not need it).  The
+ * source rows are not range-checked here (the token count is not passed). */
 int moe_permute_rows(const uint16_t* x, const int32_t* src_row, int64_t R, int64_t H,
                      uint16_t* x_perm, void* stream);
 
 /* ----------------------------------------------------------- grouped GEMMs */
+
+/* Every grouped GEMM checks its offsets on the device (offsets[0] = 0,
+ * non-decreasing, offsets[E] = R); other values set MOE_ERR_DEVICE in the
+ * status word and the call computes nothing (its outputs are undefined). */
 
 /* Grouped gate_up GEMM with the SwiGLU fused into its epilogue (MindSpeed
  * page §2 layout, §8.3 "grouped_matmul -> SwiGLU").  For each expert e and
@@ -220,7 +225,8 @@ int moe_grouped_gemm_down(const uint16_t* h, const int32_t* offsets, const uint1
  * accumulated in fp32 in increasing j, stored bf16.  Deterministic.
  *   y_perm [R, H] bf16; row_map [R] int32; w [T, k] fp32;
  *   y_shared [T, H] bf16 or NULL (the always-active shared expert, weight 1);
- *   y [T, H] bf16 (out).  Limits: k <= 32. */
+ *   y [T, H] bf16 (out).  Limits: k <= 32.  A row_map entry outside [0, T*k)
+ * sets MOE_ERR_DEVICE in the status word (row 0 is read in its place). */
 int moe_unpermute_combine(const uint16_t* y_perm, const int32_t* row_map, const float* w,
                           const uint16_t* y_shared, int64_t T, int64_t H, int64_t k, uint16_t* y,
                           void* stream);
@@ -235,7 +241,8 @@ int moe_unpermute_combine(const uint16_t* y_perm, const int32_t* row_map, const 
  *   dy_perm[row] = dY[src_row[row]]         (an exact bf16 copy; R = T*k rows)
  * The gate-weight gradient dw[t,j] = <dY[t], y_perm[row_map[t*k+j]]> is
  * produced by moe_grouped_gemm_down_bwd (as <dY . Wd^T, h>) and summed by
- * moe_route_bwd.  dy [T, H] bf16; src_row [R] int32; dy_perm [R, H] bf16. */
+ * moe_route_bwd.  dy [T, H] bf16; src_row [R] int32; dy_perm [R, H] bf16.
+ * A src_row entry outside [0, T) sets MOE_ERR_DEVICE (row 0 is read). */
 int moe_unpermute_combine_bwd(const uint16_t* dy, const int32_t* src_row, int64_t T, int64_t H,
                               int64_t k, uint16_t* dy_perm, void* stream);
 
@@ -265,7 +272,8 @@ int moe_grouped_gemm_down_bwd(const uint16_t* dy_perm, const uint16_t* h_w, cons
  *   dw[t,j] = sum_n dw_part[row_map[t*k+j], n]          (fixed order)
  *   d_logits[t, ids[t,j]] = w[t,j] * (dw[t,j] - sum_i w[t,i] dw[t,i])
  *   d_logits[t, e] = 0 for every expert not chosen by t
- *   d_logits [T, E] fp32 (out); dw [T, k] fp32 (out, nullable). */
+ *   d_logits [T, E] fp32 (out); dw [T, k] fp32 (out, nullable).
+ * A row_map entry outside [0, T*k) sets MOE_ERR_DEVICE (row 0 is read). */
 int moe_route_bwd(const float* dw_part, int64_t nparts, const int32_t* row_map, const float* w,
                   const int32_t* ids, int64_t T, int64_t E, int64_t k, float* d_logits, float* dw,
                   void* stream);
@@ -289,7 +297,9 @@ int moe_gather_dx_workspace_size(int64_t H, int64_t E, size_t* bytes);
  * (the second sum is the router's contribution d_logits . W_r^T, whose only
  * nonzero terms are the chosen experts).  d_logits/w_router may both be NULL
  * to leave the router term out (no workspace needed then).  dX [T, H] bf16
- * (out), fp32 accumulation, one bf16 rounding. */
+ * (out), fp32 accumulation, one bf16 rounding.  A row_map entry outside
+ * [0, T*k) or an id outside [0, E) sets MOE_ERR_DEVICE (row / expert 0 is
+ * read in its place). */
 int moe_gather_dx(const uint16_t* dx_perm, const int32_t* row_map, const float* d_logits,
                   const int32_t* ids, const float* w_router, int64_t T, int64_t H, int64_t E,
                   int64_t k, uint16_t* dx, void* workspace, size_t workspace_bytes, void* stream);
