@@ -295,3 +295,38 @@ def test_overlapped_forward_matches_forward():
         for xh, yh in zip(xs, ys):
             y, _ = moe.moe_forward(xh.cuda(), wr, gu, dn, cfg.k, None, sgu, sdn)
             assert torch_equal(y.cpu(), yh)
+
+
+
+# expert sizes around every tile boundary of the grouped GEMMs: empty
+# experts, 1 row, 16-row steps, 64-row boxes, 128-row tiles and their tails,
+# 256-row tiles (two halves) and their tails
+TILE_EDGE_COUNTS = [0, 1, 15, 16, 17, 63, 64, 65, 80, 127, 128, 129, 200, 255, 256, 257, 300, 383, 384,
+                    385, 511, 512, 513, 700, 1000, 0, 33]
+# at least 512 rows per expert on average: the down GEMM's 256-row tiles with
+# one- and two-half tails
+HEAVY_COUNTS = [513, 1000, 0, 700, 1024, 2047]
+
+
+@pytest.mark.parametrize("counts", [TILE_EDGE_COUNTS, HEAVY_COUNTS], ids=["edges", "heavy"])
+@pytest.mark.parametrize("H,I", [(256, 192), (320, 128)])
+def test_grouped_gemms_at_tile_edges(H, I, counts):
+    """The forward grouped GEMMs on explicit expert offsets whose sizes sit on
+    either side of every tile boundary (I = 192: a partial gate/up column
+    tile; H = 320: a partial down output tile), element by element against
+    the oracle (identity permutation, k = 1)."""
+    moe = lib()
+    E, R = len(counts), sum(counts)
+    offs = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    x = synth.normal_bf16(R + H, synth.TID_X, (R, H), 1.0)
+    gu = synth.normal_bf16(R + H, synth.TID_GATE_UP, (E * H, 2 * I), H ** -0.5)
+    dn = synth.normal_bf16(R + H, synth.TID_DOWN, (E * I, H), I ** -0.5)
+    ident = np.arange(R, dtype=np.int32)
+    perm = dict(counts=np.array(counts, dtype=np.int32), offsets=offs, row_map=ident,
+                src_row=ident)
+    _, ref = oracle.forward_permuted(x, gu, dn, np.ones((R, 1)), perm, 1, want_intermediates=True)
+    h, _, _ = moe.grouped_gemm_gate_up_swiglu(bf(x), None, i32(offs), bf(gu), I)
+    y = moe.grouped_gemm_down(h, i32(offs), bf(dn), H)
+    moe.sync_status()
+    assert_close("h", f64(h), ref["h_perm"])
+    assert_close("y_perm", f64(y), ref["y_perm"])
