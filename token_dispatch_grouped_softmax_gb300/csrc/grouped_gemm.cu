@@ -46,7 +46,9 @@
 //
 // The tile list is derived on the device from expert_offsets (no host read
 // back): forward and dgrad GEMMs are grouped along M (each expert's rows form
-// ceil(M_e/BM) row tiles, empty experts none); wgrad GEMMs are grouped along
+// ceil(M_e/BM) row tiles, empty experts none; gate_up, whose token rows a
+// gather has just written, walks the experts from the last to the first, so
+// that it starts on the rows still in L2); wgrad GEMMs are grouped along
 // K (every expert owns a fixed grid of output tiles; its K extent is M_e,
 // and an empty expert's tiles are written as zeros).  Within a wgrad tile,
 // K rows past the expert's last row are zeroed in shared memory before the
@@ -84,6 +86,11 @@ struct Traits {
   static constexpr bool kBMN = (kGateUp || MODE == FWD_DOWN || MODE == WGRAD_DOWN ||
                                 MODE == WGRAD_GATEUP || MODE == ROUTER);
   static constexpr bool kKGrouped = (MODE == WGRAD_DOWN || MODE == WGRAD_GATEUP);
+  // Tiles from the last expert to the first: the permuted token rows were
+  // written just before, in increasing row order, by a gather that moves
+  // more bytes than L2 holds, so the rows of the last experts are the ones
+  // still in L2.
+  static constexpr bool kReverse = (MODE == FWD_GATEUP);
   static constexpr bool kRouter = (MODE == ROUTER);
   // One half per CTA for the epilogues with per-element math (SwiGLU, its
   // backward), which then overlap with the next tile's MMAs through two
@@ -199,6 +206,7 @@ __device__ __forceinline__ Tile decode_tile(const GemmParams& p, const int* pref
     t.kblocks = (t.rows + BK - 1) / BK;
     t.halves = (Tr::kBM == 2 * BMH && p.m_w - t.mt * Tr::kBM > BMH) ? 2 : 1;
   } else {
+    if (Tr::kReverse) tile = prefix[p.E] - 1 - tile;
     int lo = 0, hi = p.E - 1;    // largest e with prefix[e] <= tile
     while (lo < hi) {
       const int mid = (lo + hi + 1) >> 1;
