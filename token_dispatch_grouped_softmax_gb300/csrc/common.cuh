@@ -222,9 +222,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
-// Four rows (r0..r3) of one 2-D tensor, each `box inner` elements starting at
-// column c0, written as four consecutive box rows at dst (the tensor map's
-// box must be one row high), with an L2 cache policy.
 // L2 policy that keeps lines resident (evict last): for small operands that
 // are re-read across a whole launch while large ones stream past.
 __device__ __forceinline__ uint64_t l2_policy_evict_last() {
@@ -247,6 +244,9 @@ __device__ __forceinline__ void cp_async_wait_group() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
+// Four rows (r0..r3) of one 2-D tensor, each `box inner` elements starting at
+// column c0, written as four consecutive box rows at dst (the tensor map's
+// box must be one row high), with an L2 cache policy.
 __device__ __forceinline__ void tma_gather4_hint(uint32_t dst, const CUtensorMap* map, int32_t c0,
                                                  int32_t r0, int32_t r1, int32_t r2, int32_t r3,
                                                  uint32_t bar, uint64_t pol) {
