@@ -30,6 +30,11 @@
  *   - Errors found on the device (an expert id out of range, a bounded wait
  *     that ran out) set a device status word that moe_sync_status() reads.
  *   - Sizes are int64_t.  R = T*k is the number of permuted rows.
+ *   - An empty batch (T == 0, or R == 0) is a valid call.  It writes only
+ *     the outputs whose size does not depend on the rows: zero counts and
+ *     offsets (moe_permute), zero weight gradients (the backward GEMMs,
+ *     moe_route_bwd_weight).  Its row pointers may be NULL, including the
+ *     optional ones, so an empty tensor's NULL data pointer is accepted.
  *   - Alignment: every base pointer must be 16-byte aligned; H and I must be
  *     multiples of 64 for the grouped GEMMs and of 8 elsewhere.
  */

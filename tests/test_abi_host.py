@@ -144,6 +144,8 @@ def test_combine_and_backward_validation(lib):
     # the router term needs both d_logits and w_router, and the workspace
     assert lib.moe_gather_dx(FAKE, FAKE, FAKE, FAKE, None, 4, 64, 8, 2, FAKE, FAKE, n.value, None) == INVALID
     assert lib.moe_gather_dx(FAKE, FAKE, FAKE, FAKE, FAKE, 4, 64, 8, 2, FAKE, None, 0, None) == WORKSPACE
+    # an empty batch is a no-op whatever its row pointers (an empty tensor's data pointer is NULL)
+    assert lib.moe_gather_dx(None, None, None, None, FAKE, 0, 64, 8, 2, None, None, 0, None) == 0
     assert lib.moe_route_bwd_weight(FAKE, FAKE, 4, 64, 8, None, None) == INVALID
 
 

@@ -129,6 +129,67 @@ def test_backward_empty_experts_get_zero_weight_grads():
     assert not dgu[empty].any() and not ddn[empty].any()
 
 
+def test_every_token_on_the_same_two_experts():
+    """Degenerate routing: a router bias of +40 on experts 2 and 7 sends every
+    token to those two (in either order), so six experts are empty and two
+    hold T rows each; forward and backward element by element against the
+    oracle, and zero weight gradients for the empty experts."""
+    moe = lib()
+    T, H, E, k, I = 300, 128, 8, 2, 64
+    cfg, inp = _inputs(T, H, E, k, I, seed=17)
+    inp.bias = np.zeros(E, dtype=np.float32)
+    inp.bias[[2, 7]] = 40.0
+    (x, wr, gu, dn), y, st = _forward(moe, inp, save=True)
+    g = moe.moe_backward(bf(inp.dy), st, wr, gu, dn, want_dw_router=True)
+    moe.sync_status()
+    assert npi(st.counts).tolist() == [0, 0, T, 0, 0, 0, 0, T]
+    assert (np.sort(npi(st.ids), axis=1) == np.array([2, 7])).all()
+    ref = oracle.layer_forward(inp, want_intermediates=True)
+    same, tol = compare_ids(npi(st.ids), ref["route"])
+    assert tol == 0 and same.all()
+    np.testing.assert_array_equal(npi(st.row_map), ref["perm"]["row_map"])
+    assert_close("y", f64(y), ref["y"])
+    r = ref["route"]
+    b = oracle.backward(inp.x, inp.w_router, inp.gate_up, inp.down, r["ids"], r["w"], inp.dy,
+                        want_dw=True, want_dwr=True)
+    assert_close("dw", f64(g["dw"]), b["dw"], bf16_out=False)
+    assert_close("d_logits", f64(g["d_logits"]), b["dlogits"], bf16_out=False)
+    assert_close("dX", f64(g["dx"]), b["dX"])
+    assert_close("d_w_router", f64(g["d_w_router"]), b["d_w_r"], bf16_out=False)
+    # weight gradients per expert block, as in the sampled training test
+    # (six of the eight blocks are exact zeros and would halve a whole-tensor RMS)
+    dgu = f64(g["d_gate_up"]).reshape(E, H, 2 * I)
+    ddn = f64(g["d_down"]).reshape(E, I, H)
+    rgu = b["d_gate_up"].reshape(E, H, 2 * I)
+    rdn = b["d_down"].reshape(E, I, H)
+    for e in (2, 7):
+        assert_close("d_gate_up[%d]" % e, dgu[e], rgu[e])
+        assert_close("d_down[%d]" % e, ddn[e], rdn[e])
+    empty = [0, 1, 3, 4, 5, 6]
+    assert not dgu[empty].any() and not ddn[empty].any()
+
+
+def test_empty_batch_forward_backward():
+    """T = 0: every call is a no-op that still writes what it owes: zero
+    counts and offsets, zero weight gradients, [0, H] outputs."""
+    import torch
+    moe = lib()
+    H, E, k, I = 128, 8, 2, 64
+    cfg, inp = _inputs(64, H, E, k, I, seed=11)
+    wr, gu, dn = f32(inp.w_router), bf(inp.gate_up), bf(inp.down)
+    x = torch.empty((0, H), dtype=torch.bfloat16, device=wr.device)
+    y, st = moe.moe_forward(x, wr, gu, dn, k, save_for_backward=True)
+    moe.sync_status()
+    assert tuple(y.shape) == (0, H)
+    assert not npi(st.counts).any() and not npi(st.offsets).any()
+    g = moe.moe_backward(torch.empty((0, H), dtype=torch.bfloat16, device=wr.device), st, wr, gu, dn,
+                         want_dw_router=True)
+    moe.sync_status()
+    assert tuple(g["dx"].shape) == (0, H) and tuple(g["d_logits"].shape) == (0, E)
+    for name in ("d_gate_up", "d_down", "d_w_router"):
+        assert not f64(g[name]).any(), name
+
+
 def _sampled_forward_check(cfg_name, n_tokens=192, fused="rows"):
     moe = lib()
     cfg = synth.CONFIGS[cfg_name]

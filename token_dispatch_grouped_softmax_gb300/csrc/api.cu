@@ -355,8 +355,8 @@ int moe_gather_dx(const uint16_t* dx_perm, const int32_t* row_map, const float* 
   if (T < 0 || H < 1 || E < 1 || k < 1 || k > E || T > kMaxI32 || T * k > kMaxI32)
     return MOE_ERR_INVALID_ARG;
   if (k > 32 || H % 8 != 0) return MOE_ERR_UNSUPPORTED;
+  if (T == 0) return MOE_OK;   // no rows: the optional router term's pointers may be NULL too
   if ((d_logits == nullptr) != (w_router == nullptr)) return MOE_ERR_INVALID_ARG;
-  if (T == 0) return MOE_OK;
   if (!dx_perm || !row_map || !dx || (d_logits && !ids)) return MOE_ERR_INVALID_ARG;
   if (!aligned16(dx_perm) || !aligned16(dx)) return MOE_ERR_INVALID_ARG;
   if (d_logits && (!workspace || !aligned16(workspace) ||

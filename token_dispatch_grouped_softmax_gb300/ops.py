@@ -196,7 +196,9 @@ def unpermute_combine_bwd(dy, src_row):
     _need(src_row, "src_row", torch.int32, 1)
     T, H = dy.shape
     R = src_row.shape[0]
-    k = R // max(T, 1)
+    if (T == 0) != (R == 0) or (T > 0 and R % T):
+        raise ValueError("src_row must hold T*k rows for dy [T, H]")
+    k = R // T if T > 0 else 1   # an empty batch: any k >= 1 describes it
     dy_perm = torch.empty((R, H), dtype=_BF16, device=dy.device)
     call("moe_unpermute_combine_bwd", _p(dy), _p(src_row), T, H, k, _p(dy_perm), _stream())
     return dy_perm
