@@ -29,6 +29,10 @@ def _need(t, name, dtype, ndim=None):
         raise TypeError("%s must be a torch.Tensor" % name)
     if not t.is_cuda:
         raise ValueError("%s must be a CUDA tensor (the path runs only on the GPU)" % name)
+    if t.device.index != torch.cuda.current_device():
+        # the kernels run on the current device and would be handed another GPU's memory
+        raise ValueError("%s is on %s but the current device is cuda:%d" % (name, t.device,
+                                                                           torch.cuda.current_device()))
     if t.dtype != dtype:
         raise TypeError("%s must be %s, got %s" % (name, dtype, t.dtype))
     if not t.is_contiguous():
