@@ -369,13 +369,15 @@ TILE_EDGE_COUNTS = [0, 1, 15, 16, 17, 63, 64, 65, 80, 127, 128, 129, 200, 255, 2
 HEAVY_COUNTS = [513, 1000, 0, 700, 1024, 2047]
 
 
+@pytest.mark.parametrize("pairs", [False, True], ids=["single", "pairs"])
 @pytest.mark.parametrize("counts", [TILE_EDGE_COUNTS, HEAVY_COUNTS], ids=["edges", "heavy"])
 @pytest.mark.parametrize("H,I", [(256, 192), (320, 128)])
-def test_grouped_gemms_at_tile_edges(H, I, counts):
+def test_grouped_gemms_at_tile_edges(H, I, counts, pairs):
     """The forward grouped GEMMs on explicit expert offsets whose sizes sit on
     either side of every tile boundary (I = 192: a partial gate/up column
     tile; H = 320: a partial down output tile), element by element against
-    the oracle (identity permutation, k = 1)."""
+    the oracle (identity permutation, k = 1); on single CTAs and on CTA pairs
+    (256-row tiles, tails of up to 128 rows as M = 128 pair MMAs)."""
     moe = lib()
     E, R = len(counts), sum(counts)
     offs = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
@@ -386,8 +388,12 @@ def test_grouped_gemms_at_tile_edges(H, I, counts):
     perm = dict(counts=np.array(counts, dtype=np.int32), offsets=offs, row_map=ident,
                 src_row=ident)
     _, ref = oracle.forward_permuted(x, gu, dn, np.ones((R, 1)), perm, 1, want_intermediates=True)
-    h, _, _ = moe.grouped_gemm_gate_up_swiglu(bf(x), None, i32(offs), bf(gu), I)
-    y = moe.grouped_gemm_down(h, i32(offs), bf(dn), H)
-    moe.sync_status()
+    moe.set_gemm_pairs(pairs)
+    try:
+        h, _, _ = moe.grouped_gemm_gate_up_swiglu(bf(x), None, i32(offs), bf(gu), I)
+        y = moe.grouped_gemm_down(h, i32(offs), bf(dn), H)
+        moe.sync_status()
+    finally:
+        moe.set_gemm_pairs(False)
     assert_close("h", f64(h), ref["h_perm"])
     assert_close("y_perm", f64(y), ref["y_perm"])
