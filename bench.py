@@ -521,8 +521,10 @@ def run_reference(args):
 
     cfg = synth.CONFIGS[args.workload]
     K, W = args.steps, max(args.warmup, 0)
-    # bounded: each step a sample sized so that the whole run ends within minutes
-    per_step_s = max(1.0, 60.0 / max(K + W, 1))
+    # bounded: each step a sample sized so that the whole run takes a few
+    # minutes (at least 0.5 s a step: enough tokens per core that the
+    # oracle's per-token rate holds; smaller samples leave cores idle)
+    per_step_s = max(0.5, 120.0 / max(K + W, 1))
     base = cpu_baseline(cfg, target_s=per_step_s)
     n = int(base["sample"].split()[1])
     import numpy as np
