@@ -77,13 +77,17 @@ int moe_sync_status(void* stream, uint32_t* detail);
  * default.  Not thread-safe against concurrent launches. */
 int moe_set_wait_limit_ns(uint64_t ns);
 
-/* Where the forward and dgrad grouped GEMMs run: 0 (default) on single CTAs
- * (128- or 256-row tiles), 1 on CTA pairs (clusters of two CTAs issuing 2-SM
- * tcgen05 MMAs on 256-row tiles, 128-row tails as M = 128 pair MMAs; each
- * CTA holds half of every operand tile).  Results are bit-identical either
- * way; on GB300 at the Qwen3-MoE shapes the two measure within 3%.  Applies
- * to launches after the call; not thread-safe against them. */
-int moe_set_gemm_pairs(int on);
+/* Where the forward and dgrad grouped GEMMs run: on single CTAs (128- or
+ * 256-row tiles) or on CTA pairs (clusters of two CTAs issuing 2-SM tcgen05
+ * MMAs on 256-row tiles, 128-row tails as M = 128 pair MMAs; each CTA holds
+ * half of every operand tile).  mode 0: single CTAs everywhere; 1: pairs for
+ * every forward and dgrad grouped GEMM; 2 (default): pairs for the forward
+ * gate_up GEMM only.  Results are bit-identical in every mode.  Mode 2 is
+ * the fastest measured on GB300 at the Qwen3-MoE shape (the pairs' tile count
+ * fills whole waves there; the down GEMM measured 3 us slower on pairs).
+ * Another mode returns MOE_ERR_INVALID_ARG.  Applies to launches after the
+ * call; not thread-safe against them. */
+int moe_set_gemm_pairs(int mode);
 
 /* Programmatic dependent launch: 1 (default) launches every kernel so that it
  * may start while the kernel before it on the same stream finishes (its

@@ -44,6 +44,17 @@ def test_library_exports_every_declared_symbol(lib):
         assert hasattr(lib, n), "libmoe_gb300.so does not export %s" % n
 
 
+def test_gemm_pairs_modes(lib):
+    """0 single CTAs, 1 pairs everywhere, 2 (default) pairs for gate_up only."""
+    try:
+        for mode in (0, 1, 2):
+            assert lib.moe_set_gemm_pairs(mode) == 0
+        assert lib.moe_set_gemm_pairs(3) == INVALID
+        assert lib.moe_set_gemm_pairs(-1) == INVALID
+    finally:
+        lib.moe_set_gemm_pairs(2)
+
+
 def test_version_and_error_strings(lib):
     assert lib.moe_version() == 10000
     assert lib.moe_error_string(0) == b"ok"

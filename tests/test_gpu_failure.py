@@ -17,8 +17,12 @@ from parity import assert_close
 pytestmark = pytest.mark.gpu
 
 
-def test_gemm_wait_runs_out_and_context_survives():
+@pytest.mark.parametrize("pairs", [0, 2], ids=["single", "pairs"])
+def test_gemm_wait_runs_out_and_context_survives(pairs):
+    """On single CTAs and on CTA pairs (both CTAs of a pair run their own
+    bounded waits and meet at the final cluster barrier)."""
     moe = lib()
+    moe.set_gemm_pairs(pairs)
     L = moe.load()
     T, H, I = 256, 128, 64
     x = synth.normal_bf16(31, synth.TID_X, (T, H), 1.0)
@@ -36,9 +40,12 @@ def test_gemm_wait_runs_out_and_context_survives():
         moe.set_wait_limit_ns(0)
     moe.sync_status()                 # the status word was cleared
     dn = synth.normal_bf16(31, synth.TID_SH_DOWN, (I, H), I ** -0.5)
-    h, _, _ = moe.grouped_gemm_gate_up_swiglu(bf(x), None, None, bf(gu), I)
-    y = moe.grouped_gemm_down(h, None, bf(dn), H)
-    moe.sync_status()
+    try:
+        h, _, _ = moe.grouped_gemm_gate_up_swiglu(bf(x), None, None, bf(gu), I)
+        y = moe.grouped_gemm_down(h, None, bf(dn), H)
+        moe.sync_status()
+    finally:
+        moe.set_gemm_pairs(moe.GEMM_PAIRS_GATE_UP)
     assert_close("dense FFN after the timeout", f64(y), oracle.dense_ffn(x, gu, dn))
 
 

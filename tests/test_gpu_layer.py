@@ -309,7 +309,7 @@ def test_cta_pairs_bit_identical(T, H, E, k, I, fused):
             g = moe.moe_backward(bf(inp.dy), st, wr, gu, dn)
             moe.sync_status()
         finally:
-            moe.set_gemm_pairs(False)
+            moe.set_gemm_pairs(moe.GEMM_PAIRS_GATE_UP)
         outs.append([y, st.h, st.gu_pre, st.h_w, st.y_perm] + [g[n] for n in sorted(g)])
     for a, b in zip(*outs):
         assert torch_equal(a, b)
@@ -394,6 +394,6 @@ def test_grouped_gemms_at_tile_edges(H, I, counts, pairs):
         y = moe.grouped_gemm_down(h, i32(offs), bf(dn), H)
         moe.sync_status()
     finally:
-        moe.set_gemm_pairs(False)
+        moe.set_gemm_pairs(moe.GEMM_PAIRS_GATE_UP)
     assert_close("h", f64(h), ref["h_perm"])
     assert_close("y_perm", f64(y), ref["y_perm"])

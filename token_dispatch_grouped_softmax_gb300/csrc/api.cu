@@ -19,7 +19,7 @@ DeviceInfo g_dev[kMaxDevices];
 bool g_dev_ready[kMaxDevices] = {false};
 uint64_t g_wait_limit_ns = 2000000000ull;
 int g_test_stall_producer = 0;
-int g_gemm_pairs = 0;
+int g_gemm_pairs = 2;   // CTA pairs for the forward gate_up GEMM only
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
@@ -109,8 +109,9 @@ int moe_set_wait_limit_ns(uint64_t ns) {
   return MOE_OK;
 }
 
-int moe_set_gemm_pairs(int on) {
-  moe::g_gemm_pairs = on ? 1 : 0;
+int moe_set_gemm_pairs(int mode) {
+  if (mode < 0 || mode > 2) return MOE_ERR_INVALID_ARG;
+  moe::g_gemm_pairs = mode;
   return MOE_OK;
 }
 

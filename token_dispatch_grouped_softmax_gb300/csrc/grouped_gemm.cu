@@ -1013,8 +1013,9 @@ int64_t mgrouped_tile_bound(int64_t R, int64_t E, int nt) {
 }
 
 // CTA pairs (2-SM MMAs, 256-row tiles with 128-row tails) for the M-grouped
-// GEMMs when selected (moe_set_gemm_pairs).
-bool use_pair(const DeviceInfo& dev) { return dev.gemm_pairs != 0; }
+// GEMMs as selected by moe_set_gemm_pairs: mode 1 for all of them, mode 2
+// (the default) for the forward gate_up GEMM only.
+bool use_pair(const DeviceInfo& dev, bool gate_up) { return dev.gemm_pairs == 1 || (gate_up && dev.gemm_pairs == 2); }
 
 // Single-CTA M-grouped GEMMs with a plain bf16 epilogue take 256-row tiles
 // once experts average 512 rows or more, else 128-row tiles: with few row
@@ -1084,7 +1085,7 @@ int launch_gemm_gate_up(const uint16_t* x, const int32_t* src_row, const int32_t
   p.nt = (int)((I + 127) / 128);
   p.ldo = I;
   const cudaError_t err =
-      use_pair(dev) ? run_gemm<FWD_GATEUP, 1, 2>(p, mgrouped_tile_bound<FWD_GATEUP, 1, 2>(R, E, p.nt), dev, stream)
+      use_pair(dev, true) ? run_gemm<FWD_GATEUP, 1, 2>(p, mgrouped_tile_bound<FWD_GATEUP, 1, 2>(R, E, p.nt), dev, stream)
                      : run_gemm<FWD_GATEUP, 1, 1>(p, mgrouped_tile_bound<FWD_GATEUP, 1, 1>(R, E, p.nt), dev, stream);
   return err == cudaSuccess ? 0 : 1;
 }
@@ -1102,7 +1103,7 @@ int launch_gemm_down(const uint16_t* h, const int32_t* offsets, const uint16_t* 
   p.nt = (int)((H + BN - 1) / BN);
   p.ldo = H;
   const cudaError_t err =
-      use_pair(dev) ? run_gemm<FWD_DOWN, 1, 2>(p, mgrouped_tile_bound<FWD_DOWN, 1, 2>(R, E, p.nt), dev, stream)
+      use_pair(dev, false) ? run_gemm<FWD_DOWN, 1, 2>(p, mgrouped_tile_bound<FWD_DOWN, 1, 2>(R, E, p.nt), dev, stream)
                      : run_bf16_mgrouped<FWD_DOWN>(p, R, E, dev, stream);
   return err == cudaSuccess ? 0 : 1;
 }
@@ -1116,7 +1117,7 @@ int launch_gemm_down_bwd(const uint16_t* dy_perm, const uint16_t* h_w, const flo
   if (R > 0) {  // dgu = SwiGLU'(w * (dy_perm . Wd_e^T), gu_pre)
     GemmParams p;
     fill_common(p, offsets, R, E, I, dev);
-    const bool pair = use_pair(dev);   // a pair's CTA loads 128 of the tile's 256 B rows
+    const bool pair = use_pair(dev, false);   // a pair's CTA loads 128 of the tile's 256 B rows
     if (!make_map(&p.tmA, dy_perm, R, H, 64, BMH) || !make_map(&p.tmB, down, E * I, H, 64, pair ? 128 : 256))
       return -1;
     p.aux = gu_pre;
@@ -1156,7 +1157,7 @@ int launch_gemm_gate_up_bwd(const uint16_t* dgu, const uint16_t* x, const int32_
   if (R > 0) {  // dx_perm = dgu . Wgu_e^T
     GemmParams p;
     fill_common(p, offsets, R, E, I, dev);
-    const bool pair = use_pair(dev);
+    const bool pair = use_pair(dev, false);
     if (!make_map(&p.tmA, dgu, R, 2 * I, 64, BMH) ||
         !make_map(&p.tmB, gate_up, E * H, 2 * I, 64, pair ? 128 : 256))
       return -1;

@@ -57,10 +57,15 @@ def set_wait_limit_ns(ns: int):
     call("moe_set_wait_limit_ns", int(ns))
 
 
-def set_gemm_pairs(on: bool):
-    """Forward and dgrad grouped GEMMs on CTA pairs (2-SM MMAs) or single CTAs
-    (default); the results are bit-identical."""
-    call("moe_set_gemm_pairs", 1 if on else 0)
+GEMM_PAIRS_NONE, GEMM_PAIRS_ALL, GEMM_PAIRS_GATE_UP = 0, 1, 2
+
+
+def set_gemm_pairs(mode):
+    """Where the forward and dgrad grouped GEMMs run: False / GEMM_PAIRS_NONE
+    on single CTAs, True / GEMM_PAIRS_ALL all on CTA pairs (2-SM MMAs),
+    GEMM_PAIRS_GATE_UP (the default) the forward gate_up GEMM on pairs.  The
+    results are bit-identical."""
+    call("moe_set_gemm_pairs", int(mode))
 
 
 _pdl_on = [True]
