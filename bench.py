@@ -180,10 +180,11 @@ class ClockSampler:
 
 # ------------------------------------------------------------ native arm
 
-def traffic_for(kernel_src):
+def traffic_for(*kernel_srcs):
     """dram bytes (read + write) per launch of the dominant kernel from the
-    committed ncu summary, or None when the kernel source changed since it was
-    captured (the summary records the sha256 of the source it profiled)."""
+    committed ncu summary, or None when the kernel's sources changed since it
+    was captured (the summary records the sha256 of those sources, read in
+    order and concatenated)."""
     path = os.path.join(ROOT, "profiles", "grouped_gemm_qwen3_moe.md")
     if not os.path.exists(path):
         return None
@@ -193,7 +194,7 @@ def traffic_for(kernel_src):
             if ":" in line and line.split(":")[0] in ("source_sha256", "dram_bytes_per_launch"):
                 k, v = line.split(":", 1)
                 fields[k.strip()] = v.strip()
-    h = hashlib.sha256(open(kernel_src, "rb").read()).hexdigest()
+    h = hashlib.sha256(b"".join(open(f, "rb").read() for f in kernel_srcs)).hexdigest()
     if fields.get("source_sha256") != h or "dram_bytes_per_launch" not in fields:
         return None
     return int(fields["dram_bytes_per_launch"])
@@ -356,7 +357,8 @@ def run_native(args):
     peak_tf = pk["bf16_tflops"]
     dur_s = per_kernel["gate_up"] * 1e-3
     t_hbm, t_tc = b_gate_up / (pk["hbm_gbs"] * 1e9), f_gate_up / (peak_tf * 1e12)
-    src = os.path.join(ROOT, "token_dispatch_grouped_softmax_gb300", "csrc", "grouped_gemm.cu")
+    csrc = os.path.join(ROOT, "token_dispatch_grouped_softmax_gb300", "csrc")
+    srcs = [os.path.join(csrc, "grouped_gemm.cu"), os.path.join(csrc, "common.cuh")]
     tensor_part = {"achieved": round(f_gate_up / dur_s / 1e12, 1), "peak": peak_tf, "unit": "TFLOP/s",
                    "frac": round(f_gate_up / dur_s / 1e12 / peak_tf, 4),
                    "algorithmic_flops_per_launch": f_gate_up,
@@ -368,7 +370,7 @@ def run_native(args):
     main, other = (hbm_part, tensor_part) if t_hbm >= t_tc else (tensor_part, hbm_part)
     roofline = dict({"bound": "hbm" if t_hbm >= t_tc else "tensor",
                      "kernel": "grouped_gemm_kernel<FWD_GATEUP>"}, **main)
-    roofline["traffic"] = traffic_for(src)
+    roofline["traffic"] = traffic_for(*srcs)
     roofline["floors_us"] = {"hbm": round(t_hbm * 1e6, 1), "tensor": round(t_tc * 1e6, 1)}
     roofline["other_bound"] = dict({"bound": "tensor" if t_hbm >= t_tc else "hbm"}, **other)
     roofline["experts_used"] = used
