@@ -79,8 +79,8 @@ __global__ void __launch_bounds__(256) combine_kernel(const uint16_t* __restrict
       const float wj = __shfl_sync(0xffffffffu, my_w, j);
       const uint4* src = reinterpret_cast<const uint4*>(y_perm + (int64_t)row * H);
       uint4 v0 = make_uint4(0, 0, 0, 0), v1 = make_uint4(0, 0, 0, 0);
-      if (act0) v0 = __ldg(src + c0);
-      if (act1) v1 = __ldg(src + c1);
+      if (act0) v0 = ld_stream16(src + c0);
+      if (act1) v1 = ld_stream16(src + c1);
       float f[8];
       unpack8(v0, f);
 #pragma unroll
@@ -216,8 +216,8 @@ __global__ void __launch_bounds__(256) gather_dx_kernel(const uint16_t* __restri
       const int row = __shfl_sync(0xffffffffu, my_row, j);
       const uint4* src = reinterpret_cast<const uint4*>(dx_perm + (int64_t)row * H);
       uint4 v0 = make_uint4(0, 0, 0, 0), v1 = make_uint4(0, 0, 0, 0);
-      if (act0) v0 = __ldg(src + c0);
-      if (act1) v1 = __ldg(src + c1);
+      if (act0) v0 = ld_stream16(src + c0);
+      if (act1) v1 = ld_stream16(src + c1);
       float f[8];
       unpack8(v0, f);
 #pragma unroll
