@@ -66,6 +66,8 @@ def parse():
     ap.add_argument("--no-fwd-bwd", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-deepseek", action="store_true",
+                    help="skip the DeepSeek-V3-shaped forward leg (reported under deepseek_v3)")
     ap.add_argument("--train-only", action="store_true",
                     help="time only the training step (forward + backward) for --steps steps")
     ap.add_argument("--gather", default="rows", choices=["fused", "rows"],
@@ -181,19 +183,16 @@ class ClockSampler:
 # ------------------------------------------------------------ native arm
 
 def traffic_for(*kernel_srcs):
-    """dram bytes (read + write) per launch of the dominant kernel from the
-    committed ncu summary, or None when the kernel's sources changed since it
-    was captured (the summary records the sha256 of those sources, read in
-    order and concatenated)."""
-    path = os.path.join(ROOT, "profiles", "grouped_gemm_qwen3_moe.md")
+    """dram bytes (read + write) per launch of the dominant kernel, from the
+    ncu capture summarised in profiles/grouped_gemm_qwen3_moe.md, whose two
+    machine-read figures sit beside it in profiles/grouped_gemm_qwen3_moe.json;
+    None when the kernel's sources changed since the capture (the JSON holds
+    the sha256 of those sources, read in order and concatenated)."""
+    path = os.path.join(ROOT, "profiles", "grouped_gemm_qwen3_moe.json")
     if not os.path.exists(path):
         return None
-    fields = {}
     with open(path) as f:
-        for line in f:
-            if ":" in line and line.split(":")[0] in ("source_sha256", "dram_bytes_per_launch"):
-                k, v = line.split(":", 1)
-                fields[k.strip()] = v.strip()
+        fields = json.load(f)
     h = hashlib.sha256(b"".join(open(f, "rb").read() for f in kernel_srcs)).hexdigest()
     if fields.get("source_sha256") != h or "dram_bytes_per_launch" not in fields:
         return None
@@ -220,35 +219,12 @@ def device_inputs(cfg, torch, device):
     return d
 
 
-def run_native(args):
-    import torch
-
-    import synth
-    import token_dispatch_grouped_softmax_gb300 as moe
-
-    ws, rank, local = dist_env()
-    torch.cuda.set_device(local)
-    device = torch.device("cuda", local)
-    dist = init_dist("nccl")
-    moe.build()
-    moe.load()
-    cfg = synth.CONFIGS[args.workload]
-    pk, pk_kind = peaks()
-    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=device)
-    if args.train_only:
-        res = fwd_bwd(moe, torch, torch.cuda.current_stream(), dist, device, ws, flush, pk,
-                      args.gather != "rows", K=args.steps, W=max(args.warmup, 3))
-        if rank == 0:
-            print(json.dumps({"metric": METRIC, "fwd_bwd": res}), flush=True)
-        if dist is not None:
-            dist.destroy_process_group()
-        return
-    d = device_inputs(cfg, torch, device)
-    stream = torch.cuda.current_stream()
+def make_step(moe, d, cfg, stream, fused):
+    """One forward step of the layer through the public API, with an optional
+    list of CUDA events recorded between its kernels (names: what lies
+    between consecutive events)."""
     T, H, E, k, I = cfg.T, cfg.H, cfg.E, cfg.k, cfg.I
     I_s = cfg.I_shared
-
-    fused = args.gather == "fused"
     names = ["route", "permute"] + ([] if fused else ["permute_rows"]) + ["gate_up", "down"] + \
         (["shared"] if I_s else []) + ["combine"]
 
@@ -281,6 +257,40 @@ def run_native(args):
         y = moe.unpermute_combine(y_perm, row_map, w, y_sh)
         mark()
         return y
+
+    return names, step
+
+
+def run_native(args):
+    import torch
+
+    import synth
+    import token_dispatch_grouped_softmax_gb300 as moe
+
+    ws, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    dist = init_dist("nccl")
+    moe.build()
+    moe.load()
+    cfg = synth.CONFIGS[args.workload]
+    pk, pk_kind = peaks()
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=device)
+    if args.train_only:
+        res = fwd_bwd(moe, torch, torch.cuda.current_stream(), dist, device, ws, flush, pk,
+                      args.gather != "rows", K=args.steps, W=max(args.warmup, 3))
+        if rank == 0:
+            print(json.dumps({"metric": METRIC, "fwd_bwd": res}), flush=True)
+        if dist is not None:
+            dist.destroy_process_group()
+        return
+    d = device_inputs(cfg, torch, device)
+    stream = torch.cuda.current_stream()
+    T, H, E, k, I = cfg.T, cfg.H, cfg.E, cfg.k, cfg.I
+    I_s = cfg.I_shared
+
+    fused = args.gather == "fused"
+    names, step = make_step(moe, d, cfg, stream, fused)
 
     # route (weight split + fused router, or split + router GEMM + top-k),
     # permute (one cooperative kernel, or three), row gather, gate_up, down,
@@ -412,6 +422,10 @@ def run_native(args):
         del d
         torch.cuda.empty_cache()
         out["fwd_bwd"] = fwd_bwd(moe, torch, stream, dist, device, ws, flush, pk, fused)
+    if not args.no_deepseek and args.workload != "deepseek_v3":
+        torch.cuda.empty_cache()
+        out["deepseek_v3"] = large_forward(moe, torch, stream, dist, device, ws, flush, pk, fused,
+                                           "deepseek_v3")
     if rank == 0 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(cfg, target_s=15.0)
     if rank == 0:
@@ -483,6 +497,74 @@ def fwd_bwd(moe, torch, stream, dist, device, ws, flush, pk, fused, K=30, W=3):
             "layer_tflops": round(flops * K / s / 1e12, 1), "steps": K,
             "launches_per_step": route_launches(cfg.H, cfg.E) + permute_launches(cfg.T * cfg.k, torch, device) + 3 +
                                  (0 if fused else 1) + 1 + 1 + 2 + 2 + 2}
+
+
+def large_forward(moe, torch, stream, dist, device, ws, flush, pk, fused, name, K=10, K_eager=3, W=3):
+    """The forward of a second, larger workload (the DeepSeek-V3 shape: 256
+    experts, I = 2048, a shared expert; ~512 rows per expert, so its GEMMs are
+    bound by the tensor cores): K graph-replayed steps for tokens/s, and
+    K_eager eager steps with an event between kernels for each GEMM's
+    TFLOP/s and the combine's GB/s.  L2 flushed before every step."""
+    import synth
+
+    cfg = synth.CONFIGS[name]
+    d = device_inputs(cfg, torch, device)
+    names, step = make_step(moe, d, cfg, stream, fused)
+    for _ in range(W):
+        step()
+    moe.sync_status()
+    torch.cuda.synchronize()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)] for _ in range(K_eager)]
+    barrier(dist)
+    for i in range(K_eager):
+        flush.zero_()
+        torch.cuda._sleep(SPACER_CYCLES)
+        step(evs[i])
+    torch.cuda.synchronize()
+    per = {n: sum(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(K_eager)) / K_eager
+           for j, n in enumerate(names)}
+    graph = moe.ForwardGraph(cfg.T, d["w_router"], d["gate_up"], d["down"], cfg.k, d["bias"], d["sh_gate_up"],
+                             d["sh_down"], fused_gather=fused)
+    graph.x.copy_(d["x"])
+    for _ in range(W):
+        graph.replay()
+    torch.cuda.synchronize()
+    barrier(dist)
+    gevs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
+    for i in range(K):
+        flush.zero_()
+        gevs[i][0].record(stream)
+        graph.replay()
+        gevs[i][1].record(stream)
+    torch.cuda.synchronize()
+    barrier(dist)
+    moe.sync_status()
+    s = max_over_ranks(dist, sum(a.elapsed_time(b) for a, b in gevs) / 1e3, device)
+    del graph
+    T, H, I, R, I_s = cfg.T, cfg.H, cfg.I, cfg.R, cfg.I_shared
+    peak = pk["bf16_tflops"]
+    flops = {"gate_up": 2.0 * R * H * 2 * I, "down": 2.0 * R * I * H,
+             "shared": 2.0 * T * H * 2 * I_s + 2.0 * T * I_s * H}
+
+    def tf(n):
+        return round(flops[n] / (per[n] * 1e-3) / 1e12, 1)
+    gemm_ms = sum(per[n] for n in flops if n in per)
+    comb_bytes = R * H * 2 + T * H * 2 + R * 8 + (T * H * 2 if I_s else 0)
+    del d
+    torch.cuda.empty_cache()
+    return {"workload": cfg.name, "T": T, "H": H, "E": cfg.E, "k": cfg.k, "I": I, "I_shared": I_s,
+            "value": round(ws * T * K / s, 1), "unit": "tokens/s", "ms_per_step": round(1e3 * s / K, 4),
+            "steps": K, "timing": "value: one CUDA graph replay per step; kernels: eager launches with "
+                                  "events between kernels, %d steps" % K_eager,
+            "kernels_us": {n: round(v * 1e3, 2) for n, v in per.items()},
+            "gemm": {n: {"tflops": tf(n), "frac_of_peak": round(tf(n) / peak, 4)} for n in flops if n in per},
+            "gemm_all": {"tflops": round(sum(flops.values()) / (gemm_ms * 1e-3) / 1e12, 1),
+                         "frac_of_peak": round(sum(flops.values()) / (gemm_ms * 1e-3) / 1e12 / peak, 4)},
+            "combine": {"gbs": round(comb_bytes / (per["combine"] * 1e-3) / 1e9, 1),
+                        "frac_of_hbm": round(comb_bytes / (per["combine"] * 1e-3) / 1e9 / pk["hbm_gbs"], 4)},
+            "peak_tflops": peak,
+            "gpu_launches": K * (route_launches(H, cfg.E) + permute_launches(R, torch, device) +
+                                 (0 if fused else 1) + 2 + (2 if I_s else 0) + 1)}
 
 
 # -------------------------------------------------------------- CPU oracle

@@ -37,6 +37,13 @@
  *     optional ones, so an empty tensor's NULL data pointer is accepted.
  *   - Alignment: every base pointer must be 16-byte aligned; H and I must be
  *     multiples of 64 for the grouped GEMMs and of 8 elsewhere.
+ *   - Per-device state: on its first call on a device the library looks up
+ *     and keeps, for that device ordinal, the device addresses of its own
+ *     __device__ arrays (the status word, moe_permute_noalloc's scratch) and
+ *     the kernels' launch attributes.  They belong to the device's primary
+ *     context.  A process that destroys that context (cudaDeviceReset) must
+ *     not call the library on that device again: the kept addresses would
+ *     then point into a context that no longer exists.
  */
 #ifndef MOE_GB300_H
 #define MOE_GB300_H

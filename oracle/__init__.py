@@ -129,6 +129,26 @@ def route(x, w_r, bias, k):
     return out
 
 
+def weights_for_ids(logits, ids):
+    """Renormalised gate weights of a given expert choice, from fp64 logits.
+
+    The router's last step ("InternVL3.5 接入 pure FSDP2 后端开发实践" §8.2:
+    gate -> FP32 softmax -> top-k -> 权重归一化): w_j = p_{e_j} / sum_i p_{e_i}
+    with p = softmax(logits).  The softmax denominator cancels, so this is the
+    softmax over the chosen logits alone; it is evaluated that way (shifted by
+    their maximum).  Used where the experts chosen for a token are given (for
+    instance by the device's fp32 router at an fp32-vs-fp64 near tie), so
+    that everything downstream of the choice can be checked for that choice.
+
+    logits [T, E] float64, ids [T, k] int -> w [T, k] float64.
+    """
+    logits = np.asarray(logits, dtype=np.float64)
+    ids = np.asarray(ids, dtype=np.int64)
+    z = np.take_along_axis(logits, ids, axis=1)
+    e = np.exp(z - z.max(axis=1, keepdims=True))
+    return e / e.sum(axis=1, keepdims=True)
+
+
 # -------------------------------------------------------------------- permute
 
 def permute(ids, E):

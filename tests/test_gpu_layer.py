@@ -15,7 +15,7 @@ import pytest
 import oracle
 import synth
 from gpu_helpers import bf, f32, f64, i32, lib, npi
-from parity import assert_close, compare_ids, sample_tokens
+from parity import TIE_TAU, assert_close, compare_ids, sample_tokens
 
 pytestmark = pytest.mark.gpu
 
@@ -190,42 +190,66 @@ def test_empty_batch_forward_backward():
         assert not f64(g[name]).any(), name
 
 
-def _sampled_forward_check(cfg_name, n_tokens=192, fused="rows"):
+def _permutation_of_gpu_ids(st, E):
+    """The permutation is a pure integer function of the routing ids:
+    counts, offsets, row_map and src_row must equal, bit for bit, the
+    oracle's permutation of the ids the GPU chose, whatever near ties the
+    GPU's fp32 router took either way."""
+    gids = npi(st.ids)
+    perm = oracle.permute(gids, E)
+    for key in ("counts", "offsets", "row_map", "src_row"):
+        np.testing.assert_array_equal(npi(getattr(st, key)), perm[key], err_msg=key)
+    return gids, perm
+
+
+def _sampled_forward_check(cfg_name, n_tokens=None, fused="rows", max_tied=None):
+    """The named workload at full size: routing ids against the oracle's (near
+    ties counted), the permutation bit-exact against the oracle's permutation
+    of the GPU's ids, the gate weights against the oracle's weights for the
+    GPU's choice, and y on n_tokens seeded tokens (None: every token) against
+    the oracle computed for that choice."""
     moe = lib()
     cfg = synth.CONFIGS[cfg_name]
     inp = synth.make_inputs(cfg)
     _, y, st = _forward(moe, inp, fused=fused)
     r = oracle.route(inp.x, inp.w_router, inp.bias, cfg.k)
-    same, tol = compare_ids(npi(st.ids), r)
-    assert tol <= max(4, cfg.T // 2000)   # every one of them checked to be a near tie
-    if same.all():
-        perm = oracle.permute(r["ids"], cfg.E)
-        for key in ("counts", "offsets", "row_map", "src_row"):
-            np.testing.assert_array_equal(npi(getattr(st, key)), perm[key], err_msg=key)
-    tok = sample_tokens(cfg.T, n_tokens, cfg.seed)
-    tok = tok[same[tok]]
-    yref = oracle.forward_tokens(tok, inp.x, inp.gate_up, inp.down, r["ids"], r["w"], inp.sh_gate_up,
+    same, tol = compare_ids(npi(st.ids), r, label=cfg_name)
+    assert tol <= (max(4, cfg.T // 2000) if max_tied is None else max_tied)
+    gids, _ = _permutation_of_gpu_ids(st, cfg.E)
+    w_ref = oracle.weights_for_ids(r["logits"], gids)
+    assert_close("w (%s)" % cfg_name, f64(st.w), w_ref, bf16_out=False)
+    tok = np.arange(cfg.T) if n_tokens is None else sample_tokens(cfg.T, n_tokens, cfg.seed)
+    yref = oracle.forward_tokens(tok, inp.x, inp.gate_up, inp.down, gids, w_ref, inp.sh_gate_up,
                                  inp.sh_down)
-    assert_close("y[sample]", f64(y)[tok], yref)
+    assert_close("y (%s)" % cfg_name, f64(y)[tok], yref)
     return st
 
 
 @pytest.mark.parametrize("fused", ["rows", "tma"])
-def test_qwen3_moe_forward_sampled(fused):
+def test_qwen3_moe_forward_full(fused):
+    """Every token of the Qwen3-MoE-shaped workload."""
     _sampled_forward_check("qwen3_moe", fused=fused)
 
 
-def test_skewed_routing_forward_sampled():
+def test_skewed_routing_forward_full():
+    """Every token of the skewed workload (hotspot and empty experts)."""
     st = _sampled_forward_check("qwen3_moe_skewed")
     counts = npi(st.counts)
     assert (counts == 0).sum() >= 8
 
 
 def test_deepseek_v3_forward_sampled():
-    _sampled_forward_check("deepseek_v3", n_tokens=96)
+    """1,024 seeded tokens of the DeepSeek-V3-shaped workload (with its
+    shared expert); the permutation in full."""
+    _sampled_forward_check("deepseek_v3", n_tokens=1024)
 
 
 def test_training_step_backward_sampled():
+    """The training workload (T = 8192) forward with saved activations and
+    backward.  dX, d_logits and dw on 1,024 seeded tokens, and the weight
+    gradients of 8 whole experts (the busiest, the least busy and 6 seeded
+    others), all against the oracle evaluated for the experts the GPU chose,
+    so every check runs whatever near ties the fp32 router took."""
     moe = lib()
     cfg = synth.CONFIGS["qwen3_moe_train"]
     inp = synth.make_inputs(cfg)
@@ -233,22 +257,43 @@ def test_training_step_backward_sampled():
     g = moe.moe_backward(bf(inp.dy), st, wr, gu, dn)
     moe.sync_status()
     r = oracle.route(inp.x, inp.w_router, None, cfg.k)
-    same, tol = compare_ids(npi(st.ids), r)
+    same, tol = compare_ids(npi(st.ids), r, label="qwen3_moe_train")
     assert tol <= max(4, cfg.T // 2000)
-    tok = sample_tokens(cfg.T, 96, 33)
-    tok = tok[same[tok]]
-    b = oracle.backward_tokens(tok, inp.x, inp.w_router, inp.gate_up, inp.down, r["ids"], r["w"], inp.dy)
-    assert_close("dX[sample]", f64(g["dx"])[tok], b["dX"])
-    assert_close("d_logits[sample]", f64(g["d_logits"])[tok], b["dlogits"], bf16_out=False)
-    assert_close("dw[sample]", f64(g["dw"])[tok], b["dw"], bf16_out=False)
-    if same.all():
-        H, I = cfg.H, cfg.I
-        dgu = g["d_gate_up"]
-        ddn = g["d_down"]
-        for e in (0, 77, 127):
-            rgu, rdn = oracle.backward_expert(e, inp.x, inp.gate_up, inp.down, r["ids"], r["w"], inp.dy)
-            assert_close("d_gate_up[%d]" % e, f64(dgu[e * H:(e + 1) * H]), rgu)
-            assert_close("d_down[%d]" % e, f64(ddn[e * I:(e + 1) * I]), rdn)
+    gids, perm = _permutation_of_gpu_ids(st, cfg.E)
+    w_ref = oracle.weights_for_ids(r["logits"], gids)
+    tok = sample_tokens(cfg.T, 1024, 33)
+    yref = oracle.forward_tokens(tok, inp.x, inp.gate_up, inp.down, gids, w_ref)
+    assert_close("y (train)", f64(y)[tok], yref)
+    b = oracle.backward_tokens(tok, inp.x, inp.w_router, inp.gate_up, inp.down, gids, w_ref, inp.dy)
+    assert_close("dX (train)", f64(g["dx"])[tok], b["dX"])
+    assert_close("d_logits (train)", f64(g["d_logits"])[tok], b["dlogits"], bf16_out=False)
+    assert_close("dw (train)", f64(g["dw"])[tok], b["dw"], bf16_out=False)
+    H, I = cfg.H, cfg.I
+    counts = perm["counts"]
+    rng = np.random.default_rng(cfg.seed)
+    busiest, idlest = int(np.argmax(counts)), int(np.argmin(counts))
+    others = [e for e in rng.permutation(cfg.E).tolist() if e not in (busiest, idlest)][:6]
+    experts = [busiest, idlest] + others
+    assert len(set(experts)) == 8
+    dgu, ddn = g["d_gate_up"], g["d_down"]
+    for e in experts:
+        rgu, rdn = oracle.backward_expert(e, inp.x, inp.gate_up, inp.down, gids, w_ref, inp.dy)
+        assert_close("d_gate_up[e] (train)", f64(dgu[e * H:(e + 1) * H]), rgu)
+        assert_close("d_down[e] (train)", f64(ddn[e * I:(e + 1) * I]), rdn)
+
+
+def _oracle_y(inp, x_bits):
+    """The oracle's layer output for the tokens x_bits with inp's weights;
+    asserts first that no token sits within the near-tie band of the routing
+    comparison (TIE_TAU, relative), where the fp32 device router must choose
+    as the fp64 oracle does."""
+    k = inp.cfg.k
+    r = oracle.route(x_bits, inp.w_router, inp.bias, k)
+    zk = np.abs(r["logits"][np.arange(x_bits.shape[0]), r["ids"][:, -1]])
+    assert np.all(np.minimum(r["kgap"], r["ordgap"]) > TIE_TAU * np.maximum(1.0, zk))
+    perm = oracle.permute(r["ids"], inp.cfg.E)
+    return oracle.forward_permuted(x_bits, inp.gate_up, inp.down, r["w"], perm, k, inp.sh_gate_up,
+                                   inp.sh_down)
 
 
 def torch_equal(a, b):
@@ -258,25 +303,28 @@ def torch_equal(a, b):
 
 
 def test_pipelined_forward_matches_forward():
-    """PipelinedForward (copies overlapped with the layer on two streams) gives
-    the same outputs as moe_forward, batch by batch."""
+    """PipelinedForward (copies overlapped with the layer on two streams):
+    every batch's output against the oracle, and bit for bit equal to
+    moe_forward's."""
     import torch
     moe = lib()
     cfg, inp = _inputs(256, 256, 8, 2, 128, seed=77)
     wr, gu, dn = f32(inp.w_router), bf(inp.gate_up), bf(inp.down)
-    xs = [torch.from_numpy(synth.normal_bf16(s, synth.TID_X, (256, 256), 1.0).view(np.int16))
-          .view(torch.bfloat16).pin_memory() for s in (1, 2, 3)]
+    xbits = [synth.normal_bf16(s, synth.TID_X, (256, 256), 1.0) for s in (1, 2, 3)]
+    xs = [torch.from_numpy(xb.view(np.int16)).view(torch.bfloat16).pin_memory() for xb in xbits]
     ys = [torch.empty((256, 256), dtype=torch.bfloat16).pin_memory() for _ in xs]
     moe.PipelinedForward(256, wr, gu, dn, cfg.k).run(xs, ys)
     moe.sync_status()
-    for xh, yh in zip(xs, ys):
+    for xb, xh, yh in zip(xbits, xs, ys):
+        assert_close("y (PipelinedForward)", f64(yh), _oracle_y(inp, xb))
         y, _ = moe.moe_forward(xh.cuda(), wr, gu, dn, cfg.k)
         assert torch_equal(y.cpu(), yh)
 
 
 def test_forward_graph_replays_match_forward():
     """ForwardGraph: one capture, replayed on new tokens (new routing each
-    time), gives moe_forward's outputs bit for bit, the shared expert too."""
+    time): each replay's output against the oracle, and bit for bit equal to
+    moe_forward's, the shared expert included."""
     import torch
     moe = lib()
     cfg, inp = _inputs(300, 256, 8, 2, 128, seed=91, I_shared=64)
@@ -284,9 +332,11 @@ def test_forward_graph_replays_match_forward():
     sgu, sdn = bf(inp.sh_gate_up), bf(inp.sh_down)
     g = moe.ForwardGraph(300, wr, gu, dn, cfg.k, None, sgu, sdn)
     for s in (5, 6, 7):
-        x = torch.from_numpy(synth.normal_bf16(s, synth.TID_X, (300, 256), 1.0).view(np.int16)) \
-            .view(torch.bfloat16).cuda()
+        xb = synth.normal_bf16(s, synth.TID_X, (300, 256), 1.0)
+        x = torch.from_numpy(xb.view(np.int16)).view(torch.bfloat16).cuda()
         y_graph = g(x).clone()
+        moe.sync_status()
+        assert_close("y (ForwardGraph)", f64(y_graph), _oracle_y(inp, xb))
         y_eager, _ = moe.moe_forward(x, wr, gu, dn, cfg.k, None, sgu, sdn)
         moe.sync_status()
         assert torch_equal(y_graph, y_eager)
@@ -338,9 +388,10 @@ def test_programmatic_launch_bit_identical(T, H, E, k, I):
 
 def test_overlapped_forward_matches_forward():
     """OverlappedForward (route/permute of batch i+1 overlapping the expert
-    GEMMs of batch i, on two streams) gives moe_forward's outputs bit for
-    bit, with and without a shared expert and with the row gather fused into
-    the gate_up GEMM (both read x inside the expert stage)."""
+    GEMMs of batch i, on two streams): every batch's output against the
+    oracle, and bit for bit equal to moe_forward's, with and without a shared
+    expert and with the row gather fused into the gate_up GEMM (both read x
+    inside the expert stage)."""
     import torch
     moe = lib()
     for I_s, fused in ((0, False), (64, False), (0, True)):
@@ -348,11 +399,13 @@ def test_overlapped_forward_matches_forward():
         wr, gu, dn = f32(inp.w_router), bf(inp.gate_up), bf(inp.down)
         sgu = bf(inp.sh_gate_up) if I_s else None
         sdn = bf(inp.sh_down) if I_s else None
-        xs = [torch.from_numpy(synth.normal_bf16(s, synth.TID_X, (300, 256), 1.0).view(np.int16))
-              .view(torch.bfloat16).pin_memory() for s in (11, 12, 13, 14, 15)]
+        xbits = [synth.normal_bf16(s, synth.TID_X, (300, 256), 1.0) for s in (11, 12, 13, 14, 15)]
+        xs = [torch.from_numpy(xb.view(np.int16)).view(torch.bfloat16).pin_memory() for xb in xbits]
         ys = [torch.empty((300, 256), dtype=torch.bfloat16).pin_memory() for _ in xs]
         moe.OverlappedForward(300, wr, gu, dn, cfg.k, None, sgu, sdn, fused_gather=fused).run(xs, ys)
         moe.sync_status()
+        for xb, yh in zip(xbits, ys):
+            assert_close("y (OverlappedForward)", f64(yh), _oracle_y(inp, xb))
         for xh, yh in zip(xs, ys):
             y, _ = moe.moe_forward(xh.cuda(), wr, gu, dn, cfg.k, None, sgu, sdn)
             assert torch_equal(y.cpu(), yh)

@@ -114,6 +114,22 @@ def test_route_k_equals_E_gives_softmax():
     assert np.all(np.isinf(r["kgap"]))
 
 
+def test_weights_for_ids_matches_router_and_probabilities():
+    """Pin of weights_for_ids (the renormalised weights of a given choice):
+    on the router's own choice it equals the C router's w; on any other
+    choice (a permuted, reordered and arbitrary set) it equals p_e / sum p
+    from the brute-force scipy softmax over all E experts."""
+    inp = _tiny(seed=4, E=16, k=4)
+    r = oracle.route(inp.x, inp.w_router, None, 4)
+    np.testing.assert_allclose(oracle.weights_for_ids(r["logits"], r["ids"]), r["w"], rtol=1e-13)
+    p = scipy.special.softmax(_f64(inp.x) @ inp.w_router.astype(np.float64), axis=1)
+    rng = np.random.default_rng(4)
+    other = np.stack([rng.permutation(16)[:4] for _ in range(p.shape[0])]).astype(np.int32)
+    want = np.take_along_axis(p, other.astype(np.int64), axis=1)
+    want /= want.sum(1, keepdims=True)
+    np.testing.assert_allclose(oracle.weights_for_ids(r["logits"], other), want, rtol=1e-12)
+
+
 # --------------------------------------------------------------- permute pins
 
 def _check_perm(ids, E, perm):

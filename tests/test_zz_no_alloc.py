@@ -6,8 +6,9 @@ enqueue step (which must not allocate), a runtime that has reserved all
 device memory for its own pool, or a latency-critical path that cannot pay
 for cudaMalloc's implicit synchronisation.  Its scratch is a fixed array
 inside the library instead of a caller workspace.  This file checks that two
-calls in a row give exactly what moe_permute gives with its own workspace,
-and that sizes beyond the fixed scratch are refused.  It is kept in a file of
+calls in a row give exactly what moe_permute gives with its own workspace
+and what the fp64 oracle's permutation gives, and that sizes beyond the
+fixed scratch are refused.  It is kept in a file of
 its own that pytest collects last.
 """
 import ctypes
@@ -16,6 +17,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 import synth
 from gpu_helpers import dev, f32, i32, lib, npi
 
@@ -69,12 +71,19 @@ def test_noalloc_matches_permute_on_two_calls_in_a_row():
     L = moe.load()
     cases = []
     for T, k, E, seed in ((4096, 8, 128, 1), (777, 6, 1000, 2)):
-        ids = i32(synth.distinct_ids(seed, synth.TID_IDS, T, k, E))
-        w = f32(np.random.default_rng(seed).uniform(0.0, 1.0, (T, k)))
-        cases.append((ids, w, E, _permute_with_workspace(L, ids, w, E)))
-    got = [_permute_noalloc(L, ids, w, E) for ids, w, E, _ in cases]   # two calls in a row
+        ids_h = synth.distinct_ids(seed, synth.TID_IDS, T, k, E)
+        w_h = np.random.default_rng(seed).uniform(0.0, 1.0, (T, k)).astype(np.float32)
+        ids, w = i32(ids_h), f32(w_h)
+        cases.append((ids_h, w_h, ids, w, E, _permute_with_workspace(L, ids, w, E)))
+    got = [_permute_noalloc(L, ids, w, E) for _, _, ids, w, E, _ in cases]   # two calls in a row
     moe.sync_status()
-    for (ids, w, E, ref), out in zip(cases, got):
+    for (ids_h, w_h, ids, w, E, ref), out in zip(cases, got):
+        perm = oracle.permute(ids_h, E)
+        for key in ("counts", "offsets", "row_map", "src_row"):
+            np.testing.assert_array_equal(npi(out[key]), perm[key], err_msg=key + " vs the oracle")
+        w_perm = np.empty(ids_h.size, dtype=np.float32)
+        w_perm[perm["row_map"]] = w_h.reshape(-1)   # each assignment's weight at its permuted row
+        np.testing.assert_array_equal(npi(out["w_perm"]), w_perm, err_msg="w_perm vs the oracle")
         for key in ("counts", "offsets", "row_map", "src_row", "w_perm"):
             np.testing.assert_array_equal(npi(out[key]), npi(ref[key]), err_msg=key)
 
