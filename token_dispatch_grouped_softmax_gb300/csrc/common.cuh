@@ -160,6 +160,26 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
   }
 }
 
+// The same wait made by every lane of the warp, each acquiring the phase
+// itself; true on every lane when the phase completed for all of them.
+//
+// Whatever a lane does after the wait that depends on the phase (a
+// tcgen05.ld of an accumulator the MMAs completed, a shared-memory write into
+// a stage the tensor cores released or a TMA copy filled, a copy issued into
+// such a stage) must be ordered after the phase's completion for THAT lane.
+// An mbarrier wait orders only the waiting thread; a shuffle that passes its
+// result on orders nothing in memory.  A lane-0 wait broadcast by shuffle is
+// therefore not enough: with it, the grouped down GEMM returned unwritten
+// rows and NaNs once an unrelated warp vote was compiled into its epilogue
+// (never executed), and with every lane waiting the same build is correct.
+template <bool CLUSTER = false>
+__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, volatile int* abort,
+                                               uint64_t limit_ns, uint32_t* status, uint32_t site,
+                                               uint32_t kernel = kKernGemm) {
+  const bool w = mbar_wait_bounded<CLUSTER>(bar, parity, abort, limit_ns, status, site, kernel);
+  return __all_sync(0xffffffffu, w);
+}
+
 // ------------------------------------------------------------- CTA pairs
 __device__ __forceinline__ uint32_t cluster_ctarank() {
   uint32_t r;

@@ -569,10 +569,7 @@ __global__ void __launch_bounds__(Traits<MODE, KH, CG>::kThreads, 1)
       }
       const uint32_t a_bytes = (uint32_t)((kPair ? 1 : t.halves) * A_HALF_BYTES);
       for (int kb = 0; kb < t.kblocks; ++kb) {
-        bool w = true;
-        if (lane == 0)
-          w = mbar_wait_bounded<kPair>(empty_bar(stage), phase ^ 1u, abort_flag, p.wait_limit_ns, p.status, 1);
-        ok = __shfl_sync(0xffffffffu, w ? 1 : 0, 0) != 0;
+        ok = mbar_wait_warp<kPair>(empty_bar(stage), phase ^ 1u, abort_flag, p.wait_limit_ns, p.status, 1);
         if (!ok) break;
         const uint32_t sA = ring_u32 + stage * Tr::kStageBytes;
         const uint32_t sB = sA + Tr::kABytes;
@@ -615,16 +612,12 @@ __global__ void __launch_bounds__(Traits<MODE, KH, CG>::kThreads, 1)
     for (int tile = tile0; tile < total_tiles && ok; tile += tile_step) {
       const Tile t = decode_tile<MODE, KH, CG>(p, prefix, tile);
       if (t.kblocks == 0) continue;
-      bool w = true;
-      if (lane == 0)    // the epilogue (of both CTAs) has drained this accumulator buffer
-        w = mbar_wait_bounded<kPair>(acce_bar(acc), acc_phase ^ 1u, abort_flag, p.wait_limit_ns, p.status, 2);
-      ok = __shfl_sync(0xffffffffu, w ? 1 : 0, 0) != 0;
+      // the epilogue (of both CTAs) has drained this accumulator buffer
+      ok = mbar_wait_warp<kPair>(acce_bar(acc), acc_phase ^ 1u, abort_flag, p.wait_limit_ns, p.status, 2);
       if (!ok) break;
       tc_fence_after();
       for (int kb = 0; kb < t.kblocks; ++kb) {
-        if (lane == 0)
-          w = mbar_wait_bounded<kPair>(full_bar(stage), phase, abort_flag, p.wait_limit_ns, p.status, 3);
-        ok = __shfl_sync(0xffffffffu, w ? 1 : 0, 0) != 0;
+        ok = mbar_wait_warp<kPair>(full_bar(stage), phase, abort_flag, p.wait_limit_ns, p.status, 3);
         if (!ok) break;
         const uint32_t sA = ring_u32 + stage * Tr::kStageBytes;
         const uint32_t sB = sA + Tr::kABytes;
@@ -711,10 +704,8 @@ __global__ void __launch_bounds__(Traits<MODE, KH, CG>::kThreads, 1)
         }
         continue;
       }
-      bool w = true;
-      if (lane == 0)
-        w = mbar_wait_bounded<kPair>(accf_bar(acc), acc_phase, abort_flag, p.wait_limit_ns, p.status, 4);
-      if (__shfl_sync(0xffffffffu, w ? 1 : 0, 0) == 0) break;
+      // every lane acquires the accumulator itself before the warp reads it
+      if (!mbar_wait_warp<kPair>(accf_bar(acc), acc_phase, abort_flag, p.wait_limit_ns, p.status, 4)) break;
       tc_fence_after();
       const bool active = half < t.halves;     // warp-uniform
       const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)((acc + half) * BN);

@@ -358,10 +358,7 @@ __global__ void __launch_bounds__(fr_threads<NV>(), 1) fused_router_kernel(const
     uint32_t issued = 0, last_par = 0;
     bool ok = true;
     for (int kb = 0; kb < p.kblocks; ++kb) {
-      bool w = true;
-      if (lane == 0)
-        w = mbar_wait_bounded(empty_bar(stage), phase ^ 1u, abort_flag, p.wait_limit_ns, p.status, 1, kKernRoute);
-      ok = __shfl_sync(0xffffffffu, w ? 1 : 0, 0) != 0;
+      ok = mbar_wait_warp(empty_bar(stage), phase ^ 1u, abort_flag, p.wait_limit_ns, p.status, 1, kKernRoute);
       if (!ok) break;
       if (lane == 0) {
         const uint32_t fb = full_bar(stage);
@@ -398,10 +395,7 @@ __global__ void __launch_bounds__(fr_threads<NV>(), 1) fused_router_kernel(const
     uint32_t phase = 0;
     bool ok = true, issued_any = false;
     for (int kb = 0; kb < p.kblocks; ++kb) {
-      bool w = true;
-      if (lane == 0)
-        w = mbar_wait_bounded(full_bar(stage), phase, abort_flag, p.wait_limit_ns, p.status, 2, kKernRoute);
-      ok = __shfl_sync(0xffffffffu, w ? 1 : 0, 0) != 0;
+      ok = mbar_wait_warp(full_bar(stage), phase, abort_flag, p.wait_limit_ns, p.status, 2, kKernRoute);
       if (!ok) break;
       tc_fence_after();
       if (lane == 0) {
@@ -435,9 +429,8 @@ __global__ void __launch_bounds__(fr_threads<NV>(), 1) fused_router_kernel(const
     __syncwarp();
   } else if (warp < 6) {
     // ------------------------------------- partial tile: TMEM -> shared
-    bool w = true;
-    if (lane == 0) w = mbar_wait_bounded(accf_bar, 0, abort_flag, p.wait_limit_ns, p.status, 3, kKernRoute);
-    if (__shfl_sync(0xffffffffu, w ? 1 : 0, 0) != 0) {
+    // every lane acquires the accumulator itself before the warp reads it
+    if (mbar_wait_warp(accf_bar, 0, abort_flag, p.wait_limit_ns, p.status, 3, kKernRoute)) {
       tc_fence_after();
       const int quarter = warp & 3;              // TMEM lanes 32 quarter .. +31
       const int r = quarter * 32 + lane;         // tile row of this thread
