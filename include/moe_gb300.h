@@ -140,6 +140,28 @@ int moe_route(const uint16_t* x, const float* w_router, const float* bias, int64
               int64_t E, int64_t k, int32_t* ids, float* w, float* logits, void* workspace,
               size_t workspace_bytes, void* stream);
 
+/* The router with W_r's bf16 split prepared once.  On the tensor-core path
+ * moe_route first splits W_r exactly into three bf16 terms, W = W0 + W1 + W2
+ * (24 = 3 x 8 significant bits: Henry, Tang & Heinecke, ARITH 2019), then
+ * multiplies the exact bf16 x with all three, accumulating in fp32.  While
+ * W_r does not change (inference; a training step changes it once per
+ * optimizer step) the split can be made once and reused:
+ *   moe_route_split_weight   w_split [3, H, E] bf16 (out: W0 rows, then W1,
+ *                            then W2; 3*H*E*2 bytes, caller-owned, 16-byte
+ *                            aligned) from w_router [H, E] fp32
+ *   moe_route_presplit       moe_route's arguments with w_split in place of
+ *                            w_router and its own (smaller) workspace; ids, w
+ *                            and logits are bit for bit those of moe_route
+ * Both need the tensor-core path (E % 8 == 0, H % 64 == 0, E <= 1024); other
+ * shapes return MOE_ERR_UNSUPPORTED (use moe_route).  The presplit workspace
+ * is 0 bytes when 16 <= E <= 256 and E % 16 == 0 (the fused cluster router;
+ * workspace may then be NULL), else the split-K partial logits. */
+int moe_route_split_weight(const float* w_router, int64_t H, int64_t E, uint16_t* w_split, void* stream);
+int moe_route_presplit_workspace_size(int64_t T, int64_t H, int64_t E, size_t* bytes);
+int moe_route_presplit(const uint16_t* x, const uint16_t* w_split, const float* bias, int64_t T, int64_t H,
+                       int64_t E, int64_t k, int32_t* ids, float* w, float* logits, void* workspace,
+                       size_t workspace_bytes, void* stream);
+
 /* ---------------------------------------------------------------- permute */
 
 /* Bytes of workspace moe_permute needs: per-block expert histograms, the

@@ -97,6 +97,34 @@ def test_route_validation(lib):
     assert lib.moe_route(None, None, None, 0, 64, 4, 2, None, None, None, None, 0, None) == 0
 
 
+def test_route_presplit_validation(lib):
+    """The router on a split of W_r made once: the shapes of the tensor-core
+    path only, its own (smaller) workspace, and the same argument checks."""
+    S = ctypes.c_size_t
+    n = S(0)
+    # fused cluster router (E % 16 == 0, 16 <= E <= 256): no workspace at all
+    assert lib.moe_route_presplit_workspace_size(4096, 2048, 128, ctypes.byref(n)) == 0 and n.value == 0
+    # split-K tensor-core router: the fp32 partial logits only (no split weight)
+    assert lib.moe_route_presplit_workspace_size(4096, 2048, 200, ctypes.byref(n)) == 0
+    full = S(0)
+    assert lib.moe_route_workspace_size(4096, 2048, 200, ctypes.byref(full)) == 0
+    assert 4096 * 200 * 4 <= n.value < full.value
+    assert lib.moe_route_presplit(FAKE, FAKE, None, 4096, 2048, 200, 8, FAKE, FAKE, None, FAKE, n.value - 1,
+                                  None) == WORKSPACE
+    # CUDA-core shapes have no split: refused
+    assert lib.moe_route_presplit_workspace_size(4, 64, 7, ctypes.byref(n)) == UNSUPPORTED
+    assert lib.moe_route_presplit(FAKE, FAKE, None, 4, 64, 7, 2, FAKE, FAKE, None, None, 0, None) == UNSUPPORTED
+    assert lib.moe_route_split_weight(FAKE, 60, 16, FAKE, None) == UNSUPPORTED
+    assert lib.moe_route_split_weight(FAKE, 64, 12, FAKE, None) == UNSUPPORTED
+    # argument checks as moe_route
+    assert lib.moe_route_presplit(FAKE, FAKE, None, 4, 64, 16, 17, FAKE, FAKE, None, None, 0, None) == INVALID
+    assert lib.moe_route_presplit(MISALIGNED, FAKE, None, 4, 64, 16, 2, FAKE, FAKE, None, None, 0, None) == INVALID
+    assert lib.moe_route_split_weight(None, 64, 16, FAKE, None) == INVALID
+    assert lib.moe_route_split_weight(FAKE, 64, 16, MISALIGNED, None) == INVALID
+    # T == 0 is a valid no-op
+    assert lib.moe_route_presplit(None, None, None, 0, 64, 16, 2, None, None, None, None, 0, None) == 0
+
+
 def test_permute_validation(lib):
     n = ctypes.c_size_t(0)
     assert lib.moe_permute_workspace_size(100, 8, 128, ctypes.byref(n)) == 0 and n.value >= 128 * 4

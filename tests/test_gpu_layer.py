@@ -302,6 +302,28 @@ def torch_equal(a, b):
                             b.view(torch.uint8) if b.dtype == torch.bfloat16 else b))
 
 
+def test_forward_graph_router_split_refresh():
+    """A ForwardGraph makes W_r's bf16 split once; after W_r changes in place,
+    refresh_router_split() makes the replays follow the new router (against
+    the oracle and bit for bit against moe_forward)."""
+    import torch
+    moe = lib()
+    cfg, inp = _inputs(300, 256, 16, 2, 128, seed=95)
+    wr, gu, dn = f32(inp.w_router), bf(inp.gate_up), bf(inp.down)
+    g = moe.ForwardGraph(300, wr, gu, dn, cfg.k)
+    xb = synth.normal_bf16(8, synth.TID_X, (300, 256), 1.0)
+    x = torch.from_numpy(xb.view(np.int16)).view(torch.bfloat16).cuda()
+    new_wr = synth.normal_f32(96, synth.TID_WR, (256, 16), 256 ** -0.5)
+    wr.copy_(torch.from_numpy(new_wr).cuda())
+    g.refresh_router_split()
+    y_graph = g(x).clone()
+    y_eager, _ = moe.moe_forward(x, wr, gu, dn, cfg.k)
+    moe.sync_status()
+    assert torch_equal(y_graph, y_eager)
+    inp2 = synth.MoEInputs(inp.cfg, inp.x, new_wr, None, inp.gate_up, inp.down)
+    assert_close("y (ForwardGraph, new W_r)", f64(y_graph), _oracle_y(inp2, xb))
+
+
 def test_pipelined_forward_matches_forward():
     """PipelinedForward (copies overlapped with the layer on two streams):
     every batch's output against the oracle, and bit for bit equal to

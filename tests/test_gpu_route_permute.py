@@ -32,6 +32,33 @@ def test_route_matches_oracle(T, H, E, k):
     np.testing.assert_allclose(f64(w).sum(1), 1.0, atol=1e-5)
 
 
+@pytest.mark.parametrize("T,H,E,k,bias", [(4100, 2048, 128, 8, False), (333, 256, 16, 4, True),
+                                          (97, 128, 200, 8, True), (40, 128, 1024, 6, False)])
+def test_route_presplit_equals_route(T, H, E, k, bias):
+    """W_r's split made once (moe_route_split_weight) and reused
+    (moe_route_presplit) gives moe_route's ids, weights and logits bit for
+    bit: on the fused cluster router (E = 128, 16) and the split-K path
+    (E = 200, 1024); the split itself sums back to W_r exactly."""
+    import torch
+    moe = lib()
+    cfg = synth.MoEConfig("r", T=T, H=H, E=E, k=k, I=64, seed=2 * T + E)
+    inp = synth.make_inputs(cfg, weights=False)
+    x, wr = bf(inp.x), f32(inp.w_router)
+    b = f32(synth.zipf_bias(cfg.seed, E, 1.0)) if bias else None
+    ref = moe.route(x, wr, k, b, return_logits=True)
+    w_split = moe.route_split_weight(wr)
+    for _ in range(2):   # the same split serves repeated calls
+        got = moe.route(x, wr, k, b, return_logits=True, w_split=w_split)
+        moe.sync_status()
+        for a, c in zip(ref, got):
+            assert torch.equal(a, c)
+    parts = w_split.float().cpu().numpy().astype(np.float64).reshape(3, H, E)
+    np.testing.assert_array_equal(parts.sum(0), inp.w_router.astype(np.float64))
+    ids_ref = oracle.route(inp.x, inp.w_router, synth.zipf_bias(cfg.seed, E, 1.0) if bias else None, k)
+    same, tolerated = compare_ids(npi(got[0]), ids_ref, label="presplit")
+    assert tolerated <= max(1, T // 1000)
+
+
 def test_route_bias_and_skewed_workload():
     moe = lib()
     cfg = synth.CONFIGS["qwen3_moe_skewed"]

@@ -31,6 +31,9 @@ SIGNATURES = {
     "moe_set_pdl": [INT],
     "moe_route_workspace_size": [I64, I64, I64, ctypes.POINTER(SZ)],
     "moe_route": [P, P, P, I64, I64, I64, I64, P, P, P, P, SZ, P],
+    "moe_route_split_weight": [P, I64, I64, P, P],
+    "moe_route_presplit_workspace_size": [I64, I64, I64, ctypes.POINTER(SZ)],
+    "moe_route_presplit": [P, P, P, I64, I64, I64, I64, P, P, P, P, SZ, P],
     "moe_permute_workspace_size": [I64, I64, I64, ctypes.POINTER(SZ)],
     "moe_permute": [P, P, I64, I64, I64, P, P, P, P, P, P, SZ, P],
     "moe_permute_noalloc": [P, P, I64, I64, I64, P, P, P, P, P, P],

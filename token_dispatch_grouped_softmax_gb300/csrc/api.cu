@@ -165,6 +165,39 @@ int moe_route(const uint16_t* x, const float* w_router, const float* bias, int64
                                        static_cast<cudaStream_t>(stream)));
 }
 
+int moe_route_split_weight(const float* w_router, int64_t H, int64_t E, uint16_t* w_split, void* stream) {
+  if (H < 1 || E < 1 || !w_router || !w_split) return MOE_ERR_INVALID_ARG;
+  if (E > moe::kMaxExperts || !moe::route_on_tensor_cores(H, E)) return MOE_ERR_UNSUPPORTED;
+  if (!aligned16(w_router) || !aligned16(w_split)) return MOE_ERR_INVALID_ARG;
+  return cuda_status(moe::launch_route_split(w_router, H, E, w_split, static_cast<cudaStream_t>(stream)));
+}
+
+int moe_route_presplit_workspace_size(int64_t T, int64_t H, int64_t E, size_t* bytes) {
+  if (!bytes || T < 0 || H < 1 || E < 1) return MOE_ERR_INVALID_ARG;
+  if (!moe::route_on_tensor_cores(H, E)) return MOE_ERR_UNSUPPORTED;
+  *bytes = moe::route_presplit_workspace_bytes(T, H, E);
+  return MOE_OK;
+}
+
+int moe_route_presplit(const uint16_t* x, const uint16_t* w_split, const float* bias, int64_t T, int64_t H,
+                       int64_t E, int64_t k, int32_t* ids, float* w, float* logits, void* workspace,
+                       size_t workspace_bytes, void* stream) {
+  if (T < 0 || H < 1 || E < 1 || k < 1 || k > E || T > kMaxI32 || T * k > kMaxI32)
+    return MOE_ERR_INVALID_ARG;
+  if (T > 0 && (!x || !w_split || !ids || !w)) return MOE_ERR_INVALID_ARG;
+  if (E > moe::kMaxExperts || k > 32 || !moe::route_on_tensor_cores(H, E)) return MOE_ERR_UNSUPPORTED;
+  if ((x && !aligned16(x)) || (w_split && !aligned16(w_split))) return MOE_ERR_INVALID_ARG;
+  const size_t need = moe::route_presplit_workspace_bytes(T, H, E);
+  if (T > 0 && need > 0 && (!workspace || !aligned16(workspace) || workspace_bytes < need))
+    return MOE_ERR_WORKSPACE;
+  if (T == 0) return MOE_OK;
+  moe::DeviceInfo dev;
+  int rc = moe::current_device(&dev);
+  if (rc != MOE_OK) return rc;
+  return cuda_status(moe::launch_route_presplit(x, w_split, bias, T, H, E, k, ids, w, logits, workspace, dev,
+                                                static_cast<cudaStream_t>(stream)));
+}
+
 /* ---------------------------------------------------------------- permute */
 
 int moe_permute_workspace_size(int64_t T, int64_t k, int64_t E, size_t* bytes) {

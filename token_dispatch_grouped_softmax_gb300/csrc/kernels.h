@@ -69,6 +69,13 @@ bool encode_tensor_map_2d_bf16(CUtensorMap* map, const void* base, const cuuint6
                                const cuuint32_t* estr);
 
 size_t route_workspace_bytes(int64_t T, int64_t H, int64_t E);
+bool route_on_tensor_cores(int64_t H, int64_t E);
+size_t route_presplit_workspace_bytes(int64_t T, int64_t H, int64_t E);
+cudaError_t launch_route_split(const float* w_router, int64_t H, int64_t E, uint16_t* w_split,
+                               cudaStream_t stream);
+cudaError_t launch_route_presplit(const uint16_t* x, const uint16_t* w_split, const float* bias, int64_t T,
+                                  int64_t H, int64_t E, int64_t k, int32_t* ids, float* w, float* logits,
+                                  void* ws, const DeviceInfo& dev, cudaStream_t stream);
 cudaError_t launch_route(const uint16_t* x, const float* w_router, const float* bias, int64_t T,
                          int64_t H, int64_t E, int64_t k, int32_t* ids, float* w, float* logits,
                          void* ws, const DeviceInfo& dev, cudaStream_t stream);

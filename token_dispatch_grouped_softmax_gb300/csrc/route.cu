@@ -614,6 +614,34 @@ size_t route_workspace_bytes(int64_t T, int64_t H, int64_t E) {
   return align((size_t)(T * E * 4));
 }
 
+size_t route_presplit_workspace_bytes(int64_t T, int64_t H, int64_t E) {
+  auto align = [](size_t b) { return (b + 255) & ~size_t(255); };
+  if (fused_router_ok(H, E)) return 0;
+  return align((size_t)(router_parts(T, H, E) * T * E * 4));
+}
+
+cudaError_t launch_route_split(const float* w_router, int64_t H, int64_t E, uint16_t* w_split,
+                               cudaStream_t stream) {
+  const int64_t n = H * E;
+  if (n == 0) return cudaSuccess;
+  return launch_pdl(split_router_weight_kernel, dim3((unsigned)std::min<int64_t>((n + 255) / 256, 4096)), dim3(256),
+                    0, stream, 1, w_router, n, w_split);
+}
+
+// The router on a split of W_r prepared once (launch_route_split): the same
+// kernels as launch_route on the tensor-core path, without the split.
+cudaError_t launch_route_presplit(const uint16_t* x, const uint16_t* w_split, const float* bias, int64_t T,
+                                  int64_t H, int64_t E, int64_t k, int32_t* ids, float* w, float* logits,
+                                  void* ws, const DeviceInfo& dev, cudaStream_t stream) {
+  if (T == 0) return cudaSuccess;
+  if (fused_router_ok(H, E)) return launch_fused_router(x, w_split, bias, T, H, E, k, ids, w, logits, dev, stream);
+  const int parts = router_parts(T, H, E);
+  float* part = static_cast<float*>(ws);
+  if (launch_router_logits(x, w_split, T, H, E, parts, part, dev, stream) != 0) return cudaErrorInvalidValue;
+  topk_dispatch(part, parts, bias, T, E, k, ids, w, logits, stream);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_route(const uint16_t* x, const float* w_router, const float* bias, int64_t T,
                          int64_t H, int64_t E, int64_t k, int32_t* ids, float* w, float* logits,
                          void* ws, const DeviceInfo& dev, cudaStream_t stream) {

@@ -39,18 +39,20 @@ class ForwardState:
 
 
 def moe_forward(x, w_router, gate_up, down, k, bias=None, sh_gate_up=None, sh_down=None,
-                save_for_backward=False, fused_gather=False):
+                save_for_backward=False, fused_gather=False, w_split=None):
     """y [T, H] bf16 and the ForwardState.
 
     fused_gather: the grouped gate_up GEMM gathers the token rows itself (the
     permute fused into the operand load by TMA tile::gather4); False
     (default) materialises the permuted rows first (moe_permute_rows) and
     streams them with 128-row TMA tiles, which measures ~2.5x faster for the
-    GEMM on GB300."""
+    GEMM on GB300.
+    w_split: W_r's bf16 split (ops.route_split_weight), prepared once while
+    W_r does not change; the same results as without it."""
     T, H = x.shape
     E = w_router.shape[1]
     I = down.shape[0] // E
-    ids, w = ops.route(x, w_router, k, bias)
+    ids, w = ops.route(x, w_router, k, bias, w_split=w_split)
     w_perm = None
     if save_for_backward:
         counts, offsets, row_map, src_row, w_perm = ops.permute(ids, E, w)
@@ -142,13 +144,18 @@ class ForwardGraph:
     replay overwrites.  Every step of the path stays on the device (expert
     offsets included), so one capture serves any routing.  The graph keeps
     its intermediates in its own memory pool.
+
+    The weights are fixed for the graph's life: W_r's bf16 split (the tensor
+    cores' router operand) is made once here, outside the graph.  After
+    changing W_r in place, call ``refresh_router_split()``.
     """
 
     def __init__(self, T, w_router, gate_up, down, k, bias=None, sh_gate_up=None, sh_down=None,
                  fused_gather=False):
-        H = w_router.shape[0]
+        H, E = w_router.shape
         self.args = (w_router, gate_up, down, k, bias, sh_gate_up, sh_down)
         self.fused_gather = fused_gather
+        self.w_split = ops.route_split_weight(w_router) if ops.route_supports_split(H, E) else None
         self.x = torch.zeros((T, H), dtype=torch.bfloat16, device=w_router.device)
         side = torch.cuda.Stream()
         side.wait_stream(torch.cuda.current_stream())
@@ -163,8 +170,13 @@ class ForwardGraph:
     def _forward(self):
         w_router, gate_up, down, k, bias, sh_gu, sh_dn = self.args
         y, _ = moe_forward(self.x, w_router, gate_up, down, k, bias, sh_gu, sh_dn,
-                           fused_gather=self.fused_gather)
+                           fused_gather=self.fused_gather, w_split=self.w_split)
         return y
+
+    def refresh_router_split(self):
+        """Re-derives W_r's split (in place, where the graph reads it) after W_r changed."""
+        if self.w_split is not None:
+            ops.route_split_weight(self.args[0], out=self.w_split)
 
     def replay(self):
         """Runs the layer on the current contents of ``x``; returns ``y``."""
@@ -242,13 +254,18 @@ class OverlappedForward:
     split within a batch, so every expert's weights are still read once per
     batch.  A copy stream uploads each batch and downloads its output.
     Outputs equal moe_forward's bit for bit.  Host tensors must be pinned;
-    every batch has the token count given here.
+    every batch has the token count given here.  As ForwardGraph, it makes
+    W_r's bf16 split once at construction (``refresh_router_split()`` after
+    changing W_r).
     """
 
     def __init__(self, T, w_router, gate_up, down, k, bias=None, sh_gate_up=None, sh_down=None,
                  fused_gather=False):
         H, E = w_router.shape
         I = down.shape[0] // E
+        self.w_router = w_router
+        self.w_split = ops.route_split_weight(w_router) if ops.route_supports_split(H, E) else None
+        w_split = self.w_split
         self.stream_f = torch.cuda.Stream()
         self.stream_g = torch.cuda.Stream()
         self.copy_stream = torch.cuda.Stream()
@@ -259,7 +276,7 @@ class OverlappedForward:
             st = {"x": torch.zeros((T, H), dtype=torch.bfloat16, device=w_router.device)}
 
             def front(st=st):
-                ids, w = ops.route(st["x"], w_router, k, bias)
+                ids, w = ops.route(st["x"], w_router, k, bias, w_split=w_split)
                 counts, offsets, row_map, src_row = ops.permute(ids, E)
                 x_perm = None if fused_gather else ops.permute_rows(st["x"], src_row)
                 st.update(w=w, offsets=offsets, row_map=row_map, src_row=src_row, x_perm=x_perm)
@@ -300,6 +317,11 @@ class OverlappedForward:
             st.update(ev_loaded=torch.cuda.Event(), ev_f=torch.cuda.Event(), ev_g=torch.cuda.Event(),
                       ev_stored=torch.cuda.Event())
             self.sets.append(st)
+
+    def refresh_router_split(self):
+        """Re-derives W_r's split (in place, where the graphs read it) after W_r changed."""
+        if self.w_split is not None:
+            ops.route_split_weight(self.w_router, out=self.w_split)
 
     def run(self, x_host_batches, y_host_batches):
         """y_host_batches[i] <- layer(x_host_batches[i]); returns when all are stored."""

@@ -86,8 +86,12 @@ def pdl_enabled() -> bool:
 
 # ----------------------------------------------------------------- forward
 
-def route(x, w_router, k, bias=None, return_logits=False):
-    """ids [T,k] int32, w [T,k] fp32 (and logits [T,E] fp32)."""
+def route(x, w_router, k, bias=None, return_logits=False, w_split=None):
+    """ids [T,k] int32, w [T,k] fp32 (and logits [T,E] fp32).
+
+    w_split: W_r's bf16 split from route_split_weight(w_router), made once
+    while W_r does not change (moe_route_presplit); the results are the same
+    bit for bit."""
     _need(x, "x", _BF16, 2)
     _need(w_router, "w_router", torch.float32, 2)
     if bias is not None:
@@ -99,11 +103,40 @@ def route(x, w_router, k, bias=None, return_logits=False):
     w = torch.empty((T, k), dtype=torch.float32, device=dev)
     logits = torch.empty((T, E), dtype=torch.float32, device=dev) if return_logits else None
     nbytes = ctypes.c_size_t(0)
+    if w_split is not None:
+        _need(w_split, "w_split", _BF16, 2)
+        if tuple(w_split.shape) != (3 * H, E):
+            raise ValueError("w_split must be [3H, E] (route_split_weight)")
+        call("moe_route_presplit_workspace_size", T, H, E, ctypes.byref(nbytes))
+        ws = _ws(nbytes.value, dev) if nbytes.value else None
+        call("moe_route_presplit", _p(x), _p(w_split), _p(bias), T, H, E, k, _p(ids), _p(w), _p(logits), _p(ws),
+             ws.numel() if ws is not None else 0, _stream())
+        return (ids, w, logits) if return_logits else (ids, w)
     call("moe_route_workspace_size", T, H, E, ctypes.byref(nbytes))
     ws = _ws(nbytes.value, dev)
     call("moe_route", _p(x), _p(w_router), _p(bias), T, H, E, k, _p(ids), _p(w), _p(logits), _p(ws),
          ws.numel(), _stream())
     return (ids, w, logits) if return_logits else (ids, w)
+
+
+def route_supports_split(H, E):
+    """Whether the router runs on the tensor cores at this shape (E % 8 == 0,
+    H % 64 == 0, E <= 1024), the shapes route_split_weight serves."""
+    return E % 8 == 0 and H % 64 == 0 and E <= 1024
+
+
+def route_split_weight(w_router, out=None):
+    """W_r's exact three-term bf16 split [3H, E] (W0 rows, then W1, then W2),
+    for route(..., w_split=...) while W_r does not change.  out: an existing
+    [3H, E] bf16 tensor to refresh in place (e.g. one a captured graph reads)."""
+    _need(w_router, "w_router", torch.float32, 2)
+    H, E = w_router.shape
+    w_split = torch.empty((3 * H, E), dtype=_BF16, device=w_router.device) if out is None else out
+    _need(w_split, "w_split", _BF16, 2)
+    if tuple(w_split.shape) != (3 * H, E):
+        raise ValueError("w_split must be [3H, E]")
+    call("moe_route_split_weight", _p(w_router), H, E, _p(w_split), _stream())
+    return w_split
 
 
 def permute(ids, E, w=None):
