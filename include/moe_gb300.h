@@ -348,6 +348,69 @@ int moe_gather_dx(const uint16_t* dx_perm, const int32_t* row_map, const float* 
 int moe_route_bwd_weight(const uint16_t* x, const float* d_logits, int64_t T, int64_t H, int64_t E,
                          float* d_w_router, void* stream);
 
+/* ---------------------------------------------------- expert parallelism */
+
+/* The single-device pieces of expert-parallel dispatch and combine
+ * ("Awesome-ML-SYS-Tutorial" MoE/EP guide, "Expert Parallelism": dispatch
+ * and combine by all-to-all, split sizes from per-expert token counts, the
+ * receiver's re-sort of its chunks by local expert `sort_chunks_by_idxs`;
+ * hotspot experts and EPLB-style replication).  Experts are split over the
+ * EP ranks on dim 0, so a rank's permuted rows are already grouped by the
+ * rank that owns their expert.  The transport between ranks (an all-to-all-v
+ * of NCCL or another library) is not part of this library. */
+
+/* Bytes of workspace moe_sort_chunks needs: (2*A*B + 1) int32. */
+int moe_sort_chunks_workspace_size(int64_t A, int64_t B, size_t* bytes);
+
+/* Rows that arrive as an A x B matrix of chunks in row-major (a, b) order
+ * (chunk (a, b) holds counts[a*B + b] rows) are reordered to (b, a) order:
+ * the transpose of the chunk matrix, each chunk's rows kept in order.  It is
+ * what an all-to-all does to the order of the rows of every sender (a =
+ * source rank, b = destination rank) and what the receiver's re-sort does to
+ * its chunks (a = source rank, b = local expert), after which each local
+ * expert's rows are contiguous.
+ *   counts        [A*B] int32 (device)   chunk sizes, >= 0, summing to N
+ *   src_of        [N] int32 (out)        input row at each output position
+ *   pos_of        [N] int32 (out)        output position of each input row
+ *   group_offsets [B+1] int32 (out)      first output row of each b, then N
+ *                                        (the receiver's local expert offsets)
+ * The rows themselves move with moe_permute_rows (x_out = x_in[src_of]; back
+ * again with pos_of).  Counts that are negative or do not sum to N are
+ * reported as MOE_ERR_DEVICE (outputs undefined, nothing written out of
+ * bounds).  Limits: A*B <= 2^24, N < 2^31. */
+int moe_sort_chunks(const int32_t* counts, int64_t A, int64_t B, int64_t N, int32_t* src_of, int32_t* pos_of,
+                    int32_t* group_offsets, void* workspace, size_t workspace_bytes, void* stream);
+
+/* EPLB-style expert replication, on the host (no GPU).  From each logical
+ * expert's load (e.g. the rows it received in recent steps) and n_phys >= E
+ * physical expert slots over G ranks (n_phys % G == 0):
+ *   1. each of the n_phys - E extra replicas goes to the expert with the
+ *      largest load per replica (ties to the lower index);
+ *   2. a replica's load is its share under the round-robin by token of
+ *      moe_ep_map_replicas (load / replicas, the first load % replicas
+ *      replicas one more);
+ *   3. replicas, heaviest first, each go to the least-loaded rank with a free
+ *      slot (n_phys / G slots per rank; ties to the lower rank);
+ *   4. physical ids are rank-major (rank g owns ids g*n_phys/G ...), within a
+ *      rank ordered by (expert, replica).
+ * Outputs (host arrays): phys_to_log [n_phys], rep_first [E] and rep_count
+ * [E] (replica r of expert e is physical expert rep_list[rep_first[e] + r]),
+ * rep_list [n_phys], rank_load [G] (nullable).  The pages name the method
+ * (hotspot experts, EPLB) without its steps; this is the plain greedy reading. */
+int moe_eplb_plan(const int64_t* expert_load, int64_t E, int64_t G, int64_t n_phys, int32_t* phys_to_log,
+                  int32_t* rep_first, int32_t* rep_count, int32_t* rep_list, int64_t* rank_load);
+
+/* Logical expert ids -> physical replica ids (device): assignment i = t*k + j
+ * of logical expert e goes to replica t mod rep_count[e], i.e. physical expert
+ * rep_list[rep_first[e] + t % rep_count[e]].  The replicas carry copies of
+ * the expert's weights, so the layer's output is unchanged; a replicated
+ * expert's rows are shared by its replicas.  ids out of [0, E) or a plan
+ * that points outside [0, n_phys) are reported as MOE_ERR_DEVICE (physical
+ * expert 0 is written instead). */
+int moe_ep_map_replicas(const int32_t* ids, int64_t T, int64_t k, int64_t E, const int32_t* rep_first,
+                        const int32_t* rep_count, const int32_t* rep_list, int64_t n_phys, int32_t* phys_ids,
+                        void* stream);
+
 #ifdef __cplusplus
 }
 #endif

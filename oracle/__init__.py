@@ -9,8 +9,8 @@ workloads' raw encodings (bf16 bits as uint16 for x / gate_up / down / dY /
 shared weights, fp32 for W_r and bias), which are widened exactly, or all as
 float64 (used by the finite-difference pins).  All arithmetic is fp64.
 
-Every function is pinned by tests/test_oracle_pins.py; none is "parity
-unpinned".
+Every function is pinned by tests/test_oracle_pins.py (the expert-parallel
+index functions by tests/test_oracle_ep_pins.py); none is "parity unpinned".
 """
 from __future__ import annotations
 
@@ -337,3 +337,111 @@ def layer_forward(inp, want_intermediates=False):
     else:
         y, extra = res, {}
     return dict(route=r, perm=perm, y=y, **extra)
+
+
+# ------------------------------------------------------- expert parallelism
+# The index flow of expert-parallel dispatch and combine (Awesome-ML-SYS-
+# Tutorial MoE/EP guide, gsyq.cn, "Expert Parallelism": dispatch by
+# all-to-all with split sizes from the per-expert token counts, the
+# receiver's re-sort of its chunks by local expert, combine by all-to-all;
+# hotspot experts and EPLB-style replication), as plain loops.
+
+def sort_chunks(counts):
+    """Rows in an A x B matrix of chunks, row-major (a, b) order, reordered to
+    (b, a) order, each chunk's rows kept in order.  Returns src_of [N] (the
+    input row at each output position), pos_of [N] (its inverse) and
+    group_offsets [B+1] (the first output row of each b)."""
+    counts = np.asarray(counts, dtype=np.int64)
+    A, B = counts.shape
+    start = {}
+    n = 0
+    for a in range(A):
+        for b in range(B):
+            start[(a, b)] = n
+            n += int(counts[a, b])
+    src_of, group = [], []
+    for b in range(B):
+        group.append(len(src_of))
+        for a in range(A):
+            for l in range(int(counts[a, b])):
+                src_of.append(start[(a, b)] + l)
+    group.append(len(src_of))
+    src_of = np.array(src_of, dtype=np.int32)
+    pos_of = np.empty_like(src_of)
+    pos_of[src_of] = np.arange(len(src_of), dtype=np.int32)
+    return src_of, pos_of, np.array(group, dtype=np.int32)
+
+
+def map_replicas(ids, rep_first, rep_count, rep_list):
+    """Assignment (t, j) of logical expert e goes to its replica t mod
+    rep_count[e]: physical expert rep_list[rep_first[e] + t % rep_count[e]]."""
+    ids = np.asarray(ids)
+    out = np.empty_like(ids, dtype=np.int32)
+    T, k = ids.shape
+    for t in range(T):
+        for j in range(k):
+            e = int(ids[t, j])
+            out[t, j] = rep_list[rep_first[e] + t % rep_count[e]]
+    return out
+
+
+def eplb_plan(load, G, n_phys):
+    """EPLB-style replication and placement, the greedy steps in order: extra
+    replicas one at a time to the expert with the largest load per replica
+    (lower index on ties); replica loads by the round-robin split (load //
+    rep, the first load % rep replicas one more); replicas heaviest first
+    (then lower expert, lower replica) to the least-loaded rank with a free
+    slot (n_phys // G each; lower rank on ties); physical ids rank-major,
+    within a rank by (expert, replica)."""
+    from fractions import Fraction
+    load = [int(v) for v in load]
+    E = len(load)
+    rep = [1] * E
+    for _ in range(n_phys - E):
+        best = max(range(E), key=lambda e: (Fraction(load[e], rep[e]), -e))
+        rep[best] += 1
+    reps = [(load[e] // rep[e] + (1 if r < load[e] % rep[e] else 0), e, r) for e in range(E) for r in range(rep[e])]
+    reps.sort(key=lambda x: (-x[0], x[1], x[2]))
+    slots = n_phys // G
+    rank_load, used, on = [0] * G, [0] * G, [[] for _ in range(G)]
+    for ld, e, r in reps:
+        g = min((c for c in range(G) if used[c] < slots), key=lambda c: (rank_load[c], c))
+        rank_load[g] += ld
+        used[g] += 1
+        on[g].append((e, r))
+    rep_first = np.cumsum([0] + rep[:-1]).astype(np.int32)
+    rep_list = np.empty(n_phys, np.int32)
+    phys_to_log = np.empty(n_phys, np.int32)
+    for g in range(G):
+        for i, (e, r) in enumerate(sorted(on[g])):
+            p = g * slots + i
+            phys_to_log[p] = e
+            rep_list[rep_first[e] + r] = p
+    return dict(phys_to_log=phys_to_log, rep_first=rep_first, rep_count=np.array(rep, np.int32),
+                rep_list=rep_list, rank_load=np.array(rank_load, np.int64))
+
+
+def ep_dispatch(ids_per_rank, n_phys, G):
+    """The rows each EP rank's experts receive.  ids_per_rank[s]: the (physical)
+    expert ids [T_s, k] of source rank s; rank d owns experts [d P, (d+1) P),
+    P = n_phys // G.  Returns, per destination d, a list of (source, token,
+    slot) in the order its local experts see them (local expert, then source,
+    then the source's stable permuted order) and its local expert offsets
+    [P+1]."""
+    P = n_phys // G
+    out = []
+    for d in range(G):
+        rows, offs = [], []
+        for p in range(P):
+            e = d * P + p
+            offs.append(len(rows))
+            for s, ids in enumerate(ids_per_rank):
+                perm = permute(ids, n_phys)
+                assignment = np.empty_like(perm["row_map"])     # permuted row -> assignment i = t k + j
+                assignment[perm["row_map"]] = np.arange(perm["row_map"].shape[0], dtype=np.int32)
+                for row in range(perm["offsets"][e], perm["offsets"][e + 1]):
+                    i = int(assignment[row])
+                    rows.append((s, i // ids.shape[1], i % ids.shape[1]))
+        offs.append(len(rows))
+        out.append((rows, np.array(offs, dtype=np.int32)))
+    return out

@@ -125,6 +125,32 @@ def test_route_presplit_validation(lib):
     assert lib.moe_route_presplit(None, None, None, 0, 64, 16, 2, None, None, None, None, 0, None) == 0
 
 
+def test_ep_validation(lib):
+    """The expert-parallel calls: argument checks before anything is enqueued,
+    and the host-side EPLB plan's limits."""
+    S = ctypes.c_size_t
+    n = S(0)
+    assert lib.moe_sort_chunks_workspace_size(8, 16, ctypes.byref(n)) == 0 and n.value >= (2 * 128 + 1) * 4
+    assert lib.moe_sort_chunks_workspace_size(0, 16, ctypes.byref(n)) == INVALID
+    assert lib.moe_sort_chunks(FAKE, 8, 16, 10, FAKE, FAKE, FAKE, None, 0, None) == WORKSPACE
+    assert lib.moe_sort_chunks(None, 8, 16, 10, FAKE, FAKE, FAKE, FAKE, 4096, None) == INVALID
+    assert lib.moe_sort_chunks(FAKE, 8, 16, 10, None, FAKE, FAKE, FAKE, 4096, None) == INVALID
+    assert lib.moe_sort_chunks(FAKE, 8, 16, -1, FAKE, FAKE, FAKE, FAKE, 4096, None) == INVALID
+    assert lib.moe_ep_map_replicas(FAKE, 4, 2, 8, FAKE, FAKE, FAKE, 6, FAKE, None) == INVALID   # n_phys < E
+    assert lib.moe_ep_map_replicas(None, 4, 2, 8, FAKE, FAKE, FAKE, 8, FAKE, None) == INVALID
+    assert lib.moe_ep_map_replicas(None, 0, 2, 8, FAKE, FAKE, FAKE, 8, None, None) == 0        # empty batch
+    import numpy as np
+    load = np.array([5, 3, 0, 9], dtype=np.int64)
+    out = [np.empty(8, np.int32), np.empty(4, np.int32), np.empty(4, np.int32), np.empty(8, np.int32)]
+    ptr = lambda a: ctypes.c_void_p(a.ctypes.data)
+    assert lib.moe_eplb_plan(ptr(load), 4, 3, 8, *map(ptr, out), None) == INVALID    # 8 % 3 != 0
+    assert lib.moe_eplb_plan(ptr(load), 4, 2, 3, *map(ptr, out), None) == INVALID    # fewer slots than experts
+    bad = np.array([5, -1, 0, 9], dtype=np.int64)
+    assert lib.moe_eplb_plan(ptr(bad), 4, 2, 8, *map(ptr, out), None) == INVALID     # a negative load
+    assert lib.moe_eplb_plan(ptr(load), 4, 2, 8, *map(ptr, out), None) == 0
+    assert sorted(out[3].tolist()) == list(range(8))
+
+
 def test_permute_validation(lib):
     n = ctypes.c_size_t(0)
     assert lib.moe_permute_workspace_size(100, 8, 128, ctypes.byref(n)) == 0 and n.value >= 128 * 4

@@ -59,6 +59,27 @@ def test_route_presplit_equals_route(T, H, E, k, bias):
     assert tolerated <= max(1, T // 1000)
 
 
+@pytest.mark.parametrize("H,E,k", [(2048, 128, 8), (7168, 256, 8), (256, 200, 6)])
+def test_route_is_batch_invariant(H, E, k):
+    """A token's logits, weights and experts do not depend on the tokens
+    routed with it: slices of a batch (a single token, 511 tokens, an
+    expert-parallel rank's share of 4096) routed alone give the same bits as
+    the whole batch (the fused cluster router at E = 128 and 256, the split-K
+    path at E = 200)."""
+    import torch
+    moe = lib()
+    T = 4096
+    cfg = synth.MoEConfig("r", T=T, H=H, E=E, k=k, I=64, seed=H + E)
+    inp = synth.make_inputs(cfg, weights=False)
+    x, wr = bf(inp.x), f32(inp.w_router)
+    whole = moe.route(x, wr, k, return_logits=True)
+    for t0, t1 in ((0, 1), (1000, 1511), (512, 1024), (3584, 4096)):
+        part = moe.route(x[t0:t1].contiguous(), wr, k, return_logits=True)
+        moe.sync_status()
+        for a, b in zip(whole, part):
+            assert torch.equal(a[t0:t1], b), (t0, t1)
+
+
 def test_route_bias_and_skewed_workload():
     moe = lib()
     cfg = synth.CONFIGS["qwen3_moe_skewed"]

@@ -12,6 +12,8 @@ from .ops import (GEMM_PAIRS_ALL, GEMM_PAIRS_GATE_UP, GEMM_PAIRS_NONE, gather_dx
                   grouped_gemm_down_bwd, grouped_gemm_gate_up_bwd, grouped_gemm_gate_up_swiglu, permute,
                   permute_rows, route, route_bwd, route_bwd_weight, route_split_weight, route_supports_split, set_gemm_pairs, set_pdl, set_wait_limit_ns,
                   sync_status, unpermute_combine, unpermute_combine_bwd)
+from . import ep
+from .ops import ep_map_replicas, eplb_plan, sort_chunks
 from .layer import (ForwardGraph, ForwardState, MoELayer, MoELayerFunction, OverlappedForward,
                     PipelinedForward, moe_backward, moe_forward)
 
@@ -21,6 +23,6 @@ __all__ = [
     "unpermute_combine", "unpermute_combine_bwd", "route_bwd", "grouped_gemm_down_bwd",
     "grouped_gemm_gate_up_bwd", "gather_dx", "route_bwd_weight", "sync_status", "set_wait_limit_ns", "set_gemm_pairs",
     "GEMM_PAIRS_NONE", "GEMM_PAIRS_ALL", "GEMM_PAIRS_GATE_UP",
-    "set_pdl",
+    "set_pdl", "sort_chunks", "ep_map_replicas", "eplb_plan", "ep",
     "ForwardGraph", "ForwardState", "MoELayer", "OverlappedForward", "MoELayerFunction", "PipelinedForward", "moe_forward", "moe_backward",
 ]

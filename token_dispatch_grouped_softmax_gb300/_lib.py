@@ -49,6 +49,10 @@ SIGNATURES = {
     "moe_gather_dx_workspace_size": [I64, I64, ctypes.POINTER(SZ)],
     "moe_gather_dx": [P, P, P, P, P, I64, I64, I64, I64, P, P, SZ, P],
     "moe_route_bwd_weight": [P, P, I64, I64, I64, P, P],
+    "moe_sort_chunks_workspace_size": [I64, I64, ctypes.POINTER(SZ)],
+    "moe_sort_chunks": [P, I64, I64, I64, P, P, P, P, SZ, P],
+    "moe_ep_map_replicas": [P, I64, I64, I64, P, P, P, I64, P, P],
+    "moe_eplb_plan": [P, I64, I64, I64, P, P, P, P, P],
 }
 
 _lib = None

@@ -412,3 +412,48 @@ int moe_route_bwd_weight(const uint16_t* x, const float* d_logits, int64_t T, in
 }
 
 }  // extern "C"
+
+/* ---------------------------------------------------- expert parallelism */
+
+int moe_sort_chunks_workspace_size(int64_t A, int64_t B, size_t* bytes) {
+  if (!bytes || A < 1 || B < 1 || A * B > (int64_t)1 << 24) return MOE_ERR_INVALID_ARG;
+  *bytes = moe::sort_chunks_workspace_bytes(A, B);
+  return MOE_OK;
+}
+
+int moe_sort_chunks(const int32_t* counts, int64_t A, int64_t B, int64_t N, int32_t* src_of, int32_t* pos_of,
+                    int32_t* group_offsets, void* workspace, size_t workspace_bytes, void* stream) {
+  if (A < 1 || B < 1 || A * B > (int64_t)1 << 24 || N < 0 || N > kMaxI32) return MOE_ERR_INVALID_ARG;
+  if (!counts || !group_offsets || (N > 0 && (!src_of || !pos_of))) return MOE_ERR_INVALID_ARG;
+  if (!workspace || !aligned16(workspace) || workspace_bytes < moe::sort_chunks_workspace_bytes(A, B))
+    return MOE_ERR_WORKSPACE;
+  moe::DeviceInfo dev;
+  int rc = moe::current_device(&dev);
+  if (rc != MOE_OK) return rc;
+  return cuda_status(moe::launch_sort_chunks(counts, A, B, N, src_of, pos_of, group_offsets, workspace, dev.status,
+                                             static_cast<cudaStream_t>(stream)));
+}
+
+int moe_ep_map_replicas(const int32_t* ids, int64_t T, int64_t k, int64_t E, const int32_t* rep_first,
+                        const int32_t* rep_count, const int32_t* rep_list, int64_t n_phys, int32_t* phys_ids,
+                        void* stream) {
+  if (T < 0 || k < 1 || E < 1 || n_phys < E || T * k > kMaxI32 || n_phys > kMaxI32) return MOE_ERR_INVALID_ARG;
+  if (T > 0 && (!ids || !phys_ids)) return MOE_ERR_INVALID_ARG;
+  if (!rep_first || !rep_count || !rep_list) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  moe::DeviceInfo dev;
+  int rc = moe::current_device(&dev);
+  if (rc != MOE_OK) return rc;
+  return cuda_status(moe::launch_map_replicas(ids, T * k, k, E, rep_first, rep_count, rep_list, n_phys, phys_ids,
+                                              dev.status, static_cast<cudaStream_t>(stream)));
+}
+
+int moe_eplb_plan(const int64_t* expert_load, int64_t E, int64_t G, int64_t n_phys, int32_t* phys_to_log,
+                  int32_t* rep_first, int32_t* rep_count, int32_t* rep_list, int64_t* rank_load) {
+  if (!expert_load || !phys_to_log || !rep_first || !rep_count || !rep_list) return MOE_ERR_INVALID_ARG;
+  if (E < 1 || G < 1 || n_phys < E || n_phys % G != 0 || n_phys > (int64_t)1 << 20) return MOE_ERR_INVALID_ARG;
+  for (int64_t e = 0; e < E; ++e)
+    if (expert_load[e] < 0) return MOE_ERR_INVALID_ARG;
+  moe::eplb_plan(expert_load, E, G, n_phys, phys_to_log, rep_first, rep_count, rep_list, rank_load);
+  return MOE_OK;
+}

@@ -1030,20 +1030,17 @@ cudaError_t run_bf16_mgrouped(const GemmParams& p, int64_t R, int64_t E, const D
 
 }  // namespace
 
-// K split of the router GEMM: the smallest divisor of its 64-wide K blocks
-// giving at least 228 tiles (1.5 per SM of a GB300); fixed by the shape
-// alone so that workspace sizes do not depend on the device.
+// K split of the router GEMM: the largest divisor of its 64-wide K blocks up
+// to 4.  It sets the order in which each logit's fp32 partial sums add up,
+// so it depends on H alone: a token's logits do not depend on how many
+// tokens are routed with it (nor the workspace size on the device).
 int router_parts(int64_t T, int64_t H, int64_t E) {
-  constexpr int bm = Traits<ROUTER, 1, 1>::kBM, bn = Traits<ROUTER, 1, 1>::kBN;
-  const int64_t tiles = ((T + bm - 1) / bm) * ((E + bn - 1) / bn);
+  (void)T;
+  (void)E;
   const int64_t kb = 3 * H / BK;          // 64-wide K blocks of the stacked split weight
-  int parts = 1;
-  for (int cand = 1; cand <= 48; ++cand) {
-    if (kb % cand) continue;
-    parts = cand;
-    if (tiles * cand >= 228) break;
-  }
-  return parts;
+  for (int cand = 4; cand > 1; --cand)
+    if (kb % cand == 0) return cand;
+  return 1;
 }
 
 int launch_router_logits(const uint16_t* x, const uint16_t* w_split, int64_t T, int64_t H, int64_t E,

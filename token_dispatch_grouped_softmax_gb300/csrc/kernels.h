@@ -103,6 +103,17 @@ cudaError_t launch_gather_dx(const uint16_t* dx_perm, const int32_t* row_map, co
 cudaError_t launch_route_bwd_weight(const uint16_t* x, const float* d_logits, int64_t T, int64_t H,
                                     int64_t E, float* d_w_router, cudaStream_t stream);
 
+// Expert-parallel dispatch pieces (ep.cu).
+size_t sort_chunks_workspace_bytes(int64_t A, int64_t B);
+cudaError_t launch_sort_chunks(const int32_t* counts, int64_t A, int64_t B, int64_t N, int32_t* src_of,
+                               int32_t* pos_of, int32_t* group_off, void* ws, uint32_t* status,
+                               cudaStream_t stream);
+cudaError_t launch_map_replicas(const int32_t* ids, int64_t R, int64_t k, int64_t E, const int32_t* rep_first,
+                                const int32_t* rep_count, const int32_t* rep_list, int64_t n_phys,
+                                int32_t* phys_ids, uint32_t* status, cudaStream_t stream);
+void eplb_plan(const int64_t* load, int64_t E, int64_t G, int64_t n_phys, int32_t* phys_to_log,
+               int32_t* rep_first, int32_t* rep_count, int32_t* rep_list, int64_t* rank_load);
+
 // Grouped GEMMs: 0 = enqueued, -1 = tensor map rejected, 1 = launch failed.
 int router_parts(int64_t T, int64_t H, int64_t E);
 int launch_router_logits(const uint16_t* x, const uint16_t* w_split, int64_t T, int64_t H, int64_t E,

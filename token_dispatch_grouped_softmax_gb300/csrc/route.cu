@@ -500,15 +500,20 @@ __global__ void __launch_bounds__(fr_threads<NV>(), 1) fused_router_kernel(const
 
 int fused_router_terms(int64_t E) { return E <= 128 ? 3 : 1; }
 
-// The cluster size: a divisor of the CTA's K blocks, at most 8 (the portable
-// cluster limit); with three terms per stage (one CTA per SM) the largest one
-// that keeps the grid within one wave of the SMs, else the largest.
-int fused_router_cluster(int64_t T, int64_t H, int64_t E, int num_sms) {
+// The cluster size, which is how K is split and so the order in which each
+// logit's fp32 partial sums add up: a function of H and E alone, so that a
+// token's logits, weights and experts do not depend on how many tokens are
+// routed with it (the same bits for a batch of 512 tokens as for 4096; an
+// expert-parallel rank routing its share of a batch gets what routing the
+// whole batch gives).  The largest divisor of the K blocks up to 4 with three
+// terms per stage (4: one wave of 128 clusters at 4096 tokens, the largest
+// count a single wave of 152 SMs takes at that size); up to 8 (the portable
+// cluster limit) with one.
+int fused_router_cluster(int64_t H, int64_t E) {
   const int terms = fused_router_terms(E);
   const int64_t kb = (terms == 3 ? 1 : 3) * H / 64;
-  const int64_t tiles = (T + 127) / 128;
-  for (int d = kFrMaxCluster; d > 1; --d)
-    if (kb % d == 0 && (terms == 1 || tiles * d <= num_sms)) return d;
+  for (int d = terms == 3 ? 4 : kFrMaxCluster; d > 1; --d)
+    if (kb % d == 0) return d;
   return 1;
 }
 
@@ -563,7 +568,7 @@ cudaError_t launch_fused_router(const uint16_t* x, const uint16_t* w_split, cons
     const cuuint32_t box[2] = {64, 64};
     if (!encode_tensor_map_2d_bf16(&p.tmB, w_split, dims, strides, box, estr)) return cudaErrorInvalidValue;
   }
-  const int P = fused_router_cluster(T, H, E, dev.num_sms);
+  const int P = fused_router_cluster(H, E);
   p.bias = bias;
   p.ids = ids;
   p.w = w;

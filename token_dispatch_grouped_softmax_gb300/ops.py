@@ -162,12 +162,68 @@ def permute(ids, E, w=None):
     return counts, offsets, row_map, src_row
 
 
-def permute_rows(x, src_row):
+def permute_rows(x, src_row, out=None):
+    """out[r] = x[src_row[r]] for every row r (bf16 rows of width H); out: an
+    existing contiguous [R, H] bf16 tensor (or row slice) to write into."""
     _need(x, "x", _BF16, 2)
     _need(src_row, "src_row", torch.int32, 1)
     R, H = src_row.shape[0], x.shape[1]
-    out = torch.empty((R, H), dtype=_BF16, device=x.device)
+    if out is None:
+        out = torch.empty((R, H), dtype=_BF16, device=x.device)
+    else:
+        _need(out, "out", _BF16, 2)
+        if tuple(out.shape) != (R, H):
+            raise ValueError("out must be [R, H]")
     call("moe_permute_rows", _p(x), _p(src_row), R, H, _p(out), _stream())
+    return out
+
+
+def sort_chunks(counts, N):
+    """Rows arriving as an A x B chunk matrix in (a, b) order -> (b, a) order
+    (moe_sort_chunks): src_of [N], pos_of [N] and group_offsets [B+1] (int32).
+    counts: [A, B] int32 on the device, summing to N."""
+    _need(counts, "counts", torch.int32, 2)
+    A, B = counts.shape
+    dev = counts.device
+    src_of = torch.empty(N, dtype=torch.int32, device=dev)
+    pos_of = torch.empty(N, dtype=torch.int32, device=dev)
+    group = torch.empty(B + 1, dtype=torch.int32, device=dev)
+    nbytes = ctypes.c_size_t(0)
+    call("moe_sort_chunks_workspace_size", A, B, ctypes.byref(nbytes))
+    ws = _ws(nbytes.value, dev)
+    call("moe_sort_chunks", _p(counts), A, B, N, _p(src_of), _p(pos_of), _p(group), _p(ws), ws.numel(), _stream())
+    return src_of, pos_of, group
+
+
+def ep_map_replicas(ids, rep_first, rep_count, rep_list):
+    """Logical expert ids [T, k] -> physical replica ids [T, k] (moe_ep_map_replicas);
+    the plan tensors are int32 on the device."""
+    _need(ids, "ids", torch.int32, 2)
+    for t, n in ((rep_first, "rep_first"), (rep_count, "rep_count"), (rep_list, "rep_list")):
+        _need(t, n, torch.int32, 1)
+    T, k = ids.shape
+    E, n_phys = rep_first.shape[0], rep_list.shape[0]
+    out = torch.empty_like(ids)
+    call("moe_ep_map_replicas", _p(ids), T, k, E, _p(rep_first), _p(rep_count), _p(rep_list), n_phys, _p(out),
+         _stream())
+    return out
+
+
+def eplb_plan(expert_load, G, n_phys):
+    """EPLB-style replication and placement on the host (moe_eplb_plan).
+    expert_load: per-expert loads (sequence of ints); returns a dict of numpy
+    arrays phys_to_log [n_phys], rep_first [E], rep_count [E], rep_list
+    [n_phys] (int32) and rank_load [G] (int64)."""
+    import numpy as np
+
+    load = np.ascontiguousarray(np.asarray(expert_load, dtype=np.int64))
+    E = load.shape[0]
+    out = dict(phys_to_log=np.empty(n_phys, np.int32), rep_first=np.empty(E, np.int32),
+               rep_count=np.empty(E, np.int32), rep_list=np.empty(n_phys, np.int32),
+               rank_load=np.empty(G, np.int64))
+    ptr = lambda a: ctypes.c_void_p(a.ctypes.data)
+    call("moe_eplb_plan", ptr(load), E, G, n_phys, ptr(out["phys_to_log"]), ptr(out["rep_first"]),
+         ptr(out["rep_count"]), ptr(out["rep_list"]), ptr(out["rank_load"]))
     return out
 
 
@@ -216,8 +272,8 @@ def grouped_gemm_down(h, offsets, down, H):
     return y
 
 
-def unpermute_combine(y_perm, row_map, w, y_shared=None):
-    """y [T, H] bf16."""
+def unpermute_combine(y_perm, row_map, w, y_shared=None, out=None):
+    """y [T, H] bf16 (out: an existing contiguous [T, H] bf16 tensor or row slice to write)."""
     _need(y_perm, "y_perm", _BF16, 2)
     _need(row_map, "row_map", torch.int32, 1)
     _need(w, "w", torch.float32, 2)
@@ -225,7 +281,13 @@ def unpermute_combine(y_perm, row_map, w, y_shared=None):
         _need(y_shared, "y_shared", _BF16, 2)
     T, k = w.shape
     H = y_perm.shape[1]
-    y = torch.empty((T, H), dtype=_BF16, device=y_perm.device)
+    if out is None:
+        y = torch.empty((T, H), dtype=_BF16, device=y_perm.device)
+    else:
+        _need(out, "out", _BF16, 2)
+        if tuple(out.shape) != (T, H):
+            raise ValueError("out must be [T, H]")
+        y = out
     call("moe_unpermute_combine", _p(y_perm), _p(row_map), _p(w), _p(y_shared), T, H, k, _p(y), _stream())
     return y
 
