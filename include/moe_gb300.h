@@ -84,16 +84,18 @@ int moe_sync_status(void* stream, uint32_t* detail);
  * default.  Not thread-safe against concurrent launches. */
 int moe_set_wait_limit_ns(uint64_t ns);
 
-/* Where the forward and dgrad grouped GEMMs run: on single CTAs (128- or
- * 256-row tiles) or on CTA pairs (clusters of two CTAs issuing 2-SM tcgen05
- * MMAs on 256-row tiles, 128-row tails as M = 128 pair MMAs; each CTA holds
- * half of every operand tile).  mode 0: single CTAs everywhere; 1: pairs for
- * every forward and dgrad grouped GEMM; 2 (default): pairs for the forward
- * gate_up GEMM only.  Results are bit-identical in every mode.  Mode 2 is
- * the fastest measured on GB300 at the Qwen3-MoE shape (the pairs' tile count
- * fills whole waves there; the down GEMM measured 3 us slower on pairs).
- * Another mode returns MOE_ERR_INVALID_ARG.  Applies to launches after the
- * call; not thread-safe against them. */
+/* Where the grouped GEMMs run: on single CTAs (128- or 256-row tiles) or on
+ * CTA pairs (clusters of two CTAs issuing 2-SM tcgen05 MMAs on 256-row
+ * tiles, 128-row tails as M = 128 pair MMAs; each CTA holds half of every
+ * operand tile).  mode 0: single CTAs everywhere; 1: pairs for every forward
+ * and dgrad grouped GEMM; 2 (default): pairs for the forward gate_up GEMM
+ * only; 3: pairs for the forward gate_up GEMM and the two weight-gradient
+ * GEMMs (whose expert K tails rank 0 of each pair zeroes in both CTAs'
+ * shared memory).  Results are bit-identical in every mode.  Mode 2 is the
+ * fastest measured on GB300 at the Qwen3-MoE shapes (the pairs' gate_up tile
+ * count fills whole waves there; down and the backward GEMMs measured slower
+ * on pairs).  Another mode returns MOE_ERR_INVALID_ARG.  Applies to launches
+ * after the call; not thread-safe against them. */
 int moe_set_gemm_pairs(int mode);
 
 /* Programmatic dependent launch: 1 (default) launches every kernel so that it
@@ -179,10 +181,13 @@ int moe_permute_workspace_size(int64_t T, int64_t k, int64_t E, size_t* bytes);
  *                                rows of one expert keep increasing i
  *   src_row  [R] int32 (out)     token of each permuted row (= i / k)
  *   w_perm   [R] fp32 (out) or NULL   w_perm[row_map[i]] = w[i]
- * Deterministic (no order-dependent atomics).  When all of its blocks fit on
- * the device at once (R up to about 300k assignments on a GB300) it is one
+ * Deterministic (no order-dependent atomics).  Up to 2^18 assignments and
+ * E <= 256 it is one launch of clusters of 8 CTAs that share their counts
+ * through distributed shared memory (no waits beyond the hardware cluster
+ * barrier; the workspace is not used).  Otherwise, when all of its blocks
+ * fit on the device at once (R up to about 300k assignments on a GB300), one
  * cooperative launch whose two grid barriers are bounded waits
- * (MOE_ERR_TIMEOUT in the status word if one runs out); otherwise three
+ * (MOE_ERR_TIMEOUT in the status word if one runs out); else three
  * launches.  An id outside [0, E) sets MOE_ERR_DEVICE in the status word;
  * the outputs are then undefined.  A misaligned workspace returns
  * MOE_ERR_INVALID_ARG.  Limits: E <= 1024, R < 2^31. */

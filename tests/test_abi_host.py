@@ -45,11 +45,12 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_gemm_pairs_modes(lib):
-    """0 single CTAs, 1 pairs everywhere, 2 (default) pairs for gate_up only."""
+    """0 single CTAs, 1 pairs for the forward and dgrad GEMMs, 2 pairs for
+    gate_up only, 3 gate_up and the weight-gradient GEMMs."""
     try:
-        for mode in (0, 1, 2):
+        for mode in (0, 1, 2, 3):
             assert lib.moe_set_gemm_pairs(mode) == 0
-        assert lib.moe_set_gemm_pairs(3) == INVALID
+        assert lib.moe_set_gemm_pairs(4) == INVALID
         assert lib.moe_set_gemm_pairs(-1) == INVALID
     finally:
         lib.moe_set_gemm_pairs(2)

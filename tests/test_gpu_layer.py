@@ -368,13 +368,14 @@ def test_forward_graph_replays_match_forward():
 @pytest.mark.parametrize("T,H,E,k,I", SMALL + [(4096, 256, 16, 2, 192)])
 def test_cta_pairs_bit_identical(T, H, E, k, I, fused):
     """The grouped GEMMs on CTA pairs (2-SM MMAs, 256-row tiles, M = 128 pair
-    MMAs for tails of up to 128 rows) give the single-CTA results bit for bit:
-    forward with saved activations and the whole backward."""
+    MMAs for tails of up to 128 rows; the weight-gradient GEMMs with their K
+    tails zeroed by each CTA of the pair) give the single-CTA results bit for
+    bit: forward with saved activations and the whole backward."""
     import torch
     moe = lib()
     cfg, inp = _inputs(T, H, E, k, I, seed=5 * T + I)
     outs = []
-    for pairs in (False, True):
+    for pairs in (moe.GEMM_PAIRS_NONE, moe.GEMM_PAIRS_ALL, moe.GEMM_PAIRS_GATE_UP_WGRAD):
         moe.set_gemm_pairs(pairs)
         try:
             (x, wr, gu, dn), y, st = _forward(moe, inp, save=True, fused=fused)
@@ -383,8 +384,9 @@ def test_cta_pairs_bit_identical(T, H, E, k, I, fused):
         finally:
             moe.set_gemm_pairs(moe.GEMM_PAIRS_GATE_UP)
         outs.append([y, st.h, st.gu_pre, st.h_w, st.y_perm] + [g[n] for n in sorted(g)])
-    for a, b in zip(*outs):
-        assert torch_equal(a, b)
+    for other in outs[1:]:
+        for a, b in zip(outs[0], other):
+            assert torch_equal(a, b)
 
 
 @pytest.mark.parametrize("T,H,E,k,I", [(300, 384, 6, 3, 320), (1100, 256, 4, 2, 128)])
@@ -472,3 +474,44 @@ def test_grouped_gemms_at_tile_edges(H, I, counts, pairs):
         moe.set_gemm_pairs(moe.GEMM_PAIRS_GATE_UP)
     assert_close("h", f64(h), ref["h_perm"])
     assert_close("y_perm", f64(y), ref["y_perm"])
+
+
+@pytest.mark.parametrize("counts", [TILE_EDGE_COUNTS, HEAVY_COUNTS], ids=["edges", "heavy"])
+@pytest.mark.parametrize("H,I", [(256, 192), (320, 128)])
+def test_weight_gradients_at_tile_edges(H, I, counts):
+    """The weight-gradient GEMMs, whose K is an expert's rows, on expert sizes
+    either side of every 64-row K block (and empty experts): on single CTAs
+    (two 128-row halves) and on CTA pairs (each CTA zeroes its own stage's
+    rows past the expert), bit for bit the same; and against the expert
+    blocks of the oracle's backward (identity permutation, k = 1).  H = 320
+    and I = 192 leave the last 256-row tile with 64 rows, which the second
+    CTA of a pair has none of."""
+    import torch
+    moe = lib()
+    E, R = len(counts), sum(counts)
+    offs = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    x = synth.normal_bf16(R + I, synth.TID_X, (R, H), 1.0)
+    gu = synth.normal_bf16(R + I, synth.TID_GATE_UP, (E * H, 2 * I), H ** -0.5)
+    dn = synth.normal_bf16(R + I, synth.TID_DOWN, (E * I, H), I ** -0.5)
+    dy = synth.normal_bf16(R + I, synth.TID_DY, (R, H), 1.0)
+    ids = np.repeat(np.arange(E, dtype=np.int32), counts).reshape(R, 1)
+    w1 = np.ones((R, 1))
+    ref = oracle.backward(x, np.zeros((H, E), np.float32), gu, dn, ids, w1, dy)
+    xb, dyb = bf(x), bf(dy)
+    outs = []
+    for pairs in (moe.GEMM_PAIRS_GATE_UP, moe.GEMM_PAIRS_GATE_UP_WGRAD):
+        moe.set_gemm_pairs(pairs)
+        try:
+            w_perm = torch.ones(R, dtype=torch.float32, device=xb.device)
+            h, gu_pre, h_w = moe.grouped_gemm_gate_up_swiglu(xb, None, i32(offs), bf(gu), I, w_perm=w_perm,
+                                                             save_for_backward=True)
+            dgu, d_down, _ = moe.grouped_gemm_down_bwd(dyb, h_w, gu_pre, w_perm, i32(offs), bf(dn))
+            _, d_gu = moe.grouped_gemm_gate_up_bwd(dgu, xb, None, i32(offs), bf(gu))
+            moe.sync_status()
+        finally:
+            moe.set_gemm_pairs(moe.GEMM_PAIRS_GATE_UP)
+        outs.append((d_down, d_gu))
+    for a, b in zip(*outs):
+        assert torch_equal(a, b)
+    assert_close("d_down", f64(outs[1][0]), ref["d_down"])
+    assert_close("d_gate_up", f64(outs[1][1]), ref["d_gate_up"])

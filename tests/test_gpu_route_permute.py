@@ -118,11 +118,14 @@ def test_route_exact_ties_lower_index_first():
 @pytest.mark.parametrize("T,k,E,kind", [(64, 2, 8, "distinct"), (1, 1, 1, "distinct"), (4096, 8, 128, "distinct"),
                                         (5000, 3, 7, "uniform"), (777, 8, 1024, "distinct"),
                                         (16384, 8, 256, "distinct"), (3000, 4, 64, "sparse"),
+                                        (32768, 8, 256, "distinct"), (33000, 8, 128, "distinct"),
                                         (45000, 8, 128, "distinct")])
 def test_permute_bit_exact(T, k, E, kind):
-    """The one-launch cooperative permute, and (T = 45000, R = 360k: more
-    256-assignment blocks than fit on the device at once) its three-launch
-    fallback."""
+    """Every launch path of the permute: the cluster launch (R <= 2^18 and
+    E <= 256; T = 32768, k = 8 is its largest size, 2048-assignment chunks),
+    the one-launch cooperative permute (E = 1024; R = 264k), and (T = 45000,
+    R = 360k: more 256-assignment blocks than fit on the device at once) the
+    three-launch fallback."""
     moe = lib()
     if kind == "distinct":
         ids = synth.distinct_ids(T + k, synth.TID_IDS, T, k, E)

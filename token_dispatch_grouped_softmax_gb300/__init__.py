@@ -8,7 +8,7 @@ memory, streams) into the C entry points.  Nothing here computes the layer.
 """
 from ._build import build, up_to_date
 from ._lib import MoEError, lib_path, load
-from .ops import (GEMM_PAIRS_ALL, GEMM_PAIRS_GATE_UP, GEMM_PAIRS_NONE, gather_dx, grouped_gemm_down,
+from .ops import (GEMM_PAIRS_ALL, GEMM_PAIRS_GATE_UP, GEMM_PAIRS_GATE_UP_WGRAD, GEMM_PAIRS_NONE, gather_dx, grouped_gemm_down,
                   grouped_gemm_down_bwd, grouped_gemm_gate_up_bwd, grouped_gemm_gate_up_swiglu, permute,
                   permute_rows, route, route_bwd, route_bwd_weight, route_split_weight, route_supports_split, set_gemm_pairs, set_pdl, set_wait_limit_ns,
                   sync_status, unpermute_combine, unpermute_combine_bwd)
@@ -22,7 +22,7 @@ __all__ = [
     "route", "route_split_weight", "route_supports_split", "permute", "permute_rows", "grouped_gemm_gate_up_swiglu", "grouped_gemm_down",
     "unpermute_combine", "unpermute_combine_bwd", "route_bwd", "grouped_gemm_down_bwd",
     "grouped_gemm_gate_up_bwd", "gather_dx", "route_bwd_weight", "sync_status", "set_wait_limit_ns", "set_gemm_pairs",
-    "GEMM_PAIRS_NONE", "GEMM_PAIRS_ALL", "GEMM_PAIRS_GATE_UP",
+    "GEMM_PAIRS_NONE", "GEMM_PAIRS_ALL", "GEMM_PAIRS_GATE_UP", "GEMM_PAIRS_GATE_UP_WGRAD",
     "set_pdl", "sort_chunks", "ep_map_replicas", "eplb_plan", "ep",
     "ForwardGraph", "ForwardState", "MoELayer", "OverlappedForward", "MoELayerFunction", "PipelinedForward", "moe_forward", "moe_backward",
 ]

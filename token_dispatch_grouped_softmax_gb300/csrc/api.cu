@@ -110,7 +110,7 @@ int moe_set_wait_limit_ns(uint64_t ns) {
 }
 
 int moe_set_gemm_pairs(int mode) {
-  if (mode < 0 || mode > 2) return MOE_ERR_INVALID_ARG;
+  if (mode < 0 || mode > 3) return MOE_ERR_INVALID_ARG;
   moe::g_gemm_pairs = mode;
   return MOE_OK;
 }

@@ -192,6 +192,23 @@ __device__ __forceinline__ void cluster_sync_all() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
+// The two halves of the cluster barrier, for work that fits between them:
+// the arrive releases this thread's earlier accesses (loads included), the
+// wait acquires every other thread's.
+__device__ __forceinline__ void cluster_arrive_release() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait_acquire() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// int32 load from a shared::cluster address (see ld_shared_cluster_f32).
+__device__ __forceinline__ int32_t ld_shared_cluster_s32(uint32_t addr) {
+  int32_t v;
+  asm volatile("ld.shared::cluster.s32 %0, [%1];" : "=r"(v) : "r"(addr));
+  return v;
+}
+
 // The shared::cluster address of this CTA's shared-memory location `addr`
 // in CTA `rank` of the cluster.
 __device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
@@ -321,6 +338,18 @@ __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
 // async proxy (TMA and the tensor cores).
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// The same for every state space (shared::cluster included).
+__device__ __forceinline__ void fence_proxy_async_all() { asm volatile("fence.proxy.async;" ::: "memory"); }
+
+// Orders this thread's earlier memory accesses at cluster scope (stores into
+// another CTA's shared memory before what the thread does next).
+__device__ __forceinline__ void fence_acq_rel_cluster() { asm volatile("fence.acq_rel.cluster;" ::: "memory"); }
+
+// 16 zero bytes to a shared::cluster address (possibly another CTA's memory).
+__device__ __forceinline__ void st_shared_cluster_zero16(uint32_t addr) {
+  asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %1, %1, %1};" ::"r"(addr), "r"(0u) : "memory");
 }
 
 // ---------------------------------------------------------------- tcgen05

@@ -97,17 +97,17 @@ struct Traits {
   // accumulators, and for the router (few, narrow tiles: its K is split
   // instead); either for the plain bf16-store GEMMs.  A CTA pair holds one
   // half per CTA and half of each B tile, so a 256 x 256 tile moves 32 KB per
-  // CTA per K block and keeps two accumulators.  (The weight-gradient GEMMs
+  // CTA per K block and keeps two accumulators.  The weight-gradient GEMMs
   // zero a tile's K rows past its expert in shared memory once the copies
-  // have landed, which the second CTA of a pair cannot see: they run on
-  // single CTAs.)
+  // have landed; in a pair rank 0's MMA warp zeroes both CTAs' stages (the
+  // second CTA's through distributed shared memory).
   static_assert(KH == 1 || KH == 2, "one or two halves");
   static_assert(CG == 1 || CG == 2, "one CTA or a pair");
   static_assert(KH == 1 || (MODE != FWD_GATEUP && MODE != DGRAD_DOWN && MODE != ROUTER),
                 "per-element epilogues use one half");
-  static_assert(CG == 1 || (KH == 1 && MODE != ROUTER && MODE != WGRAD_DOWN && MODE != WGRAD_GATEUP),
-                "a pair holds one half per CTA; the router and wgrad run on single CTAs");
-  static_assert(KH == 2 || (MODE != WGRAD_DOWN && MODE != WGRAD_GATEUP), "wgrad uses 256-row tiles");
+  static_assert(CG == 1 || (KH == 1 && MODE != ROUTER), "a pair holds one half per CTA; the router runs on single CTAs");
+  static_assert(KH == 2 || CG == 2 || (MODE != WGRAD_DOWN && MODE != WGRAD_GATEUP),
+                "wgrad uses 256-row tiles (two halves, or a pair)");
   static constexpr int kH = KH;
   static constexpr int kBM = kH * BMH * CG;          // rows of a tile
   static constexpr int kAccBufs = 2 / kH;
@@ -433,6 +433,28 @@ __device__ __forceinline__ void zero_k_tail(uint8_t* stage, int kvalid, int lane
   __syncwarp();
 }
 
+// The same for a CTA pair, from rank 0's MMA warp once both CTAs' copies of
+// the stage have landed: its own stage, and the second CTA's (same offset in
+// that CTA's shared memory) through distributed shared memory.  The writes
+// are made visible at cluster scope and to the tensor cores' async proxy
+// before the pair MMA that reads both stages is issued.
+template <int STAGE_BYTES>
+__device__ __forceinline__ void zero_k_tail_pair(uint8_t* stage, int kvalid, int lane) {
+  constexpr int kChunks = STAGE_BYTES / MN_CHUNK_BYTES;
+  uint8_t* unit = stage + (lane & 7) * 16;
+  const uint32_t peer = mapa_shared(smem_u32(unit), 1);
+#pragma unroll
+  for (int chunk = 0; chunk < kChunks; ++chunk)
+    for (int row = kvalid + (lane >> 3); row < BK; row += 4) {
+      const int off = chunk * MN_CHUNK_BYTES + row * 128;
+      *reinterpret_cast<uint4*>(unit + off) = make_uint4(0, 0, 0, 0);
+      st_shared_cluster_zero16(peer + (uint32_t)off);
+    }
+  fence_acq_rel_cluster();
+  fence_proxy_async_all();
+  __syncwarp();
+}
+
 template <int MODE, int KH, int CG>
 __global__ void __launch_bounds__(Traits<MODE, KH, CG>::kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ GemmParams p) {
@@ -627,8 +649,10 @@ __global__ void __launch_bounds__(Traits<MODE, KH, CG>::kThreads, 1)
         if (!ok) break;
         const uint32_t sA = ring_u32 + stage * Tr::kStageBytes;
         const uint32_t sB = sA + Tr::kABytes;
-        if (Tr::kKGrouped && t.rows - kb * BK < BK)   // K rows past the expert's last row
-          zero_k_tail<Tr::kStageBytes>(ring + stage * Tr::kStageBytes, t.rows - kb * BK, lane);
+        if (Tr::kKGrouped && t.rows - kb * BK < BK) {   // K rows past the expert's last row
+          if (kPair) zero_k_tail_pair<Tr::kStageBytes>(ring + stage * Tr::kStageBytes, t.rows - kb * BK, lane);
+          else zero_k_tail<Tr::kStageBytes>(ring + stage * Tr::kStageBytes, t.rows - kb * BK, lane);
+        }
         tc_fence_after();
         if (lane == 0) {
 #pragma unroll
@@ -1010,9 +1034,13 @@ int64_t mgrouped_tile_bound(int64_t R, int64_t E, int nt) {
 }
 
 // CTA pairs (2-SM MMAs, 256-row tiles with 128-row tails) for the M-grouped
-// GEMMs as selected by moe_set_gemm_pairs: mode 1 for all of them, mode 2
-// (the default) for the forward gate_up GEMM only.
-bool use_pair(const DeviceInfo& dev, bool gate_up) { return dev.gemm_pairs == 1 || (gate_up && dev.gemm_pairs == 2); }
+// GEMMs as selected by moe_set_gemm_pairs: mode 1 for all of them, modes 2
+// and 3 for the forward gate_up GEMM only; and for the weight-gradient GEMMs
+// (256-row tiles: two halves on one CTA, or one per CTA of a pair) in mode 3.
+bool use_pair(const DeviceInfo& dev, bool gate_up) {
+  return dev.gemm_pairs == 1 || (gate_up && (dev.gemm_pairs == 2 || dev.gemm_pairs == 3));
+}
+bool use_pair_wgrad(const DeviceInfo& dev) { return dev.gemm_pairs == 3; }
 
 // Single-CTA M-grouped GEMMs with a plain bf16 epilogue take 256-row tiles
 // once experts average 512 rows or more, else 128-row tiles: with few row
@@ -1139,7 +1167,9 @@ int launch_gemm_down_bwd(const uint16_t* dy_perm, const uint16_t* h_w, const flo
     p.mt_w = (int)((I + 2 * BMH - 1) / (2 * BMH));
     p.nt = (int)((H + BN - 1) / BN);
     p.ldo = H;
-    if (run_gemm<WGRAD_DOWN, 2, 1>(p, E * p.mt_w * p.nt, dev, stream) != cudaSuccess) return 1;
+    const cudaError_t err = use_pair_wgrad(dev) ? run_gemm<WGRAD_DOWN, 1, 2>(p, E * p.mt_w * p.nt, dev, stream)
+                                                : run_gemm<WGRAD_DOWN, 2, 1>(p, E * p.mt_w * p.nt, dev, stream);
+    if (err != cudaSuccess) return 1;
   }
   return 0;
 }
@@ -1179,7 +1209,9 @@ int launch_gemm_gate_up_bwd(const uint16_t* dgu, const uint16_t* x, const int32_
     p.mt_w = (int)((H + 2 * BMH - 1) / (2 * BMH));
     p.nt = (int)((2 * I + BN - 1) / BN);
     p.ldo = 2 * I;
-    if (run_gemm<WGRAD_GATEUP, 2, 1>(p, E * p.mt_w * p.nt, dev, stream) != cudaSuccess) return 1;
+    const cudaError_t err = use_pair_wgrad(dev) ? run_gemm<WGRAD_GATEUP, 1, 2>(p, E * p.mt_w * p.nt, dev, stream)
+                                                : run_gemm<WGRAD_GATEUP, 2, 1>(p, E * p.mt_w * p.nt, dev, stream);
+    if (err != cudaSuccess) return 1;
   }
   return 0;
 }

@@ -56,7 +56,8 @@ struct DeviceInfo {
   uint32_t* status;        // device address of the status word
   uint64_t wait_limit_ns;  // bound of every device-side spin wait
   int test_stall_producer; // test hook of the bounded-wait path (grouped GEMMs)
-  int gemm_pairs;          // CTA pairs: 0 none, 1 every forward / dgrad grouped GEMM, 2 forward gate_up only
+  int gemm_pairs;          // CTA pairs: 0 none, 1 every forward / dgrad grouped GEMM, 2 forward gate_up only,
+                           // 3 forward gate_up and the weight-gradient GEMMs
 };
 
 // Device information of the current device (status word address, SM count).

@@ -361,6 +361,168 @@ __global__ void __launch_bounds__(kPermThreads) permute_fused_kernel(
   }
 }
 
+// One launch without a grid-wide barrier, for up to kClusterPermuteMaxR
+// assignments and E <= kPermThreads: clusters of kPermCluster CTAs.  CTA b
+// ranks chunk b (`chunk` assignments); the chunks of cluster c form group c.
+// Every cluster counts every group, its CTA r taking groups r, r + 8, ...
+// (one histogram each, in its shared memory), so after one cluster barrier
+// each CTA reads from its cluster's shared memory the per-expert totals and
+// the counts before its chunk: the groups before its cluster's, then the
+// chunks of the lower CTAs of its own cluster.  Each CTA thus counts R / 8
+// ids plus its chunk, and no CTA waits for one outside its cluster.
+constexpr int kPermCluster = 8;
+constexpr int kPermMaxSlots = 2;   // groups counted per CTA, so at most 16 clusters
+constexpr int64_t kClusterPermuteMaxR = int64_t(1) << 18;
+
+__global__ void __launch_bounds__(kPermThreads) permute_cluster_kernel(
+    const int32_t* __restrict__ ids, const float* __restrict__ w, int64_t R, int k, int E, int chunk,
+    int32_t* __restrict__ counts, int32_t* __restrict__ offsets, int32_t* __restrict__ row_map,
+    int32_t* __restrict__ src_row, float* __restrict__ w_perm, uint32_t* status) {
+  pdl_wait();
+  pdl_trigger();
+  // [kPermMaxSlots][E] group counts | [kPermWarps][E] warp counts, then bases |
+  // [E] chunk counts | [E] totals, then offsets | [E] counts before the chunk | [40] scan
+  extern __shared__ int32_t sh[];
+  int32_t* ghist = sh;
+  int32_t* wcnt = ghist + kPermMaxSlots * E;
+  int32_t* chist = wcnt + kPermWarps * E;
+  int32_t* off = chist + E;
+  int32_t* pre = off + E;
+  int32_t* wtot = pre + E;
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  const int r = (int)cluster_ctarank();
+  const int c = (int)(blockIdx.x / kPermCluster);
+  const int nclus = (int)(gridDim.x / kPermCluster);
+  const int per_warp = chunk / kPermWarps;
+  const int64_t slice0 = (int64_t)blockIdx.x * chunk + (int64_t)wid * per_warp;
+  const int64_t group_len = (int64_t)kPermCluster * chunk;
+
+  for (int q = threadIdx.x; q < (kPermMaxSlots + kPermWarps) * E; q += kPermThreads) sh[q] = 0;
+  __syncthreads();
+  // 1. this chunk, per warp; the ids are checked here
+  for (int s = 0; s < per_warp; s += 32) {
+    const int64_t i = slice0 + s + lane;
+    if (i < R) {
+      const int e = ids[i];
+      if (e < 0 || e >= E) report_status(status, kStatusDevice, kKernPermute, 1);
+      else atomicAdd(&wcnt[wid * E + e], 1);   // counts only: the order of increments is irrelevant
+    }
+  }
+  // 2. this CTA's groups, eight loads in flight per thread
+  for (int j = 0; j < kPermMaxSlots; ++j) {
+    const int g = r + kPermCluster * j;
+    if (g >= nclus) break;
+    const int64_t g0 = (int64_t)g * group_len;
+    const int64_t g1 = g0 + group_len < R ? g0 + group_len : R;
+    int32_t* hj = ghist + j * E;
+    int64_t i = g0 + threadIdx.x;
+    for (; i + 7 * kPermThreads < g1; i += 8 * kPermThreads) {
+      int e[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) e[u] = ids[i + u * kPermThreads];
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        if ((unsigned)e[u] < (unsigned)E) atomicAdd(&hj[e[u]], 1);
+    }
+    for (; i < g1; i += kPermThreads) {
+      const int e = ids[i];
+      if ((unsigned)e < (unsigned)E) atomicAdd(&hj[e], 1);
+    }
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += kPermThreads) {
+    int32_t s = 0;
+    for (int w2 = 0; w2 < kPermWarps; ++w2) s += wcnt[w2 * E + e];
+    chist[e] = s;
+  }
+  // 3. every histogram of the cluster is complete: totals, and the counts
+  //    before this chunk, summed in a fixed order from the cluster's CTAs
+  cluster_sync_all();
+  const uint32_t ghist_u32 = smem_u32(ghist), chist_u32 = smem_u32(chist);
+  for (int q = threadIdx.x; q < 2 * E; q += kPermThreads) {
+    const int e = q < E ? q : q - E;
+    const int ng = q < E ? nclus : c;
+    int32_t s = 0;
+    for (int g = 0; g < ng; ++g)
+      s += ld_shared_cluster_s32(
+          mapa_shared(ghist_u32 + 4u * (uint32_t)((g / kPermCluster) * E + e), (uint32_t)(g % kPermCluster)));
+    if (q < E) {
+      off[e] = s;
+    } else {
+      for (int r2 = 0; r2 < r; ++r2) s += ld_shared_cluster_s32(mapa_shared(chist_u32 + 4u * (uint32_t)e, (uint32_t)r2));
+      pre[e] = s;
+    }
+  }
+  // this CTA's reads of the others' memory are done; it waits for theirs
+  // before it leaves (the wait at the end)
+  cluster_arrive_release();
+  __syncthreads();
+  // 4. offsets: exclusive scan of the totals (E <= kPermThreads, one per thread)
+  {
+    const int e = threadIdx.x;
+    const int32_t v = e < E ? off[e] : 0;
+    int32_t incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int32_t n = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += n;
+    }
+    if (lane == 31) wtot[wid] = incl;
+    __syncthreads();
+    if (wid == 0) {
+      const int32_t t = lane < kPermWarps ? wtot[lane] : 0;
+      int32_t s2 = t;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int32_t n = __shfl_up_sync(0xffffffffu, s2, o);
+        if (lane >= o) s2 += n;
+      }
+      if (lane < kPermWarps) wtot[lane] = s2 - t;
+    }
+    __syncthreads();
+    const int32_t ex = wtot[wid] + incl - v;
+    if (e < E) {
+      off[e] = ex;
+      if (blockIdx.x == 0) {
+        counts[e] = v;
+        offsets[e] = ex;
+        if (e == E - 1) offsets[E] = ex + v;
+      }
+    }
+    __syncthreads();
+  }
+  // 5. warp bases: offsets[e] + the counts before the chunk + lower warps'
+  for (int e = threadIdx.x; e < E; e += kPermThreads) {
+    int32_t run = off[e] + pre[e];
+    for (int w2 = 0; w2 < kPermWarps; ++w2) {
+      const int32_t n = wcnt[w2 * E + e];
+      wcnt[w2 * E + e] = run;
+      run += n;
+    }
+  }
+  __syncthreads();
+  // 6. stable ranking inside each warp's slice (as permute_scatter_kernel)
+  int32_t* my = wcnt + wid * E;
+  for (int s = 0; s < per_warp; s += 32) {
+    const int64_t i = slice0 + s + lane;
+    const bool valid = i < R;
+    int e = valid ? ids[i] : -1;
+    if (e < 0 || e >= E) e = E + lane;
+    const uint32_t peers = __match_any_sync(0xffffffffu, e);
+    const uint32_t lower = peers & ((1u << lane) - 1u);
+    if (e < E) {
+      const int32_t row = my[e] + __popc(lower);
+      row_map[i] = row;
+      src_row[row] = (int32_t)(i / k);
+      if (w_perm) w_perm[row] = w[i];
+    }
+    __syncwarp();
+    if (e < E && (peers >> lane) == 1u) my[e] += __popc(peers);
+    __syncwarp();
+  }
+  cluster_wait_acquire();
+}
+
 // src_rows: rows of x (a source row outside [0, src_rows) is reported and
 // row 0 read instead), or 0: unchecked.
 __global__ void permute_rows_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ src_row,
@@ -441,6 +603,16 @@ cudaError_t launch_permute(const int32_t* ids, const float* w, int64_t T, int64_
   int32_t* hist = static_cast<int32_t*>(ws);
   const int64_t R = T * k;
   const int64_t nb = (R + kChunk - 1) / kChunk;
+  if (!noalloc && R > 0 && R <= kClusterPermuteMaxR && E <= kPermThreads) {
+    // one cluster launch: chunks of 256 x m assignments, at most 128 of them
+    constexpr int64_t kMaxChunks = (int64_t)kPermCluster * kPermCluster * kPermMaxSlots;
+    const int64_t chunk = kChunk * ((nb + kMaxChunks - 1) / kMaxChunks);
+    const int64_t nbc = (R + chunk - 1) / chunk;
+    const int64_t grid = (nbc + kPermCluster - 1) / kPermCluster * kPermCluster;
+    const size_t smem = ((size_t)(kPermMaxSlots + kPermWarps + 3) * E + 40) * sizeof(int32_t);
+    return launch_pdl(permute_cluster_kernel, dim3((unsigned)grid), dim3(kPermThreads), smem, stream, kPermCluster,
+                      ids, w, R, (int)k, (int)E, (int)chunk, counts, offsets, row_map, src_row, w_perm, dev.status);
+  }
   if (!noalloc && nb > 0 && nb <= permute_fused_capacity(dev, E)) {
     // one cooperative launch (every block resident), after zeroing its barrier counters
     const size_t hist_bytes = ((size_t)(nb * E * sizeof(int32_t)) + 255) & ~size_t(255);

@@ -388,9 +388,17 @@ __global__ void __launch_bounds__(fr_threads<NV>(), 1) fused_router_kernel(const
     }
   } else if (warp == 1) {
     // ------------------------------------------------------- MMA issuer
-    // D fp32, A bf16 K-major, B bf16 MN-major, N = E, M = 128
-    const uint32_t idesc = (1u << 4) | (1u << 7) | (1u << 10) | (1u << 16) | ((uint32_t)(p.E >> 3) << 17) |
-                           ((uint32_t)(128 >> 4) << 24);
+    // D fp32, A bf16 K-major, B bf16 MN-major, M = 128.  One term (K = 3H
+    // stacked): N = E.  Three terms: the stage holds the terms' 64-expert
+    // chunks side by side (term q, chunk c at q * nchunks + c), so each MMA
+    // takes up to four chunks (N = 256) into the TMEM columns of the same
+    // index; term q's partial logits are then at columns 64 q nchunks + e
+    // and the drain adds them.  Two MMAs per K step at E = 128, not three.
+    auto idesc_n = [](int n) {
+      return (1u << 4) | (1u << 7) | (1u << 10) | (1u << 16) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
+    };
+    const int nch = p.terms * p.nchunks;                   // chunks in a stage's B
+    const int per_mma = p.terms == 3 ? 4 : p.nchunks;      // chunks per MMA
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true, issued_any = false;
@@ -400,12 +408,14 @@ __global__ void __launch_bounds__(fr_threads<NV>(), 1) fused_router_kernel(const
       tc_fence_after();
       if (lane == 0) {
         const uint32_t sA = smem_u32(ring + stage * stage_bytes);
-        for (int q = 0; q < p.terms; ++q) {
-          const uint32_t sB = sA + kFrABytes + q * p.nchunks * kFrChunkBytes;
+        for (int j0 = 0; j0 < nch; j0 += per_mma) {
+          const int nj = nch - j0 < per_mma ? nch - j0 : per_mma;
+          const uint32_t idesc = idesc_n(p.terms == 3 ? 64 * nj : p.E);
+          const uint32_t sB = sA + kFrABytes + j0 * kFrChunkBytes;
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            tc_mma_bf16(tmem_base, umma_desc(sA + kk * 32, 16, 1024),
-                        umma_desc(sB + kk * 2048, kFrChunkBytes, 1024), idesc, (kb | q | kk) != 0 ? 1u : 0u);
+            tc_mma_bf16(tmem_base + 64u * (uint32_t)j0, umma_desc(sA + kk * 32, 16, 1024),
+                        umma_desc(sB + kk * 2048, kFrChunkBytes, 1024), idesc, (kb | kk) != 0 ? 1u : 0u);
         }
         tc_commit(empty_bar(stage));
       }
@@ -435,12 +445,31 @@ __global__ void __launch_bounds__(fr_threads<NV>(), 1) fused_router_kernel(const
       const int quarter = warp & 3;              // TMEM lanes 32 quarter .. +31
       const int r = quarter * 32 + lane;         // tile row of this thread
       float* prow = part + r * ldp;
-      for (int c0 = 0; c0 < p.E; c0 += 32) {   // E % 16 == 0: 4-column groups are whole
-        float v[32];
-        tmem_ld32(tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)c0, v);
+      const uint32_t lane_base = tmem_base + ((uint32_t)(quarter * 32) << 16);
+      if (p.terms == 3) {
+        // (term 0 + term 1) + term 2, 16 columns at a time
+        const uint32_t cs = 64u * (uint32_t)p.nchunks;
+        for (int c0 = 0; c0 < p.E; c0 += 16) {   // E % 16 == 0
+          float v[16], u[16];
+          tmem_ld16(lane_base + (uint32_t)c0, v);
+          tmem_ld16(lane_base + cs + (uint32_t)c0, u);
 #pragma unroll
-        for (int q = 0; q < 32; q += 4)
-          if (c0 + q < p.E) *reinterpret_cast<float4*>(prow + c0 + q) = make_float4(v[q], v[q + 1], v[q + 2], v[q + 3]);
+          for (int q = 0; q < 16; ++q) v[q] += u[q];
+          tmem_ld16(lane_base + 2u * cs + (uint32_t)c0, u);
+#pragma unroll
+          for (int q = 0; q < 16; ++q) v[q] += u[q];
+#pragma unroll
+          for (int q = 0; q < 16; q += 4)
+            *reinterpret_cast<float4*>(prow + c0 + q) = make_float4(v[q], v[q + 1], v[q + 2], v[q + 3]);
+        }
+      } else {
+        for (int c0 = 0; c0 < p.E; c0 += 32) {   // E % 16 == 0: 4-column groups are whole
+          float v[32];
+          tmem_ld32(lane_base + (uint32_t)c0, v);
+#pragma unroll
+          for (int q = 0; q < 32; q += 4)
+            if (c0 + q < p.E) *reinterpret_cast<float4*>(prow + c0 + q) = make_float4(v[q], v[q + 1], v[q + 2], v[q + 3]);
+        }
       }
     }
   }
@@ -582,7 +611,9 @@ cudaError_t launch_fused_router(const uint16_t* x, const uint16_t* w_split, cons
   p.terms = fused_router_terms(E);
   p.kblocks = (int)((p.terms == 3 ? 1 : 3) * H / 64 / P);
   p.nchunks = (int)((E + 63) / 64);
-  p.tmem_cols = E <= 32 ? 32u : E <= 64 ? 64u : E <= 128 ? 128u : 256u;
+  // three terms: 3 x 64 nchunks columns (192 or 384); one term: E
+  const int64_t cols = p.terms == 3 ? 3 * 64 * p.nchunks : E;
+  p.tmem_cols = cols <= 32 ? 32u : cols <= 64 ? 64u : cols <= 128 ? 128u : cols <= 256 ? 256u : 512u;
   // NV: logits per lane, four consecutive experts per vector
   if (E <= 128) return launch_fused_router_nv<4>(p, P, T, dev, stream);
   return launch_fused_router_nv<8>(p, P, T, dev, stream);

@@ -57,13 +57,14 @@ def set_wait_limit_ns(ns: int):
     call("moe_set_wait_limit_ns", int(ns))
 
 
-GEMM_PAIRS_NONE, GEMM_PAIRS_ALL, GEMM_PAIRS_GATE_UP = 0, 1, 2
+GEMM_PAIRS_NONE, GEMM_PAIRS_ALL, GEMM_PAIRS_GATE_UP, GEMM_PAIRS_GATE_UP_WGRAD = 0, 1, 2, 3
 
 
 def set_gemm_pairs(mode):
-    """Where the forward and dgrad grouped GEMMs run: False / GEMM_PAIRS_NONE
-    on single CTAs, True / GEMM_PAIRS_ALL all on CTA pairs (2-SM MMAs),
-    GEMM_PAIRS_GATE_UP (the default) the forward gate_up GEMM on pairs.  The
+    """Where the grouped GEMMs run: False / GEMM_PAIRS_NONE on single CTAs,
+    True / GEMM_PAIRS_ALL every forward and dgrad GEMM on CTA pairs (2-SM
+    MMAs), GEMM_PAIRS_GATE_UP the forward gate_up GEMM on pairs,
+    GEMM_PAIRS_GATE_UP_WGRAD that and the two weight-gradient GEMMs.  The
     results are bit-identical."""
     call("moe_set_gemm_pairs", int(mode))
 
