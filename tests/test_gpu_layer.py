@@ -115,6 +115,26 @@ def test_backward_elementwise(T, H, E, k, I, fused):
     assert_close("d_w_router", f64(g["d_w_router"]), b["d_w_r"], bf16_out=False)
 
 
+@pytest.mark.parametrize("T,H,E,k,I", [(200, 320, 256, 8, 64), (1000, 192, 128, 8, 64), (64, 128, 256, 12, 64),
+                                     (40, 128, 512, 6, 64)])
+def test_backward_dx_router_term_shapes(T, H, E, k, I):
+    """dX with the router term (d_logits . W_r^T on the chosen experts) and
+    d_logits against the oracle's backward at expert counts the layer tests
+    do not reach: E = 256 (k = 8 and k = 12), E = 128 with 1000 tokens, and
+    E = 512 (the split-K router)."""
+    moe = lib()
+    cfg, inp = _inputs(T, H, E, k, I, seed=11 * T + E)
+    (x, wr, gu, dn), y, st = _forward(moe, inp, save=True)
+    g = moe.moe_backward(bf(inp.dy), st, wr, gu, dn)
+    moe.sync_status()
+    r = oracle.route(inp.x, inp.w_router, None, k)
+    same, tol = compare_ids(npi(st.ids), r)
+    assert same.all(), "near-tie routing at a small shape"
+    b = oracle.backward(inp.x, inp.w_router, inp.gate_up, inp.down, r["ids"], r["w"], inp.dy, want_dw=False)
+    assert_close("d_logits", f64(g["d_logits"]), b["dlogits"], bf16_out=False)
+    assert_close("dX", f64(g["dx"]), b["dX"])
+
+
 def test_backward_empty_experts_get_zero_weight_grads():
     moe = lib()
     cfg, inp = _inputs(40, 128, 32, 1, 64, seed=5)
