@@ -12,11 +12,21 @@ Backward: combine_bwd -> down_bwd -> route_bwd -> gate_up_bwd -> gather_dx.
 """
 from __future__ import annotations
 
+import contextlib
 from dataclasses import dataclass
 
 import torch
 
 from . import ops
+
+
+def _range(name):
+    """An NVTX range around one step of the layer, so that a profiler's
+    timeline (Nsight Systems, Nsight Compute's NVTX filters) shows which
+    library call enqueued each kernel; inside a CUDA graph capture the ranges
+    mark the capture only."""
+    nvtx = getattr(torch.cuda, "nvtx", None)
+    return nvtx.range(name) if nvtx is not None else contextlib.nullcontext()
 
 
 @dataclass
@@ -52,27 +62,35 @@ def moe_forward(x, w_router, gate_up, down, k, bias=None, sh_gate_up=None, sh_do
     T, H = x.shape
     E = w_router.shape[1]
     I = down.shape[0] // E
-    ids, w = ops.route(x, w_router, k, bias, w_split=w_split)
+    with _range("moe.route"):
+        ids, w = ops.route(x, w_router, k, bias, w_split=w_split)
     w_perm = None
-    if save_for_backward:
-        counts, offsets, row_map, src_row, w_perm = ops.permute(ids, E, w)
-    else:
-        counts, offsets, row_map, src_row = ops.permute(ids, E)
+    with _range("moe.permute"):
+        if save_for_backward:
+            counts, offsets, row_map, src_row, w_perm = ops.permute(ids, E, w)
+        else:
+            counts, offsets, row_map, src_row = ops.permute(ids, E)
     x_perm = None
     if fused_gather:
-        h, gu_pre, h_w = ops.grouped_gemm_gate_up_swiglu(x, src_row, offsets, gate_up, I, w_perm=w_perm,
-                                                         save_for_backward=save_for_backward)
+        with _range("moe.gate_up"):
+            h, gu_pre, h_w = ops.grouped_gemm_gate_up_swiglu(x, src_row, offsets, gate_up, I, w_perm=w_perm,
+                                                             save_for_backward=save_for_backward)
     else:
-        x_perm = ops.permute_rows(x, src_row)
-        h, gu_pre, h_w = ops.grouped_gemm_gate_up_swiglu(x_perm, None, offsets, gate_up, I, w_perm=w_perm,
-                                                         save_for_backward=save_for_backward)
-    y_perm = ops.grouped_gemm_down(h, offsets, down, H)
+        with _range("moe.permute_rows"):
+            x_perm = ops.permute_rows(x, src_row)
+        with _range("moe.gate_up"):
+            h, gu_pre, h_w = ops.grouped_gemm_gate_up_swiglu(x_perm, None, offsets, gate_up, I, w_perm=w_perm,
+                                                             save_for_backward=save_for_backward)
+    with _range("moe.down"):
+        y_perm = ops.grouped_gemm_down(h, offsets, down, H)
     y_shared = None
     if sh_gate_up is not None:
         I_s = sh_down.shape[0]
-        hs, _, _ = ops.grouped_gemm_gate_up_swiglu(x, None, None, sh_gate_up, I_s)
-        y_shared = ops.grouped_gemm_down(hs, None, sh_down, H)
-    y = ops.unpermute_combine(y_perm, row_map, w, y_shared)
+        with _range("moe.shared_expert"):
+            hs, _, _ = ops.grouped_gemm_gate_up_swiglu(x, None, None, sh_gate_up, I_s)
+            y_shared = ops.grouped_gemm_down(hs, None, sh_down, H)
+    with _range("moe.combine"):
+        y = ops.unpermute_combine(y_perm, row_map, w, y_shared)
     st = ForwardState(x, ids, w, counts, offsets, row_map, src_row, h, y_perm, w_perm, gu_pre, h_w, x_perm,
                       y_shared)
     return y, st
@@ -85,17 +103,23 @@ def moe_backward(dy, st: ForwardState, w_router, gate_up, down, want_dw_router=F
     T, H = st.x.shape
     E = w_router.shape[1]
     k = st.w.shape[1]
-    dy_perm = ops.unpermute_combine_bwd(dy, st.src_row)
-    dgu, d_down, dw_part = ops.grouped_gemm_down_bwd(dy_perm, st.h_w, st.gu_pre, st.w_perm, st.offsets, down)
-    d_logits, dw = ops.route_bwd(dw_part, st.row_map, st.w, st.ids, E)
-    if st.x_perm is not None:
-        dx_perm, d_gate_up = ops.grouped_gemm_gate_up_bwd(dgu, st.x_perm, None, st.offsets, gate_up)
-    else:
-        dx_perm, d_gate_up = ops.grouped_gemm_gate_up_bwd(dgu, st.x, st.src_row, st.offsets, gate_up)
-    dx = ops.gather_dx(dx_perm, st.row_map, T, k, d_logits, st.ids, w_router)
+    with _range("moe.combine_bwd"):
+        dy_perm = ops.unpermute_combine_bwd(dy, st.src_row)
+    with _range("moe.down_bwd"):
+        dgu, d_down, dw_part = ops.grouped_gemm_down_bwd(dy_perm, st.h_w, st.gu_pre, st.w_perm, st.offsets, down)
+    with _range("moe.route_bwd"):
+        d_logits, dw = ops.route_bwd(dw_part, st.row_map, st.w, st.ids, E)
+    with _range("moe.gate_up_bwd"):
+        if st.x_perm is not None:
+            dx_perm, d_gate_up = ops.grouped_gemm_gate_up_bwd(dgu, st.x_perm, None, st.offsets, gate_up)
+        else:
+            dx_perm, d_gate_up = ops.grouped_gemm_gate_up_bwd(dgu, st.x, st.src_row, st.offsets, gate_up)
+    with _range("moe.gather_dx"):
+        dx = ops.gather_dx(dx_perm, st.row_map, T, k, d_logits, st.ids, w_router)
     out = dict(dx=dx, d_logits=d_logits, d_gate_up=d_gate_up, d_down=d_down, dw=dw)
     if want_dw_router:
-        out["d_w_router"] = ops.route_bwd_weight(st.x, d_logits)
+        with _range("moe.route_bwd_weight"):
+            out["d_w_router"] = ops.route_bwd_weight(st.x, d_logits)
     return out
 
 
