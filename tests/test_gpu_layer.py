@@ -535,3 +535,62 @@ def test_weight_gradients_at_tile_edges(H, I, counts):
         assert torch_equal(a, b)
     assert_close("d_down", f64(outs[1][0]), ref["d_down"])
     assert_close("d_gate_up", f64(outs[1][1]), ref["d_gate_up"])
+
+
+def _sweep_shapes(n, seed):
+    """n seeded layer shapes off the hand-picked ones: odd and prime expert
+    counts (2 to 256, so the fused router, the split-K router and the
+    cluster permute's chunk sizes all turn up), k from 1 to 8, T from 1 to
+    700 (ragged 128-row tiles and expert tails), H and I from 64 to 448."""
+    rng = np.random.default_rng(seed)
+    shapes = []
+    for _ in range(n):
+        E = int(rng.choice([2, 3, 5, 7, 12, 16, 24, 31, 48, 64, 100, 128, 160, 256]))
+        k = int(rng.integers(1, min(E, 8) + 1))
+        shapes.append((int(rng.integers(1, 701)), 64 * int(rng.integers(1, 8)), E, k, 64 * int(rng.integers(1, 8))))
+    return shapes
+
+
+@pytest.mark.parametrize("T,H,E,k,I", _sweep_shapes(16, 20261202))
+def test_seeded_shape_sweep_forward_backward(T, H, E, k, I):
+    """Forward (saving activations) and backward through the layer at seeded
+    irregular shapes, every output against the oracle: the ids bit for bit
+    up to the stated near-tie rule, the permutation bit for bit against the
+    oracle's permutation of the GPU's ids, y and all gradients element by
+    element for the experts the GPU chose."""
+    moe = lib()
+    cfg, inp = _inputs(T, H, E, k, I, seed=T * 7 + E * 13 + k)
+    (x, wr, gu, dn), y, st = _forward(moe, inp, save=True)
+    g = moe.moe_backward(bf(inp.dy), st, wr, gu, dn, want_dw_router=True)
+    moe.sync_status()
+    r = oracle.route(inp.x, inp.w_router, None, k)
+    same, tol = compare_ids(npi(st.ids), r, label="sweep")
+    assert tol <= 1
+    gids, perm = _permutation_of_gpu_ids(st, E)
+    w_ref = oracle.weights_for_ids(r["logits"], gids)
+    assert_close("w", f64(st.w), w_ref, bf16_out=False)
+    ref = oracle.forward_permuted(inp.x, inp.gate_up, inp.down, w_ref, perm, k)
+    assert_close("y", f64(y), ref)
+    b = oracle.backward(inp.x, inp.w_router, inp.gate_up, inp.down, gids, w_ref, inp.dy, want_dw=True,
+                        want_dwr=True)
+    assert_close("dX", f64(g["dx"]), b["dX"])
+    assert_close("d_logits", f64(g["d_logits"]), b["dlogits"], bf16_out=False)
+    assert_close("dw", f64(g["dw"]), b["dw"], bf16_out=False)
+    assert_close("d_w_router", f64(g["d_w_router"]), b["d_w_r"], bf16_out=False)
+    # The weight gradients are sums over an expert's rows (here as few as 1 to
+    # 14) of products with one rounded bf16 operand, dgu or w h: their
+    # allowance uses u * sum|a||b| over those products (see parity.py), from
+    # the operands as the GPU stored them (moe_backward's own deterministic
+    # calls, repeated).
+    dy_perm = moe.ops.unpermute_combine_bwd(bf(inp.dy), st.src_row)
+    dgu, _, _ = moe.ops.grouped_gemm_down_bwd(dy_perm, st.h_w, st.gu_pre, st.w_perm, st.offsets, dn)
+    moe.sync_status()
+    xp, dg, hw, dyp = f64(st.x_perm), f64(dgu), f64(st.h_w), f64(dy_perm)
+    offs = npi(st.offsets)
+    abs_gu, abs_dn = np.zeros((E * H, 2 * I)), np.zeros((E * I, H))
+    for e in range(E):
+        a, z = offs[e], offs[e + 1]
+        abs_gu[e * H:(e + 1) * H] = np.abs(xp[a:z]).T @ np.abs(dg[a:z])
+        abs_dn[e * I:(e + 1) * I] = np.abs(hw[a:z]).T @ np.abs(dyp[a:z])
+    assert_close("d_gate_up", f64(g["d_gate_up"]), b["d_gate_up"], operand_abs=abs_gu)
+    assert_close("d_down", f64(g["d_down"]), b["d_down"], operand_abs=abs_dn)
