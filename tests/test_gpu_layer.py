@@ -15,7 +15,7 @@ import pytest
 import oracle
 import synth
 from gpu_helpers import bf, f32, f64, i32, lib, npi
-from parity import TIE_TAU, assert_close, compare_ids, sample_tokens
+from parity import TIE_TAU, U_BF16, assert_close, bf16_allowance, compare_ids, sample_tokens
 
 pytestmark = pytest.mark.gpu
 
@@ -587,10 +587,21 @@ def test_seeded_shape_sweep_forward_backward(T, H, E, k, I):
     moe.sync_status()
     xp, dg, hw, dyp = f64(st.x_perm), f64(dgu), f64(st.h_w), f64(dy_perm)
     offs = npi(st.offsets)
+    own_gu, own_dn = np.zeros((E * H, 2 * I)), np.zeros((E * I, H))
     abs_gu, abs_dn = np.zeros((E * H, 2 * I)), np.zeros((E * I, H))
     for e in range(E):
         a, z = offs[e], offs[e + 1]
+        own_gu[e * H:(e + 1) * H] = xp[a:z].T @ dg[a:z]
+        own_dn[e * I:(e + 1) * I] = hw[a:z].T @ dyp[a:z]
         abs_gu[e * H:(e + 1) * H] = np.abs(xp[a:z]).T @ np.abs(dg[a:z])
         abs_dn[e * I:(e + 1) * I] = np.abs(hw[a:z]).T @ np.abs(dyp[a:z])
     assert_close("d_gate_up", f64(g["d_gate_up"]), b["d_gate_up"], operand_abs=abs_gu)
     assert_close("d_down", f64(g["d_down"]), b["d_down"], operand_abs=abs_dn)
+    # and the two GEMMs themselves: the fp64 product of their stored operands,
+    # within the bf16 store (half an ulp) and fp32 accumulation (2^-16 of
+    # sum|a||b|, far below a bf16 ulp); a row of another expert leaking into
+    # an expert's K tail would move an output by a whole product
+    for name, got, own, ab in (("d_gate_up", g["d_gate_up"], own_gu, abs_gu), ("d_down", g["d_down"], own_dn, abs_dn)):
+        err = np.abs(f64(got) - own)
+        bound = bf16_allowance(own) - U_BF16 * np.abs(own) + 2.0 ** -16 * ab
+        assert np.all(err <= bound), "%s vs its own operands: worst excess %.3g" % (name, (err - bound).max())
