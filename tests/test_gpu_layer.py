@@ -605,3 +605,30 @@ def test_seeded_shape_sweep_forward_backward(T, H, E, k, I):
         err = np.abs(f64(got) - own)
         bound = bf16_allowance(own) - U_BF16 * np.abs(own) + 2.0 ** -16 * ab
         assert np.all(err <= bound), "%s vs its own operands: worst excess %.3g" % (name, (err - bound).max())
+
+
+@pytest.mark.parametrize("T,H,E,k,I", _sweep_shapes(8, 777))
+def test_seeded_shape_sweep_launch_variants_bit_identical(T, H, E, k, I):
+    """At seeded irregular shapes, the forward (saving activations) and the
+    backward give the same bits in every CTA-pair mode (single CTAs, pairs
+    for the forward and dgrad GEMMs, pairs for gate_up and the
+    weight-gradient GEMMs) and with the row gather fused into the gate_up
+    load, as in the default launch (which the shape sweep above checks
+    against the oracle)."""
+    moe = lib()
+    cfg, inp = _inputs(T, H, E, k, I, seed=T * 5 + E * 11 + k)
+    variants = [(moe.GEMM_PAIRS_GATE_UP, "rows"), (moe.GEMM_PAIRS_NONE, "rows"), (moe.GEMM_PAIRS_ALL, "rows"),
+                (moe.GEMM_PAIRS_GATE_UP_WGRAD, "rows"), (moe.GEMM_PAIRS_GATE_UP, "tma")]
+    outs = []
+    for pairs, fused in variants:
+        moe.set_gemm_pairs(pairs)
+        try:
+            (x, wr, gu, dn), y, st = _forward(moe, inp, save=True, fused=fused)
+            gr = moe.moe_backward(bf(inp.dy), st, wr, gu, dn, want_dw_router=True)
+            moe.sync_status()
+        finally:
+            moe.set_gemm_pairs(moe.GEMM_PAIRS_GATE_UP)
+        outs.append([y, st.ids, st.row_map, st.h, st.gu_pre, st.h_w, st.y_perm] + [gr[n] for n in sorted(gr)])
+    for (pairs, fused), other in zip(variants[1:], outs[1:]):
+        for i, (a, b) in enumerate(zip(outs[0], other)):
+            assert torch_equal(a, b), "pairs mode %d, gather %s: output %d differs" % (pairs, fused, i)
