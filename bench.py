@@ -247,7 +247,7 @@ def make_step(moe, d, cfg, stream, fused):
         if fused:
             h, _, _ = moe.grouped_gemm_gate_up_swiglu(d["x"], src_row, offsets, d["gate_up"], I)
         else:
-            x_perm = moe.permute_rows(d["x"], src_row)
+            x_perm = moe.permute_rows_scatter(d["x"], row_map, k)
             mark()
             h, _, _ = moe.grouped_gemm_gate_up_swiglu(x_perm, None, offsets, d["gate_up"], I)
         mark()

@@ -223,6 +223,20 @@ int moe_permute_noalloc(const int32_t* ids, const float* w, int64_t T, int64_t k
 int moe_permute_rows(const uint16_t* x, const int32_t* src_row, int64_t R, int64_t H,
                      uint16_t* x_perm, void* stream);
 
+/* The same rows moved token by token (MindSpeed page §8.3 permute, the
+ * materialised form): x_perm[row_map[t*k + j]] = x[t] for t < T, j < k.
+ * Each token row is read once and written to its k permuted rows, so x is
+ * read from memory once whatever its size (moe_permute_rows reads each token
+ * row k times, in permuted order).  With row_map from moe_permute (a
+ * permutation of [0, T*k)) every row of x_perm is written exactly once and
+ * the result equals moe_permute_rows with its src_row bit for bit.
+ *   x        [T, H] bf16;  row_map [T*k] int32;  x_perm [T*k, H] bf16
+ * H % 8 == 0, 1 <= k <= 32, x and x_perm 16-byte aligned.  A row_map entry
+ * outside [0, T*k) sets MOE_ERR_DEVICE in the status word and that copy is
+ * not written. */
+int moe_permute_rows_scatter(const uint16_t* x, const int32_t* row_map, int64_t T, int64_t k, int64_t H,
+                             uint16_t* x_perm, void* stream);
+
 /* ----------------------------------------------------------- grouped GEMMs */
 
 /* Every grouped GEMM checks its offsets on the device (offsets[0] = 0,

@@ -178,6 +178,43 @@ def test_combine_matches_oracle(T, H, k, shared):
     assert_close("y", f64(y), ref)
 
 
+@pytest.mark.parametrize("T,k,E,H", [(100, 4, 8, 256), (1, 1, 1, 8), (333, 8, 64, 1000), (50, 32, 40, 2056),
+                                     (2049, 8, 128, 2048)])
+def test_permute_rows_scatter_matches_oracle(T, k, E, H):
+    """The token-by-token row move (each x row read once, written to its k
+    permuted rows) against the oracle's row gather of the same permutation,
+    bit for bit: H = 1000 and 2056 end inside a 1024-column slice; k = 32 is
+    the largest k."""
+    import torch
+    moe = lib()
+    ids = synth.distinct_ids(T + H, synth.TID_IDS, T, k, E)
+    perm = oracle.permute(ids, E)
+    _, _, row_map, _ = moe.permute(i32(ids), E)
+    x = synth.normal_bf16(T + k, synth.TID_X, (T, H), 1.0)
+    xp = moe.permute_rows_scatter(bf(x), row_map, k)
+    moe.sync_status()
+    np.testing.assert_array_equal(f64(xp), oracle.permute_rows(synth.bf16_to_f32(x), perm["src_row"]))
+
+
+def test_permute_rows_scatter_reports_a_bad_destination():
+    """A row_map entry outside [0, T*k) is reported (MOE_ERR_DEVICE) and that
+    copy is not written; the other rows are."""
+    import torch
+    moe = lib()
+    T, k, H = 16, 2, 64
+    rm = torch.arange(T * k, dtype=torch.int32, device="cuda")
+    rm[5] = T * k
+    x = torch.ones((T, H), dtype=torch.bfloat16, device="cuda")
+    out = torch.zeros((T * k, H), dtype=torch.bfloat16, device="cuda")
+    moe.ops.call("moe_permute_rows_scatter", moe.ops._p(x), moe.ops._p(rm), T, k, H, moe.ops._p(out),
+                 moe.ops._stream())
+    with pytest.raises(moe.MoEError) as ei:
+        moe.sync_status()
+    assert ei.value.status == 6
+    o = out.float().cpu().numpy()
+    assert (o[5] == 0).all() and (np.delete(o, 5, axis=0) == 1).all()
+
+
 def test_permute_rows_gathers():
     moe = lib()
     T, k, E, H = 100, 4, 8, 256

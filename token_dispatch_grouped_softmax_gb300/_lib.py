@@ -38,6 +38,7 @@ SIGNATURES = {
     "moe_permute": [P, P, I64, I64, I64, P, P, P, P, P, P, SZ, P],
     "moe_permute_noalloc": [P, P, I64, I64, I64, P, P, P, P, P, P],
     "moe_permute_rows": [P, P, I64, I64, P, P],
+    "moe_permute_rows_scatter": [P, P, I64, I64, I64, P, P],
     "moe_grouped_gemm_gate_up_swiglu": [P, P, P, P, I64, I64, I64, I64, I64, P, P, P, P, P],
     "moe_grouped_gemm_down": [P, P, P, I64, I64, I64, I64, P, P],
     "moe_unpermute_combine": [P, P, P, P, I64, I64, I64, P, P],

@@ -236,6 +236,20 @@ int moe_permute_rows(const uint16_t* x, const int32_t* src_row, int64_t R, int64
                                               static_cast<cudaStream_t>(stream)));
 }
 
+int moe_permute_rows_scatter(const uint16_t* x, const int32_t* row_map, int64_t T, int64_t k, int64_t H,
+                             uint16_t* x_perm, void* stream) {
+  if (T < 0 || H < 1 || k < 1 || T > kMaxI32 || T * k > kMaxI32) return MOE_ERR_INVALID_ARG;
+  if (k > 32 || H % 8 != 0) return MOE_ERR_UNSUPPORTED;
+  if (T == 0) return MOE_OK;
+  if (!x || !row_map || !x_perm) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(x_perm)) return MOE_ERR_INVALID_ARG;
+  moe::DeviceInfo dev;
+  const int rc = moe::current_device(&dev);
+  if (rc != MOE_OK) return rc;
+  return cuda_status(moe::launch_scatter_rows(x, row_map, T, k, H, x_perm, dev.status,
+                                              static_cast<cudaStream_t>(stream)));
+}
+
 /* ----------------------------------------------------------- grouped GEMMs */
 
 static int gemm_shape_check(int64_t R, int64_t H, int64_t E, int64_t I) {

@@ -86,10 +86,12 @@ struct Traits {
   static constexpr bool kBMN = (kGateUp || MODE == FWD_DOWN || MODE == WGRAD_DOWN ||
                                 MODE == WGRAD_GATEUP || MODE == ROUTER);
   static constexpr bool kKGrouped = (MODE == WGRAD_DOWN || MODE == WGRAD_GATEUP);
-  // Tiles from the last expert to the first: the permuted token rows were
-  // written just before, in increasing row order, by a gather that moves
-  // more bytes than L2 holds, so the rows of the last experts are the ones
-  // still in L2.
+  // Tiles from the last expert to the first: when the permuted token rows
+  // were written just before in increasing row order (moe_permute_rows, a
+  // gather that moves more bytes than L2 holds), the rows of the last
+  // experts are the ones still in L2.  Rows moved token by token
+  // (moe_permute_rows_scatter) end in L2 in no expert order; either order
+  // measures the same then.
   static constexpr bool kReverse = (MODE == FWD_GATEUP);
   static constexpr bool kRouter = (MODE == ROUTER);
   // One half per CTA for the epilogues with per-element math (SwiGLU, its

@@ -87,6 +87,8 @@ cudaError_t launch_permute(const int32_t* ids, const float* w, int64_t T, int64_
                            float* w_perm, void* ws, const DeviceInfo& dev, cudaStream_t stream,
                            bool noalloc = false);
 // src_rows: rows of x, checked on the device (0: unchecked)
+cudaError_t launch_scatter_rows(const uint16_t* x, const int32_t* row_map, int64_t T, int64_t k, int64_t H,
+                                uint16_t* x_perm, uint32_t* status, cudaStream_t stream);
 cudaError_t launch_permute_rows(const uint16_t* x, const int32_t* src_row, int64_t R, int64_t H,
                                 uint16_t* x_perm, int64_t src_rows, uint32_t* status, cudaStream_t stream);
 

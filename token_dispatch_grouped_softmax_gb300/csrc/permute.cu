@@ -552,6 +552,53 @@ __global__ void permute_rows_kernel(const uint16_t* __restrict__ x, const int32_
   }
 }
 
+// The same rows moved token by token: x_perm[row_map[t*k + j]] = x[t] for
+// j < k.  One warp per (token, slice of up to 1024 columns) reads its slice
+// of x[t] once (four 16-byte chunks per lane) and writes it to the token's
+// k rows.  Where x is larger than L2 this reads it from DRAM once, where the
+// gather above reads each token row k times in permuted (scattered) order.
+// A destination outside [0, T*k) is reported and not written.
+constexpr int kScatterChunks = 128;   // 16-byte chunks per warp (1024 bf16)
+
+__global__ void scatter_rows_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ row_map, int64_t T,
+                                    int k, int H, uint16_t* __restrict__ x_perm, uint32_t* status) {
+  pdl_wait();
+  pdl_trigger();
+  const int nch = H / 8;
+  const int slices = (nch + kScatterChunks - 1) / kScatterChunks;
+  const int64_t gw = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int64_t t = gw / slices;
+  if (t >= T) return;
+  const int c0 = (int)(gw - t * slices) * kScatterChunks;
+  const int lane = threadIdx.x & 31;
+  const int64_t R = T * k;
+  int my_row = -1;
+  if (lane < k) {
+    my_row = row_map[t * k + lane];
+    if (my_row < 0 || (int64_t)my_row >= R) {
+      report_status(status, kStatusDevice, kKernPermute, 4);
+      my_row = -1;
+    }
+  }
+  const uint4* src = reinterpret_cast<const uint4*>(x + t * H);
+  uint4 v[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const int c = c0 + lane + 32 * q;
+    v[q] = c < nch ? ld_stream16(src + c) : make_uint4(0, 0, 0, 0);
+  }
+  for (int j = 0; j < k; ++j) {
+    const int row = __shfl_sync(0xffffffffu, my_row, j);
+    if (row < 0) continue;   // warp-uniform
+    uint4* dst = reinterpret_cast<uint4*>(x_perm + (int64_t)row * H);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int c = c0 + lane + 32 * q;
+      if (c < nch) dst[c] = v[q];
+    }
+  }
+}
+
 }  // namespace
 
 // Workspace: hist [nblocks][E]; with the one-launch path also totals [E]
@@ -640,6 +687,15 @@ cudaError_t launch_permute(const int32_t* ids, const float* w, int64_t T, int64_
                                           status, stream);
   return enqueue_permute<kChunk>(ids, w, T * k, k, E, counts, offsets, row_map, src_row, w_perm, hist, status,
                                  stream);
+}
+
+cudaError_t launch_scatter_rows(const uint16_t* x, const int32_t* row_map, int64_t T, int64_t k, int64_t H,
+                                uint16_t* x_perm, uint32_t* status, cudaStream_t stream) {
+  if (T == 0) return cudaSuccess;
+  const int64_t slices = (H / 8 + kScatterChunks - 1) / kScatterChunks;
+  const int64_t warps = T * slices;
+  return launch_pdl(scatter_rows_kernel, dim3((unsigned)((warps + 7) / 8)), dim3(256), 0, stream, 1, x, row_map, T,
+                    (int)k, (int)H, x_perm, status);
 }
 
 cudaError_t launch_permute_rows(const uint16_t* x, const int32_t* src_row, int64_t R, int64_t H,

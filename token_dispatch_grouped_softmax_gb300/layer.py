@@ -54,7 +54,7 @@ def moe_forward(x, w_router, gate_up, down, k, bias=None, sh_gate_up=None, sh_do
 
     fused_gather: the grouped gate_up GEMM gathers the token rows itself (the
     permute fused into the operand load by TMA tile::gather4); False
-    (default) materialises the permuted rows first (moe_permute_rows) and
+    (default) materialises the permuted rows first (moe_permute_rows_scatter) and
     streams them with 128-row TMA tiles, which measures ~2.5x faster for the
     GEMM on GB300.
     w_split: W_r's bf16 split (ops.route_split_weight), prepared once while
@@ -77,7 +77,7 @@ def moe_forward(x, w_router, gate_up, down, k, bias=None, sh_gate_up=None, sh_do
                                                              save_for_backward=save_for_backward)
     else:
         with _range("moe.permute_rows"):
-            x_perm = ops.permute_rows(x, src_row)
+            x_perm = ops.permute_rows_scatter(x, row_map, k)
         with _range("moe.gate_up"):
             h, gu_pre, h_w = ops.grouped_gemm_gate_up_swiglu(x_perm, None, offsets, gate_up, I, w_perm=w_perm,
                                                              save_for_backward=save_for_backward)
@@ -302,7 +302,7 @@ class OverlappedForward:
             def front(st=st):
                 ids, w = ops.route(st["x"], w_router, k, bias, w_split=w_split)
                 counts, offsets, row_map, src_row = ops.permute(ids, E)
-                x_perm = None if fused_gather else ops.permute_rows(st["x"], src_row)
+                x_perm = None if fused_gather else ops.permute_rows_scatter(st["x"], row_map, k)
                 st.update(w=w, offsets=offsets, row_map=row_map, src_row=src_row, x_perm=x_perm)
 
             def back(st=st):

@@ -179,6 +179,20 @@ def permute_rows(x, src_row, out=None):
     return out
 
 
+def permute_rows_scatter(x, row_map, k):
+    """x_perm [T*k, H] bf16 with x_perm[row_map[t*k + j]] = x[t]: the rows of
+    permute_rows(x, src_row) for the same permutation, moved token by token
+    (each token row read once)."""
+    _need(x, "x", _BF16, 2)
+    _need(row_map, "row_map", torch.int32, 1)
+    T, H = x.shape
+    if row_map.shape[0] != T * k:
+        raise ValueError("row_map must hold T*k entries")
+    out = torch.empty((T * k, H), dtype=_BF16, device=x.device)
+    call("moe_permute_rows_scatter", _p(x), _p(row_map), T, k, H, _p(out), _stream())
+    return out
+
+
 def sort_chunks(counts, N):
     """Rows arriving as an A x B chunk matrix in (a, b) order -> (b, a) order
     (moe_sort_chunks): src_of [N], pos_of [N] and group_offsets [B+1] (int32).
