@@ -167,6 +167,22 @@ def test_permute_validation(lib):
     assert pm(FAKE, None, 100, 8, 128, FAKE, FAKE, FAKE, FAKE, None, MISALIGNED, n.value, None) == INVALID
 
 
+def test_permute_rows_validation(lib):
+    """The row moves: gather (src_row) and scatter (row_map)."""
+    g, sc = lib.moe_permute_rows, lib.moe_permute_rows_scatter
+    assert g(FAKE, FAKE, 64, 60, FAKE, None) == UNSUPPORTED                 # H % 8
+    assert g(None, FAKE, 64, 64, FAKE, None) == INVALID
+    assert g(MISALIGNED, FAKE, 64, 64, FAKE, None) == INVALID
+    assert g(None, None, 0, 64, None, None) == 0                            # no rows
+    assert sc(FAKE, FAKE, 16, 33, 64, FAKE, None) == UNSUPPORTED            # k > 32
+    assert sc(FAKE, FAKE, 16, 2, 60, FAKE, None) == UNSUPPORTED             # H % 8
+    assert sc(FAKE, FAKE, 16, 0, 64, FAKE, None) == INVALID
+    assert sc(FAKE, None, 16, 2, 64, FAKE, None) == INVALID
+    assert sc(FAKE, FAKE, 16, 2, 64, MISALIGNED, None) == INVALID
+    assert sc(FAKE, FAKE, 1 << 30, 8, 64, FAKE, None) == INVALID            # T*k past int32
+    assert sc(None, None, 0, 2, 64, None, None) == 0                        # an empty batch
+
+
 def test_gemm_validation(lib):
     f = lib.moe_grouped_gemm_gate_up_swiglu
     # H not a multiple of 64
