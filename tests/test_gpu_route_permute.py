@@ -16,7 +16,7 @@ pytestmark = pytest.mark.gpu
                                      (4100, 2048, 128, 8)])
 def test_route_matches_oracle(T, H, E, k):
     """Shapes of the three router paths: the fused cluster kernel (16 <= E <=
-    256, E % 16 == 0; clusters of 3, 6 and 8 CTAs, a partial 64-expert
+    256, E % 16 == 0; clusters of 1 to 4 CTAs, 3 for E > 128, a partial 64-expert
     chunk, ragged 128-token tiles), the split-K tensor-core GEMM with a
     separate top-k (E % 8 == 0 otherwise) and the CUDA-core GEMM."""
     moe = lib()
