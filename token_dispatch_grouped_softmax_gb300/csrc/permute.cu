@@ -553,12 +553,16 @@ __global__ void permute_rows_kernel(const uint16_t* __restrict__ x, const int32_
 }
 
 // The same rows moved token by token: x_perm[row_map[t*k + j]] = x[t] for
-// j < k.  One warp per (token, slice of up to 1024 columns) reads its slice
-// of x[t] once (four 16-byte chunks per lane) and writes it to the token's
+// j < k.  One warp per (token, slice of kScatterChunks 16-byte chunks) reads its slice
+// of x[t] once (kScatterPerLane 16-byte chunks per lane) and writes it to the token's
 // k rows.  Where x is larger than L2 this reads it from DRAM once, where the
 // gather above reads each token row k times in permuted (scattered) order.
 // A destination outside [0, T*k) is reported and not written.
-constexpr int kScatterChunks = 128;   // 16-byte chunks per warp (1024 bf16)
+// 16-byte chunks per warp: 64 (512 bf16).  Measured in the layer at the
+// Qwen3-MoE shape / the DeepSeek-V3 shape: 32 chunks 26.2 / 313 us, 64
+// 26.3 / 313, 128 27.2 / 318, 256 28.2 / 318.
+constexpr int kScatterChunks = 64;
+constexpr int kScatterPerLane = kScatterChunks / 32;
 
 __global__ void scatter_rows_kernel(const uint16_t* __restrict__ x, const int32_t* __restrict__ row_map, int64_t T,
                                     int k, int H, uint16_t* __restrict__ x_perm, uint32_t* status) {
@@ -581,9 +585,9 @@ __global__ void scatter_rows_kernel(const uint16_t* __restrict__ x, const int32_
     }
   }
   const uint4* src = reinterpret_cast<const uint4*>(x + t * H);
-  uint4 v[4];
+  uint4 v[kScatterPerLane];
 #pragma unroll
-  for (int q = 0; q < 4; ++q) {
+  for (int q = 0; q < kScatterPerLane; ++q) {
     const int c = c0 + lane + 32 * q;
     v[q] = c < nch ? ld_stream16(src + c) : make_uint4(0, 0, 0, 0);
   }
@@ -592,7 +596,7 @@ __global__ void scatter_rows_kernel(const uint16_t* __restrict__ x, const int32_
     if (row < 0) continue;   // warp-uniform
     uint4* dst = reinterpret_cast<uint4*>(x_perm + (int64_t)row * H);
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
+    for (int q = 0; q < kScatterPerLane; ++q) {
       const int c = c0 + lane + 32 * q;
       if (c < nch) dst[c] = v[q];
     }
