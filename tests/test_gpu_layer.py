@@ -135,6 +135,23 @@ def test_backward_dx_router_term_shapes(T, H, E, k, I):
     assert_close("dX", f64(g["dx"]), b["dX"])
 
 
+def test_dy_rows_gather_equals_scatter():
+    """The combine's backward moves dY rows to permuted order: the gather
+    (moe_unpermute_combine_bwd, by src_row) and the token-by-token scatter
+    the layer uses (moe_permute_rows_scatter, by row_map) give the same bits,
+    and the oracle's rows."""
+    import torch
+    moe = lib()
+    cfg, inp = _inputs(300, 256, 16, 4, 64, seed=17)
+    (x, wr, gu, dn), y, st = _forward(moe, inp, save=True)
+    dy = bf(inp.dy)
+    a = moe.ops.unpermute_combine_bwd(dy, st.src_row)
+    b = moe.ops.permute_rows_scatter(dy, st.row_map, cfg.k)
+    moe.sync_status()
+    assert torch_equal(a, b)
+    np.testing.assert_array_equal(f64(b), oracle.permute_rows(synth.bf16_to_f32(inp.dy), npi(st.src_row)))
+
+
 def test_backward_empty_experts_get_zero_weight_grads():
     moe = lib()
     cfg, inp = _inputs(40, 128, 32, 1, 64, seed=5)

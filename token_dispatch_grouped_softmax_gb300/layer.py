@@ -8,7 +8,8 @@ MoE/EP guide: shared experts are always active).  All calls are enqueued on
 the current stream with no host synchronisation: expert_offsets stay on the
 device and the grouped GEMMs read them there.
 
-Backward: combine_bwd -> down_bwd -> route_bwd -> gate_up_bwd -> gather_dx.
+Backward: combine_bwd (dY rows to permuted order) -> down_bwd -> route_bwd ->
+gate_up_bwd -> gather_dx.
 """
 from __future__ import annotations
 
@@ -104,7 +105,9 @@ def moe_backward(dy, st: ForwardState, w_router, gate_up, down, want_dw_router=F
     E = w_router.shape[1]
     k = st.w.shape[1]
     with _range("moe.combine_bwd"):
-        dy_perm = ops.unpermute_combine_bwd(dy, st.src_row)
+        # dy_perm[row] = dY[src_row[row]], moved token by token (each dY row read
+        # once; the same bits as ops.unpermute_combine_bwd, the gather)
+        dy_perm = ops.permute_rows_scatter(dy, st.row_map, k)
     with _range("moe.down_bwd"):
         dgu, d_down, dw_part = ops.grouped_gemm_down_bwd(dy_perm, st.h_w, st.gu_pre, st.w_perm, st.offsets, down)
     with _range("moe.route_bwd"):
