@@ -234,6 +234,28 @@ def test_permuted_equals_bruteforce_dense():
     np.testing.assert_allclose(yt, yd, rtol=1e-12, atol=1e-12 * np.abs(yd).max())
 
 
+@pytest.mark.parametrize("skew,I_s", [(False, 0), (True, 0), (False, 32)])
+def test_layer_forward_equals_per_token_definition(skew, I_s):
+    """Pin of the composition: layer_forward (route -> permute -> permuted
+    experts -> combine, with the router bias of a skewed config and a shared
+    expert) equals the per-token definition computed by brute force: every
+    expert on every token, masked by the routing the bias produces, plus the
+    shared FFN on every token."""
+    cfg = synth.MoEConfig("pin", T=48, H=64, E=6, k=2, I=32, seed=5, skew=skew, I_shared=I_s)
+    inp = synth.make_inputs(cfg, bias_scale=1.0 if skew else None)
+    res = oracle.layer_forward(inp)
+    r = oracle.route(inp.x, inp.w_router, inp.bias, cfg.k)
+    np.testing.assert_array_equal(res["route"]["ids"], r["ids"])
+    yd = oracle.forward_dense(inp.x, inp.gate_up, inp.down, r["ids"], r["w"], inp.sh_gate_up, inp.sh_down)
+    np.testing.assert_allclose(res["y"], yd, rtol=1e-12, atol=1e-12 * np.abs(yd).max())
+    if skew:
+        assert inp.bias is not None and not np.array_equal(
+            r["ids"], oracle.route(inp.x, inp.w_router, None, cfg.k)["ids"])   # the bias changes the routing
+    if I_s:
+        y_no_shared = oracle.forward_dense(inp.x, inp.gate_up, inp.down, r["ids"], r["w"])
+        assert np.abs(res["y"] - y_no_shared).max() > 1e-3                     # the shared expert is added
+
+
 def test_dense_ffn_matches_library_matmul():
     """Pin: the SwiGLU FFN against numpy matmuls (library routine), which also
     fixes gate = first I columns, up = last I columns, and operand orientation."""
