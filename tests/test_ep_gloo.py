@@ -1,7 +1,7 @@
 """Expert-parallel dispatch and combine across real processes (gloo, world
-size 2, CPU only), with the oracle's arithmetic.
+sizes 2 and 4, CPU only), with the oracle's arithmetic.
 
-Each rank holds half of the tokens and half of the experts (split on dim 0).
+Each rank holds 1/G of the tokens and of the experts (split on dim 0).
 It routes its tokens, permutes them by expert, exchanges the per-expert
 counts (all-gather), sends each rank its rows (all-to-all-v with the split
 sizes from the counts), re-sorts the received chunks by local expert
@@ -12,10 +12,14 @@ The gathered output must equal the single-process layer.  This checks the
 host side of the exchange (split sizes, chunk orders) with a real
 collective; no GPU is involved.
 """
+import pytest
 from test_bench_multirank import _run_ranks
 
 
-def test_ep_dispatch_combine_two_ranks_equals_the_layer():
+@pytest.mark.parametrize("world", [2, 4])
+def test_ep_dispatch_combine_across_ranks_equals_the_layer(world):
+    """2 and 4 ranks (4 and 2 experts per rank; with 4 ranks a rank may
+    receive nothing from some sources)."""
     outs = _run_ranks("""
         import numpy as np
         import torch
@@ -68,5 +72,5 @@ def test_ep_dispatch_combine_two_ranks_equals_the_layer():
             print("max err %.3g rows per rank %s" % (err, S.sum(0).tolist()))
             assert err < 1e-12
         dist.destroy_process_group()
-    """)
+    """, world=world)
     assert outs[0].startswith("max err")
