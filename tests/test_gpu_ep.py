@@ -143,3 +143,39 @@ def test_eplb_replicas_balance_skewed_routing():
                                                         balanced["rows_per_rank"].max() / mean))
     assert plain["rows_per_rank"].max() > 1.3 * mean        # the hotspots overload one rank (1.41x)
     assert balanced["rows_per_rank"].max() < 1.1 * mean     # the plan spreads them (1.0x planned)
+
+
+@pytest.mark.parametrize("G", [1, 2, 8])
+def test_ep_fused_dispatch_equals_local_layer(G):
+    """The receivers' gate_up GEMMs gather their rows straight from the
+    senders' token rows (no dispatch copy, no re-sort copy): the local
+    layer's output bit for bit, at T = 300 tokens (uneven token ranges) and
+    at the Qwen3-MoE shape over 8 ranks."""
+    import torch
+    from token_dispatch_grouped_softmax_gb300 import ep
+    moe = lib()
+    for cfg in (synth.MoEConfig("ep", T=300, H=256, E=16, k=4, I=128, seed=60 + G), synth.CONFIGS["qwen3_moe"]):
+        if cfg.E % G:
+            continue
+        inp, x, wr, gu, dn, _ = _layer_inputs(moe, cfg)
+        y_fused = ep.ep_forward_emulated(x, wr, gu, dn, cfg.k, G, fused_dispatch=True)
+        y_local, _ = moe.moe_forward(x, wr, gu, dn, cfg.k)
+        moe.sync_status()
+        assert torch.equal(y_fused.view(torch.int16), y_local.view(torch.int16)), cfg.name
+
+
+def test_ep_fused_dispatch_with_eplb_replicas():
+    """The fused dispatch over physical experts (EPLB replicas of the skewed
+    workload's hotspots), equal to the local layer bit for bit."""
+    import torch
+    from token_dispatch_grouped_softmax_gb300 import ep
+    moe = lib()
+    cfg = synth.CONFIGS["qwen3_moe_skewed"]
+    inp, x, wr, gu, dn, bias = _layer_inputs(moe, cfg)
+    y_local, st = moe.moe_forward(x, wr, gu, dn, cfg.k, bias)
+    plan = ep.EPLBPlan.build(npi(st.counts).astype(np.int64), 8, cfg.E + 32)
+    weights = ep.replicate_weights(gu, dn, plan.phys_to_log)
+    y = ep.ep_forward_emulated(x, wr, gu, dn, cfg.k, 8, bias=bias, plan=plan, phys_weights=weights,
+                               fused_dispatch=True)
+    moe.sync_status()
+    assert torch.equal(y.view(torch.int16), y_local.view(torch.int16))

@@ -27,6 +27,17 @@ EPLB replicas, which is what the tests check.  A multi-GPU deployment replaces
 the two transposes by an all-to-all-v of the same split sizes; this library
 has no multi-GPU path of its own.
 
+With fused_dispatch=True the receivers' gate_up GEMMs gather their A rows
+straight from the senders' token rows (the grouped GEMM's TMA tile::gather4
+load, through the composed index: receiver row -> (local expert, source) ->
+the source's permuted row -> token), so neither the dispatch all-to-all nor
+the re-sort copies a row: the data movement of an MC2-style fused
+all-to-all + grouped GEMM ("FSDPTurbo EP/EFSDP" §3, the mc2 dispatcher; the
+guide's DeepEP passage, compute starting as tokens arrive), on one device.
+The composed index is built on the host from the sources' permutations.  On
+GB300 the gathered load is slower than materialising the rows (it is bound
+by the gather instruction rate), so it is off by default.
+
 EPLB-style replication (the guide's hotspot experts): ``EPLBPlan`` gives hot
 experts extra physical replicas (moe_eplb_plan, on the host) and spreads the
 physical experts over the ranks; ``moe_ep_map_replicas`` sends each (token,
@@ -94,7 +105,7 @@ def token_ranges(T, G):
 
 
 def ep_forward_emulated(x, w_router, gate_up, down, k, G, bias=None, plan: EPLBPlan | None = None,
-                        phys_weights=None, stats=None):
+                        phys_weights=None, stats=None, fused_dispatch=False):
     """The layer forward with experts split over G ranks, every rank's
     single-device steps run on this GPU in turn (see the module docstring).
 
@@ -103,6 +114,8 @@ def ep_forward_emulated(x, w_router, gate_up, down, k, G, bias=None, plan: EPLBP
     the physical experts are the logical ones.  stats (a dict, optional)
     receives rows_per_rank [G] (the rows each rank's experts computed) and
     splits [G, G] (rows sent from source s to destination d).
+    fused_dispatch: the receivers' gate_up GEMMs gather their rows from the
+    senders' token rows (see the module docstring).
     Returns y [T, H] bf16, equal to moe_forward's bit for bit."""
     T, H = x.shape
     E = w_router.shape[1]
@@ -136,17 +149,24 @@ def ep_forward_emulated(x, w_router, gate_up, down, k, G, bias=None, plan: EPLBP
     if stats is not None:
         stats["splits"] = S
         stats["rows_per_rank"] = n_recv
-    # the send buffers side by side: every source gathers its rows into its slice
-    send = torch.empty((N, H), dtype=torch.bfloat16, device=dev)
     base = np.concatenate([[0], np.cumsum(n_send)]).astype(np.int64)
-    for s_i, s in enumerate(src):
-        ops.permute_rows(s["x"], s["src_row"], out=send[base[s_i]:base[s_i + 1]])
-    # 3. all-to-all: (source, destination) chunks -> (destination, source)
     S_dev = torch.from_numpy(S.astype(np.int32)).to(dev)
     a2a_src, a2a_pos, _ = ops.sort_chunks(S_dev, N)
-    recv = ops.permute_rows(send, a2a_src)
+    if fused_dispatch:
+        # the token of each row a receiver's experts see, in (local expert, source) order
+        src_rows = [s["src_row"].cpu().numpy().astype(np.int64) for s in src]
+        src_offs = [np.concatenate([[0], np.cumsum(C_h[s_i])]).astype(np.int64) for s_i in range(G)]
+        t0s = [t0 for (t0, _) in ranges]
+        recv = None
+    else:
+        # the send buffers side by side: every source gathers its rows into its slice
+        send = torch.empty((N, H), dtype=torch.bfloat16, device=dev)
+        for s_i, s in enumerate(src):
+            ops.permute_rows(s["x"], s["src_row"], out=send[base[s_i]:base[s_i + 1]])
+        # 3. all-to-all: (source, destination) chunks -> (destination, source)
+        recv = ops.permute_rows(send, a2a_src)
     # 4. every destination: re-sort by local expert, grouped GEMMs, sort back
-    y_recv = torch.empty_like(recv)
+    y_recv = torch.empty((N, H), dtype=torch.bfloat16, device=dev)
     rbase = np.concatenate([[0], np.cumsum(n_recv)]).astype(np.int64)
     for d in range(G):
         n_d = int(n_recv[d])
@@ -155,10 +175,15 @@ def ep_forward_emulated(x, w_router, gate_up, down, k, G, bias=None, plan: EPLBP
         # what rank d learns from the count exchange: [G_src, P] (source, local expert)
         recv_counts = torch.from_numpy(np.ascontiguousarray(C_h[:, d * P:(d + 1) * P]).astype(np.int32)).to(dev)
         s_src, s_pos, local_offsets = ops.sort_chunks(recv_counts, n_d)
-        rows = ops.permute_rows(recv[rbase[d]:rbase[d] + n_d], s_src)
         gu_d = gu_p[d * P * H:(d + 1) * P * H]
         dn_d = dn_p[d * P * I:(d + 1) * P * I]
-        h, _, _ = ops.grouped_gemm_gate_up_swiglu(rows, None, local_offsets, gu_d, I)
+        if fused_dispatch:
+            tok = np.concatenate([src_rows[s_i][src_offs[s_i][d * P + e]:src_offs[s_i][d * P + e + 1]] + t0s[s_i]
+                                  for e in range(P) for s_i in range(G)]).astype(np.int32)
+            h, _, _ = ops.grouped_gemm_gate_up_swiglu(x, torch.from_numpy(tok).to(dev), local_offsets, gu_d, I)
+        else:
+            rows = ops.permute_rows(recv[rbase[d]:rbase[d] + n_d], s_src)
+            h, _, _ = ops.grouped_gemm_gate_up_swiglu(rows, None, local_offsets, gu_d, I)
         y_sorted = ops.grouped_gemm_down(h, local_offsets, dn_d, H)
         ops.permute_rows(y_sorted, s_pos, out=y_recv[rbase[d]:rbase[d] + n_d])
     # 5. all-to-all back: (destination, source) -> (source, destination); combine
