@@ -299,7 +299,9 @@ int moe_unpermute_combine(const uint16_t* y_perm, const int32_t* row_map, const 
  * The gate-weight gradient dw[t,j] = <dY[t], y_perm[row_map[t*k+j]]> is
  * produced by moe_grouped_gemm_down_bwd (as <dY . Wd^T, h>) and summed by
  * moe_route_bwd.  dy [T, H] bf16; src_row [R] int32; dy_perm [R, H] bf16.
- * A src_row entry outside [0, T) sets MOE_ERR_DEVICE (row 0 is read). */
+ * A src_row entry outside [0, T) sets MOE_ERR_DEVICE (row 0 is read).
+ * moe_permute_rows_scatter(dy, row_map, ...) computes the same dy_perm bit
+ * for bit, reading each dY row once. */
 int moe_unpermute_combine_bwd(const uint16_t* dy, const int32_t* src_row, int64_t T, int64_t H,
                               int64_t k, uint16_t* dy_perm, void* stream);
 
